@@ -1,0 +1,285 @@
+"""CPU oracle for the streamed-expert MoE layer -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The product (the CUDA library and its
+binding) never does, and the oracle shares no code with it: both sides are fed
+by the seeded generators in ``workload/`` and nothing else.
+
+The arithmetic lives in ``oracle.c`` (plain single-threaded C, built twice:
+fp32 and fp64); this module only loads it and marshals numpy arrays.
+
+Pins: every function here is checked in ``tests/test_oracle_*.py`` against
+closed forms, brute force, hand-written traces and the pages' fixed facts.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+EPS = 1e-6
+K_ACTIVE = 8
+
+
+def _lib_path(bits: int) -> str:
+    return os.path.join(_HERE, "liboracle%d.so" % bits)
+
+
+def build(force: bool = False) -> None:
+    """Compile the fp32 and fp64 oracles (-O2, no FMA contraction, no fast-math, SSE2)."""
+    for bits, defs in ((32, ["-DREAL=float", "-DREAL_IS_DOUBLE=0"]),
+                       (64, ["-DREAL=double", "-DREAL_IS_DOUBLE=1"])):
+        out = _lib_path(bits)
+        if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(_SRC):
+            tmp = out + ".tmp%d" % os.getpid()
+            subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                                   "-fno-fast-math", "-msse2", "-mfpmath=sse", *defs, "-o", tmp, _SRC, "-lm"])
+            os.replace(tmp, out)
+
+
+class Expert(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p * 3), ("s", ctypes.c_void_p * 3), ("b", ctypes.c_void_p * 3)]
+
+
+class CacheEvent(ctypes.Structure):
+    _fields_ = [("step", ctypes.c_int32), ("layer", ctypes.c_int32), ("expert", ctypes.c_int32),
+                ("hit", ctypes.c_int32), ("slot", ctypes.c_int32), ("evicted", ctypes.c_int32)]
+
+
+_libs: dict = {}
+
+
+def lib(bits: int = 32):
+    if bits not in _libs:
+        build()
+        L = ctypes.CDLL(_lib_path(bits))
+        R = ctypes.c_float if bits == 32 else ctypes.c_double
+        vp, i32 = ctypes.c_void_p, ctypes.c_int
+        L.or_half_to_float.restype = ctypes.c_float
+        L.or_half_to_float.argtypes = [ctypes.c_uint16]
+        L.or_bf16_to_float.restype = ctypes.c_float
+        L.or_bf16_to_float.argtypes = [ctypes.c_uint16]
+        L.or_float_to_bf16.restype = ctypes.c_uint16
+        L.or_float_to_bf16.argtypes = [ctypes.c_float]
+        L.or_rms_scale.restype = R
+        L.or_rms_scale.argtypes = [vp, i32, ctypes.c_double]
+        L.or_normalise.argtypes = [vp, i32, R, vp]
+        L.or_router_logits.argtypes = [vp, i32, vp, i32, vp, R, vp]
+        L.or_topk.argtypes = [vp, i32, i32, vp]
+        L.or_softmax_selected.argtypes = [vp, vp, i32, vp]
+        L.or_dequant.restype = R
+        L.or_dequant.argtypes = [ctypes.c_uint8, ctypes.c_uint16, ctypes.c_uint16]
+        L.or_dequant_matrix.argtypes = [vp, vp, vp, i32, i32, i32, vp]
+        L.or_gelu.restype = R
+        L.or_gelu.argtypes = [R]
+        L.or_expert_ffn.argtypes = [vp, i32, i32, ctypes.POINTER(Expert), i32, vp]
+        L.or_shared_ffn.argtypes = [vp, i32, i32, vp, vp, vp, i32, vp]
+        L.or_route.argtypes = [vp, i32, vp, i32, vp, i32, ctypes.c_double, ctypes.POINTER(R), vp, vp, vp]
+        L.or_layer_combine.argtypes = [vp, i32, i32, R, i32, ctypes.POINTER(Expert), vp, i32, vp, vp, vp,
+                                       i32, vp, vp]
+        L.or_lfu_new.restype = vp
+        L.or_lfu_new.argtypes = [i32, i32]
+        L.or_lfu_free.argtypes = [vp]
+        L.or_lfu_step.restype = i32
+        L.or_lfu_step.argtypes = [vp, i32, i32, vp, i32, ctypes.POINTER(CacheEvent)]
+        L.or_lfu_state.argtypes = [vp, i32, vp, vp, vp]
+        L.or_real_bytes.restype = i32
+        _libs[bits] = L
+    return _libs[bits]
+
+
+def _dt(bits):
+    return np.float32 if bits == 32 else np.float64
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data
+
+
+# ------------------------------------------------------------------------ scalar pieces
+
+def half_to_float(h: int) -> float:
+    return lib().or_half_to_float(h)
+
+
+def float_to_bf16(f: float) -> int:
+    return lib().or_float_to_bf16(f)
+
+
+def gelu(v: float, bits: int = 32) -> float:
+    return lib(bits).or_gelu(v)
+
+
+def dequant(q: int, s: int, b: int, bits: int = 32) -> float:
+    return lib(bits).or_dequant(q, s, b)
+
+
+def dequant_matrix(q, s, b, bf16_ops: bool = False, bits: int = 32) -> np.ndarray:
+    R, K = q.shape
+    q, qp = _c(q, np.uint8)
+    s, sp = _c(s, np.uint16)
+    b, bp = _c(b, np.uint16)
+    W = np.empty((R, K), _dt(bits))
+    lib(bits).or_dequant_matrix(qp, sp, bp, R, K, int(bf16_ops), W.ctypes.data)
+    return W
+
+
+# ----------------------------------------------------------------------------- routing
+
+def rms_scale(x, bits: int = 32, eps: float = EPS) -> float:
+    x, xp = _c(x, np.uint16)
+    return lib(bits).or_rms_scale(xp, x.shape[-1], eps)
+
+
+def normalise(x, r, bits: int = 32) -> np.ndarray:
+    x, xp = _c(x, np.uint16)
+    n = np.empty(x.shape[-1], _dt(bits))
+    lib(bits).or_normalise(xp, x.shape[-1], r, n.ctypes.data)
+    return n
+
+
+def router_logits(x, Wr, bias=None, r=None, bits: int = 32) -> np.ndarray:
+    x, xp = _c(x, np.uint16)
+    Wr, wp = _c(Wr, np.uint16)
+    E, H = Wr.shape
+    if r is None:
+        r = rms_scale(x, bits)
+    bp = None
+    if bias is not None:
+        bias, bp = _c(bias, np.float32)
+    z = np.empty(E, _dt(bits))
+    lib(bits).or_router_logits(xp, H, wp, E, bp, r, z.ctypes.data)
+    return z
+
+
+def topk(z, k: int = K_ACTIVE, bits: int = 32) -> np.ndarray:
+    z, zp = _c(z, _dt(bits))
+    idx = np.empty(k, np.int32)
+    lib(bits).or_topk(zp, z.shape[0], k, idx.ctypes.data)
+    return idx
+
+
+def softmax_selected(z, idx, bits: int = 32) -> np.ndarray:
+    z, zp = _c(z, _dt(bits))
+    idx, ip = _c(idx, np.int32)
+    w = np.empty(idx.shape[0], _dt(bits))
+    lib(bits).or_softmax_selected(zp, ip, idx.shape[0], w.ctypes.data)
+    return w
+
+
+def route(x, Wr, bias=None, k: int = K_ACTIVE, bits: int = 32, eps: float = EPS):
+    """One token's routing -> (r, z[E], idx[k] best first, w[k])."""
+    x, xp = _c(x, np.uint16)
+    Wr, wp = _c(Wr, np.uint16)
+    E, H = Wr.shape
+    bp = None
+    if bias is not None:
+        bias, bp = _c(bias, np.float32)
+    R = ctypes.c_float if bits == 32 else ctypes.c_double
+    r = R()
+    z = np.empty(E, _dt(bits))
+    idx = np.empty(k, np.int32)
+    w = np.empty(k, _dt(bits))
+    lib(bits).or_route(xp, H, wp, E, bp, k, eps, ctypes.byref(r), z.ctypes.data, idx.ctypes.data, w.ctypes.data)
+    return r.value, z, idx, w
+
+
+# --------------------------------------------------------------------------------- FFN
+
+def _expert_struct(ex: dict, keep: list) -> Expert:
+    st = Expert()
+    for m, name in enumerate(("gate", "up", "down")):
+        q, s, b = ex[name]
+        q, qp = _c(q, np.uint8)
+        s, sp = _c(s, np.uint16)
+        b, bp = _c(b, np.uint16)
+        keep += [q, s, b]
+        st.q[m], st.s[m], st.b[m] = qp, sp, bp
+    return st
+
+
+def expert_ffn(n, ex: dict, bf16_ops: bool = False, bits: int = 32) -> np.ndarray:
+    """y = Wd (gelu(Wg n) * (Wu n)) for one logical expert (see workload.expert)."""
+    n, np_ = _c(n, _dt(bits))
+    I, H = ex["gate"][0].shape
+    keep: list = []
+    st = _expert_struct(ex, keep)
+    y = np.empty(H, _dt(bits))
+    lib(bits).or_expert_ffn(np_, H, I, ctypes.byref(st), int(bf16_ops), y.ctypes.data)
+    return y
+
+
+def shared_ffn(n, Wg, Wu, Wd, bf16_ops: bool = False, bits: int = 32) -> np.ndarray:
+    n, np_ = _c(n, _dt(bits))
+    S, H = Wg.shape
+    Wg, gp = _c(Wg, np.uint16)
+    Wu, up = _c(Wu, np.uint16)
+    Wd, dp = _c(Wd, np.uint16)
+    y = np.empty(H, _dt(bits))
+    lib(bits).or_shared_ffn(np_, H, S, gp, up, dp, int(bf16_ops), y.ctypes.data)
+    return y
+
+
+def layer_combine(x, r, experts: list, w, shared=None, bf16_ops: bool = False, bits: int = 32):
+    """out = bf16(x + delta), delta = shared + sum_i w_i y_i (experts given in top-k order).
+
+    Returns (out bf16 bits [H], delta [H])."""
+    x, xp = _c(x, np.uint16)
+    H = x.shape[0]
+    k = len(experts)
+    I = experts[0]["gate"][0].shape[0] if k else 0
+    keep: list = []
+    arr = (Expert * max(k, 1))()
+    for i, ex in enumerate(experts):
+        arr[i] = _expert_struct(ex, keep)
+    w, wp = _c(w, _dt(bits))
+    S, gp, up, dp = 0, None, None, None
+    if shared is not None:
+        Wg, Wu, Wd = shared
+        S = Wg.shape[0]
+        Wg, gp = _c(Wg, np.uint16)
+        Wu, up = _c(Wu, np.uint16)
+        Wd, dp = _c(Wd, np.uint16)
+    out = np.empty(H, np.uint16)
+    delta = np.empty(H, _dt(bits))
+    lib(bits).or_layer_combine(xp, H, I, r, k, arr, wp, S, gp, up, dp, int(bf16_ops), out.ctypes.data,
+                               delta.ctypes.data)
+    return out, delta
+
+
+# --------------------------------------------------------------------------------- LFU
+
+class LFU:
+    """Per-layer LFU expert-cache simulator (events are (step, layer, expert, hit, slot, evicted))."""
+
+    def __init__(self, n_layers: int, n_slots: int):
+        self._L = lib()
+        self._h = self._L.or_lfu_new(n_layers, n_slots)
+        self.n_slots = n_slots
+
+    def step(self, step: int, layer: int, ids) -> list:
+        ids, ip = _c(ids, np.int32)
+        ev = (CacheEvent * max(1, ids.shape[0]))()
+        rc = self._L.or_lfu_step(self._h, step, layer, ip, ids.shape[0], ev)
+        if rc < 0:
+            raise ValueError("no evictable slot")
+        return [(e.step, e.layer, e.expert, e.hit, e.slot, e.evicted) for e in ev[:ids.shape[0]]]
+
+    def state(self, layer: int):
+        S = self.n_slots
+        ex = np.empty(S, np.int32)
+        cnt = np.empty(S, np.int64)
+        lu = np.empty(S, np.int64)
+        self._L.or_lfu_state(self._h, layer, ex.ctypes.data, cnt.ctypes.data, lu.ctypes.data)
+        return ex, cnt, lu
+
+    def __del__(self):
+        try:
+            self._L.or_lfu_free(self._h)
+        except Exception:
+            pass

@@ -1,0 +1,430 @@
+"""Pins of the CPU oracle against things other than itself (CPU only).
+
+Each test ties one oracle function to a fixed fact of the pages, a closed form,
+a brute-force enumeration, an independent library routine or a hand-worked
+trace, so that a dropped term, a wrong sign or index or a transposed operand in
+the oracle fails somewhere here.
+
+Pages cited (by title):
+  [HN]  "Show HN: mecanismo de codigo aberto executando Gemma 4 26B em 2 GB de RAM em
+         qualquer Mac com serie M" (hndistilled.com), section "Abordagem tecnica (MoE +
+         streaming por SSD)".
+  [DT]  "Como executar um modelo de 26 bilhoes de parametros em dois gigabytes de memoria
+         em um Mac comum" (devtrends.cc), section "Qual e o principal truque da arquitetura".
+"""
+import itertools
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workload as W
+from golden_io import load_lfu_trace, lfu_trace_names
+
+H, I, E, K_ACT, SLOTS, LAYERS = 2816, 704, 128, 8, 16, 30
+
+
+# ----------------------------------------------------------------------- fixed facts
+
+def expert_payload_bytes(H, I, group=64):
+    """Bytes of one expert at 4 bits: codes (half a byte each) + fp16 scale and bias per group."""
+    per_matrix = I * H // 2 + 2 * (I * H // group) * 2
+    return 3 * per_matrix
+
+
+def test_fact_expert_size_3_36_MB():
+    # [HN]: one expert is 3.36 MB at 4 bits.
+    payload = expert_payload_bytes(H, I)
+    assert payload == 3_345_408
+    stride = -(-payload // 16384) * 16384
+    assert stride == 3_358_720
+    assert f"{stride / 1e6:.2f}" == "3.36"
+    assert f"{payload / 1e6:.2f}" == "3.35"
+
+
+def test_fact_bytes_per_token_band():
+    # [HN]: 60-70% hit rate and 250-320 MB read per token, 30 layers x 8 experts.
+    per_expert = 3_358_720
+    lo = LAYERS * K_ACT * per_expert * (1 - 0.70) / 1e6
+    hi = LAYERS * K_ACT * per_expert * (1 - 0.60) / 1e6
+    assert 240 < lo < 250 and 320 < hi < 325      # overlaps the quoted 250-320 MB
+    # [DT]: ~14.3 GB of 4-bit weights with a 1.35 GB resident core.
+    total = LAYERS * E * expert_payload_bytes(H, I) / 1e9 + 1.35
+    assert abs(total - 14.3) < 0.15
+
+
+def test_fact_eight_active_experts_distinct():
+    # [DT]: the router of each layer picks 8 experts for the token.
+    x = W.hidden(0, 0, 1, H)[0]
+    Wr = W.router_weights(0, 0, E, H)
+    r, z, idx, w = O.route(x, Wr)
+    assert idx.shape == (8,) and len(set(idx.tolist())) == 8
+    assert np.all((idx >= 0) & (idx < E))
+
+
+def test_fact_sixteen_slots_lfu_resident():
+    # [DT]: 16 slots with LFU; after each step all 8 current experts are resident.
+    rng = np.random.default_rng(0)
+    lfu = O.LFU(1, SLOTS)
+    for step in range(200):
+        ids = rng.choice(E, 8, replace=False).astype(np.int32)
+        lfu.step(step, 0, ids)
+        ex, cnt, lu = lfu.state(0)
+        assert set(ids.tolist()) <= set(ex.tolist())
+        assert (ex >= 0).sum() <= SLOTS
+
+
+# ------------------------------------------------------------------------- encodings
+
+def test_half_to_float_all_codes():
+    codes = np.arange(65536, dtype=np.uint16)
+    ref = codes.view(np.float16).astype(np.float32)
+    got = np.array([O.half_to_float(int(c)) for c in codes], np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def _nearest_bf16_bruteforce(f32):
+    """Round an fp32 to bf16 by comparing the two neighbouring bf16 values exactly."""
+    u = int(np.float32(f32).view(np.uint32))
+    lo = u >> 16
+    cand = [lo, lo + 1]
+    vals = [Fraction(float(np.uint32((c & 0xFFFF) << 16).view(np.float32))) for c in cand]
+    x = Fraction(float(f32))
+    d = [abs(v - x) for v in vals]
+    if d[0] < d[1]:
+        return cand[0] & 0xFFFF
+    if d[1] < d[0]:
+        return cand[1] & 0xFFFF
+    return cand[0] & 0xFFFF if cand[0] % 2 == 0 else cand[1] & 0xFFFF
+
+
+def test_float_to_bf16_round_nearest_even():
+    rng = np.random.default_rng(1)
+    bits = rng.integers(0, 2**32, 4000, dtype=np.uint64).astype(np.uint32)
+    bits = bits[((bits >> 23) & 0xFF) < 0xFE]         # finite, away from overflow
+    ties = (rng.integers(0, 2**15, 400).astype(np.uint32) << 16) | 0x8000   # exact halfway cases
+    ties = ties[((ties >> 23) & 0xFF) < 0xFE]
+    for b in np.concatenate([bits, ties.astype(np.uint32)]):
+        f = np.uint32(b).view(np.float32)
+        assert O.float_to_bf16(float(f)) == _nearest_bf16_bruteforce(f), hex(int(b))
+
+
+# -------------------------------------------------------------------------- dequant
+
+def test_dequant_zero_code_is_bias_exactly():
+    s = W.uniform_f16(W.key(9, W.T_S), 500, W.SCALE_LO, W.SCALE_HI)
+    b = W.uniform_f16(W.key(9, W.T_B), 500, W.BIAS_LO, W.BIAS_HI)
+    for si, bi in zip(s, b):
+        assert O.dequant(0, int(si), int(bi)) == np.float16(np.uint16(bi).view(np.float16)).astype(np.float32)
+
+
+def test_dequant_single_rounding_of_exact_value():
+    # s*q + b computed exactly (Fraction), then rounded once to fp32 (numpy, RN-even).
+    s = W.uniform_f16(W.key(10, W.T_S), 300, W.SCALE_LO, W.SCALE_HI)
+    b = W.uniform_f16(W.key(10, W.T_B), 300, W.BIAS_LO, W.BIAS_HI)
+    for si, bi in zip(s, b):
+        sv = Fraction(float(np.uint16(si).view(np.float16)))
+        bv = Fraction(float(np.uint16(bi).view(np.float16)))
+        for q in range(16):
+            exact = sv * q + bv
+            want = np.float32(float(exact))   # float(exact) is exact here (<= 53 bits); one fp32 rounding
+            assert O.dequant(q, int(si), int(bi)) == want
+
+
+def test_dequant_power_of_two_exact_and_requant_roundtrip():
+    for sexp in (-8, -7, -6):
+        s16 = int(np.float16(2.0 ** sexp).view(np.uint16))
+        for b in (-0.0625, 0.0, 0.03125):
+            b16 = int(np.float16(b).view(np.uint16))
+            for q in range(16):
+                assert O.dequant(q, s16, b16) == q * 2.0 ** sexp + b
+    s = W.uniform_f16(W.key(11, W.T_S), 400, W.SCALE_LO, W.SCALE_HI)
+    b = W.uniform_f16(W.key(11, W.T_B), 400, W.BIAS_LO, W.BIAS_HI)
+    for si, bi in zip(s, b):
+        sv = float(np.uint16(si).view(np.float16))
+        bv = float(np.uint16(bi).view(np.float16))
+        for q in range(16):
+            w = O.dequant(q, int(si), int(bi))
+            assert round((w - bv) / sv) == q
+
+
+def test_dequant_matrix_layout_and_bf16_variant():
+    R, K = 5, 192
+    q, s, b = W.expert_matrix(3, 0, 0, 0, R, K)
+    Wm = O.dequant_matrix(q, s, b)
+    Wb = O.dequant_matrix(q, s, b, bf16_ops=True)
+    sf, bf = W.f16_to_f32(s), W.f16_to_f32(b)
+    for j in range(R):
+        for k in range(K):
+            g = k // 64
+            assert Wm[j, k] == np.float32(float(Fraction(float(sf[j, g])) * int(q[j, k]) + Fraction(float(bf[j, g]))))
+            assert O.float_to_bf16(float(Wm[j, k])) == _nearest_bf16_bruteforce(Wm[j, k])
+            assert Wb[j, k] == W.bf16_to_f32(np.array([_nearest_bf16_bruteforce(Wm[j, k])], np.uint16))[0]
+
+
+# --------------------------------------------------------------------------- RMSNorm, router
+
+def test_rms_scale_matches_fp64_closed_form():
+    for seed in range(5):
+        x = W.hidden(seed, 0, 1, H)[0]
+        xf = W.bf16_to_f32(x).astype(np.float64)
+        ref = 1.0 / math.sqrt(float(np.mean(xf * xf)) + 1e-6)
+        r = O.rms_scale(x)
+        assert abs(r - ref) <= 4 * np.spacing(np.float32(ref))
+
+
+def test_router_logits_within_fp32_bound_of_exact():
+    x = W.hidden(2, 0, 1, H)[0]
+    Wr = W.router_weights(2, 0, E, H)
+    bias, _ = W.zipf_bias(2, 0, E, 1.1)
+    r = O.rms_scale(x)
+    z = O.router_logits(x, Wr, bias, r)
+    xf = W.bf16_to_f32(x).astype(np.float64)
+    Wf = W.bf16_to_f32(Wr).astype(np.float64)
+    exact = r * (Wf @ xf) + bias.astype(np.float64)
+    bound = (H * 2.0 ** -24 * (np.abs(Wf) @ np.abs(xf)) * r + np.abs(exact) * 2.0 ** -22)
+    assert np.all(np.abs(z - exact) <= bound)
+
+
+def _rank_key(z, e):
+    return (-(z if not math.isnan(z) else -math.inf), e)
+
+
+def test_topk_bruteforce_small_with_ties():
+    rng = np.random.default_rng(5)
+    for trial in range(60):
+        En = int(rng.integers(8, 13))
+        k = int(rng.integers(1, min(8, En) + 1))
+        z = rng.integers(-3, 4, En).astype(np.float32)       # many deliberate ties
+        if trial % 5 == 0:
+            z[rng.integers(0, En)] = -0.0
+        best = None
+        for subset in itertools.combinations(range(En), k):
+            inside = set(subset)
+            ok = all(_rank_key(float(z[a]), a) < _rank_key(float(z[b]), b)
+                     for a in inside for b in range(En) if b not in inside)
+            if ok:
+                assert best is None
+                best = subset
+        want = sorted(best, key=lambda e: _rank_key(float(z[e]), e))
+        assert O.topk(z, k).tolist() == want
+
+
+def test_topk_full_sort_E128():
+    rng = np.random.default_rng(6)
+    for _ in range(50):
+        z = (rng.standard_normal(E) * 2).astype(np.float32)
+        z[rng.integers(0, E, 10)] = z[rng.integers(0, E)]       # ties
+        order = np.lexsort((np.arange(E), -z.astype(np.float64)))
+        assert O.topk(z, 8).tolist() == order[:8].tolist()
+
+
+def test_routing_weights_sum_to_one_and_descend():
+    for seed in range(20):
+        x = W.hidden(seed, 0, 1, H)[0]
+        Wr = W.router_weights(seed, 0, E, H)
+        r, z, idx, w = O.route(x, Wr)
+        s = np.float32(0)
+        for v in w:
+            s = np.float32(s + v)
+        assert abs(float(s) - 1.0) <= 8 * 2.0 ** -24
+        assert np.all(np.diff(w) <= 0)
+        # softmax over the selected 8 == full softmax restricted and renormalised (fp64)
+        zz = z.astype(np.float64)
+        p = np.exp(zz - zz.max())
+        p = p / p.sum()
+        ref = p[idx] / p[idx].sum()
+        assert np.allclose(w, ref, rtol=1e-6, atol=0)
+
+
+# ----------------------------------------------------------------------------- GELU
+
+def test_gelu_special_values_and_identity():
+    assert O.gelu(0.0) == 0.0
+    for v in (10.0, 20.0, 50.0):
+        assert O.gelu(v) == np.float32(v)
+    assert abs(O.gelu(-20.0)) < 1e-30
+    for v in np.linspace(-8, 8, 161):
+        v = float(np.float32(v))
+        # gelu(v) - gelu(-v) = v for the tanh form (odd part of 0.5 v (1 + tanh(.)))
+        assert abs((O.gelu(v, 64) - O.gelu(-v, 64)) - v) < 1e-12 * max(1.0, abs(v))
+
+
+def test_gelu_close_to_exact_gaussian_cdf_form():
+    # The tanh form approximates v * Phi(v) within ~1e-3 (Hendrycks & Gimpel 2016);
+    # dropping the cubic term or mis-scaling the constant exceeds this bound.
+    for v in np.linspace(-6, 6, 241):
+        exact = v * 0.5 * (1 + math.erf(v / math.sqrt(2)))
+        assert abs(O.gelu(float(v), 64) - exact) < 1.1e-3
+
+
+def test_gelu_fp32_within_bound_of_fp64():
+    # relative 2e-6, plus the cancellation in 1 + tanh(.) for negative v: |v|/2 * ulp(1)
+    for v in np.linspace(-12, 12, 481):
+        v32 = float(np.float32(v))
+        a, b = O.gelu(v32, 32), O.gelu(v32, 64)
+        assert abs(a - b) <= 2e-6 * abs(b) + 4e-8 * abs(v32)
+
+
+# ---------------------------------------------------------------------- expert FFN
+
+def _const_f16(v, shape):
+    return np.full(shape, np.float16(v).view(np.uint16), np.uint16)
+
+
+def test_expert_ffn_permutation_closed_form():
+    """Gate = permutation, up = all-ones rows, down = another permutation (s = 1, b = 0):
+    y_j = gelu(n_{pi(sigma(j))}) * sum(n). Pins nibble/row/column indexing of all three
+    matrices, the GELU gate and the down projection; a transposed operand fails."""
+    Hs, Is = 256, 128
+    rng = np.random.default_rng(7)
+    pi = rng.permutation(Hs)[:Is]          # gate row j picks column pi[j]
+    sigma = rng.integers(0, Is, Hs)        # down row j picks column sigma[j]
+    qg = np.zeros((Is, Hs), np.uint8)
+    qg[np.arange(Is), pi] = 1
+    qu = np.zeros((Is, Hs), np.uint8)
+    qd = np.zeros((Hs, Is), np.uint8)
+    qd[np.arange(Hs), sigma] = 1
+    one, zero = _const_f16(1.0, (Is, Hs // 64)), _const_f16(0.0, (Is, Hs // 64))
+    ex = {"gate": (qg, one, zero),
+          "up": (qu, _const_f16(0.5, (Is, Hs // 64)), one),     # q = 0 -> every weight is b = 1
+          "down": (qd, _const_f16(1.0, (Hs, Is // 64)), _const_f16(0.0, (Hs, Is // 64)))}
+    n = rng.standard_normal(Hs).astype(np.float64)
+    y = O.expert_ffn(n, ex, bits=64)
+    S = n.sum()
+    gel = lambda v: 0.5 * v * (1 + math.tanh(math.sqrt(2 / math.pi) * (v + 0.044715 * v ** 3)))
+    want = np.array([gel(n[pi[sigma[j]]]) * S for j in range(Hs)])
+    assert np.allclose(y, want, rtol=1e-12, atol=1e-12)
+
+
+def test_expert_ffn_group_constant_code():
+    """A constant code c in one group of a row gives (s c + b) * sum_{k in group} n_k."""
+    Hs, Is = 320, 64
+    rng = np.random.default_rng(8)
+    n = rng.standard_normal(Hs)
+    for g in range(Hs // 64):
+        q = np.zeros((Is, Hs), np.uint8)
+        c = int(rng.integers(1, 16))
+        q[:, 64 * g:64 * g + 64] = c
+        s = _const_f16(0.0, (Is, Hs // 64))
+        b = _const_f16(0.0, (Is, Hs // 64))
+        s[:, g] = np.float16(0.125).view(np.uint16)
+        b[:, g] = np.float16(-0.25).view(np.uint16)
+        Wm = O.dequant_matrix(q, s, b, bits=64)
+        assert np.allclose(Wm @ n, (0.125 * c - 0.25) * n[64 * g:64 * g + 64].sum(), rtol=1e-12)
+
+
+def test_shared_ffn_closed_form():
+    Hs, Ss = 192, 96
+    rng = np.random.default_rng(9)
+    pi = rng.permutation(Hs)[:Ss]
+    sigma = rng.integers(0, Ss, Hs)
+    one = np.float32(1.0).view(np.uint32) >> 16
+    two = np.float32(2.0).view(np.uint32) >> 16
+    Wg = np.zeros((Ss, Hs), np.uint16)
+    Wg[np.arange(Ss), pi] = one
+    Wu = np.full((Ss, Hs), two, np.uint16)
+    Wd = np.zeros((Hs, Ss), np.uint16)
+    Wd[np.arange(Hs), sigma] = one
+    n = rng.standard_normal(Hs)
+    y = O.shared_ffn(n, Wg, Wu, Wd, bits=64)
+    gel = lambda v: 0.5 * v * (1 + math.tanh(math.sqrt(2 / math.pi) * (v + 0.044715 * v ** 3)))
+    want = np.array([gel(n[pi[sigma[j]]]) * 2 * n.sum() for j in range(Hs)])
+    assert np.allclose(y, want, rtol=1e-12, atol=1e-12)
+
+
+def test_layer_combine_weighted_sum_closed_form():
+    """delta = shared + sum_i w_i y_i with per-expert closed forms, out = bf16(x + delta)."""
+    Hs, Is, Ss, k = 128, 64, 64, 3
+    rng = np.random.default_rng(10)
+    x = W.hidden(4, 0, 1, Hs)[0]
+    r = O.rms_scale(x, 64)
+    n = O.normalise(x, r, 64)
+    experts, ys = [], []
+    for i in range(k):
+        ex = W.expert(20 + i, 0, 0, Hs, Is)
+        experts.append(ex)
+        ys.append(O.expert_ffn(n, ex, bits=64))
+    Wg, Wu, Wd = W.shared_weights(4, 0, Hs, Ss)
+    ysh = O.shared_ffn(n, Wg, Wu, Wd, bits=64)
+    w = np.array([0.5, 0.3, 0.2])
+    out, delta = O.layer_combine(x, r, experts, w, (Wg, Wu, Wd), bits=64)
+    want = ysh + sum(w[i] * ys[i] for i in range(k))
+    assert np.allclose(delta, want, rtol=1e-13, atol=1e-13)
+    xf = W.bf16_to_f32(x).astype(np.float64)
+    for j in range(Hs):
+        assert out[j] == _nearest_bf16_bruteforce(np.float32(xf[j] + delta[j]))
+
+
+def test_fp32_oracle_bounded_by_fp64_oracle_full_layer():
+    """Whole layer at full shapes (H=2816, I=704, E=128, shared 2112): fp32 vs fp64 oracle."""
+    S = 2112
+    x = W.hidden(0, 0, 1, H)[0]
+    Wr = W.router_weights(0, 0, E, H)
+    r32, z32, idx, w32 = O.route(x, Wr, bits=32)
+    r64, z64, idx64, w64 = O.route(x, Wr, bits=64)
+    assert idx.tolist() == idx64.tolist()
+    assert abs(r32 - r64) <= 2 * np.spacing(np.float32(r64))
+    experts = W.experts_parallel(0, 0, idx, H, I)
+    shared = W.shared_weights(0, 0, H, S)
+    out32, d32 = O.layer_combine(x, r32, experts, w32, shared, bits=32)
+    out64, d64 = O.layer_combine(x, r64, experts, w64, shared, bits=64)
+    rel = np.max(np.abs(d32 - d64)) / np.max(np.abs(d64))
+    assert rel < 1e-5
+    # bf16 outputs agree except for rare rounding-boundary flips of one bf16 ulp
+    diff = np.abs(W.bf16_to_f32(out32) - W.bf16_to_f32(out64))
+    assert np.all(diff <= np.abs(W.bf16_to_f32(out64)) * 2.0 ** -7 + 1e-30)
+
+
+def test_oracle_precisions():
+    assert O.lib(32).or_real_bytes() == 4
+    assert O.lib(64).or_real_bytes() == 8
+
+
+# ------------------------------------------------------------------------------ LFU
+
+@pytest.mark.parametrize("name", lfu_trace_names())
+def test_lfu_golden_traces(name):
+    slots, layers, inputs, events = load_lfu_trace(name)
+    lfu = O.LFU(layers, slots)
+    got = []
+    for step, layer, ids in inputs:
+        got += lfu.step(step, layer, np.array(ids, np.int32))
+    assert got == events
+
+
+def test_lfu_invariants_random_long_run():
+    rng = np.random.default_rng(11)
+    Ls, S, En, k = 3, 16, 128, 8
+    lfu = O.LFU(Ls, S)
+    cold = [0] * Ls
+    for step in range(300):
+        for layer in range(Ls):
+            hot = rng.choice(24, 5, replace=False)
+            ids = np.unique(np.concatenate([hot, rng.choice(En, 8, replace=False)]))[:k]
+            rng.shuffle(ids)
+            before_ex, before_cnt, before_lu = lfu.state(layer)
+            ev = lfu.step(step, layer, ids.astype(np.int32))
+            ex, cnt, lu = lfu.state(layer)
+            hits = sum(e[3] for e in ev)
+            misses = len(ev) - hits
+            assert hits + misses == len(ids)
+            assert set(ids.tolist()) <= set(ex.tolist()) and (ex >= 0).sum() <= S
+            evictions = sum(1 for e in ev if e[5] >= 0)
+            cold_fills = sum(1 for e in ev if e[3] == 0 and e[5] < 0)
+            cold[layer] += cold_fills
+            assert evictions == misses - cold_fills
+            for e in ev:
+                assert e[5] not in ids.tolist()
+                if e[3]:
+                    assert before_ex[e[4]] == e[2]
+                elif e[5] >= 0:
+                    # the victim had the minimum count among the slots it could have taken
+                    cand = [s for s in range(S) if before_ex[s] not in ids.tolist()]
+                    assert before_cnt[e[4]] == min(before_cnt[s] for s in cand) or e[4] in [
+                        x[4] for x in ev if x[3] == 0]
+    assert all(c <= S for c in cold)
