@@ -1,0 +1,301 @@
+#!/usr/bin/env python
+"""Benchmark of the streamed-expert MoE decode path on B300.
+
+Default workload: a 30-layer MoE-only stack (H=2816, E=128 experts of
+I=704, top-8, int4 group-64 experts with fp16 scale/bias, bf16 shared expert
+2816->2112->2816), all experts resident in HBM, batch 1, decode steps with
+the stack output fed back as the next input. One step = one token through all
+30 layers. Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain single-threaded C reference
+of the same layer) on the host cores, on a bounded sample of the same
+workload. Multi-GPU runs are independent replicas (one sequence per GPU).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE decode tok/s (1 B300) and expert-weight HBM GB/s as % of peak"
+H, I, E, K_ACT, S, L = 2816, 704, 128, 8, 2112, 30
+SEED = 1
+WORKLOAD = ("30-layer MoE-only decode stack: H=2816, 128 experts of I=704 (int4 codes, fp16 scale+bias per 64), "
+            "top-8 softmax routing, GELU-gated FFNs, bf16 shared expert 2816->2112->2816, RMSNorm; batch 1, "
+            "output fed back each step; all experts resident in HBM; seed 1")
+
+# algorithmic bytes per launch (weights read + activations), per kernel kind
+ROUTED_GU = K_ACT * 2 * (I * H // 2 + I * (H // 64) * 4)       # 17,842,176
+SHARED_GU = 2 * S * H * 2                                       # 23,789,568
+ROUTED_D = K_ACT * (H * I // 2 + H * (I // 64) * 4)            # 8,921,088
+SHARED_D = H * S * 2                                            # 11,894,784
+ROUTER = E * H * 2                                              # 720,896
+ACT_X = H * 2
+ACT_H = (K_ACT * I + S) * 4
+BYTES = {
+    "router": ROUTER + ACT_X + E * 4 + K_ACT * 8,
+    "gateup": ROUTED_GU + SHARED_GU + ACT_X + ACT_H,
+    "down": ROUTED_D + SHARED_D + ACT_H + 2 * ACT_X,
+}
+BYTES["layer"] = ROUTER + ROUTED_GU + SHARED_GU + ROUTED_D + SHARED_D + 2 * ACT_X
+ROUTED_PER_TOKEN = L * (ROUTED_GU + ROUTED_D)                  # expert-weight bytes per token
+WEIGHTS_PER_TOKEN = L * (ROUTER + ROUTED_GU + SHARED_GU + ROUTED_D + SHARED_D)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle baseline
+
+def oracle_baseline(n_layers: int = 6):
+    """Time the CPU oracle on a bounded sample: the first n_layers of step 0 of the stack
+    (routing + 8 experts + shared expert + combine), single thread. Returns tok/s for 30 layers."""
+    import oracle as O
+    import workload as W
+    O.build()
+    x = W.hidden(SEED, 0, 1, H)[0]
+    elapsed = 0.0
+    for l in range(n_layers):
+        Wr = W.router_weights(SEED, l, E, H)
+        shared = W.shared_weights(SEED, l, H, S)
+        t0 = time.perf_counter()
+        r, z, idx, w = O.route(x, Wr)
+        elapsed += time.perf_counter() - t0
+        experts = W.experts_parallel(SEED, l, idx, H, I)      # generation is not timed
+        t0 = time.perf_counter()
+        x, _ = O.layer_combine(x, r, experts, w, shared)
+        elapsed += time.perf_counter() - t0
+    per_layer = elapsed / n_layers
+    return {"value": 1.0 / (per_layer * L), "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "sample": "%d of the 30 layers of one decode step (step 0, seed %d), single-threaded fp32 C oracle; "
+                      "tok/s = 1 / (30 x mean layer time); weight generation not timed" % (n_layers, SEED),
+            "seconds": elapsed}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args, rank, world):
+    import torch
+    import bit_expert_streaming_layer_b300 as B
+    from workload.model import SyntheticStack, hidden_tensor
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stack = SyntheticStack(SEED, L, H=H, I=I, E=E, k=K_ACT, S=S, resident=True, device=dev)
+    x0 = hidden_tensor(SEED, 0, 1, H, device=dev)[0]
+    a = torch.empty(H, dtype=torch.bfloat16, device=dev)
+    b = torch.empty(H, dtype=torch.bfloat16, device=dev)
+    scratch = torch.empty(H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    a.copy_(x0)
+
+    def step(src, dst):
+        B.tf_stack_decode(stack.layers, src, dst, scratch, None, stream)
+
+    cur, nxt = a, b
+    for _ in range(args.warmup):
+        step(cur, nxt)
+        cur, nxt = nxt, cur
+    torch.cuda.synchronize()
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    prof_steps = min(args.steps, args.profile_steps)
+    B.tf_profile_begin(prof_steps * L)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(cur, nxt)
+        cur, nxt = nxt, cur
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    prof = B.tf_profile_end()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    assert not torch.isnan(cur.float()).any(), "NaN in the stack output"
+
+    # end to end through the public API with host buffers: H2D input, D2H output, every step
+    hx = torch.empty(H, dtype=torch.bfloat16, pin_memory=True)
+    hy = torch.empty(H, dtype=torch.bfloat16, pin_memory=True)
+    hx.copy_(x0.cpu())
+    e2e_steps = args.steps
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        a.copy_(hx, non_blocking=True)
+        step(a, b)
+        hy.copy_(b, non_blocking=True)
+        stream.synchronize()
+        hx.copy_(hy)
+    e2e_s = time.perf_counter() - t0
+
+    gpu_launches = sum(n for _, n in prof.values())
+    stack.close()
+    return ms, prof, clocks, gpu_launches, e2e_s, e2e_steps
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1024)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--profile-steps", type=int, default=64,
+                    help="timed steps whose kernels are bracketed by CUDA events (the first ones)")
+    ap.add_argument("--oracle-layers", type=int, default=6)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        steps_s = []
+        base = None
+        for _ in range(max(1, args.steps if args.steps <= 3 else 1)):
+            base = oracle_baseline(args.oracle_layers)
+            steps_s.append(base["seconds"])
+        line = {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": "tok/s", "n_gpus": args.gpus,
+                "steps": 1, "warmup": 0, "ms_per_step": 1000.0 / base["value"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "layers": L},
+                "cpu_baseline": {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")},
+                "e2e": {"value": base["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+
+    ms, prof, clocks, launches, e2e_s, e2e_steps = run_ours(args, rank, world)
+    if rank != 0:
+        return
+    tok_s = world * args.steps / (ms / 1000.0)
+    ms_step = ms / args.steps
+    peak, peak_kind = peaks()
+    # dominant kernel: largest summed event time among the timed launches
+    timed = {k: v for k, v in prof.items() if v[1] > 0}
+    cap = min(args.steps, args.profile_steps) * L
+    dom = max(timed, key=lambda k: timed[k][0])
+    dom_ms, dom_n = timed[dom]
+    n_timed = min(dom_n, cap)
+    avg_s = dom_ms / n_timed / 1000.0
+    achieved = BYTES[dom] / avg_s / 1e9
+    per_kernel = {k: {"event_ms_total": round(v[0], 4), "launches": int(v[1]),
+                      "timed_launches": int(min(v[1], cap)),
+                      "avg_us": round(v[0] / max(1, min(v[1], cap)) * 1000, 3),
+                      "bytes_per_launch": BYTES.get(k)} for k, v in timed.items()}
+    expert_gbs = ROUTED_PER_TOKEN * args.steps / (ms / 1000.0) / 1e9
+    line = {
+        "metric": METRIC, "value": round(tok_s, 2), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers": L, "batch": 1, "steps_fed_back": args.steps,
+                   "l2": "no flush: each step streams 1.895 GB of weights, 15x the 126 MB L2",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "expert_weight_gbs": round(expert_gbs, 1),
+        "expert_weight_frac_of_peak": round(expert_gbs / peak, 4),
+        "weight_gbs": round(WEIGHTS_PER_TOKEN * args.steps / (ms / 1000.0) / 1e9, 1),
+        "weight_frac_of_peak": round(WEIGHTS_PER_TOKEN * args.steps / (ms / 1000.0) / 1e9 / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind + " (hbm_gbs)",
+                     "bytes_per_launch": BYTES[dom], "traffic": None},
+        "kernels": per_kernel,
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "e2e": {"value": round(world * e2e_steps / e2e_s, 2), "unit": "tok/s", "h2d_bytes_per_step": H * 2,
+                "d2h_bytes_per_step": H * 2},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        base = oracle_baseline(args.oracle_layers)
+        line["cpu_baseline"] = {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,499 @@
+// C-ABI entry points that enqueue device work: routing, the decode FFN, the
+// dequant export, layer handles, the (cached) layer step and the decode stack.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "tf_internal.h"
+
+namespace tf {
+
+tf_status cuda_status(int err, const char* what) {
+    if (err == 0) return TF_OK;
+    return fail(TF_ERR_CUDA, "%s: %s", what, cudaGetErrorString((cudaError_t)err));
+}
+
+static int g_copy_countdown = 0;  // failure injection for the miss-fill engine (0 = off)
+
+// ------------------------------------------------------------- profiling
+struct Prof {
+    bool on = false;
+    int capacity = 0;
+    std::vector<cudaEvent_t> ev[TF_KERNEL_COUNT];  // 2 per timed launch
+    int64_t launches[TF_KERNEL_COUNT] = {};
+};
+static Prof g_prof;
+
+void prof_before(int kind, void* stream) {
+    if (!g_prof.on) return;
+    const int64_t n = g_prof.launches[kind];
+    if (n < g_prof.capacity) cudaEventRecord(g_prof.ev[kind][2 * n], (cudaStream_t)stream);
+}
+
+void prof_after(int kind, void* stream) {
+    if (!g_prof.on) return;
+    const int64_t n = g_prof.launches[kind]++;
+    if (n < g_prof.capacity) cudaEventRecord(g_prof.ev[kind][2 * n + 1], (cudaStream_t)stream);
+}
+
+static void prof_release() {
+    for (auto& v : g_prof.ev) {
+        for (cudaEvent_t e : v) cudaEventDestroy(e);
+        v.clear();
+    }
+    g_prof.on = false;
+    g_prof.capacity = 0;
+}
+
+static bool valid_dims(int H, int I) { return H > 0 && I > 0 && H % TF_GROUP == 0 && I % TF_GROUP == 0; }
+
+static tf_status check_table(const tf_expert_table* t, const char* fn) {
+    if (!t || !t->base) return fail(TF_ERR_INVALID_ARG, "%s: expert table or its base is NULL", fn);
+    if (!aligned16(t->base) || t->stride % 16)
+        return fail(TF_ERR_INVALID_ARG, "%s: expert base and stride must be 16-byte aligned", fn);
+    return TF_OK;
+}
+
+static ExpertRef table_ref(const tf_expert_table* t, const int32_t* idx) {
+    ExpertRef r;
+    std::memset(&r, 0, sizeof(r));
+    r.base = static_cast<const char*>(t->base);
+    r.stride = t->stride;
+    r.slot_map = t->slot_of_expert;
+    r.idx = idx;
+    r.use_ptrs = 0;
+    return r;
+}
+
+struct RouterWs {
+    uint32_t* counters;
+    float* logits;
+};
+
+static size_t router_ws_bytes(int T, int E) {
+    return align_up((size_t)T * 4, 256) + align_up((size_t)T * E * 4, 256);
+}
+
+static RouterWs carve_router(void* ws, int T) {
+    RouterWs r;
+    char* p = static_cast<char*>(ws);
+    r.counters = reinterpret_cast<uint32_t*>(p);
+    r.logits = reinterpret_cast<float*>(p + align_up((size_t)T * 4, 256));
+    return r;
+}
+
+}  // namespace tf
+
+using namespace tf;
+
+// ------------------------------------------------------------------ handles
+
+struct tf_layer {
+    tf_layer_desc d;
+    int T_max = 0;
+    ExpertLayout lay;
+    char* ws = nullptr;
+    size_t ws_bytes = 0;
+    uint32_t* counters = nullptr;
+    float* logits = nullptr;
+    int32_t* idx = nullptr;
+    float* w = nullptr;
+    float* rms = nullptr;
+    float* h_routed = nullptr;
+    float* h_shared = nullptr;
+    int32_t* h_idx = nullptr;        // pinned staging for the cached step
+    cudaEvent_t ev_idx = nullptr, ev_copies = nullptr, ev_t0 = nullptr, ev_shared = nullptr, ev_c0 = nullptr;
+};
+
+namespace {
+
+struct LayerCarve {
+    size_t counters, logits, idx, w, rms, h_routed, h_shared, total;
+};
+
+LayerCarve layer_carve(const tf_layer_desc* d, int T_max) {
+    LayerCarve c;
+    size_t o = 0;
+    c.counters = o; o += align_up((size_t)T_max * 4, 256);
+    c.logits = o;   o += align_up((size_t)T_max * d->E * 4, 256);
+    c.idx = o;      o += align_up((size_t)T_max * d->k * 4, 256);
+    c.w = o;        o += align_up((size_t)T_max * d->k * 4, 256);
+    c.rms = o;      o += align_up((size_t)T_max * 4, 256);
+    c.h_routed = o; o += align_up((size_t)d->k * d->I * 4, 256);
+    c.h_shared = o; o += align_up((size_t)(d->S > 0 ? d->S : 1) * 4, 256);
+    c.total = o;
+    return c;
+}
+
+tf_status check_desc(const tf_layer_desc* d, const char* fn) {
+    if (!d) return fail(TF_ERR_INVALID_ARG, "%s: descriptor is NULL", fn);
+    if (!valid_dims(d->H, d->I)) return fail(TF_ERR_INVALID_ARG, "%s: H=%d I=%d must be multiples of 64", fn, d->H, d->I);
+    if (d->E < 1 || d->E > TF_MAX_E) return fail(TF_ERR_INVALID_ARG, "%s: E=%d out of range", fn, d->E);
+    if (d->k < 1 || d->k > TF_MAX_K || d->k > d->E) return fail(TF_ERR_INVALID_ARG, "%s: k=%d out of range", fn, d->k);
+    if (d->S < 0 || d->S % TF_GROUP) return fail(TF_ERR_INVALID_ARG, "%s: S=%d must be a multiple of 64", fn, d->S);
+    if (!d->W_r || !aligned16(d->W_r)) return fail(TF_ERR_INVALID_ARG, "%s: W_r NULL or misaligned", fn);
+    if (d->S > 0 && (!d->W_sg || !d->W_su || !d->W_sd || !aligned16(d->W_sg) || !aligned16(d->W_su) ||
+                     !aligned16(d->W_sd)))
+        return fail(TF_ERR_INVALID_ARG, "%s: shared-expert weights NULL or misaligned", fn);
+    if (!(d->eps >= 0.0f)) return fail(TF_ERR_INVALID_ARG, "%s: eps must be >= 0", fn);
+    return TF_OK;
+}
+
+DecodeParams decode_params(const tf_layer* l, const void* x, void* out, float* delta, const ExpertRef& ex,
+                           const float* w, const float* rms_in) {
+    DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.x = static_cast<const uint16_t*>(x);
+    p.out = static_cast<uint16_t*>(out);
+    p.delta = delta;
+    p.H = l->d.H;
+    p.I = l->d.I;
+    p.k = l->d.k;
+    p.S = l->d.S;
+    p.eps = l->d.eps;
+    p.rms_in = rms_in;
+    p.ex = ex;
+    p.w = w;
+    p.Wsg = static_cast<const uint16_t*>(l->d.W_sg);
+    p.Wsu = static_cast<const uint16_t*>(l->d.W_su);
+    p.Wsd = static_cast<const uint16_t*>(l->d.W_sd);
+    p.h_routed = l->h_routed;
+    p.h_shared = l->h_shared;
+    p.off_gu_sb = l->lay.gu_sb;
+    p.off_d_codes = l->lay.d_codes;
+    p.off_d_sb = l->lay.d_sb;
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+// ------------------------------------------------------------------ routing
+
+size_t tf_router_workspace_bytes(int T, int E) {
+    if (T <= 0 || E <= 0) return 0;
+    return router_ws_bytes(T, E);
+}
+
+tf_status tf_router_topk(const void* x, int T, int H, const void* W_r, int E, const float* logit_bias, int bias_stride,
+                         int k, int32_t* idx, float* w, float* logits, float* rms, void* workspace, size_t ws_bytes,
+                         void* stream) {
+    const char* fn = "tf_router_topk";
+    if (!x || !W_r || !idx || !w || !workspace) return fail(TF_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (T <= 0 || H <= 0 || H % TF_GROUP) return fail(TF_ERR_INVALID_ARG, "%s: T=%d H=%d invalid", fn, T, H);
+    if (E < 1 || E > TF_MAX_E) return fail(TF_ERR_INVALID_ARG, "%s: E=%d out of range", fn, E);
+    if (k < 1 || k > TF_MAX_K || k > E) return fail(TF_ERR_INVALID_ARG, "%s: k=%d out of range", fn, k);
+    if (logit_bias && bias_stride != 0 && bias_stride != E)
+        return fail(TF_ERR_INVALID_ARG, "%s: bias_stride must be 0 or E", fn);
+    if (ws_bytes < router_ws_bytes(T, E)) return fail(TF_ERR_INVALID_ARG, "%s: workspace too small", fn);
+    RouterWs r = carve_router(workspace, T);
+    clear_error();
+    return cuda_status(launch_router_topk(static_cast<const uint16_t*>(x), T, H, static_cast<const uint16_t*>(W_r), E,
+                                          logit_bias, bias_stride, k, idx, w, logits ? logits : r.logits, rms,
+                                          r.counters, 1e-6f, stream),
+                       fn);
+}
+
+// ------------------------------------------------------------------ dequant
+
+tf_status tf_dequant_expert(const void* blob, int H, int I, int matrix, int as_bf16, void* out, void* stream) {
+    ExpertLayout L;
+    if (!blob || !out) return fail(TF_ERR_INVALID_ARG, "tf_dequant_expert: null pointer");
+    if (!expert_layout(H, I, &L) || matrix < 0 || matrix > 2)
+        return fail(TF_ERR_INVALID_ARG, "tf_dequant_expert: bad H/I/matrix");
+    clear_error();
+    const size_t off_sb = matrix < 2 ? L.gu_sb : L.d_sb;
+    const size_t off_codes = matrix < 2 ? L.gu_codes : L.d_codes;
+    return cuda_status(launch_dequant(static_cast<const char*>(blob), H, I, matrix, as_bf16, out, off_sb, off_codes,
+                                      stream),
+                       "tf_dequant_expert");
+}
+
+// --------------------------------------------------------------- decode FFN
+
+size_t tf_moe_decode_workspace_bytes(int H, int I, int k) {
+    if (!valid_dims(H, I) || k < 1 || k > TF_MAX_K) return 0;
+    return align_up((size_t)k * I * 4, 256);
+}
+
+tf_status tf_moe_ffn_decode(const void* x, void* out, const tf_expert_table* table, const int32_t* idx, const float* w,
+                            int k, int H, int I, float* delta, void* workspace, size_t ws_bytes, void* stream) {
+    const char* fn = "tf_moe_ffn_decode";
+    if (!x || !out || !idx || !w || !workspace) return fail(TF_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!valid_dims(H, I)) return fail(TF_ERR_INVALID_ARG, "%s: H=%d I=%d must be multiples of 64", fn, H, I);
+    if (k < 1 || k > TF_MAX_K) return fail(TF_ERR_INVALID_ARG, "%s: k=%d out of range", fn, k);
+    if (tf_status s = check_table(table, fn)) return s;
+    if (ws_bytes < tf_moe_decode_workspace_bytes(H, I, k)) return fail(TF_ERR_INVALID_ARG, "%s: workspace too small", fn);
+    ExpertLayout L;
+    expert_layout(H, I, &L);
+    DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.x = static_cast<const uint16_t*>(x);
+    p.out = static_cast<uint16_t*>(out);
+    p.delta = delta;
+    p.H = H;
+    p.I = I;
+    p.k = k;
+    p.S = 0;
+    p.eps = 1e-6f;
+    p.rms_in = nullptr;
+    p.ex = table_ref(table, idx);
+    p.w = w;
+    p.h_routed = static_cast<float*>(workspace);
+    p.off_gu_sb = L.gu_sb;
+    p.off_d_codes = L.d_codes;
+    p.off_d_sb = L.d_sb;
+    clear_error();
+    int e = launch_gateup(p, 0, k * I, stream);
+    if (!e) e = launch_down(p, 1, 0, stream);
+    return cuda_status(e, fn);
+}
+
+// ------------------------------------------------------------------ layers
+
+size_t tf_layer_workspace_bytes(const tf_layer_desc* d, int T_max) {
+    if (check_desc(d, "tf_layer_workspace_bytes") != TF_OK || T_max < 1) return 0;
+    return layer_carve(d, T_max).total;
+}
+
+tf_status tf_layer_create(const tf_layer_desc* d, int T_max, void* workspace, size_t ws_bytes, tf_layer** out) {
+    const char* fn = "tf_layer_create";
+    if (!out) return fail(TF_ERR_INVALID_ARG, "%s: out is NULL", fn);
+    *out = nullptr;
+    if (tf_status s = check_desc(d, fn)) return s;
+    if (T_max < 1) return fail(TF_ERR_INVALID_ARG, "%s: T_max=%d", fn, T_max);
+    LayerCarve c = layer_carve(d, T_max);
+    if (!workspace || ws_bytes < c.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return fail(TF_ERR_INVALID_ARG, "%s: workspace NULL, misaligned or smaller than %zu bytes", fn, c.total);
+    tf_layer* l = new (std::nothrow) tf_layer();
+    if (!l) return fail(TF_ERR_OOM, "%s: out of host memory", fn);
+    l->d = *d;
+    l->T_max = T_max;
+    expert_layout(d->H, d->I, &l->lay);
+    l->ws = static_cast<char*>(workspace);
+    l->ws_bytes = ws_bytes;
+    l->counters = reinterpret_cast<uint32_t*>(l->ws + c.counters);
+    l->logits = reinterpret_cast<float*>(l->ws + c.logits);
+    l->idx = reinterpret_cast<int32_t*>(l->ws + c.idx);
+    l->w = reinterpret_cast<float*>(l->ws + c.w);
+    l->rms = reinterpret_cast<float*>(l->ws + c.rms);
+    l->h_routed = reinterpret_cast<float*>(l->ws + c.h_routed);
+    l->h_shared = reinterpret_cast<float*>(l->ws + c.h_shared);
+    cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&l->h_idx), TF_MAX_K * sizeof(int32_t), cudaHostAllocDefault);
+    if (e != cudaSuccess) {
+        delete l;
+        return fail(TF_ERR_OOM, "%s: pinned staging: %s", fn, cudaGetErrorString(e));
+    }
+    cudaEvent_t* evs[] = {&l->ev_idx, &l->ev_copies, &l->ev_t0, &l->ev_shared, &l->ev_c0};
+    for (cudaEvent_t* ev : evs) {
+        e = cudaEventCreate(ev);
+        if (e != cudaSuccess) {
+            tf_layer_destroy(l);
+            return cuda_status(e, fn);
+        }
+    }
+    *out = l;
+    return TF_OK;
+}
+
+tf_status tf_layer_destroy(tf_layer* l) {
+    if (!l) return TF_OK;
+    cudaEvent_t evs[] = {l->ev_idx, l->ev_copies, l->ev_t0, l->ev_shared, l->ev_c0};
+    for (cudaEvent_t ev : evs)
+        if (ev) cudaEventDestroy(ev);
+    if (l->h_idx) cudaFreeHost(l->h_idx);
+    delete l;
+    return TF_OK;
+}
+
+tf_status tf_layer_routing(tf_layer* l, int32_t** idx, float** w, float** logits, float** rms) {
+    if (!l) return fail(TF_ERR_INVALID_ARG, "tf_layer_routing: layer is NULL");
+    if (idx) *idx = l->idx;
+    if (w) *w = l->w;
+    if (logits) *logits = l->logits;
+    if (rms) *rms = l->rms;
+    return TF_OK;
+}
+
+tf_status tf_profile_begin(int capacity) {
+    if (capacity < 1) return fail(TF_ERR_INVALID_ARG, "tf_profile_begin: capacity < 1");
+    prof_release();
+    for (int k = 0; k < TF_KERNEL_COUNT; ++k) {
+        g_prof.launches[k] = 0;
+        g_prof.ev[k].resize(2 * (size_t)capacity, nullptr);
+        for (auto& e : g_prof.ev[k]) {
+            if (cudaError_t err = cudaEventCreate(&e)) {
+                e = nullptr;
+                prof_release();
+                return cuda_status(err, "tf_profile_begin");
+            }
+        }
+    }
+    g_prof.capacity = capacity;
+    g_prof.on = true;
+    return TF_OK;
+}
+
+tf_status tf_profile_end(double* ms, int64_t* launches) {
+    if (!ms || !launches) return fail(TF_ERR_INVALID_ARG, "tf_profile_end: null pointer");
+    if (!g_prof.on) return fail(TF_ERR_INVALID_ARG, "tf_profile_end: profiling is not on");
+    g_prof.on = false;
+    tf_status st = TF_OK;
+    for (int k = 0; k < TF_KERNEL_COUNT; ++k) {
+        const int64_t n = g_prof.launches[k] < g_prof.capacity ? g_prof.launches[k] : g_prof.capacity;
+        double total = 0.0;
+        for (int64_t i = 0; i < n; ++i) {
+            if (cudaError_t err = cudaEventSynchronize(g_prof.ev[k][2 * i + 1])) {
+                st = cuda_status(err, "tf_profile_end");
+                break;
+            }
+            float t = 0.f;
+            cudaEventElapsedTime(&t, g_prof.ev[k][2 * i], g_prof.ev[k][2 * i + 1]);
+            total += t;
+        }
+        ms[k] = total;
+        launches[k] = g_prof.launches[k];
+    }
+    prof_release();
+    return st;
+}
+
+tf_status tf_test_fail_nth_copy(int n) {
+    if (n < 0) return fail(TF_ERR_INVALID_ARG, "tf_test_fail_nth_copy: n < 0");
+    g_copy_countdown = n;
+    return TF_OK;
+}
+
+tf_status tf_layer_step(tf_layer* l, tf_expert_cache* cache, int layer, int64_t step, const void* h_expert_store,
+                        const void* x, void* out, int T, const float* logit_bias, int bias_stride,
+                        void* compute_stream, void* copy_stream, int measure, tf_step_stats* stats) {
+    const char* fn = "tf_layer_step";
+    if (!l || !x || !out) return fail(TF_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (T < 1 || T > l->T_max) return fail(TF_ERR_INVALID_ARG, "%s: T=%d outside [1, %d]", fn, T, l->T_max);
+    if (logit_bias && bias_stride != 0 && bias_stride != l->d.E)
+        return fail(TF_ERR_INVALID_ARG, "%s: bias_stride must be 0 or E", fn);
+    const tf_layer_desc& d = l->d;
+    if (!cache) {
+        if (tf_status s = check_table(&d.experts, fn)) return s;
+    } else {
+        if (T != 1) return fail(TF_ERR_NOT_SUPPORTED, "%s: the cached step runs one token", fn);
+        if (!h_expert_store) return fail(TF_ERR_INVALID_ARG, "%s: a cached step needs the pinned expert store", fn);
+        if (!copy_stream) return fail(TF_ERR_INVALID_ARG, "%s: a cached step needs a copy stream", fn);
+    }
+    if (T != 1) return fail(TF_ERR_NOT_SUPPORTED, "%s: T > 1 goes through tf_moe_ffn_grouped", fn);
+    if (stats) std::memset(stats, 0, sizeof(*stats));
+    clear_error();
+    cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
+    if (measure && stats) {
+        if (int e = cudaEventRecord(l->ev_t0, cs)) return cuda_status(e, fn);
+    }
+    int e = launch_router_topk(static_cast<const uint16_t*>(x), 1, d.H, static_cast<const uint16_t*>(d.W_r), d.E,
+                               logit_bias, bias_stride, d.k, l->idx, l->w, l->logits, l->rms, l->counters, d.eps, cs);
+    if (e) return cuda_status(e, fn);
+
+    if (!cache) {
+        DecodeParams p = decode_params(l, x, out, nullptr, table_ref(&d.experts, l->idx), l->w, l->rms);
+        e = launch_gateup(p, 0, d.k * d.I + d.S, cs);
+        if (!e) e = launch_down(p, 1, d.S > 0, cs);
+        return cuda_status(e, fn);
+    }
+
+    // ---- cached step: ids to the host, shared branch, miss fills, routed experts
+    tf_expert_cache* c = cache;
+    if (layer < 0 || layer >= c->n_layers) return fail(TF_ERR_INVALID_ARG, "%s: bad layer %d", fn, layer);
+    if (!c->d_slot_pool || c->n_experts != d.E || c->slot_bytes < l->lay.payload || c->n_slots < d.k)
+        return fail(TF_ERR_INVALID_ARG, "%s: cache does not match the layer (pool, E, slot size or slot count)", fn);
+    cudaStream_t ps = static_cast<cudaStream_t>(copy_stream);
+    const int k = d.k;
+    if ((e = cudaMemcpyAsync(l->h_idx, l->idx, (size_t)k * 4, cudaMemcpyDeviceToHost, cs))) return cuda_status(e, fn);
+    if ((e = cudaEventRecord(l->ev_idx, cs))) return cuda_status(e, fn);
+    ExpertRef none;
+    std::memset(&none, 0, sizeof(none));
+    DecodeParams p = decode_params(l, x, out, nullptr, none, l->w, l->rms);
+    if (d.S > 0 && (e = launch_gateup(p, k * d.I, k * d.I + d.S, cs))) return cuda_status(e, fn);
+    if (measure && stats && (e = cudaEventRecord(l->ev_shared, cs))) return cuda_status(e, fn);
+    if ((e = cudaEventSynchronize(l->ev_idx))) return cuda_status(e, fn);  // the one host wait: the CPU decides the I/O
+    int32_t ids[TF_MAX_K], slot[TF_MAX_K];
+    uint8_t hit[TF_MAX_K];
+    std::memcpy(ids, l->h_idx, (size_t)k * 4);
+    if (tf_status s = tf_expert_cache_lookup(c, layer, step, ids, k, slot, hit)) return s;
+    int32_t admitted[TF_MAX_K];
+    int na = 0;
+    uint64_t bytes = 0;
+    if (measure && stats && (e = cudaEventRecord(l->ev_c0, ps))) return cuda_status(e, fn);
+    const char* pool = static_cast<const char*>(c->d_slot_pool);
+    const char* store = static_cast<const char*>(h_expert_store);
+    for (int i = 0; i < k; ++i) {
+        if (hit[i]) continue;
+        int32_t s = -1, evicted = -1;
+        tf_status st = tf_expert_cache_admit(c, layer, step, ids[i], ids, k, &s, &evicted);
+        if (st == TF_OK) {
+            slot[i] = s;
+            admitted[na++] = s;
+            char* dst = const_cast<char*>(pool) + ((size_t)layer * c->n_slots + s) * c->slot_bytes;
+            const char* src = store + ((size_t)layer * d.E + ids[i]) * c->slot_bytes;
+            if (g_copy_countdown > 0 && --g_copy_countdown == 0)
+                e = (int)cudaErrorInvalidValue;  // injected failure: the copy is not enqueued
+            else
+                e = (int)cudaMemcpyAsync(dst, src, l->lay.payload, cudaMemcpyHostToDevice, ps);
+            if (e) st = cuda_status(e, "tf_layer_step: expert copy");
+            bytes += l->lay.payload;
+        }
+        if (st != TF_OK) {
+            for (int j = 0; j < na; ++j) tf_expert_cache_invalidate(c, layer, admitted[j]);
+            std::string msg = tf_last_error();
+            return fail(st, "%s: miss fill failed, %d admitted slot(s) rolled back: %s", fn, na, msg.c_str());
+        }
+    }
+    if ((e = cudaEventRecord(l->ev_copies, ps))) return cuda_status(e, fn);
+    if ((e = cudaStreamWaitEvent(cs, l->ev_copies, 0))) return cuda_status(e, fn);
+    ExpertRef r;
+    std::memset(&r, 0, sizeof(r));
+    r.use_ptrs = 1;
+    for (int i = 0; i < k; ++i) r.ptr[i] = pool + ((size_t)layer * c->n_slots + slot[i]) * c->slot_bytes;
+    p.ex = r;
+    e = launch_gateup(p, 0, k * d.I, cs);
+    if (!e) e = launch_down(p, 1, d.S > 0, cs);
+    if (e) return cuda_status(e, fn);
+    if (stats) {
+        stats->misses = na;
+        stats->hits = k - na;
+        stats->bytes_fetched = bytes;
+        if (measure) {
+            if ((e = cudaStreamSynchronize(cs))) return cuda_status(e, fn);
+            float t_shared = 0.f, t_copies = 0.f, t_copy = 0.f;
+            if (d.S > 0) cudaEventElapsedTime(&t_shared, l->ev_t0, l->ev_shared);
+            cudaEventElapsedTime(&t_copies, l->ev_t0, l->ev_copies);
+            cudaEventElapsedTime(&t_copy, l->ev_c0, l->ev_copies);
+            stats->shared_ms = t_shared;
+            stats->copy_ms = t_copy;
+            stats->stall_ms = t_copies > t_shared ? t_copies - t_shared : 0.f;
+        }
+    }
+    return TF_OK;
+}
+
+tf_status tf_stack_decode(tf_layer* const* layers, int L, const void* x, void* out, void* scratch,
+                          const float* const* logit_bias, void* stream) {
+    const char* fn = "tf_stack_decode";
+    if (!layers || L < 1 || !x || !out || !scratch) return fail(TF_ERR_INVALID_ARG, "%s: bad arguments", fn);
+    if (scratch == x || scratch == out) return fail(TF_ERR_INVALID_ARG, "%s: scratch must not alias x or out", fn);
+    for (int i = 0; i < L; ++i)
+        if (!layers[i] || layers[i]->d.H != layers[0]->d.H)
+            return fail(TF_ERR_INVALID_ARG, "%s: layer %d is NULL or has another H", fn, i);
+    const void* cur = x;
+    for (int i = 0; i < L; ++i) {
+        void* dst = ((L - 1 - i) % 2 == 0) ? out : scratch;
+        tf_status s = tf_layer_step(layers[i], nullptr, i, 0, nullptr, cur, dst, 1,
+                                    logit_bias ? logit_bias[i] : nullptr, 0, stream, nullptr, 0, nullptr);
+        if (s) return s;
+        cur = dst;
+    }
+    return TF_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,92 @@
+// Internal declarations shared by the host code and the CUDA translation units
+// of libtf.so. Not part of the ABI (see include/tf.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "tf.h"
+
+namespace tf {
+
+// ------------------------------------------------------------------ errors
+void set_error(const char* fmt, ...);
+void clear_error();
+tf_status fail(tf_status s, const char* fmt, ...);
+// Maps a cudaError_t (passed as int) to TF_ERR_CUDA with a message, TF_OK if 0.
+tf_status cuda_status(int err, const char* what);
+
+// ------------------------------------------------------------------ layout
+struct ExpertLayout {
+    int H = 0, I = 0;
+    size_t gu_codes = 0;   // offset of the gate/up codes (always 0)
+    size_t gu_sb = 0;      // offset of the gate/up {s,b} pairs
+    size_t d_codes = 0;    // offset of the down codes
+    size_t d_sb = 0;       // offset of the down {s,b} pairs
+    size_t payload = 0;    // bytes of one packed expert
+    size_t slot = 0;       // payload rounded up to 16 KiB
+};
+bool expert_layout(int H, int I, ExpertLayout* L);
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------ kernel args
+// Where the k experts of one token live: either explicit device pointers (the
+// cached path, resolved on the host) or a table (base/stride/map + device idx).
+struct ExpertRef {
+    const char* ptr[TF_MAX_K];   // used when use_ptrs != 0
+    const char* base;
+    size_t stride;
+    const int32_t* slot_map;     // nullable
+    const int32_t* idx;          // device [k]
+    int use_ptrs;
+};
+
+struct DecodeParams {
+    const uint16_t* x;           // bf16 [H] (layer input)
+    uint16_t* out;               // bf16 [H]
+    float* delta;                // nullable fp32 [H]
+    int H, I, k, S;
+    float eps;
+    const float* rms_in;         // nullable device [1]: r from the router (else recomputed)
+    ExpertRef ex;
+    const float* w;              // device [k]
+    const uint16_t* Wsg;         // bf16 [S,H] (S > 0)
+    const uint16_t* Wsu;
+    const uint16_t* Wsd;         // bf16 [H,S]
+    float* h_routed;             // fp32 [k, I]
+    float* h_shared;             // fp32 [S]
+    size_t off_gu_sb, off_d_codes, off_d_sb;
+};
+
+// Event bracketing of launches while profiling is on (tf_api.cu).
+void prof_before(int kind, void* stream);
+void prof_after(int kind, void* stream);
+
+// Launchers (defined in tf_decode.cu). They return a CUDA error code (0 = ok).
+int launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* Wr, int E, const float* bias,
+                       int bias_stride, int k, int32_t* idx, float* w, float* logits, float* rms,
+                       uint32_t* counters, float eps, void* stream);
+// Row-pair units [u0, u1): routed units are [0, k*I), shared units [k*I, k*I + S).
+int launch_gateup(const DecodeParams& p, int u0, int u1, void* stream);
+// Down projection + combine: with_routed / with_shared select the terms.
+int launch_down(const DecodeParams& p, int with_routed, int with_shared, void* stream);
+int launch_dequant(const char* blob, int H, int I, int matrix, int as_bf16, void* out,
+                   size_t off_sb, size_t off_codes, void* stream);
+
+}  // namespace tf
+
+// Per-layer LFU metadata (host). Defined here so the layer step can reach the
+// slot pool; the policy itself lives in tf_host.cpp.
+struct tf_expert_cache {
+    int n_layers = 0, n_slots = 0, n_experts = 0;
+    size_t slot_bytes = 0;
+    void* d_slot_pool = nullptr;
+    std::vector<int32_t> expert;     // [L][S], -1 = empty
+    std::vector<int64_t> count;      // uses since admission
+    std::vector<int64_t> last_use;   // step of the last use
+    std::vector<tf_cache_event> trace;
+};

@@ -1,0 +1,351 @@
+/*
+ * tf.h -- C ABI of the streamed-expert MoE layer for NVIDIA B300 (sm_103a).
+ *
+ * The operations follow the per-token, per-layer flow described on the page
+ * "Como executar um modelo de 26 bilhoes de parametros em dois gigabytes de
+ * memoria em um Mac comum" (devtrends.cc), section "Qual e o principal truque
+ * da arquitetura": a router picks 8 experts per layer, a 16-slot LFU cache of
+ * expert weights is consulted, missing experts are fetched from slower memory
+ * while the GPU computes the shared-expert branch, and the expert FFNs run on
+ * the 4-bit weights. The same page, section "Sem dependencias do llama.cpp e
+ * MLX", lists the kernels (quantisation, GEMV, MoE, RMSNorm); section
+ * "Desempenho no mundo real" describes prefill in which one loaded expert
+ * serves a group of rows (the grouped entry point).
+ *
+ * Conventions
+ *  - Every call returns tf_status; nothing throws across the ABI.
+ *    tf_last_error() gives a thread-local message for the last failure.
+ *  - Arguments are checked before any launch. A bad argument returns
+ *    TF_ERR_INVALID_ARG and launches nothing.
+ *  - The caller owns every device and pinned-host buffer passed in and keeps it
+ *    alive until the work enqueued on the given stream(s) has finished. The
+ *    library owns only its opaque handles (tf_expert_cache, tf_layer) and what
+ *    they allocate at creation (a few pinned staging words and CUDA events),
+ *    and frees them in *_destroy.
+ *  - Device work is enqueued on the caller's cudaStream_t (passed as void*;
+ *    NULL = legacy default stream). Calls return after enqueueing, except the
+ *    cached layer step, whose one host wait is documented there.
+ *  - No call allocates device memory: scratch comes from a caller-provided
+ *    workspace of the size the matching *_workspace_bytes() returns. A
+ *    workspace must be zero-filled once before its first use; the kernels
+ *    leave it in that state.
+ *  - bf16 and fp16 values are passed as their 16-bit patterns (uint16_t) or as
+ *    untyped device pointers; fp32 as float.
+ *
+ * Number formats
+ *  - Hidden states x, out: bf16, row-major [T, H].
+ *  - Router weights W_r: bf16 [E, H] row-major.
+ *  - Shared expert: bf16 gate [S, H], up [S, H], down [H, S], row-major.
+ *  - Routed expert: 4-bit affine codes q in 0..15 with one fp16 scale s and one
+ *    fp16 bias b per group of 64 consecutive K values of one output row; the
+ *    weight is W = s*q + b (fp32, a single rounding since s*q is exact).
+ *    Logical shapes: gate [I, H], up [I, H], down [H, I]. H and I are
+ *    multiples of 64.
+ *
+ * Packed expert blob (one contiguous block per expert; offsets from
+ * tf_expert_offsets, all 16-byte aligned):
+ *    [0] gate/up codes : 2*I rows of H/2 bytes; row 2j = gate row j, row 2j+1 =
+ *                        up row j. Byte m of a row holds column 2m in its low
+ *                        nibble and column 2m+1 in its high nibble.
+ *    [1] gate/up (s,b) : 2*I rows x H/64 groups of {fp16 s, fp16 b} (4 bytes),
+ *                        rows interleaved like [0].
+ *    [2] down codes    : H rows of I/2 bytes, same nibble order.
+ *    [3] down (s,b)    : H rows x I/64 groups of {fp16 s, fp16 b}.
+ *  The payload is 3*(I*H/2 + 4*I*H/64) bytes: 3,345,408 B for H = 2816,
+ *  I = 704. tf_expert_slot_bytes rounds it up to 16 KiB (3,358,720 B, the
+ *  "3.36 MB per expert at 4 bits" of the page "Show HN: mecanismo de codigo
+ *  aberto executando Gemma 4 26B em 2 GB de RAM em qualquer Mac com serie M",
+ *  section "Abordagem tecnica (MoE + streaming por SSD)"), the stride of a
+ *  cache slot and of the resident expert array.
+ *
+ * Numerics
+ *  - RMSNorm: r = 1/sqrt(sum(x^2)/H + eps), unit gain, n = r*x (fp32).
+ *  - Router: z_e = r * sum_k W_r[e,k] x_k (+ bias_e). The sum of x^2 and the
+ *    router dot products use a fixed order (32 strided partial sums, then a
+ *    xor butterfly 16, 8, 4, 2, 1) with IEEE-rounded mul/add/div/sqrt, so the
+ *    selected experts are reproducible bit for bit. Top-k: larger logit first,
+ *    equal logits -> lower expert index. Routing weights: softmax over the k
+ *    selected logits (they sum to 1).
+ *  - Expert FFN: g = Wg n, u = Wu n, h = gelu_tanh(g) * u, y = Wd h, fp32.
+ *  - Layer: delta = shared(n) + sum_i w_i y_i (i in top-k order, fp32),
+ *    out = bf16(x + delta), round to nearest even.
+ */
+#ifndef TF_H
+#define TF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t tf_status;
+enum {
+    TF_OK = 0,
+    TF_ERR_INVALID_ARG = 1,   /* a null pointer, a bad size or alignment; nothing was launched */
+    TF_ERR_CUDA = 2,          /* a CUDA runtime call failed; see tf_last_error() */
+    TF_ERR_OOM = 3,           /* a pinned or workspace allocation could not be satisfied */
+    TF_ERR_TIMEOUT = 4,       /* a bounded device-side wait ran out */
+    TF_ERR_NOT_SUPPORTED = 5  /* a valid request this build does not implement */
+};
+
+#define TF_GROUP 64
+#define TF_MAX_K 32
+#define TF_MAX_E 1024
+
+/* Thread-local text of the last error, "" if none. Never NULL. */
+const char* tf_last_error(void);
+/* Static name of a status code. */
+const char* tf_status_string(tf_status s);
+/* Library version string. */
+const char* tf_version(void);
+
+/* ------------------------------------------------------------------ layout */
+
+/* Payload bytes of one packed expert (0 if H or I is not a positive multiple of 64). */
+size_t tf_expert_payload_bytes(int H, int I);
+/* Payload rounded up to 16 KiB: stride of a cache slot / resident expert. */
+size_t tf_expert_slot_bytes(int H, int I);
+/* Byte offsets of the four sections of a packed expert (see the header comment). */
+tf_status tf_expert_offsets(int H, int I, size_t off[4]);
+
+/*
+ * Host-side packer (no GPU). Inputs are the logical matrices, concatenated in
+ * the order gate, up, down:
+ *   q : uint8 codes 0..15, gate [I*H] then up [I*H] then down [H*I] (row-major)
+ *   s : fp16 scales, gate [I*H/64], up [I*H/64], down [H*I/64]
+ *   b : fp16 biases, same shapes as s
+ * blob_out receives tf_expert_payload_bytes(H, I) bytes. A code above 15 is an
+ * INVALID_ARG (nothing is written past the check).
+ */
+tf_status tf_pack_expert(const uint8_t* q, const uint16_t* s, const uint16_t* b, int H, int I,
+                         void* blob_out);
+
+/* --------------------------------------------------------------- routing */
+
+/*
+ * Router GEMV, top-k and routing weights for T tokens (RMSNorm folded in).
+ * Devtrends page, section "Qual e o principal truque da arquitetura": the
+ * router of each layer determines which 8 experts the current token needs.
+ *   x          device bf16 [T, H]
+ *   W_r        device bf16 [E, H]
+ *   logit_bias device fp32, NULL, or [E] (bias_stride = 0) or [T, E] (bias_stride = E)
+ *   idx        device int32 [T, k]  out: experts, best first
+ *   w          device fp32  [T, k]  out: routing weights, sum 1
+ *   logits     device fp32  [T, E]  out, nullable: z
+ *   rms        device fp32  [T]     out, nullable: r
+ *   workspace  device, >= tf_router_workspace_bytes(T, E) bytes, zeroed once
+ * 1 <= k <= min(E, 32), E <= 1024, H a positive multiple of 64.
+ */
+size_t tf_router_workspace_bytes(int T, int E);
+tf_status tf_router_topk(const void* x, int T, int H, const void* W_r, int E, const float* logit_bias,
+                         int bias_stride, int k, int32_t* idx, float* w, float* logits, float* rms,
+                         void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------- expert table */
+
+/*
+ * Where the packed experts live in device memory. Expert e is at
+ *   base + (slot_of_expert ? slot_of_expert[e] : e) * stride
+ * (slot_of_expert is a device int32 [E] map, NULL for a resident array).
+ * base and stride must be 16-byte aligned.
+ */
+typedef struct {
+    const void* base;
+    size_t stride;
+    const int32_t* slot_of_expert;
+} tf_expert_table;
+
+/* Dequantise one matrix (0 gate, 1 up, 2 down) of a packed device expert to a
+ * dense row-major device array: fp32 (as_bf16 = 0) or bf16 (as_bf16 = 1).
+ * Parity export. */
+tf_status tf_dequant_expert(const void* blob, int H, int I, int matrix, int as_bf16, void* out,
+                            void* stream);
+
+/* ------------------------------------------------------------- MoE FFN */
+
+/*
+ * Routed-expert FFN of one token with the weighted combine into the residual:
+ *   out = x + sum_i w[i] * E_idx[i](RMSNorm(x))      (i in top-k order)
+ * HN page "Show HN: ...", section "Abordagem tecnica (MoE + streaming por
+ * SSD)": only a small subset of experts is active per token; devtrends page,
+ * section "Sem dependencias do llama.cpp e MLX": fused 4-bit GEMV and MoE kernels.
+ *   x, out     device bf16 [H]; out may alias x
+ *   idx, w     device int32 [k], fp32 [k] (e.g. from tf_router_topk)
+ *   delta      device fp32 [H], nullable: the fp32 update out - x before rounding
+ *   workspace  >= tf_moe_decode_workspace_bytes(H, I, k), zeroed once
+ */
+size_t tf_moe_decode_workspace_bytes(int H, int I, int k);
+tf_status tf_moe_ffn_decode(const void* x, void* out, const tf_expert_table* table, const int32_t* idx,
+                            const float* w, int k, int H, int I, float* delta, void* workspace,
+                            size_t ws_bytes, void* stream);
+
+/*
+ * Grouped (batched / prefill) routed-expert FFN for T tokens: tokens are
+ * grouped by expert (histogram, exclusive scan, stable permutation by
+ * (expert, token, rank)), each expert's rows run as one dequant-to-bf16
+ * tensor-core GEMM with fp32 accumulation (gate/up with the GELU gate fused,
+ * then down), and each token sums its k results in top-k order:
+ *   out[t] = x[t] + sum_i w[t,i] * E_idx[t,i](RMSNorm(x[t]))
+ * Devtrends page, section "Desempenho no mundo real": during prefill one
+ * loaded expert is applied to a whole group of rows at once.
+ *   x, out     device bf16 [T, H] (out must not alias x)
+ *   idx, w     device int32 [T, k], fp32 [T, k]
+ *   delta      device fp32 [T, H], nullable
+ *   perm_out   device int32 [T*k], nullable: the (expert, token, rank)-sorted pair order
+ *   counts_out device int32 [E], nullable: tokens per expert
+ */
+size_t tf_moe_grouped_workspace_bytes(int T, int H, int I, int E, int k);
+tf_status tf_moe_ffn_grouped(const void* x, void* out, int T, const tf_expert_table* table, int E,
+                             const int32_t* idx, const float* w, int k, int H, int I, float* delta,
+                             int32_t* perm_out, int32_t* counts_out, void* workspace, size_t ws_bytes,
+                             void* stream);
+
+/* ---------------------------------------------------------- expert cache */
+
+/*
+ * Per-layer LFU cache of expert slots in HBM (metadata on the host).
+ * Devtrends page, section "Qual e o principal truque da arquitetura": the
+ * runtime checks a local expert cache of 16 slots managed by LFU and loads a
+ * missing expert from storage. Policy, per (step, layer):
+ *  - lookup: each resident id is a hit (count += 1, last_use = step);
+ *  - admit (each miss, in top-k order): the lowest empty slot, else the slot
+ *    not holding any of the pinned ids with the smallest count, then the
+ *    oldest last_use, then the lowest index; it restarts at count 1,
+ *    last_use = step. Counts never decay.
+ * d_slot_pool (caller-owned, may be NULL for metadata-only use) holds
+ * n_layers * n_slots slots of slot_bytes each: slot s of layer l is at
+ * d_slot_pool + (l * n_slots + s) * slot_bytes.
+ * Every lookup/admit appends (step, layer, expert, hit, slot, evicted) events
+ * to an internal trace, read back with tf_expert_cache_trace.
+ */
+typedef struct tf_expert_cache tf_expert_cache;
+
+typedef struct {
+    int32_t step, layer, expert, hit, slot, evicted;
+} tf_cache_event;
+
+tf_status tf_expert_cache_create(int n_layers, int n_slots, int n_experts, size_t slot_bytes,
+                                 void* d_slot_pool, tf_expert_cache** out);
+/* ids[n] in top-k order -> slot_or_minus1[n], hit[n]; hits are counted. */
+tf_status tf_expert_cache_lookup(tf_expert_cache* c, int layer, int64_t step, const int32_t* ids, int n,
+                                 int32_t* slot_or_minus1, uint8_t* hit);
+/* Pick and claim a slot for a missing expert (metadata only; the copy is the caller's). */
+tf_status tf_expert_cache_admit(tf_expert_cache* c, int layer, int64_t step, int32_t expert,
+                                const int32_t* pinned_ids, int n_pinned, int32_t* slot,
+                                int32_t* evicted_or_minus1);
+/* Mark a slot empty again (used to roll back an admit whose copy failed). */
+tf_status tf_expert_cache_invalidate(tf_expert_cache* c, int layer, int32_t slot);
+/* Copy up to cap trace events into buf (oldest first); *n = number of events recorded in total. */
+tf_status tf_expert_cache_trace(tf_expert_cache* c, tf_cache_event* buf, size_t cap, size_t* n);
+/* Slot contents of one layer: expert id (-1 empty), count and last_use per slot. */
+tf_status tf_expert_cache_state(tf_expert_cache* c, int layer, int32_t* expert, int64_t* count,
+                                int64_t* last_use);
+tf_status tf_expert_cache_destroy(tf_expert_cache* c);
+
+/* ------------------------------------------------------------ layer step */
+
+/*
+ * One MoE layer (no attention): router + top-k, optional shared expert,
+ * routed experts and the combine. With a cache, missing experts are copied
+ * from pinned host memory by the copy engine on copy_stream while the shared
+ * expert runs on compute_stream (the pages' overlap of expert reads with the
+ * shared-expert branch, devtrends page, section "Qual e o principal truque da
+ * arquitetura").
+ */
+typedef struct {
+    int H, I, E, k, S;          /* S = shared-expert width, 0 = no shared expert */
+    float eps;                  /* RMSNorm epsilon (1e-6 in the model configuration) */
+    const void* W_r;            /* device bf16 [E, H] */
+    const void* W_sg;           /* device bf16 [S, H] or NULL when S = 0 */
+    const void* W_su;           /* device bf16 [S, H] */
+    const void* W_sd;           /* device bf16 [H, S] */
+    tf_expert_table experts;    /* resident experts (used when no cache is given) */
+} tf_layer_desc;
+
+typedef struct tf_layer tf_layer;
+
+/* Workspace of a layer handle for up to T_max tokens per step. */
+size_t tf_layer_workspace_bytes(const tf_layer_desc* d, int T_max);
+/* The handle copies the descriptor and binds the caller's zeroed workspace. */
+tf_status tf_layer_create(const tf_layer_desc* d, int T_max, void* workspace, size_t ws_bytes,
+                          tf_layer** out);
+tf_status tf_layer_destroy(tf_layer* l);
+/* Device pointers to the routing of the last step: idx [T,k], w [T,k], logits [T,E], rms [T]. */
+tf_status tf_layer_routing(tf_layer* l, int32_t** idx, float** w, float** logits, float** rms);
+
+typedef struct {
+    int32_t hits, misses;          /* cache lookups of this step (0 without a cache) */
+    uint64_t bytes_fetched;        /* host -> device expert bytes enqueued */
+    float copy_ms;                 /* copy-stream time of the miss fills (measure = 1 only) */
+    float shared_ms;               /* compute-stream time of the shared-expert branch (measure = 1) */
+    float stall_ms;                /* max(0, copies end - shared branch end) (measure = 1) */
+} tf_step_stats;
+
+/*
+ * out = layer(x). T tokens (T = 1 with a cache). logit_bias as in tf_router_topk.
+ * Without a cache all work is enqueued on compute_stream and the call returns.
+ * With a cache (T = 1), the call enqueues the router and the shared branch,
+ * waits on the host for the k selected ids (one small device->host copy: the
+ * CPU decides the I/O), updates the LFU metadata for layer `layer` at `step`,
+ * enqueues one cudaMemcpyAsync per miss from h_expert_store (pinned, expert
+ * (layer, e) at h_expert_store + (layer*E + e) * slot_bytes) on copy_stream,
+ * makes compute_stream wait for them, enqueues the routed experts and returns.
+ * If a copy cannot be enqueued the admitted slots of this step are rolled back
+ * to empty and TF_ERR_CUDA is returned. stats (nullable) is filled; with
+ * measure = 1 the call also synchronises to time the copy and shared branches.
+ */
+tf_status tf_layer_step(tf_layer* l, tf_expert_cache* cache, int layer, int64_t step,
+                        const void* h_expert_store, const void* x, void* out, int T,
+                        const float* logit_bias, int bias_stride, void* compute_stream,
+                        void* copy_stream, int measure, tf_step_stats* stats);
+
+/*
+ * A decode step through L resident layers for one token: x_{l+1} = layer_l(x_l),
+ * x_0 = x, out = x_L. Intermediate activations go to `scratch` (device bf16
+ * [H], may alias nothing else). logit_bias[l] may be NULL.
+ */
+tf_status tf_stack_decode(tf_layer* const* layers, int L, const void* x, void* out, void* scratch,
+                          const float* const* logit_bias, void* stream);
+
+/* ----------------------------------------------------------- measurement */
+
+/*
+ * Per-kernel timing for measurement. Between tf_profile_begin and
+ * tf_profile_end every launch of the library's kernels is bracketed by two
+ * CUDA events recorded on the stream it is launched on (events are created in
+ * tf_profile_begin, outside any timed region). tf_profile_end waits for the
+ * events and returns, per kernel kind, the summed event time in ms and the
+ * number of launches (arrays of TF_KERNEL_COUNT). Launches beyond `capacity`
+ * per kind are counted but not timed.
+ */
+enum {
+    TF_KERNEL_ROUTER = 0,      /* RMS scale + router GEMV + top-k */
+    TF_KERNEL_GATEUP = 1,      /* fused int4 / bf16 gate-up GEMV with the GELU gate */
+    TF_KERNEL_DOWN = 2,        /* down GEMV + weighted combine */
+    TF_KERNEL_LAYER = 3,       /* fused persistent decode-layer kernel */
+    TF_KERNEL_PERMUTE = 4,     /* token x expert histogram / scan / permute */
+    TF_KERNEL_GEMM = 5,        /* grouped dequant-to-bf16 tensor-core GEMM */
+    TF_KERNEL_COMBINE = 6,     /* unpermute-combine */
+    TF_KERNEL_OTHER = 7,
+    TF_KERNEL_COUNT = 8
+};
+tf_status tf_profile_begin(int capacity);
+tf_status tf_profile_end(double* ms, int64_t* launches);
+
+/* ---------------------------------------------------------- test hooks */
+
+/*
+ * Failure injection for the miss-fill engine, host side only (no GPU fault):
+ * the n-th expert copy enqueued from now on (1-based) is reported as failed
+ * instead of being enqueued, as if cudaMemcpyAsync had returned an error.
+ * n = 0 disarms. Used to test the roll-back of admitted cache slots.
+ */
+tf_status tf_test_fail_nth_copy(int n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TF_H */
