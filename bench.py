@@ -49,7 +49,7 @@ BYTES = {
     "gateup": ROUTED_GU + SHARED_GU + ACT_X + ACT_H,
     "down": ROUTED_D + SHARED_D + ACT_H + 2 * ACT_X,
 }
-BYTES["layer"] = ROUTER + ROUTED_GU + SHARED_GU + ROUTED_D + SHARED_D + 2 * ACT_X
+BYTES["layer"] = L * (ROUTER + ROUTED_GU + SHARED_GU + ROUTED_D + SHARED_D + 2 * ACT_X)   # one launch = 30 layers
 ROUTED_PER_TOKEN = L * (ROUTED_GU + ROUTED_D)                  # expert-weight bytes per token
 WEIGHTS_PER_TOKEN = L * (ROUTER + ROUTED_GU + SHARED_GU + ROUTED_D + SHARED_D)
 
@@ -152,6 +152,10 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     stack = SyntheticStack(SEED, L, H=H, I=I, E=E, k=K_ACT, S=S, resident=True, device=dev)
+    fused = None
+    if args.path == "fused":
+        fws = torch.zeros(B.tf_stack_workspace_bytes(L, E), dtype=torch.uint8, device=dev)
+        fused = B.Stack(stack.layers, fws)
     x0 = hidden_tensor(SEED, 0, 1, H, device=dev)[0]
     a = torch.empty(H, dtype=torch.bfloat16, device=dev)
     b = torch.empty(H, dtype=torch.bfloat16, device=dev)
@@ -160,7 +164,10 @@ def run_ours(args, rank, world):
     a.copy_(x0)
 
     def step(src, dst):
-        B.tf_stack_decode(stack.layers, src, dst, scratch, None, stream)
+        if fused is not None:
+            B.tf_stack_step(fused, src, dst, stream)
+        else:
+            B.tf_stack_decode(stack.layers, src, dst, scratch, None, stream)
 
     cur, nxt = a, b
     for _ in range(args.warmup):
@@ -175,7 +182,7 @@ def run_ours(args, rank, world):
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.start()
     prof_steps = min(args.steps, args.profile_steps)
-    B.tf_profile_begin(prof_steps * L)
+    B.tf_profile_begin(prof_steps * (1 if args.path == "fused" else L))
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     ev0.record(stream)
@@ -186,6 +193,8 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     prof = B.tf_profile_end()
     clocks = sampler.stop()
+    if fused is not None:
+        B.tf_stack_check(fused, stream)
     ms = ev0.elapsed_time(ev1)
     if world > 1:
         t = torch.tensor([ms], device=dev)
@@ -209,6 +218,9 @@ def run_ours(args, rank, world):
     e2e_s = time.perf_counter() - t0
 
     gpu_launches = sum(n for _, n in prof.values())
+    if fused is not None:
+        B.tf_stack_check(fused, stream)
+        fused.close()
     stack.close()
     return ms, prof, clocks, gpu_launches, e2e_s, e2e_steps
 
@@ -219,6 +231,8 @@ def main():
     ap.add_argument("--steps", type=int, default=1024)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--path", choices=["fused", "layers"], default="fused",
+                    help="fused: one persistent kernel per step; layers: three kernels per layer")
     ap.add_argument("--profile-steps", type=int, default=64,
                     help="timed steps whose kernels are bracketed by CUDA events (the first ones)")
     ap.add_argument("--oracle-layers", type=int, default=6)
@@ -260,7 +274,7 @@ def main():
     peak, peak_kind = peaks()
     # dominant kernel: largest summed event time among the timed launches
     timed = {k: v for k, v in prof.items() if v[1] > 0}
-    cap = min(args.steps, args.profile_steps) * L
+    cap = min(args.steps, args.profile_steps) * (1 if args.path == "fused" else L)
     dom = max(timed, key=lambda k: timed[k][0])
     dom_ms, dom_n = timed[dom]
     n_timed = min(dom_n, cap)
@@ -275,7 +289,7 @@ def main():
         "metric": METRIC, "value": round(tok_s, 2), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "layers": L, "batch": 1, "steps_fed_back": args.steps,
+        "config": {"workload": WORKLOAD, "layers": L, "batch": 1, "steps_fed_back": args.steps, "path": args.path,
                    "l2": "no flush: each step streams 1.895 GB of weights, 15x the 126 MB L2",
                    "parallelism": "replicas" if world > 1 else "single"},
         "expert_weight_gbs": round(expert_gbs, 1),

@@ -85,6 +85,13 @@ SIGNATURES = {
     "tf_layer_step": (_S, [_vp, _vp, _i32, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _vp, _i32,
                            ctypes.POINTER(StepStats)]),
     "tf_stack_decode": (_S, [ctypes.POINTER(_vp), _i32, _vp, _vp, _vp, ctypes.POINTER(_vp), _vp]),
+    "tf_stack_workspace_bytes": (_sz, [_i32, _i32]),
+    "tf_stack_create": (_S, [ctypes.POINTER(_vp), _i32, ctypes.POINTER(_vp), _vp, _sz, ctypes.POINTER(_vp)]),
+    "tf_stack_step": (_S, [_vp, _vp, _vp, _vp]),
+    "tf_stack_check": (_S, [_vp, _vp]),
+    "tf_stack_layer_buffers": (_S, [_vp, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                    ctypes.POINTER(_vp)]),
+    "tf_stack_destroy": (_S, [_vp]),
     "tf_profile_begin": (_S, [_i32]),
     "tf_profile_end": (_S, [_vp, _vp]),
     "tf_test_fail_nth_copy": (_S, [_i32]),
@@ -349,6 +356,52 @@ def tf_stack_decode(layers, x, out, scratch, logit_bias=None, stream=None) -> No
         bias = (ctypes.c_void_p * L)(*[_ptr(b) for b in logit_bias])
     _check(lib().tf_stack_decode(arr, L, _ptr(x), _ptr(out), _ptr(scratch), bias, _stream(stream)),
            "tf_stack_decode")
+
+
+class Stack:
+    """Owner of a tf_stack handle (fused persistent decode kernel over resident layers).
+    `workspace` must be a device tensor of tf_stack_workspace_bytes(L, E) bytes kept alive by the caller."""
+
+    def __init__(self, layers, workspace, logit_bias=None):
+        L = len(layers)
+        arr = (ctypes.c_void_p * L)(*[l.handle for l in layers])
+        bias = None
+        if logit_bias is not None:
+            bias = (ctypes.c_void_p * L)(*[_ptr(b) for b in logit_bias])
+        h = ctypes.c_void_p()
+        self.layers, self.workspace, self.L = layers, workspace, L
+        _check(lib().tf_stack_create(arr, L, bias, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     ctypes.byref(h)), "tf_stack_create")
+        self.handle = h.value
+
+    def layer_buffers(self, layer: int):
+        p = [ctypes.c_void_p() for _ in range(4)]
+        _check(lib().tf_stack_layer_buffers(self.handle, layer, *[ctypes.byref(v) for v in p]),
+               "tf_stack_layer_buffers")
+        return [v.value for v in p]
+
+    def close(self):
+        if self.handle:
+            lib().tf_stack_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def tf_stack_workspace_bytes(L: int, E: int) -> int:
+    return lib().tf_stack_workspace_bytes(L, E)
+
+
+def tf_stack_step(stack: Stack, x, out, stream=None) -> None:
+    _check(lib().tf_stack_step(stack.handle, _ptr(x), _ptr(out), _stream(stream)), "tf_stack_step")
+
+
+def tf_stack_check(stack: Stack, stream=None) -> None:
+    _check(lib().tf_stack_check(stack.handle, _stream(stream)), "tf_stack_check")
 
 
 def tf_profile_begin(capacity: int) -> None:

@@ -170,6 +170,10 @@ DecodeParams decode_params(const tf_layer* l, const void* x, void* out, float* d
 
 }  // namespace
 
+namespace tf {
+void layer_desc_of(const tf_layer* l, tf_layer_desc* out) { *out = l->d; }
+}  // namespace tf
+
 extern "C" {
 
 // ------------------------------------------------------------------ routing

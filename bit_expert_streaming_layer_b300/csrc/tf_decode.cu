@@ -15,124 +15,14 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "tf_device.cuh"
 #include "tf_internal.h"
 
 namespace tf {
 
 namespace {
 
-constexpr unsigned FULL = 0xffffffffu;
-
-__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-__device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
-__device__ __forceinline__ float h2f(uint32_t h16) { return __half2float(__ushort_as_half((unsigned short)h16)); }
-
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-// Code p (0..7) of a 32-bit word of packed nibbles, as the fp32 value 128 + q.
-// The nibble is moved to bits 16..19 under the exponent of 128.0f, where one
-// mantissa step is exactly 1 (Kim et al. 2022 / Frantar et al. 2024 use the
-// same magic-exponent conversion for fp16).
-template <int P>
-__device__ __forceinline__ float q128(uint32_t w) {
-    uint32_t v;
-    if constexpr (P == 4) v = w;
-    else if constexpr (P < 4) v = w << (16 - 4 * P);
-    else v = w >> (4 * P - 16);
-    return __uint_as_float((v & 0x000f0000u) | 0x43000000u);
-}
-
-// sum_p (128 + q_p) * n[p] over the 8 codes of one word.
-__device__ __forceinline__ float dot8_q128(uint32_t w, float4 a, float4 b, float acc) {
-    acc = fmaf(q128<0>(w), a.x, acc);
-    acc = fmaf(q128<1>(w), a.y, acc);
-    acc = fmaf(q128<2>(w), a.z, acc);
-    acc = fmaf(q128<3>(w), a.w, acc);
-    acc = fmaf(q128<4>(w), b.x, acc);
-    acc = fmaf(q128<5>(w), b.y, acc);
-    acc = fmaf(q128<6>(w), b.z, acc);
-    acc = fmaf(q128<7>(w), b.w, acc);
-    return acc;
-}
-
-// sum over 8 bf16 weights (one 16-byte chunk) times n.
-__device__ __forceinline__ float dot8_bf16(uint4 w, float4 a, float4 b, float acc) {
-    acc = fmaf(bf_lo(w.x), a.x, acc);
-    acc = fmaf(bf_hi(w.x), a.y, acc);
-    acc = fmaf(bf_lo(w.y), a.z, acc);
-    acc = fmaf(bf_hi(w.y), a.w, acc);
-    acc = fmaf(bf_lo(w.z), b.x, acc);
-    acc = fmaf(bf_hi(w.z), b.y, acc);
-    acc = fmaf(bf_lo(w.w), b.z, acc);
-    acc = fmaf(bf_hi(w.w), b.w, acc);
-    return acc;
-}
-
-// Contribution of a 32-code chunk: sum_k (s q_k + b) n_k = s (P - 128 S) + b S,
-// with P = sum (128 + q_k) n_k and S = sum n_k; sb holds {fp16 s, fp16 b}.
-__device__ __forceinline__ float chunk_affine(uint32_t sb, float P, float S) {
-    const float s = h2f(sb & 0xffffu), b = h2f(sb >> 16);
-    return fmaf(s, fmaf(-128.0f, S, P), b * S);
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
-    return v;
-}
-
-// Fixed-order warp sum: lane l holds the partial over k = l (mod 32); the xor
-// butterfly 16, 8, 4, 2, 1 gives every lane the same IEEE-rounded result.
-__device__ __forceinline__ float warp_sum_canonical(float v) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(FULL, v, o));
-    return v;
-}
-
-__device__ __forceinline__ float gelu_tanh(float v) {
-    const float c = 0.7978845608028654f, a = 0.044715f;
-    const float inner = c * (v + a * v * v * v);
-    return 0.5f * v * (1.0f + tanhf(inner));
-}
-
-// r = 1/sqrt(sum x^2 / H + eps) in the canonical order; call with a full warp.
-__device__ __forceinline__ float rms_scale_warp(const uint16_t* x, int H, float eps, int lane) {
-    float p = 0.0f;
-    for (int k = lane; k < H; k += 32) {
-        const float v = bf2f(x[k]);
-        p = fmaf(v, v, p);  // v*v is exact in fp32: one rounding, as in the canonical sum
-    }
-    p = warp_sum_canonical(p);
-    const float ms = __fdiv_rn(p, (float)H);
-    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
-}
-
-// Ranking used by top-k: larger logit first, equal -> lower index, NaN last;
-// ib < 0 marks "no candidate yet".
-__device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib) {
-    if (ia < 0) return false;
-    if (ib < 0) return true;
-    const bool na = isnan(a), nb = isnan(b);
-    if (na || nb) return (na == nb) ? (ia < ib) : nb;
-    if (a > b) return true;
-    if (a < b) return false;
-    return ia < ib;
-}
-
-__device__ __forceinline__ const char* expert_ptr(const ExpertRef& r, int i) {
-    if (r.use_ptrs) return r.ptr[i];
-    int e = r.idx[i];
-    if (r.slot_map) e = r.slot_map[e];
-    return r.base + (size_t)e * r.stride;
-}
+using namespace dev;
 
 // ------------------------------------------------------------------- router
 
@@ -143,16 +33,40 @@ k_router_topk(const uint16_t* __restrict__ x, int H, const uint16_t* __restrict_
               const float* __restrict__ bias, int bias_stride, int k, int32_t* __restrict__ idx,
               float* __restrict__ wout, float* __restrict__ logits, float* __restrict__ rms,
               uint32_t* __restrict__ counters, float eps) {
+    // shared: x [H] then one W_r row [H] per warp (bf16), staged with 16-byte loads
+    extern __shared__ float4 rsm4[];
+    uint16_t* sx = reinterpret_cast<uint16_t*>(rsm4);
     const int t = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint16_t* xt = x + (size_t)t * H;
-    const float r = rms_scale_warp(xt, H, eps, lane);
+    uint16_t* sw = sx + (size_t)(warp + 1) * H;
+    const int nvec = H / 8;
     const int e = blockIdx.x * RT_WARPS + warp;
+    {
+        const uint4* gx = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+        uint4* dx = reinterpret_cast<uint4*>(sx);
+#pragma unroll 4
+        for (int v = threadIdx.x; v < nvec; v += blockDim.x) dx[v] = __ldg(gx + v);
+        if (e < E) {
+            const char* gw = reinterpret_cast<const char*>(Wr + (size_t)e * H);
+            uint4* dw = reinterpret_cast<uint4*>(sw);
+#pragma unroll 4
+            for (int v = lane; v < nvec; v += 32) dw[v] = ldg_stream(gw + 16 * (size_t)v);
+        }
+    }
+    __syncthreads();
+    // r in the canonical order (every warp computes the same value)
+    float p = 0.0f;
+#pragma unroll 8
+    for (int kk = lane; kk < H; kk += 32) {
+        const float v = bf2f(sx[kk]);
+        p = fmaf(v, v, p);  // exact square, one rounding per term
+    }
+    p = warp_sum_canonical(p);
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(p, (float)H), eps)));
     if (e < E) {
-        const uint16_t* wr = Wr + (size_t)e * H;
         float d = 0.0f;
 #pragma unroll 8
-        for (int kk = lane; kk < H; kk += 32) d = fmaf(bf2f(wr[kk]), bf2f(xt[kk]), d);  // exact products
+        for (int kk = lane; kk < H; kk += 32) d = fmaf(bf2f(sw[kk]), bf2f(sx[kk]), d);  // exact products
         d = warp_sum_canonical(d);
         float z = __fmul_rn(r, d);
         if (bias) z = __fadd_rn(z, bias[(size_t)t * bias_stride + e]);
@@ -177,48 +91,14 @@ k_router_topk(const uint16_t* __restrict__ x, int H, const uint16_t* __restrict_
     // Last CTA of token t: top-k over all E logits, then softmax over the k.
     __shared__ float s_z[TF_MAX_E];
     __shared__ unsigned char s_taken[TF_MAX_E];
-    __shared__ float s_selz[TF_MAX_K];
-    __shared__ int s_sel[TF_MAX_K];
     for (int j = threadIdx.x; j < E; j += blockDim.x) {
         s_z[j] = __ldcg(logits + (size_t)t * E + j);
         s_taken[j] = 0;
     }
     __syncthreads();
     if (warp == 0) {
-        for (int i = 0; i < k; ++i) {
-            float best = 0.0f;
-            int bi = -1;
-            for (int j = lane; j < E; j += 32)
-                if (!s_taken[j] && ranks_before(s_z[j], j, best, bi)) { best = s_z[j]; bi = j; }
-#pragma unroll
-            for (int o = 16; o; o >>= 1) {
-                const float ob = __shfl_xor_sync(FULL, best, o);
-                const int oi = __shfl_xor_sync(FULL, bi, o);
-                if (ranks_before(ob, oi, best, bi)) { best = ob; bi = oi; }
-            }
-            if (lane == 0) {
-                s_sel[i] = bi;
-                s_selz[i] = best;
-                s_taken[bi] = 1;
-            }
-            __syncwarp();
-        }
-        if (lane == 0) {
-            float zmax = s_selz[0];
-            for (int i = 1; i < k; ++i)
-                if (s_selz[i] > zmax) zmax = s_selz[i];
-            float ev[TF_MAX_K];
-            float sum = 0.0f;
-            for (int i = 0; i < k; ++i) {
-                ev[i] = expf(__fsub_rn(s_selz[i], zmax));
-                sum = __fadd_rn(sum, ev[i]);
-            }
-            for (int i = 0; i < k; ++i) {
-                idx[(size_t)t * k + i] = s_sel[i];
-                wout[(size_t)t * k + i] = __fdiv_rn(ev[i], sum);
-            }
-            counters[t] = 0;  // leave the workspace zeroed for the next call
-        }
+        warp_topk_softmax(s_z, s_taken, E, k, lane, idx + (size_t)t * k, wout + (size_t)t * k);
+        if (lane == 0) counters[t] = 0;  // leave the workspace zeroed for the next call
     }
 }
 
@@ -236,7 +116,16 @@ __device__ __forceinline__ void load_normalised(const DecodeParams& p, float* n,
     }
     __syncthreads();
     const float r = s_r;
-    for (int kk = threadIdx.x; kk < p.H; kk += blockDim.x) n[kk] = __fmul_rn(r, bf2f(p.x[kk]));
+    const uint4* gx = reinterpret_cast<const uint4*>(p.x);
+#pragma unroll 2
+    for (int v = threadIdx.x; v < p.H / 8; v += blockDim.x) {
+        const uint4 xv = __ldg(gx + v);
+        float4* d = reinterpret_cast<float4*>(n + 8 * v);
+        d[0] = make_float4(__fmul_rn(r, bf_lo(xv.x)), __fmul_rn(r, bf_hi(xv.x)), __fmul_rn(r, bf_lo(xv.y)),
+                           __fmul_rn(r, bf_hi(xv.y)));
+        d[1] = make_float4(__fmul_rn(r, bf_lo(xv.z)), __fmul_rn(r, bf_hi(xv.z)), __fmul_rn(r, bf_lo(xv.w)),
+                           __fmul_rn(r, bf_hi(xv.w)));
+    }
     __syncthreads();
     for (int c = threadIdx.x; c < p.H / 32; c += blockDim.x) {
         float s = 0.0f;
@@ -267,36 +156,64 @@ __global__ void __launch_bounds__(GU_WARPS * 32) k_gateup(DecodeParams p, int u0
             const char* uq = gq + H / 2;
             const uint32_t* gsb = reinterpret_cast<const uint32_t*>(blob + p.off_gu_sb + (size_t)(2 * j) * (H / 64) * 4);
             const uint32_t* usb = gsb + H / 64;
-            for (int c = lane; c < nchunk; c += 32) {
-                const uint4 qg = ldg_stream(gq + 16 * c);
-                const uint4 qu = ldg_stream(uq + 16 * c);
-                const uint32_t sbg = __ldg(gsb + (c >> 1));
-                const uint32_t sbu = __ldg(usb + (c >> 1));
-                const float4* nn = n4 + 8 * c;
-                float pg = 0.0f, pu = 0.0f;
-                pg = dot8_q128(qg.x, nn[0], nn[1], pg);
-                pu = dot8_q128(qu.x, nn[0], nn[1], pu);
-                pg = dot8_q128(qg.y, nn[2], nn[3], pg);
-                pu = dot8_q128(qu.y, nn[2], nn[3], pu);
-                pg = dot8_q128(qg.z, nn[4], nn[5], pg);
-                pu = dot8_q128(qu.z, nn[4], nn[5], pu);
-                pg = dot8_q128(qg.w, nn[6], nn[7], pg);
-                pu = dot8_q128(qu.w, nn[6], nn[7], pu);
-                const float S = csum[c];
-                ag += chunk_affine(sbg, pg, S);
-                au += chunk_affine(sbu, pu, S);
+            for (int c0 = 0; c0 < nchunk; c0 += 96) {   // up to 3 chunks per lane, loads issued first
+                uint4 qg[3], qu[3];
+                uint32_t sbg[3], sbu[3];
+#pragma unroll
+                for (int t = 0; t < 3; ++t) {
+                    const int c = c0 + lane + 32 * t;
+                    if (c < nchunk) {
+                        qg[t] = ldg_stream(gq + 16 * c);
+                        qu[t] = ldg_stream(uq + 16 * c);
+                        sbg[t] = __ldg(gsb + (c >> 1));
+                        sbu[t] = __ldg(usb + (c >> 1));
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < 3; ++t) {
+                    const int c = c0 + lane + 32 * t;
+                    if (c < nchunk) {
+                        const float4* nn = n4 + 8 * c;
+                        float pg = 0.0f, pu = 0.0f;
+                        pg = dot8_q128(qg[t].x, nn[0], nn[1], pg);
+                        pu = dot8_q128(qu[t].x, nn[0], nn[1], pu);
+                        pg = dot8_q128(qg[t].y, nn[2], nn[3], pg);
+                        pu = dot8_q128(qu[t].y, nn[2], nn[3], pu);
+                        pg = dot8_q128(qg[t].z, nn[4], nn[5], pg);
+                        pu = dot8_q128(qu[t].z, nn[4], nn[5], pu);
+                        pg = dot8_q128(qg[t].w, nn[6], nn[7], pg);
+                        pu = dot8_q128(qu[t].w, nn[6], nn[7], pu);
+                        const float S = csum[c];
+                        ag += chunk_affine(sbg[t], pg, S);
+                        au += chunk_affine(sbu[t], pu, S);
+                    }
+                }
             }
             dst = p.h_routed + (size_t)i * I + j;
         } else {
             const int j = u - routed_units;
             const char* gw = reinterpret_cast<const char*>(p.Wsg + (size_t)j * H);
             const char* uw = reinterpret_cast<const char*>(p.Wsu + (size_t)j * H);
-            for (int c = lane; c < H / 8; c += 32) {
-                const uint4 a = ldg_stream(gw + 16 * c);
-                const uint4 b = ldg_stream(uw + 16 * c);
-                const float4 n0 = n4[2 * c], n1 = n4[2 * c + 1];
-                ag = dot8_bf16(a, n0, n1, ag);
-                au = dot8_bf16(b, n0, n1, au);
+            const int nv = H / 8;
+            for (int c0 = 0; c0 < nv; c0 += 128) {     // up to 4 16-byte chunks per lane per batch
+                uint4 a[4], b[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const int c = c0 + lane + 32 * t;
+                    if (c < nv) {
+                        a[t] = ldg_stream(gw + 16 * c);
+                        b[t] = ldg_stream(uw + 16 * c);
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const int c = c0 + lane + 32 * t;
+                    if (c < nv) {
+                        const float4 n0 = n4[2 * c], n1 = n4[2 * c + 1];
+                        ag = dot8_bf16(a[t], n0, n1, ag);
+                        au = dot8_bf16(b[t], n0, n1, au);
+                    }
+                }
             }
             dst = p.h_shared + j;
         }
@@ -322,9 +239,18 @@ __global__ void __launch_bounds__(DN_WARPS * 32) k_down(DecodeParams p, int with
     float* hs = hr + down_hs_offset(kr, I);          // [S], 16-byte aligned for float4 reads
     __shared__ float s_w[TF_MAX_K];
     __shared__ const char* s_ptr[TF_MAX_K];
-    for (int t = threadIdx.x; t < kr * I; t += blockDim.x) hr[t] = __ldcg(p.h_routed + t);
-    if (with_shared)
-        for (int t = threadIdx.x; t < S; t += blockDim.x) hs[t] = __ldcg(p.h_shared + t);
+    {
+        const float4* g = reinterpret_cast<const float4*>(p.h_routed);
+        float4* d = reinterpret_cast<float4*>(hr);
+#pragma unroll 4
+        for (int t = threadIdx.x; t < kr * I / 4; t += blockDim.x) d[t] = __ldcg(g + t);
+        if (with_shared) {
+            const float4* gs = reinterpret_cast<const float4*>(p.h_shared);
+            float4* ds = reinterpret_cast<float4*>(hs);
+#pragma unroll 4
+            for (int t = threadIdx.x; t < S / 4; t += blockDim.x) ds[t] = __ldcg(gs + t);
+        }
+    }
     if (threadIdx.x < kr) {
         s_w[threadIdx.x] = p.w[threadIdx.x];
         s_ptr[threadIdx.x] = expert_ptr(p.ex, threadIdx.x);
@@ -344,25 +270,50 @@ __global__ void __launch_bounds__(DN_WARPS * 32) k_down(DecodeParams p, int with
     const float4* hs4 = reinterpret_cast<const float4*>(hs);
     for (int j = blockIdx.x * DN_WARPS + warp; j < H; j += gridDim.x * DN_WARPS) {
         float acc = 0.0f, accs = 0.0f;
-        for (int t = lane; t < ntask; t += 32) {
-            const int i = t / cpr, c = t - (t / cpr) * cpr;
-            const char* blob = s_ptr[i];
-            const uint4 q = ldg_stream(blob + p.off_d_codes + (size_t)j * (I / 2) + 16 * c);
-            const uint32_t sb =
-                __ldg(reinterpret_cast<const uint32_t*>(blob + p.off_d_sb + (size_t)j * (I / 64) * 4) + (c >> 1));
-            const float4* hh = hr4 + (i * I + 32 * c) / 4;
-            float P = 0.0f;
-            P = dot8_q128(q.x, hh[0], hh[1], P);
-            P = dot8_q128(q.y, hh[2], hh[3], P);
-            P = dot8_q128(q.z, hh[4], hh[5], P);
-            P = dot8_q128(q.w, hh[6], hh[7], P);
-            acc = fmaf(s_w[i], chunk_affine(sb, P, hcs[i * cpr + c]), acc);
+        for (int t0 = 0; t0 < ntask; t0 += 192) {      // up to 6 chunks per lane, loads first
+            uint4 q[6];
+            uint32_t sb[6];
+#pragma unroll
+            for (int u = 0; u < 6; ++u) {
+                const int t = t0 + lane + 32 * u;
+                if (t < ntask) {
+                    const int i = t / cpr, c = t - (t / cpr) * cpr;
+                    const char* blob = s_ptr[i];
+                    q[u] = ldg_stream(blob + p.off_d_codes + (size_t)j * (I / 2) + 16 * c);
+                    sb[u] = __ldg(reinterpret_cast<const uint32_t*>(blob + p.off_d_sb + (size_t)j * (I / 64) * 4) +
+                                  (c >> 1));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 6; ++u) {
+                const int t = t0 + lane + 32 * u;
+                if (t < ntask) {
+                    const int i = t / cpr, c = t - (t / cpr) * cpr;
+                    const float4* hh = hr4 + (i * I + 32 * c) / 4;
+                    float P = 0.0f;
+                    P = dot8_q128(q[u].x, hh[0], hh[1], P);
+                    P = dot8_q128(q[u].y, hh[2], hh[3], P);
+                    P = dot8_q128(q[u].z, hh[4], hh[5], P);
+                    P = dot8_q128(q[u].w, hh[6], hh[7], P);
+                    acc = fmaf(s_w[i], chunk_affine(sb[u], P, hcs[i * cpr + c]), acc);
+                }
+            }
         }
         if (with_shared) {
             const char* dw = reinterpret_cast<const char*>(p.Wsd + (size_t)j * S);
-            for (int c = lane; c < S / 8; c += 32) {
-                const uint4 a = ldg_stream(dw + 16 * c);
-                accs = dot8_bf16(a, hs4[2 * c], hs4[2 * c + 1], accs);
+            const int nv = S / 8;
+            for (int c0 = 0; c0 < nv; c0 += 288) {
+                uint4 a[9];
+#pragma unroll
+                for (int u = 0; u < 9; ++u) {
+                    const int c = c0 + lane + 32 * u;
+                    if (c < nv) a[u] = ldg_stream(dw + 16 * c);
+                }
+#pragma unroll
+                for (int u = 0; u < 9; ++u) {
+                    const int c = c0 + lane + 32 * u;
+                    if (c < nv) accs = dot8_bf16(a[u], hs4[2 * c], hs4[2 * c + 1], accs);
+                }
             }
         }
         acc = warp_sum(acc);
@@ -400,8 +351,14 @@ int launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* Wr, int 
                        int bias_stride, int k, int32_t* idx, float* w, float* logits, float* rms,
                        uint32_t* counters, float eps, void* stream) {
     dim3 grid((E + RT_WARPS - 1) / RT_WARPS, T);
+    const size_t smem = (size_t)(RT_WARPS + 1) * H * 2;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_router_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        attr = true;
+    }
     prof_before(TF_KERNEL_ROUTER, stream);
-    k_router_topk<<<grid, RT_WARPS * 32, 0, (cudaStream_t)stream>>>(x, H, Wr, E, bias, bias_stride, k, idx, w,
+    k_router_topk<<<grid, RT_WARPS * 32, smem, (cudaStream_t)stream>>>(x, H, Wr, E, bias, bias_stride, k, idx, w,
                                                                     logits, rms, counters, eps);
     prof_after(TF_KERNEL_ROUTER, stream);
     return (int)cudaGetLastError();

@@ -62,6 +62,9 @@ struct DecodeParams {
     size_t off_gu_sb, off_d_codes, off_d_sb;
 };
 
+// Descriptor a layer handle was created with (tf_api.cu).
+void layer_desc_of(const tf_layer* l, tf_layer_desc* out);
+
 // Event bracketing of launches while profiling is on (tf_api.cu).
 void prof_before(int kind, void* stream);
 void prof_after(int kind, void* stream);

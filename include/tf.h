@@ -309,6 +309,40 @@ tf_status tf_layer_step(tf_layer* l, tf_expert_cache* cache, int layer, int64_t 
 tf_status tf_stack_decode(tf_layer* const* layers, int L, const void* x, void* out, void* scratch,
                           const float* const* logit_bias, void* stream);
 
+/* ------------------------------------------------- fused decode stack */
+
+/*
+ * The whole stack of resident layers for one decode token in ONE persistent,
+ * cooperative kernel (one CTA per SM). Same operations and output as
+ * tf_stack_decode (router, top-k, shared expert, routed experts, combine per
+ * layer); the weight bytes of every layer are streamed by a producer thread per
+ * CTA into a shared-memory ring (cp.async.bulk), independent of the data
+ * dependencies between layers. Built for the model shape H = 2816, I = 704,
+ * S = 2112, k = 8 (any E <= 1024, same for all layers); other shapes return
+ * TF_ERR_NOT_SUPPORTED (use tf_stack_decode).
+ *   layers      L layer handles with resident expert tables
+ *   logit_bias  host array of L device pointers (fp32 [E]) or NULL; the
+ *               pointers are fixed at creation, their contents may change
+ *   workspace   device, >= tf_stack_workspace_bytes(L, E), 256-byte aligned;
+ *               holds per-layer routing, h, activations and sync words.
+ *               tf_stack_create zero-fills it (synchronously).
+ * Device-side waits between CTAs are bounded (2 s); when one runs out the
+ * kernel records it and returns early. tf_stack_check synchronises the
+ * stream, reports that as TF_ERR_TIMEOUT and re-arms the workspace.
+ */
+typedef struct tf_stack tf_stack;
+size_t tf_stack_workspace_bytes(int L, int E);
+tf_status tf_stack_create(tf_layer* const* layers, int L, const float* const* logit_bias, void* workspace,
+                          size_t ws_bytes, tf_stack** out);
+/* out = stack(x) for one token; x, out device bf16 [H], 16-byte aligned, out != x. */
+tf_status tf_stack_step(tf_stack* s, const void* x, void* out, void* stream);
+tf_status tf_stack_check(tf_stack* s, void* stream);
+/* Device buffers of one layer of the last step: idx [k], w [k], logits [E], output [H] (bf16;
+ * the last layer's output is the call's `out`). */
+tf_status tf_stack_layer_buffers(tf_stack* s, int layer, int32_t** idx, float** w, float** logits,
+                                 void** act_out);
+tf_status tf_stack_destroy(tf_stack* s);
+
 /* ----------------------------------------------------------- measurement */
 
 /*

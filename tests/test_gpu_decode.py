@@ -54,7 +54,7 @@ def _router_case(T, H, E, k, bias_mode, seed=11):
         stride = E
     elif bias_mode == "ties":
         b = np.zeros(E, np.float32)
-        b[[2, 5, 9, E - 1]] = 5.0
+        b[[2, 5, 9, E - 1]] = 50.0      # far above every other logit: the tied group is the top 4
         bias = torch.from_numpy(b).to(DEV)
     ws = torch.zeros(B.tf_router_workspace_bytes(T, E), dtype=torch.uint8, device=DEV)
     idx = torch.full((T, k), -7, dtype=torch.int32, device=DEV)
