@@ -30,3 +30,22 @@ def elem_rel_err(a, r, floor: float = 1e-3) -> float:
 
 def bf16_to_f64(bits) -> np.ndarray:
     return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16_ulp(v) -> np.ndarray:
+    """Spacing of bf16 numbers at |v| (v as float64)."""
+    v = np.abs(np.asarray(v, np.float64))
+    e = np.floor(np.log2(np.maximum(v, 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+def delta_rel_err(out_bits, x_bits, delta_ref) -> float:
+    """Error of the layer update recovered from a bf16 output, out - x, against the
+    reference fp32 update, after allowing the output's own rounding: out is the
+    bf16 of x + delta, so out - x can differ from delta by half an ulp of out, and
+    a rounding-boundary flip adds one more ulp (1.5 ulp of out in all)."""
+    o = bf16_to_f64(out_bits)
+    x = bf16_to_f64(x_bits)
+    d = np.asarray(delta_ref, np.float64)
+    excess = np.maximum(np.abs((o - x) - d) - 1.5 * bf16_ulp(o), 0.0)
+    return float(np.max(excess) / max(np.max(np.abs(d)), 1e-30))

@@ -13,7 +13,7 @@ import torch
 import bit_expert_streaming_layer_b300 as B
 import oracle as O
 import workload as W
-from parity import CONTRACT_TOL, bf16_to_f64, elem_rel_err, max_rel_err
+from parity import CONTRACT_TOL, bf16_to_f64, delta_rel_err, elem_rel_err, max_rel_err
 from workload.model import SyntheticStack, bf16_bits, expert_logical_concat, hidden_tensor, _u16_to_bf16_tensor
 
 pytestmark = pytest.mark.gpu
@@ -168,9 +168,8 @@ def _check_layer(stack, l, x_bits, out_bits, layer_idx=None, bias=None):
     out_o, delta_o = O.layer_combine(x_bits, r, experts, w, shared)
     got = bf16_to_f64(out_bits)
     assert not np.isnan(got).any()
-    xf = bf16_to_f64(x_bits)
     assert max_rel_err(got, bf16_to_f64(out_o)) <= CONTRACT_TOL
-    assert max_rel_err(got - xf, delta_o) <= CONTRACT_TOL
+    assert delta_rel_err(out_bits, x_bits, delta_o) <= CONTRACT_TOL
     return idx
 
 

@@ -13,7 +13,7 @@ import torch
 import bit_expert_streaming_layer_b300 as B
 import oracle as O
 import workload as W
-from parity import CONTRACT_TOL, bf16_to_f64, max_rel_err
+from parity import CONTRACT_TOL, bf16_to_f64, delta_rel_err, max_rel_err
 from workload.model import SyntheticStack, bf16_bits, hidden_tensor
 
 pytestmark = pytest.mark.gpu
@@ -36,8 +36,9 @@ def _check_layer(seed, l, x_bits, out_bits, idx_g, w_g, logits_g, bias=None):
     got = bf16_to_f64(out_bits)
     assert not np.isnan(got).any()
     assert max_rel_err(got, bf16_to_f64(out_o)) <= CONTRACT_TOL
-    assert max_rel_err(got - bf16_to_f64(x_bits), delta_o) <= CONTRACT_TOL
-    return max_rel_err(got - bf16_to_f64(x_bits), delta_o)
+    err = delta_rel_err(out_bits, x_bits, delta_o)
+    assert err <= CONTRACT_TOL
+    return err
 
 
 def _make(seed, L, bias=None):
