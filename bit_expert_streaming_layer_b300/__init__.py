@@ -67,6 +67,7 @@ SIGNATURES = {
     "tf_moe_decode_workspace_bytes": (_sz, [_i32, _i32, _i32]),
     "tf_moe_ffn_decode": (_S, [_vp, _vp, ctypes.POINTER(ExpertTable), _vp, _vp, _i32, _i32, _i32, _vp, _vp, _sz,
                                _vp]),
+    "tf_moe_ffn_decode_noalloc": (_S, [_vp, _vp, ctypes.POINTER(ExpertTable), _vp, _vp, _i32, _i32, _i32, _vp, _vp]),
     "tf_moe_grouped_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "tf_moe_ffn_grouped": (_S, [_vp, _vp, _i32, ctypes.POINTER(ExpertTable), _i32, _vp, _vp, _i32, _i32, _i32, _vp,
                                 _vp, _vp, _vp, _sz, _vp]),
@@ -217,6 +218,17 @@ def tf_moe_decode_workspace_bytes(H: int, I: int, k: int) -> int:
 def tf_moe_ffn_decode(x, out, table: ExpertTable, idx, w, k, H, I, delta, workspace, ws_bytes, stream=None) -> None:
     _check(lib().tf_moe_ffn_decode(_ptr(x), _ptr(out), ctypes.byref(table), _ptr(idx), _ptr(w), k, H, I, _ptr(delta),
                                    _ptr(workspace), ws_bytes, _stream(stream)), "tf_moe_ffn_decode")
+
+
+TF_NOALLOC_MAX_KI = 65536
+
+
+def tf_moe_ffn_decode_noalloc(x, out, table: ExpertTable, idx, w, k, H, I, delta, stream=None) -> None:
+    """tf_moe_ffn_decode without a workspace: the scratch is a fixed array inside libtf.so
+    (for callers that cannot allocate device memory). Calls that overlap on the GPU share
+    that array and race; the first call on a device should come before any stream capture."""
+    _check(lib().tf_moe_ffn_decode_noalloc(_ptr(x), _ptr(out), ctypes.byref(table), _ptr(idx), _ptr(w), k, H, I,
+                                           _ptr(delta), _stream(stream)), "tf_moe_ffn_decode_noalloc")
 
 
 def tf_moe_grouped_workspace_bytes(T, H, I, E, k) -> int:

@@ -4,6 +4,7 @@
 
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -248,6 +249,81 @@ tf_status tf_moe_ffn_decode(const void* x, void* out, const tf_expert_table* tab
     p.ex = table_ref(table, idx);
     p.w = w;
     p.h_routed = static_cast<float*>(workspace);
+    p.off_gu_sb = L.gu_sb;
+    p.off_d_codes = L.d_codes;
+    p.off_d_sb = L.d_sb;
+    clear_error();
+    int e = launch_gateup(p, 0, k * I, stream);
+    if (!e) e = launch_down(p, 1, 0, stream);
+    return cuda_status(e, fn);
+}
+
+}  // extern "C"
+
+// ------------------------------------------- decode FFN without allocation
+//
+// Scratch for tf_moe_ffn_decode_noalloc: the k x I fp32 gate/up activations
+// that the gate/up kernel writes and the down kernel reads. It lives in the
+// library image, so every GPU that loads libtf.so holds these bytes until the
+// process exits, and every call of that entry point shares them.
+namespace {
+
+constexpr size_t NOALLOC_H_FLOATS = TF_NOALLOC_MAX_KI;
+__device__ __align__(256) float g_noalloc_h[NOALLOC_H_FLOATS];
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+float* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
+std::mutex g_noalloc_mu;
+
+// Device address of g_noalloc_h on the current device, looked up once per
+// device. In host code the array's name is only a host-side shadow; passing it
+// to a kernel would hand the GPU a wrong address.
+tf_status noalloc_scratch(float** out, const char* fn) {
+    int dev = -1;
+    if (cudaError_t e = cudaGetDevice(&dev)) return cuda_status(e, fn);
+    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return fail(TF_ERR_NOT_SUPPORTED, "%s: device %d out of range", fn, dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_h)) return cuda_status(e, fn);
+        g_noalloc_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return TF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+tf_status tf_moe_ffn_decode_noalloc(const void* x, void* out, const tf_expert_table* table, const int32_t* idx,
+                                    const float* w, int k, int H, int I, float* delta, void* stream) {
+    const char* fn = "tf_moe_ffn_decode_noalloc";
+    if (!x || !out || !idx || !w) return fail(TF_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!valid_dims(H, I)) return fail(TF_ERR_INVALID_ARG, "%s: H=%d I=%d must be multiples of 64", fn, H, I);
+    if (k < 1 || k > TF_MAX_K) return fail(TF_ERR_INVALID_ARG, "%s: k=%d out of range", fn, k);
+    if ((size_t)k * (size_t)I > NOALLOC_H_FLOATS)
+        return fail(TF_ERR_INVALID_ARG, "%s: k*I = %zu exceeds the built-in scratch of %zu floats", fn,
+                    (size_t)k * (size_t)I, NOALLOC_H_FLOATS);
+    if (tf_status s = check_table(table, fn)) return s;
+    float* scratch = nullptr;
+    if (tf_status s = noalloc_scratch(&scratch, fn)) return s;
+    ExpertLayout L;
+    expert_layout(H, I, &L);
+    DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.x = static_cast<const uint16_t*>(x);
+    p.out = static_cast<uint16_t*>(out);
+    p.delta = delta;
+    p.H = H;
+    p.I = I;
+    p.k = k;
+    p.S = 0;
+    p.eps = 1e-6f;
+    p.rms_in = nullptr;
+    p.ex = table_ref(table, idx);
+    p.w = w;
+    p.h_routed = scratch;  // fully written by the gate/up kernel before the down kernel reads it
     p.off_gu_sb = L.gu_sb;
     p.off_d_codes = L.d_codes;
     p.off_d_sb = L.d_sb;

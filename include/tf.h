@@ -182,6 +182,34 @@ tf_status tf_moe_ffn_decode(const void* x, void* out, const tf_expert_table* tab
                             size_t ws_bytes, void* stream);
 
 /*
+ * tf_moe_ffn_decode for callers that cannot allocate device memory. The pages
+ * have no counterpart: this entry point exists for hosts such as a plugin
+ * inside another runtime that owns the device heap, code that runs while a
+ * stream is being captured, or an embedded loop with a fixed memory budget,
+ * where cudaMalloc is unavailable or forbidden and no workspace can be
+ * provided.
+ *
+ * Same operation, arguments and result as tf_moe_ffn_decode, minus the
+ * workspace. The k x I fp32 gate/up scratch comes from a fixed array compiled
+ * into libtf.so (TF_NOALLOC_MAX_KI floats, 256 KiB), which every GPU that
+ * loads the library keeps until the process exits. The call allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ *  - k * I > TF_NOALLOC_MAX_KI returns TF_ERR_INVALID_ARG (nothing launched);
+ *    the model shape (k = 8, I = 704) uses 5,632 of the 65,536 floats.
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress) and keeps it for later
+ *    calls on that device; make that first call before any stream capture.
+ *  - Every call, on any stream, uses the same array. Calls whose kernels
+ *    overlap on the GPU (other streams, or host threads racing each other)
+ *    race on it and produce wrong results: serialise them. The scratch needs
+ *    no zeroing: each call overwrites all of it that it reads.
+ */
+#define TF_NOALLOC_MAX_KI 65536
+tf_status tf_moe_ffn_decode_noalloc(const void* x, void* out, const tf_expert_table* table,
+                                    const int32_t* idx, const float* w, int k, int H, int I,
+                                    float* delta, void* stream);
+
+/*
  * Grouped (batched / prefill) routed-expert FFN for T tokens: tokens are
  * grouped by expert (histogram, exclusive scan, stable permutation by
  * (expert, token, rank)), each expert's rows run as one dequant-to-bf16
