@@ -32,7 +32,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE decode tok/s (1 B300) and expert-weight HBM GB/s as % of peak"
 H, I, E, K_ACT, S, L = 2816, 704, 128, 8, 2112, 30
 SEED = 1
-WORKLOAD = ("30-layer MoE-only decode stack: H=2816, 128 experts of I=704 (int4 codes, fp16 scale+bias per 64), "
+WORKLOAD_FMT = ("%d-layer MoE-only decode stack: H=2816, 128 experts of I=704 (int4 codes, fp16 scale+bias per 64), "
             "top-8 softmax routing, GELU-gated FFNs, bf16 shared expert 2816->2112->2816, RMSNorm; batch 1, "
             "output fed back each step; all experts resident in HBM; seed 1")
 
@@ -49,9 +49,19 @@ BYTES = {
     "gateup": ROUTED_GU + SHARED_GU + ACT_X + ACT_H,
     "down": ROUTED_D + SHARED_D + ACT_H + 2 * ACT_X,
 }
-BYTES["layer"] = L * (ROUTER + ROUTED_GU + SHARED_GU + ROUTED_D + SHARED_D + 2 * ACT_X)   # one launch = 30 layers
-ROUTED_PER_TOKEN = L * (ROUTED_GU + ROUTED_D)                  # expert-weight bytes per token
-WEIGHTS_PER_TOKEN = L * (ROUTER + ROUTED_GU + SHARED_GU + ROUTED_D + SHARED_D)
+
+
+def set_layers(n_layers: int) -> None:
+    """Per-token byte counts for a stack of n_layers (30 in the benchmark workload)."""
+    global L, ROUTED_PER_TOKEN, WEIGHTS_PER_TOKEN, WORKLOAD
+    L = n_layers
+    WORKLOAD = WORKLOAD_FMT % L
+    BYTES["layer"] = L * (ROUTER + ROUTED_GU + SHARED_GU + ROUTED_D + SHARED_D + 2 * ACT_X)   # one launch = L layers
+    ROUTED_PER_TOKEN = L * (ROUTED_GU + ROUTED_D)                  # expert-weight bytes per token
+    WEIGHTS_PER_TOKEN = L * (ROUTER + ROUTED_GU + SHARED_GU + ROUTED_D + SHARED_D)
+
+
+set_layers(L)
 
 
 def peaks():
@@ -237,7 +247,10 @@ def main():
                     help="timed steps whose kernels are bracketed by CUDA events (the first ones)")
     ap.add_argument("--oracle-layers", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=L,
+                    help="stack depth; the benchmark workload is 30, fewer only for small profiling captures")
     args = ap.parse_args()
+    set_layers(args.layers)
     args.warmup = max(args.warmup, 3)
 
     rank = int(os.environ.get("RANK", 0))
