@@ -166,6 +166,7 @@ def run_ours(args, rank, world):
     if args.path == "fused":
         fws = torch.zeros(B.tf_stack_workspace_bytes(L, E), dtype=torch.uint8, device=dev)
         fused = B.Stack(stack.layers, fws)
+        fused.set_prefetch(args.prefetch)
     x0 = hidden_tensor(SEED, 0, 1, H, device=dev)[0]
     a = torch.empty(H, dtype=torch.bfloat16, device=dev)
     b = torch.empty(H, dtype=torch.bfloat16, device=dev)
@@ -247,6 +248,8 @@ def main():
                     help="timed steps whose kernels are bracketed by CUDA events (the first ones)")
     ap.add_argument("--oracle-layers", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefetch", action="store_true",
+                    help="fused path: prefetch the next layer's shared weights into L2 (measured slower)")
     ap.add_argument("--layers", type=int, default=L,
                     help="stack depth; the benchmark workload is 30, fewer only for small profiling captures")
     args = ap.parse_args()
@@ -303,6 +306,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "layers": L, "batch": 1, "steps_fed_back": args.steps, "path": args.path,
+                   "l2_prefetch": args.path == "fused" and args.prefetch,
                    "l2": "no flush: each step streams 1.895 GB of weights, 15x the 126 MB L2",
                    "parallelism": "replicas" if world > 1 else "single"},
         "expert_weight_gbs": round(expert_gbs, 1),

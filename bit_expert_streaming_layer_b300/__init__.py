@@ -88,6 +88,8 @@ SIGNATURES = {
     "tf_stack_decode": (_S, [ctypes.POINTER(_vp), _i32, _vp, _vp, _vp, ctypes.POINTER(_vp), _vp]),
     "tf_stack_workspace_bytes": (_sz, [_i32, _i32]),
     "tf_stack_create": (_S, [ctypes.POINTER(_vp), _i32, ctypes.POINTER(_vp), _vp, _sz, ctypes.POINTER(_vp)]),
+    "tf_stack_set_prefetch": (_S, [_vp, _i32]),
+    "tf_stack_set_trace": (_S, [_vp, _vp, _sz]),
     "tf_stack_step": (_S, [_vp, _vp, _vp, _vp]),
     "tf_stack_check": (_S, [_vp, _vp]),
     "tf_stack_layer_buffers": (_S, [_vp, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
@@ -385,6 +387,14 @@ class Stack:
         _check(lib().tf_stack_create(arr, L, bias, _ptr(workspace), workspace.numel() * workspace.element_size(),
                                      ctypes.byref(h)), "tf_stack_create")
         self.handle = h.value
+
+    def set_prefetch(self, on: bool) -> None:
+        _check(lib().tf_stack_set_prefetch(self.handle, 1 if on else 0), "tf_stack_set_prefetch")
+
+    def set_trace(self, buf) -> None:
+        """buf: device tensor of >= L * 16 int64 (or None to stop tracing)."""
+        nbytes = 0 if buf is None else buf.numel() * buf.element_size()
+        _check(lib().tf_stack_set_trace(self.handle, _ptr(buf), nbytes), "tf_stack_set_trace")
 
     def layer_buffers(self, layer: int):
         p = [ctypes.c_void_p() for _ in range(4)]

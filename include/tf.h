@@ -343,25 +343,41 @@ tf_status tf_stack_decode(tf_layer* const* layers, int L, const void* x, void* o
  * The whole stack of resident layers for one decode token in ONE persistent,
  * cooperative kernel (one CTA per SM). Same operations and output as
  * tf_stack_decode (router, top-k, shared expert, routed experts, combine per
- * layer); the weight bytes of every layer are streamed by a producer thread per
- * CTA into a shared-memory ring (cp.async.bulk), independent of the data
- * dependencies between layers. Built for the model shape H = 2816, I = 704,
- * S = 2112, k = 8 (any E <= 1024, same for all layers); other shapes return
- * TF_ERR_NOT_SUPPORTED (use tf_stack_decode).
+ * layer). Every worker warp streams the weight rows of its tasks into its own
+ * shared-memory ring (cp.async.bulk) ahead of computing them; optionally the
+ * next layer's data-independent weights are prefetched into L2.
+ * Values that cross CTAs (router logits, h, layer outputs) are published as
+ * tagged words and polled; no device-wide fence or barrier is used. Built for
+ * the model shape H = 2816, I = 704, S = 2112, k = 8 and an even E in
+ * [8, 256], the same for all layers; other shapes return TF_ERR_NOT_SUPPORTED
+ * (use tf_stack_decode).
  *   layers      L layer handles with resident expert tables
  *   logit_bias  host array of L device pointers (fp32 [E]) or NULL; the
  *               pointers are fixed at creation, their contents may change
  *   workspace   device, >= tf_stack_workspace_bytes(L, E), 256-byte aligned;
- *               holds per-layer routing, h, activations and sync words.
- *               tf_stack_create zero-fills it (synchronously).
- * Device-side waits between CTAs are bounded (2 s); when one runs out the
- * kernel records it and returns early. tf_stack_check synchronises the
- * stream, reports that as TF_ERR_TIMEOUT and re-arms the workspace.
+ *               holds per-layer tagged routing, h and outputs, the launch
+ *               epoch and the error word. tf_stack_create initialises it
+ *               (synchronously); each launch advances the epoch on the device,
+ *               so steps may be enqueued back to back or captured in a graph.
+ * Device-side waits are bounded (2 s); when one runs out the kernel records it
+ * and returns early. tf_stack_check synchronises the stream, reports that as
+ * TF_ERR_TIMEOUT and re-initialises the workspace.
  */
 typedef struct tf_stack tf_stack;
 size_t tf_stack_workspace_bytes(int L, int E);
 tf_status tf_stack_create(tf_layer* const* layers, int L, const float* const* logit_bias, void* workspace,
                           size_t ws_bytes, tf_stack** out);
+/* L2 prefetch of the next layer's data-independent weights (router, shared
+ * expert) while a layer runs: on (1) or off (0, the default). */
+tf_status tf_stack_set_prefetch(tf_stack* s, int on);
+/* Phase trace for measurement: with a device buffer of L * 256 * 8 uint64 set,
+ * each step writes, for layer l and CTA c, at buffer[(256 l + c) * 8 + slot],
+ * the %globaltimer (ns) at which the CTA's first control warp 0 saw the whole
+ * layer input, 1 published x and n, 2 saw all router logits, 3 published the
+ * top-k, 4 saw the h counter complete, 5 staged its part of h; 6 the CTA's last
+ * worker warp finished its h-producing tasks, 7 its layer work. NULL turns
+ * tracing off. */
+tf_status tf_stack_set_trace(tf_stack* s, void* buffer, size_t bytes);
 /* out = stack(x) for one token; x, out device bf16 [H], 16-byte aligned, out != x. */
 tf_status tf_stack_step(tf_stack* s, const void* x, void* out, void* stream);
 tf_status tf_stack_check(tf_stack* s, void* stream);
