@@ -1,25 +1,834 @@
-// Grouped (batched / prefill) routed-expert FFN: token x expert histogram,
-// exclusive scan, stable permutation, grouped dequant-to-bf16 GEMMs and the
+// Grouped (batched / prefill) routed-expert FFN on the 5th-generation tensor
+// cores: token x expert histogram, exclusive scan, stable permutation, grouped
+// dequant-to-bf16 tcgen05 GEMMs with fp32 accumulation in TMEM, and the
 // unpermute-combine.
+//
+// Page "Como executar um modelo de 26 bilhoes de parametros em dois gigabytes de
+// memoria em um Mac comum", section "Desempenho no mundo real": during prefill
+// one loaded expert is applied to a whole group of rows. Here every expert's
+// rows are gathered into one contiguous block (the permutation), each block
+// runs as GEMMs against that expert's weights, and every token then sums its k
+// results in top-k order.
+//
+// GEMM orientation (swap-AB): the weights are the M side (128 rows per tile,
+// dequantised from int4 to bf16 in shared memory), the tokens are the N side
+// (up to 256 per tile, loaded by TMA). D[m, n] = sum_k W[m, k] X[n, k] lives in
+// TMEM as 128 lanes x N fp32 columns; two accumulators let the epilogue of one
+// tile overlap the MMAs of the next. Warp roles in a 512-thread CTA:
+//   warp 0      TMA producer: int4 codes (3-D tensor map over all experts),
+//               scales/biases (bulk copy), token rows (2-D tensor map, SW128)
+//   warp 1      TMEM owner; lane 0 issues tcgen05.mma and tcgen05.commit
+//   warps 4..7  epilogue: tcgen05.ld, GELU-gate (gate/up) or plain (down), store
+//   warps 8..15 dequant: codes -> bf16 = RN(s q + b) into the SW128 A tile
+// Numerics (the configuration's "dequant-to-bf16 GEMMs with fp32 accumulate"):
+// n, the dequantised weights and h are bf16; products accumulate in fp32.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
+
+#include "tf_device.cuh"
 #include "tf_internal.h"
+
+namespace tf {
+namespace grouped {
+
+using namespace dev;
+
+constexpr int NB = 256;                // tokens per GEMM tile (MMA N <= 256)
+constexpr int BM = 128;                // weight rows per GEMM tile (MMA M)
+constexpr int BK = 64;                 // K per pipeline stage (one quant group, 128 bytes of bf16)
+constexpr int BOX_ROWS = 16;           // token rows per TMA box
+constexpr int NA = 3, NBST = 3, NCS = 4;
+constexpr int A_BYTES = BM * BK * 2;             // 16 KB
+constexpr int B_BYTES = NB * BK * 2;             // 32 KB
+constexpr int C_BYTES = BM * BK / 2;             // 4 KB of codes per stage
+constexpr int SB_MAX = BM * (2816 / 64) * 4;     // 22,528 B of {s,b} per tile (K up to 2816)
+constexpr int GEMM_THREADS = 512;
+constexpr int N_DQ_WARPS = 8;
+constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
+
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + NA * A_BYTES;
+constexpr int OFF_C = OFF_B + NBST * B_BYTES;
+constexpr int OFF_SB = OFF_C + NCS * C_BYTES;
+constexpr int OFF_BAR = OFF_SB + 2 * SB_MAX;
+enum {
+    BAR_CF = 0,                  // codes full [NCS]
+    BAR_CE = BAR_CF + NCS,       // codes empty [NCS]
+    BAR_AF = BAR_CE + NCS,       // A full [NA]
+    BAR_AE = BAR_AF + NA,        // A empty [NA]
+    BAR_BF = BAR_AE + NA,        // B full [NBST]
+    BAR_BE = BAR_BF + NBST,      // B empty [NBST]
+    BAR_SF = BAR_BE + NBST,      // sb full [2]
+    BAR_SE = BAR_SF + 2,         // sb empty [2]
+    BAR_DF = BAR_SE + 2,         // accumulator full [2]
+    BAR_DE = BAR_DF + 2,         // accumulator empty [2]
+    N_BARS = BAR_DE + 2
+};
+constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;   // tmem base, abort flag
+constexpr size_t GEMM_SMEM = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KB
+static_assert(OFF_B % 1024 == 0 && OFF_C % 1024 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "SW128 tiles");
+
+struct GemmParams {
+    const char* ebase;          // resident experts: expert e at ebase + e * estride
+    unsigned long long estride;
+    unsigned long long off_sb;  // offset of this matrix's {s,b} section in an expert
+    int K;                      // reduction length (H for gate/up, I for down)
+    int MT;                     // weight-row tiles per expert (2I/128 or H/128)
+    int E;
+    const int32_t* counts;      // [E] rows per expert
+    const int32_t* offsets;     // [E+1] first permuted row of each expert
+    const int32_t* tiles;       // [E+1] prefix of tiles (MT * ceil(count / NB)) per expert
+    int mode;                   // 0: gate/up -> h bf16 [P, I]; 1: down -> y fp32 [P, H]
+    uint16_t* hout;
+    float* yout;
+    int ldo;                    // row length of the output (I or H)
+    uint32_t* err;
+};
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_wait_hint(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(1000u)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t gtimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(dst),
+        "l"(map), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// tcgen05 (TMEM allocation, MMA, commit, loads, ordering fences)
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_ld8(uint32_t taddr, float* v) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzled
+// layout (rows of 128 bytes, 8-row atoms of 1 KB): start address >> 4, leading
+// byte offset 16 B (unused for this layout), stride byte offset 1024 B between
+// 8-row groups, descriptor version 1, layout SWIZZLE_128B (2).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3ffffu) >> 4);
+    d |= (uint64_t)(16u >> 4) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N (multiple of 16, <= 256) and M = 128.
+__device__ __forceinline__ uint32_t idesc_bf16(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+// Bounded mbarrier wait of one thread; on timeout or abort it raises the CTA's
+// abort flag (and the global error word) and returns false.
+__device__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, uint32_t* err) {
+    if (mbar_wait_hint(bar, parity)) return true;
+    const uint64_t t0 = gtimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_wait_hint(bar, parity)) return true;
+        if ((n & 7u) == 0) {
+            if (*abort_flag) return false;
+            if (gtimer() - t0 > TIMEOUT_NS) {
+                *abort_flag = 1u;
+                atomicOr(err, 1u);
+                return false;
+            }
+        }
+    }
+}
+
+// Work item w -> (expert, token block, weight tile), weight tiles fastest so that
+// consecutive items share their token rows in L2.
+struct Item {
+    int e, row0, nrows, mt;
+};
+__device__ __forceinline__ Item decode_item(const GemmParams& p, int w) {
+    int lo = 0, hi = p.E;  // largest e with tiles[e] <= w
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(p.tiles + mid) <= w) lo = mid;
+        else hi = mid;
+    }
+    Item it;
+    it.e = lo;
+    const int local = w - __ldg(p.tiles + lo);
+    const int nb = local / p.MT;
+    it.mt = local - nb * p.MT;
+    it.row0 = __ldg(p.offsets + lo) + nb * NB;
+    const int rem = __ldg(p.counts + lo) - nb * NB;
+    it.nrows = rem < NB ? rem : NB;
+    return it;
+}
+
+// 128 + q for byte B of x (bytes hold one code), as fp32.
+template <int B>
+__device__ __forceinline__ float byte128(uint32_t x) {
+    return __uint_as_float(__byte_perm(x, 0x43000000u, 0x7054u | (B << 8)));
+}
+// Eight codes of one word -> eight bf16 weights RN(fl(s q + b)) packed in a uint4.
+__device__ __forceinline__ uint4 dequant8(uint32_t q, float s, float b) {
+    const uint32_t lo = q & 0x0f0f0f0fu, hi = (q >> 4) & 0x0f0f0f0fu;  // codes 0,2,4,6 / 1,3,5,7
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float qe = (j == 0 ? byte128<0>(lo) : j == 1 ? byte128<1>(lo) : j == 2 ? byte128<2>(lo) : byte128<3>(lo)) -
+                         128.0f;  // exact
+        const float qo = (j == 0 ? byte128<0>(hi) : j == 1 ? byte128<1>(hi) : j == 2 ? byte128<2>(hi) : byte128<3>(hi)) -
+                         128.0f;
+        const __nv_bfloat162 v = __floats2bfloat162_rn(fmaf(s, qe, b), fmaf(s, qo, b));  // s q exact: one rounding each
+        o[j] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    k_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    auto bar = [&](int i) { return smem_u32(&bars[i]); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC + 4);
+    const int KS = p.K / BK;
+    const int total = __ldg(p.tiles + p.E);
+    const int gpr = p.K / 64;  // quant groups per weight row
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NCS; ++i) {
+            mbar_init(bar(BAR_CF + i), 1);
+            mbar_init(bar(BAR_CE + i), N_DQ_WARPS);
+        }
+        for (int i = 0; i < NA; ++i) {
+            mbar_init(bar(BAR_AF + i), N_DQ_WARPS);
+            mbar_init(bar(BAR_AE + i), 1);
+        }
+        for (int i = 0; i < NBST; ++i) {
+            mbar_init(bar(BAR_BF + i), 1);
+            mbar_init(bar(BAR_BE + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(BAR_SF + i), 1);
+            mbar_init(bar(BAR_SE + i), N_DQ_WARPS);
+            mbar_init(bar(BAR_DF + i), 1);
+            mbar_init(bar(BAR_DE + i), 4);
+        }
+        *abort_flag = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ================================================ TMA producer
+        if (lane == 0) {
+            int ci = 0, bi = 0, it_local = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
+                const Item it = decode_item(p, w);
+                const int sbi = it_local & 1;
+                if (!(ok = wait_bar(bar(BAR_SE + sbi), ((it_local >> 1) & 1) ^ 1, abort_flag, p.err))) break;
+                const uint32_t sb_bytes = (uint32_t)(BM * gpr * 4);
+                mbar_expect_tx(bar(BAR_SF + sbi), sb_bytes);
+                bulk_g2s(smem_u32(smem + OFF_SB + sbi * SB_MAX),
+                         p.ebase + (size_t)it.e * p.estride + p.off_sb + (size_t)it.mt * BM * gpr * 4, sb_bytes,
+                         bar(BAR_SF + sbi));
+                const int nbox = (it.nrows + BOX_ROWS - 1) / BOX_ROWS;
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int cs = ci % NCS;
+                    if (!(ok = wait_bar(bar(BAR_CE + cs), ((ci / NCS) & 1) ^ 1, abort_flag, p.err))) break;
+                    mbar_expect_tx(bar(BAR_CF + cs), C_BYTES);
+                    tma_load_3d(smem_u32(smem + OFF_C + cs * C_BYTES), &tmA, ks * (BK / 2), it.mt * BM, it.e,
+                                bar(BAR_CF + cs));
+                    ++ci;
+                    const int bs = bi % NBST;
+                    if (!(ok = wait_bar(bar(BAR_BE + bs), ((bi / NBST) & 1) ^ 1, abort_flag, p.err))) break;
+                    mbar_expect_tx(bar(BAR_BF + bs), (uint32_t)(nbox * BOX_ROWS * BK * 2));
+                    for (int r = 0; r < nbox; ++r)
+                        tma_load_2d(smem_u32(smem + OFF_B + bs * B_BYTES + r * BOX_ROWS * BK * 2), &tmB, ks * BK,
+                                    it.row0 + r * BOX_ROWS, bar(BAR_BF + bs));
+                    ++bi;
+                }
+            }
+            // let every copy this thread issued land before the CTA can exit
+            for (int j = ci - NCS; j < ci; ++j)
+                if (j >= 0) wait_bar(bar(BAR_CF + j % NCS), (j / NCS) & 1, abort_flag, p.err);
+            for (int j = bi - NBST; j < bi; ++j)
+                if (j >= 0) wait_bar(bar(BAR_BF + j % NBST), (j / NBST) & 1, abort_flag, p.err);
+        }
+    } else if (warp == 1) {
+        // ================================================ MMA issuer
+        if (lane == 0) {
+            int ai = 0, bi = 0, it_local = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
+                const Item it = decode_item(p, w);
+                const int ab = it_local & 1;
+                if (!(ok = wait_bar(bar(BAR_DE + ab), ((it_local >> 1) & 1) ^ 1, abort_flag, p.err))) break;
+                tc_fence_after();
+                const int n_mma = ((it.nrows + 15) / 16) * 16;
+                const uint32_t idesc = idesc_bf16(n_mma);
+                const uint32_t d_tmem = tmem + (uint32_t)(ab * NB);
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int as = ai % NA, bs = bi % NBST;
+                    if (!(ok = wait_bar(bar(BAR_AF + as), (ai / NA) & 1, abort_flag, p.err))) break;
+                    if (!(ok = wait_bar(bar(BAR_BF + bs), (bi / NBST) & 1, abort_flag, p.err))) break;
+                    tc_fence_after();
+                    const uint64_t ad = sw128_desc(smem_u32(smem + OFF_A + as * A_BYTES));
+                    const uint64_t bd = sw128_desc(smem_u32(smem + OFF_B + bs * B_BYTES));
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)  // 32 bytes of K per MMA: +2 in the start-address field
+                        tc_mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (ks | k) != 0);
+                    tc_commit(bar(BAR_AE + as));
+                    tc_commit(bar(BAR_BE + bs));
+                    ++ai;
+                    ++bi;
+                }
+                if (!ok) break;
+                tc_commit(bar(BAR_DF + ab));
+            }
+            // the MMAs issued so far complete before TMEM is released
+            if (ai > 0) wait_bar(bar(BAR_AE + (ai - 1) % NA), ((ai - 1) / NA) & 1, abort_flag, p.err);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ================================================ epilogue
+        const int q = warp & 3;
+        const int m = q * 32 + lane;  // TMEM lane = weight row within the tile
+        int it_local = 0;
+        for (int w = blockIdx.x; w < total; w += gridDim.x, ++it_local) {
+            const Item it = decode_item(p, w);
+            const int ab = it_local & 1;
+            int okw = 1;
+            if (lane == 0) okw = wait_bar(bar(BAR_DF + ab), (it_local >> 1) & 1, abort_flag, p.err);
+            if (!__shfl_sync(FULL, okw, 0)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * NB);
+            const int nchunks = (it.nrows + 7) / 8;
+            if (p.mode == 0) {
+                const int j = (it.mt * BM + m) >> 1;  // h column (gate row 2j, up row 2j+1)
+                const bool up = m & 1;
+                for (int c = 0; c < nchunks; ++c) {
+                    float v[8];
+                    tc_ld8(tbase + (uint32_t)(c * 8), v);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float other = __shfl_xor_sync(FULL, v[i], 1);
+                        const float g = up ? other : v[i], u = up ? v[i] : other;
+                        const int n = c * 8 + i;
+                        if ((i & 1) == (int)up && n < it.nrows) {
+                            const float hv = gelu_tanh(g) * u;
+                            p.hout[(size_t)(it.row0 + n) * p.ldo + j] = f2bf(hv);
+                        }
+                    }
+                }
+            } else {
+                const int jg = it.mt * BM + m;
+                for (int c = 0; c < nchunks; ++c) {
+                    float v[8];
+                    tc_ld8(tbase + (uint32_t)(c * 8), v);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int n = c * 8 + i;
+                        if (n < it.nrows) p.yout[(size_t)(it.row0 + n) * p.ldo + jg] = v[i];
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(BAR_DE + ab));
+        }
+    } else if (warp >= 8) {
+        // ================================================ dequant
+        const int t = threadIdx.x - 8 * 32;  // 0..255
+        const int r = t >> 1, hf = t & 1;    // weight row in the tile, half of the 64-code group
+        int ci = 0, ai = 0, it_local = 0;
+        bool ok = true;
+        for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
+            const int sbi = it_local & 1;
+            int okw = 1;
+            if (lane == 0) okw = wait_bar(bar(BAR_SF + sbi), (it_local >> 1) & 1, abort_flag, p.err);
+            if (!(ok = __shfl_sync(FULL, okw, 0))) break;
+            const uint32_t* sbrow = reinterpret_cast<const uint32_t*>(smem + OFF_SB + sbi * SB_MAX) + r * gpr;
+            for (int ks = 0; ks < KS; ++ks) {
+                const int cs = ci % NCS, as = ai % NA;
+                okw = 1;
+                if (lane == 0) {
+                    okw = wait_bar(bar(BAR_CF + cs), (ci / NCS) & 1, abort_flag, p.err);
+                    if (okw) okw = wait_bar(bar(BAR_AE + as), ((ai / NA) & 1) ^ 1, abort_flag, p.err);
+                }
+                if (!(ok = __shfl_sync(FULL, okw, 0))) break;
+                const uint4 qv = *reinterpret_cast<const uint4*>(smem + OFF_C + cs * C_BYTES + r * 32 + hf * 16);
+                const uint32_t sbw = sbrow[ks];
+                const float s = h2f(sbw & 0xffffu), b = h2f(sbw >> 16);
+                unsigned char* arow = smem + OFF_A + as * A_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+                const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int chunk = hf * 4 + c;  // 16-byte chunk of the 128-byte row
+                    *reinterpret_cast<uint4*>(arow + ((chunk ^ (r & 7)) << 4)) = dequant8(qw[c], s, b);
+                }
+                fence_proxy_async();  // generic-proxy writes, read next by the tensor core
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(BAR_AF + as));
+                    mbar_arrive(bar(BAR_CE + cs));
+                }
+                ++ci;
+                ++ai;
+            }
+            if (!ok) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(BAR_SE + sbi));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------ routing -> permutation
+
+// One CTA: tokens per expert, exclusive scan, GEMM tile prefixes.
+__global__ void __launch_bounds__(1024) k_group_hist(const int32_t* __restrict__ idx, int P, int E, int mt_gu,
+                                                      int mt_d, int32_t* counts, int32_t* offsets, int32_t* tiles_gu,
+                                                      int32_t* tiles_d) {
+    __shared__ int32_t cnt[TF_MAX_E];
+    __shared__ int32_t wsum[32];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        const int e = __ldg(idx + p);
+        if ((unsigned)e < (unsigned)E) atomicAdd(&cnt[e], 1);
+    }
+    __syncthreads();
+    // exclusive scans of counts and of tiles (E <= 1024: one expert per thread)
+    const int e = threadIdx.x;
+    const int c = e < E ? cnt[e] : 0;
+    const int nb = (c + NB - 1) / NB;
+    int vals[2] = {c, nb};
+    int excl[2];
+    for (int s = 0; s < 2; ++s) {
+        int v = vals[s];
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        int x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(FULL, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) wsum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int z = wsum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(FULL, z, o);
+                if (lane >= o) z += y;
+            }
+            wsum[lane] = z;
+        }
+        __syncthreads();
+        excl[s] = x - v + (warp > 0 ? wsum[warp - 1] : 0);
+        __syncthreads();
+    }
+    if (e < E) {
+        counts[e] = c;
+        offsets[e] = excl[0];
+        tiles_gu[e] = excl[1] * mt_gu;
+        tiles_d[e] = excl[1] * mt_d;
+    }
+    if (e == E - 1) {
+        offsets[E] = excl[0] + c;
+        tiles_gu[E] = (excl[1] + nb) * mt_gu;
+        tiles_d[E] = (excl[1] + nb) * mt_d;
+    }
+}
+
+// CTA e: stable positions of the pairs routed to expert e (pairs p = t * k + i in
+// increasing p, i.e. sorted by (expert, token, rank)).
+__global__ void __launch_bounds__(1024) k_group_pos(const int32_t* __restrict__ idx, int P,
+                                                     const int32_t* __restrict__ offsets, int32_t* perm,
+                                                     int32_t* inv) {
+    __shared__ int32_t wcnt[32];
+    __shared__ int32_t base_s;
+    const int e = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) base_s = offsets[e];
+    __syncthreads();
+    for (int p0 = 0; p0 < P; p0 += blockDim.x) {
+        const int p = p0 + threadIdx.x;
+        const bool mine = p < P && __ldg(idx + p) == e;
+        const unsigned ball = __ballot_sync(FULL, mine);
+        if (lane == 0) wcnt[warp] = __popc(ball);
+        __syncthreads();
+        int before = 0, total = 0;
+        for (int w2 = 0; w2 < 32; ++w2) {
+            const int v = wcnt[w2];
+            before += w2 < warp ? v : 0;
+            total += v;
+        }
+        const int base = base_s;
+        if (mine) {
+            const int pos = base + before + __popc(ball & ((1u << lane) - 1u));
+            perm[pos] = p;
+            inv[p] = pos;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) base_s = base + total;
+        __syncthreads();
+    }
+}
+
+// Pairs whose expert id is out of range get no row: their inverse is -1.
+__global__ void k_group_inv_init(const int32_t* __restrict__ idx, int P, int E, int32_t* inv) {
+    const int p = blockIdx.x * blockDim.x + threadIdx.x;
+    if (p < P && (unsigned)__ldg(idx + p) >= (unsigned)E) inv[p] = -1;
+}
+
+// r_t = 1/sqrt(mean(x_t^2) + eps) in the canonical order, one warp per token.
+__global__ void k_group_rms(const uint16_t* __restrict__ x, int T, int H, float eps, float* rms) {
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    const float r = rms_scale_warp(x + (size_t)t * H, H, eps, lane);
+    if (lane == 0) rms[t] = r;
+}
+
+// Row pos of the permuted activations: bf16(r_t * x_t), t = perm[pos] / k.
+__global__ void k_group_gather(const uint16_t* __restrict__ x, const float* __restrict__ rms,
+                               const int32_t* __restrict__ perm, int P, int k, int H, uint16_t* xp) {
+    const int pos = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (pos >= P) return;
+    const int t = __ldg(perm + pos) / k;
+    const float r = __ldg(rms + t);
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)pos * H);
+    for (int v = lane; v < H / 8; v += 32) {
+        const uint4 a = __ldg(src + v);
+        uint4 o;
+        o.x = (uint32_t)f2bf(__fmul_rn(r, bf_lo(a.x))) | ((uint32_t)f2bf(__fmul_rn(r, bf_hi(a.x))) << 16);
+        o.y = (uint32_t)f2bf(__fmul_rn(r, bf_lo(a.y))) | ((uint32_t)f2bf(__fmul_rn(r, bf_hi(a.y))) << 16);
+        o.z = (uint32_t)f2bf(__fmul_rn(r, bf_lo(a.z))) | ((uint32_t)f2bf(__fmul_rn(r, bf_hi(a.z))) << 16);
+        o.w = (uint32_t)f2bf(__fmul_rn(r, bf_lo(a.w))) | ((uint32_t)f2bf(__fmul_rn(r, bf_hi(a.w))) << 16);
+        dst[v] = o;
+    }
+}
+
+// out[t] = bf16(x[t] + sum_i w[t,i] y[inv[t k + i]]), summed in top-k order.
+__global__ void k_group_combine(const uint16_t* __restrict__ x, const float* __restrict__ y,
+                                const int32_t* __restrict__ inv, const float* __restrict__ w, int k, int H,
+                                const uint32_t* err, uint16_t* out, float* delta) {
+    const int t = blockIdx.x;
+    if (*err) {  // a GEMM wait timed out: the outputs are NaN, never stale or partial values
+        for (int j = threadIdx.x; j < H; j += blockDim.x) {
+            out[(size_t)t * H + j] = 0x7fc0u;
+            if (delta) delta[(size_t)t * H + j] = __int_as_float(0x7fc00000);
+        }
+        return;
+    }
+    __shared__ int32_t rows[TF_MAX_K];
+    __shared__ float ws[TF_MAX_K];
+    if (threadIdx.x < k) {
+        rows[threadIdx.x] = __ldg(inv + (size_t)t * k + threadIdx.x);
+        ws[threadIdx.x] = __ldg(w + (size_t)t * k + threadIdx.x);
+    }
+    __syncthreads();
+    for (int j = threadIdx.x * 4; j < H; j += blockDim.x * 4) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < k; ++i) {
+            if (rows[i] < 0) continue;
+            const float4 v = __ldg(reinterpret_cast<const float4*>(y + (size_t)rows[i] * H + j));
+            acc.x = fmaf(ws[i], v.x, acc.x);
+            acc.y = fmaf(ws[i], v.y, acc.y);
+            acc.z = fmaf(ws[i], v.z, acc.z);
+            acc.w = fmaf(ws[i], v.w, acc.w);
+        }
+        const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + (size_t)t * H + j));
+        const float o0 = bf_lo(xv.x) + acc.x, o1 = bf_hi(xv.x) + acc.y;
+        const float o2 = bf_lo(xv.y) + acc.z, o3 = bf_hi(xv.y) + acc.w;
+        *reinterpret_cast<uint2*>(out + (size_t)t * H + j) =
+            make_uint2((uint32_t)f2bf(o0) | ((uint32_t)f2bf(o1) << 16), (uint32_t)f2bf(o2) | ((uint32_t)f2bf(o3) << 16));
+        if (delta) *reinterpret_cast<float4*>(delta + (size_t)t * H + j) = acc;
+    }
+}
+
+// ------------------------------------------------------------------ host
+
+struct Carve {
+    size_t err, counts, offsets, tiles_gu, tiles_d, perm, inv, rms, xp, hb, y, total;
+};
+
+Carve carve(int T, int H, int I, int E, int k) {
+    Carve c;
+    const size_t P = (size_t)T * k;
+    size_t o = 0;
+    c.err = o; o += 256;
+    c.counts = o; o += align_up((size_t)E * 4, 256);
+    c.offsets = o; o += align_up((size_t)(E + 1) * 4, 256);
+    c.tiles_gu = o; o += align_up((size_t)(E + 1) * 4, 256);
+    c.tiles_d = o; o += align_up((size_t)(E + 1) * 4, 256);
+    c.perm = o; o += align_up(P * 4, 256);
+    c.inv = o; o += align_up(P * 4, 256);
+    c.rms = o; o += align_up((size_t)T * 4, 256);
+    c.xp = o; o += align_up(P * H * 2, 256);
+    c.hb = o; o += align_up(P * I * 2, 256);
+    c.y = o; o += align_up(P * H * 4, 256);
+    c.total = o;
+    return c;
+}
+
+// The driver's tensor-map encoder, looked up through the runtime so that the
+// library needs no link-time dependency on the driver library.
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encoder();
+    if (!fn) return false;
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace grouped
+}  // namespace tf
 
 using namespace tf;
 
 extern "C" {
 
 size_t tf_moe_grouped_workspace_bytes(int T, int H, int I, int E, int k) {
-    if (T < 1 || H < 1 || I < 1 || E < 1 || k < 1) return 0;
-    return 256;
+    if (T < 1 || H < 64 || I < 64 || E < 1 || E > TF_MAX_E || k < 1 || k > TF_MAX_K) return 0;
+    return grouped::carve(T, H, I, E, k).total;
 }
 
 tf_status tf_moe_ffn_grouped(const void* x, void* out, int T, const tf_expert_table* table, int E, const int32_t* idx,
                              const float* w, int k, int H, int I, float* delta, int32_t* perm_out, int32_t* counts_out,
                              void* workspace, size_t ws_bytes, void* stream) {
-    (void)x; (void)out; (void)T; (void)table; (void)E; (void)idx; (void)w; (void)k; (void)H; (void)I; (void)delta;
-    (void)perm_out; (void)counts_out; (void)workspace; (void)ws_bytes; (void)stream;
-    return fail(TF_ERR_NOT_SUPPORTED, "tf_moe_ffn_grouped: not built yet");
+    using namespace grouped;
+    const char* fn = "tf_moe_ffn_grouped";
+    if (!x || !out || !table || !idx || !w || !workspace) return fail(TF_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (x == out) return fail(TF_ERR_INVALID_ARG, "%s: out must not alias x", fn);
+    if (T < 1) return fail(TF_ERR_INVALID_ARG, "%s: T=%d", fn, T);
+    if (H % 128 || I % 64 || H > 2816 || H < 128 || I < 64)
+        return fail(TF_ERR_INVALID_ARG, "%s: H must be a multiple of 128 (<= 2816) and I a multiple of 64 (H=%d I=%d)",
+                    fn, H, I);
+    if (E < 1 || E > TF_MAX_E || k < 1 || k > TF_MAX_K || k > E)
+        return fail(TF_ERR_INVALID_ARG, "%s: E=%d k=%d out of range", fn, E, k);
+    if (!table->base || !aligned16(table->base) || table->stride % 16)
+        return fail(TF_ERR_INVALID_ARG, "%s: expert table base and stride must be 16-byte aligned", fn);
+    if (table->slot_of_expert)
+        return fail(TF_ERR_NOT_SUPPORTED, "%s: the grouped path takes a resident expert table (no slot map)", fn);
+    if (!aligned16(x) || !aligned16(out) || (delta && !aligned16(delta)))
+        return fail(TF_ERR_INVALID_ARG, "%s: x, out and delta must be 16-byte aligned", fn);
+    if ((size_t)T * k > (size_t)INT32_MAX / 4) return fail(TF_ERR_INVALID_ARG, "%s: T*k too large", fn);
+    const Carve c = carve(T, H, I, E, k);
+    if (ws_bytes < c.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return fail(TF_ERR_INVALID_ARG, "%s: workspace misaligned or smaller than %zu bytes", fn, c.total);
+    ExpertLayout lay;
+    expert_layout(H, I, &lay);
+    if (table->stride < lay.payload) return fail(TF_ERR_INVALID_ARG, "%s: expert stride below the payload size", fn);
+
+    char* ws = static_cast<char*>(workspace);
+    uint32_t* err = reinterpret_cast<uint32_t*>(ws + c.err);
+    int32_t* counts = reinterpret_cast<int32_t*>(ws + c.counts);
+    int32_t* offsets = reinterpret_cast<int32_t*>(ws + c.offsets);
+    int32_t* tiles_gu = reinterpret_cast<int32_t*>(ws + c.tiles_gu);
+    int32_t* tiles_d = reinterpret_cast<int32_t*>(ws + c.tiles_d);
+    int32_t* perm = reinterpret_cast<int32_t*>(ws + c.perm);
+    int32_t* inv = reinterpret_cast<int32_t*>(ws + c.inv);
+    float* rms = reinterpret_cast<float*>(ws + c.rms);
+    uint16_t* xp = reinterpret_cast<uint16_t*>(ws + c.xp);
+    uint16_t* hb = reinterpret_cast<uint16_t*>(ws + c.hb);
+    float* y = reinterpret_cast<float*>(ws + c.y);
+    const int P = T * k;
+
+    // tensor maps: codes of every expert (3-D), permuted activations and h (2-D, SW128)
+    CUtensorMap tmA_gu, tmA_d, tmB_gu, tmB_d;
+    const char* base = static_cast<const char*>(table->base);
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)H / 2, (cuuint64_t)2 * I, (cuuint64_t)E};
+        cuuint64_t str[2] = {(cuuint64_t)H / 2, (cuuint64_t)table->stride};
+        cuuint32_t box[3] = {BK / 2, BM, 1};
+        if (!encode(&tmA_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base + lay.gu_codes, dims, str, box,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+            return fail(TF_ERR_CUDA, "%s: tensor map of the gate/up codes", fn);
+    }
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)I / 2, (cuuint64_t)H, (cuuint64_t)E};
+        cuuint64_t str[2] = {(cuuint64_t)I / 2, (cuuint64_t)table->stride};
+        cuuint32_t box[3] = {BK / 2, BM, 1};
+        if (!encode(&tmA_d, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base + lay.d_codes, dims, str, box,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+            return fail(TF_ERR_CUDA, "%s: tensor map of the down codes", fn);
+    }
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)P};
+        cuuint64_t str[1] = {(cuuint64_t)H * 2};
+        cuuint32_t box[2] = {BK, BOX_ROWS};
+        if (!encode(&tmB_gu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xp, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return fail(TF_ERR_CUDA, "%s: tensor map of the permuted activations", fn);
+    }
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)I, (cuuint64_t)P};
+        cuuint64_t str[1] = {(cuuint64_t)I * 2};
+        cuuint32_t box[2] = {BK, BOX_ROWS};
+        if (!encode(&tmB_d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, hb, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return fail(TF_ERR_CUDA, "%s: tensor map of h", fn);
+    }
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_group_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GEMM_SMEM);
+        if (e != cudaSuccess) return cuda_status(e, fn);
+        attr_set = true;
+    }
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    clear_error();
+
+    const int mt_gu = 2 * I / BM, mt_d = H / BM;
+    prof_before(TF_KERNEL_PERMUTE, stream);
+    k_group_rms<<<(T + 7) / 8, 256, 0, st>>>(static_cast<const uint16_t*>(x), T, H, 1e-6f, rms);
+    k_group_hist<<<1, 1024, 0, st>>>(idx, P, E, mt_gu, mt_d, counts, offsets, tiles_gu, tiles_d);
+    k_group_pos<<<E, 1024, 0, st>>>(idx, P, offsets, perm, inv);
+    k_group_inv_init<<<(P + 255) / 256, 256, 0, st>>>(idx, P, E, inv);
+    k_group_gather<<<(P + 7) / 8, 256, 0, st>>>(static_cast<const uint16_t*>(x), rms, perm, P, k, H, xp);
+    prof_after(TF_KERNEL_PERMUTE, stream);
+    if (cudaError_t e = cudaGetLastError()) return cuda_status(e, fn);
+
+    GemmParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    gp.ebase = base;
+    gp.estride = table->stride;
+    gp.E = E;
+    gp.counts = counts;
+    gp.offsets = offsets;
+    gp.err = err;
+
+    prof_before(TF_KERNEL_GEMM, stream);
+    gp.off_sb = lay.gu_sb;
+    gp.K = H;
+    gp.MT = mt_gu;
+    gp.tiles = tiles_gu;
+    gp.mode = 0;
+    gp.hout = hb;
+    gp.ldo = I;
+    k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmA_gu, tmB_gu, gp);
+    gp.off_sb = lay.d_sb;
+    gp.K = I;
+    gp.MT = mt_d;
+    gp.tiles = tiles_d;
+    gp.mode = 1;
+    gp.hout = nullptr;
+    gp.yout = y;
+    gp.ldo = H;
+    k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmA_d, tmB_d, gp);
+    prof_after(TF_KERNEL_GEMM, stream);
+    if (cudaError_t e = cudaGetLastError()) return cuda_status(e, fn);
+
+    prof_before(TF_KERNEL_COMBINE, stream);
+    k_group_combine<<<T, 256, 0, st>>>(static_cast<const uint16_t*>(x), y, inv, w, k, H, err,
+                                       static_cast<uint16_t*>(out), delta);
+    prof_after(TF_KERNEL_COMBINE, stream);
+    if (perm_out) cudaMemcpyAsync(perm_out, perm, (size_t)P * 4, cudaMemcpyDeviceToDevice, st);
+    if (counts_out) cudaMemcpyAsync(counts_out, counts, (size_t)E * 4, cudaMemcpyDeviceToDevice, st);
+    return cuda_status(cudaGetLastError(), fn);
 }
 
 }  // extern "C"

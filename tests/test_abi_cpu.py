@@ -116,10 +116,29 @@ def test_device_entry_points_reject_bad_arguments_before_launch():
     assert L.tf_layer_create(ctypes.byref(d), 1, 256, 1 << 30, ctypes.byref(h)) == 1
     assert b"shared" in L.tf_last_error()
     assert L.tf_layer_step(None, None, 0, 0, None, None, None, 1, None, 0, None, None, 0, None) == 1
+    # grouped path: shapes, aliasing, alignment and table kind are checked before any launch
+    t = B.ExpertTable(256, 3358720, None)
+    ws = B.tf_moe_grouped_workspace_bytes(4, 2816, 704, 128, 8)
+    grouped = L.tf_moe_ffn_grouped
+    assert grouped(256, 256, 4, ctypes.byref(t), 128, 256, 256, 8, 2816, 704, None, None, None, 256, ws, None) == 1
+    assert b"alias" in L.tf_last_error()
+    assert grouped(256, 512, 4, ctypes.byref(t), 128, 256, 256, 8, 2880, 704, None, None, None, 256, ws, None) == 1
+    assert grouped(256, 512, 4, ctypes.byref(t), 128, 256, 256, 33, 2816, 704, None, None, None, 256, ws, None) == 1
+    assert grouped(256, 512, 4, ctypes.byref(t), 128, 256, 256, 8, 2816, 704, None, None, None, 256, ws - 1,
+                   None) == 1
+    assert grouped(256, 512, 4, ctypes.byref(t), 128, 256, 256, 8, 2816, 704, None, None, None, 128, ws, None) == 1
+    tm = B.ExpertTable(256, 3358720, 512)   # a slot map: the grouped path takes resident experts only
+    assert grouped(256, 512, 4, ctypes.byref(tm), 128, 256, 256, 8, 2816, 704, None, None, None, 256, ws,
+                   None) == 5
 
 
 def test_workspace_sizes():
     assert B.tf_router_workspace_bytes(1, 128) == 256 + 512
+    # grouped: error word, routing tables, permuted activations, h and y for T*k rows
+    T, k, H, I, E = 4096, 8, 2816, 704, 128
+    P = T * k
+    assert B.tf_moe_grouped_workspace_bytes(T, H, I, E, k) >= P * H * 2 + P * I * 2 + P * H * 4
+    assert B.tf_moe_grouped_workspace_bytes(T, H, I, 2000, k) == 0
     assert B.tf_moe_decode_workspace_bytes(2816, 704, 8) == 8 * 704 * 4
     d = B.layer_desc(2816, 704, 128, 8, 2112, 16, 16, 16, 16, B.ExpertTable(16, 16, None))
     assert B.tf_layer_workspace_bytes(d, 1) > 8 * 704 * 4 + 2112 * 4
