@@ -236,6 +236,121 @@ def run_ours(args, rank, world):
     return ms, prof, clocks, gpu_launches, e2e_s, e2e_steps
 
 
+# ------------------------------------------------------------------ prefill-shaped layer (grouped path)
+
+PREFILL_T = 4096
+PREFILL_FLOP = 2 * PREFILL_T * K_ACT * (2 * I * H + H * I)   # 389.8 GFLOP: gate/up + down GEMMs
+PREFILL_WORKLOAD = ("prefill-shaped MoE layer: 4096 tokens x H=2816, 128 experts of I=704 (int4 g64, fp16 scale+bias), "
+                    "top-8 of router logits + Zipf(1.2) popularity bias, grouped dequant-to-bf16 tcgen05 GEMMs with "
+                    "fp32 accumulation, weighted combine; seed 4")
+
+
+def tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["bf16_tflops"]), "measured (bf16_tflops, burst)"
+    return 1800.0, "fallback"
+
+
+def prefill_cpu_baseline(seed, x_bits, idx, w, n_tokens=2):
+    """The oracle (bf16-operand reading) on n_tokens tokens of the layer; tok/s."""
+    import oracle as O
+    import workload as W
+    O.build()
+    elapsed = 0.0
+    for t in range(n_tokens):
+        experts = W.experts_parallel(seed, 0, idx[t], H, I)   # generation is not timed
+        t0 = time.perf_counter()
+        r = O.rms_scale(x_bits[t])
+        O.layer_combine(x_bits[t], r, experts, w[t], None, bf16_ops=True)
+        elapsed += time.perf_counter() - t0
+    return {"value": n_tokens / elapsed, "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "sample": "%d of the 4096 tokens (all 8 experts each), single-threaded fp32 C oracle in its "
+                      "bf16-operand reading; expert generation not timed" % n_tokens}
+
+
+def run_prefill(args):
+    import torch
+    import bit_expert_streaming_layer_b300 as B
+    import workload as W
+    from workload.model import _u16_to_bf16_tensor, bf16_bits, hidden_tensor, pack_layer_experts
+
+    seed, T = 4, PREFILL_T
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    slot = B.tf_expert_slot_bytes(H, I)
+    host = torch.empty(E * slot, dtype=torch.uint8, pin_memory=True)
+    pack_layer_experts(seed, 0, E, H, I, host)
+    experts = host.to(dev)
+    table = B.expert_table(experts, slot)
+    Wr = _u16_to_bf16_tensor(W.router_weights(seed, 0, E, H)).to(dev)
+    bias = torch.from_numpy(W.zipf_bias(seed, 0, E, 1.2)[0]).to(dev)
+    x = hidden_tensor(seed, 0, T, H, device=dev)
+    out = torch.empty_like(x)
+    idx = torch.empty(T, K_ACT, dtype=torch.int32, device=dev)
+    w = torch.empty(T, K_ACT, dtype=torch.float32, device=dev)
+    rws = torch.zeros(B.tf_router_workspace_bytes(T, E), dtype=torch.uint8, device=dev)
+    gws = torch.zeros(B.tf_moe_grouped_workspace_bytes(T, H, I, E, K_ACT), dtype=torch.uint8, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        B.tf_router_topk(x, T, H, Wr, E, bias, 0, K_ACT, idx, w, None, None, rws, rws.numel(), stream)
+        B.tf_moe_ffn_grouped(x, out, T, table, E, idx, w, K_ACT, H, I, None, None, counts, gws, gws.numel(), stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(0)
+    sampler.start()
+    B.tf_profile_begin(args.steps)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    prof = B.tf_profile_end()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    gemm_ms = prof["gemm"][0] / max(1, min(prof["gemm"][1], args.steps))
+    peak, peak_kind = tensor_peak()
+    achieved = PREFILL_FLOP / (gemm_ms / 1e3) / 1e12
+    cnt = counts.cpu().numpy()
+    # end to end: host tokens in, host outputs back, every step
+    hx = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
+    hy = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
+    hx.copy_(x.cpu())
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        x.copy_(hx, non_blocking=True)
+        step()
+        hy.copy_(out, non_blocking=True)
+        stream.synchronize()
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    line = {
+        "metric": "prefill-shaped MoE layer tok/s (1 B300)", "value": round(T / (ms / 1e3), 1), "unit": "tok/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": PREFILL_WORKLOAD, "tokens": T, "l2": "inputs 0.4 GB of experts + 0.6 GB workspace, "
+                   "far above the 126 MB L2"},
+        "roofline": {"bound": "tensor", "kernel": "gemm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "flop_per_launch_pair": PREFILL_FLOP, "traffic": None},
+        "kernels": {k: {"event_ms_total": round(v[0], 4), "launches": int(v[1])} for k, v in prof.items() if v[1]},
+        "expert_load": {"max_tokens": int(cnt.max()), "experts_used": int((cnt > 0).sum())},
+        "gpu_launches": int(sum(v[1] for v in prof.values())),
+        "clocks": clocks,
+        "e2e": {"value": round(T / e2e_s, 1), "unit": "tok/s", "h2d_bytes_per_step": T * H * 2,
+                "d2h_bytes_per_step": T * H * 2},
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = prefill_cpu_baseline(seed, bf16_bits(x), idx.cpu().numpy(), w.cpu().numpy())
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -250,6 +365,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefetch", action="store_true",
                     help="fused path: prefetch the next layer's shared weights into L2 (measured slower)")
+    ap.add_argument("--workload", choices=["decode", "prefill"], default="decode",
+                    help="decode: the 30-layer decode stack (the headline line); prefill: the 4096-token grouped layer")
     ap.add_argument("--layers", type=int, default=L,
                     help="stack depth; the benchmark workload is 30, fewer only for small profiling captures")
     args = ap.parse_args()
@@ -274,6 +391,11 @@ def main():
                 "cpu_baseline": {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")},
                 "e2e": {"value": base["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
+        return
+
+    if args.workload == "prefill":
+        if rank == 0:
+            run_prefill(args)
         return
 
     if world > 1:
