@@ -14,26 +14,31 @@
 //   router : one row of W_r (bf16), fixed-order dot product -> one logit
 //   sgu    : one shared gate/up row pair (bf16, two stages) -> one h_shared
 //   rgu    : two gate/up row pairs of one selected expert (int4) -> two h_routed
-//   down   : two output rows: shared down (bf16, two stages) and the eight
-//            experts' down rows (int4, one stage), weighted combine, residual
-//            add, bf16 output
+//   down   : two output rows: shared down (bf16, two stages, needs h_shared)
+//            then the eight experts' down rows (int4, one stage, needs
+//            h_routed), weighted combine, residual add, bf16 output
 // A worker only blocks when its next copy needs the layer's top-8 experts.
+// Because the shared-down rows only need h_shared, which is complete long
+// before h_routed, they are computed while the routed gate/up work finishes,
+// and the routed-down copies are already in flight when h_routed is ready.
 //
-// Synchronisation. Every value that crosses CTAs (router logits, h, the layer
-// output) is published as one 32- or 64-bit word that carries the value and a
-// tag (launch epoch x 64 + layer); a reader polls the words it needs until all
-// tags are current. No fence is on the dependency chain: GPU-scope fences cost
-// microseconds while the SM's memory pipeline is full of weight copies. Two
-// relaxed counters per layer (bumped once per CTA, without ordering) only tell
-// the readers when polling is worth starting. Four control warps per CTA poll and stage: warp 0 stages the
-// layer input (x, r, n = r x) and computes the CTA's own copy of the top-8 from
-// the tagged logits, and warps 0..3 stage h for the down projections; each
-// stage is published to the workers with an mbarrier. The epoch lives in the
-// workspace; CTA 0 advances it once the last layer's output is complete, so a
-// launch needs nothing from the host but its pointers.
+// Synchronisation. Every value that crosses CTAs is published as a word that
+// carries its own tag, and a reader checks the tags of the words it needs:
+// router logits as 64-bit (tag, fp32) words, the layer output as 32-bit
+// (tag, bf16) words, h as fp32 words whose 4 lowest mantissa bits hold the tag
+// (a perturbation of at most 15 ulp). No fence is on the dependency chain:
+// GPU-scope fences cost microseconds while the SM's memory pipeline is full of
+// weight copies. Relaxed counters (bumped once per CTA per phase, unordered)
+// only tell the readers when to look. Four control warps per CTA do the
+// looking: they bring the whole tagged block (x, logits, h_shared, h_routed)
+// into shared memory with one bulk copy, check the tags in place (copying
+// again while any is stale), and publish to the workers with an mbarrier.
+// Control warp 0 also computes the CTA's own copy of the top-8. The epoch
+// lives in the workspace; CTA 0 advances it once the last layer's output is
+// complete, so a launch needs nothing from the host but its pointers.
 //
-// While a layer runs, each worker prefetches into L2 the data-independent
-// weights (router rows, shared expert) of its tasks in the next layer.
+// Optionally each worker prefetches into L2 the data-independent weights
+// (router rows, shared expert) of its tasks in the next layer.
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -73,29 +78,30 @@ constexpr int RGU_BYTES = 4 * GU_ROW + 4 * GU_SB;   // 6336
 constexpr int DN_SB_OFF = K * 2 * D_ROW;            // 5632
 constexpr int DN_BYTES = DN_SB_OFF + K * 4 * D_SB;  // 7040
 constexpr int H_FLOATS = K * I + S;                 // h_routed then h_shared
-constexpr int H_QUARTER = H_FLOATS / NCTRL;         // 1936 words per control warp
 constexpr unsigned long long TIMEOUT_NS = 2000000000ull;  // 2 s per wait
 constexpr uint32_t SUSPEND_NS = 1000;      // suspend hint of a blocking mbarrier test
-constexpr uint32_t HINT_SLEEP_NS = 256;    // pause between two reads of a hint counter
+constexpr uint32_t HINT_SLEEP_NS = 64;     // pause between two reads of a hint counter
+constexpr int CTRL_BAR = 1;                // named barrier of the control warps
 static_assert(HW == 32 * WPL, "lane ownership of the K = H words");
 static_assert(ROW_BF <= STAGE && RGU_BYTES <= STAGE && DN_BYTES <= STAGE && SROW_BF <= STAGE, "stage size");
-static_assert(H_FLOATS % (8 * NCTRL) == 0 && (K * I) % 8 == 0, "h quarters hold whole 8-float words");
-static_assert((H_QUARTER / 2 + 31) / 32 <= 32 && (H / 4) / 32 <= 32, "poll masks fit 32 bits");
+static_assert((K * I) % (8 * NCTRL) == 0 && S % (8 * NCTRL) == 0, "control warps check whole 8-float words");
 
 // shared-memory layout
 constexpr int OFF_RING = 0;
 constexpr int OFF_XS = OFF_RING + NWORK * NS * STAGE;   // bf16 x [H]
 constexpr int OFF_N = OFF_XS + H * 2;                    // fp32 n [H]
 constexpr int OFF_SN = OFF_N + H * 4;                    // fp32 word sums of n [HW]
-constexpr int OFF_H = OFF_SN + HW * 4;                   // fp32 h_routed [K*I], h_shared [S]
+constexpr int OFF_H = OFF_SN + HW * 4;                   // tagged fp32 h_routed [K*I], h_shared [S]; also the
+                                                         // landing zone of the tagged layer input
 constexpr int OFF_SH = OFF_H + H_FLOATS * 4;             // fp32 word sums of h_routed [K*I/8]
-constexpr int OFF_Z = OFF_SH + (K * I / 8) * 4;          // top-k scratch: fp32 z [MAX_E], taken [MAX_E]
-constexpr int OFF_RT = OFF_Z + MAX_E * 5;                // routing cache [2 layers]: expert ptrs, weights, ids
+constexpr int OFF_Z = OFF_SH + (K * I / 8) * 4;          // tagged logits [MAX_E] (64-bit words), then top-k keys [MAX_E]
+constexpr int OFF_RT = OFF_Z + MAX_E * 12;               // routing cache [2 layers]: expert ptrs, weights, ids
 constexpr int RT_BYTES = 2 * (K * 8 + K * 4 + K * 4);
 constexpr int OFF_BAR = OFF_RT + RT_BYTES;               // mbarriers
-constexpr int N_BAR = NWORK * NS + 4;                    // stages, XREADY, TOPKREADY, HREADY, HHINT
-constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;            // r, epoch
-constexpr size_t SMEM_BYTES = OFF_MISC + 16;
+enum { B_X = NWORK * NS, B_K, B_HS, B_HR, B_LOAD, N_BAR };
+constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;            // r, epoch, CTA phase counters, stale count
+constexpr size_t SMEM_BYTES = OFF_MISC + 32;
+static_assert(H * 4 <= H_FLOATS * 4, "the tagged layer input fits the h area");
 static_assert(OFF_H % 16 == 0 && OFF_N % 16 == 0 && OFF_RT % 16 == 0 && OFF_BAR % 8 == 0 && OFF_Z % 16 == 0,
               "alignment");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -110,15 +116,16 @@ struct LayerDesc {
     const int32_t* slot_map;
     const float* bias;
     unsigned long long* zt;   // tagged logits [E]: (tag << 32) | fp32 bits
-    unsigned long long* ht;   // tagged h [H_FLOATS]: routed [K*I] then shared [S]
+    uint32_t* ht;             // tagged h [H_FLOATS]: routed [K*I] then shared [S], tag in the 4 low mantissa bits
     uint32_t* xt;             // tagged output [H]: (tag16 << 16) | bf16
     float* logits;            // plain copies for inspection, written by CTA 0
     int32_t* idx;
     float* w;
     uint16_t* act_out;        // plain bf16 output (the last layer also writes the call's `out`)
-    uint32_t* cnt_z;          // router rows of this layer scored (pacing hint, += E per launch)
-    uint32_t* cnt_h;          // CTAs whose h tasks of this layer are done (pacing hint, += gridDim per launch)
-    uint32_t* cnt_out;        // CTAs whose output rows of this layer are done (same)
+    uint32_t* cnt_z;          // router rows scored (pacing hint, += E per launch)
+    uint32_t* cnt_hs;         // CTAs whose shared gate/up tasks are done (+= gridDim per launch)
+    uint32_t* cnt_hr;         // CTAs whose routed gate/up tasks are done (+= gridDim per launch)
+    uint32_t* cnt_out;        // CTAs whose output rows are done (+= gridDim per launch)
     int E;
     float eps;
     unsigned long long off_gu_sb, off_d_codes, off_d_sb;
@@ -138,13 +145,13 @@ struct Params {
 // Trace slots per (layer, CTA) (ns stamps of %globaltimer), written when
 // Params::trace is set: trace[(layer * TRACE_CTAS + cta) * TRACE_SLOTS + slot].
 enum {
-    TR_X_READY = 0,      // control warp 0 saw the whole layer input
+    TR_X_READY = 0,      // the control warps hold the whole layer input
     TR_X_STAGED = 1,     // ... published x, r, n
-    TR_Z_READY = 2,      // ... saw all router logits
+    TR_Z_READY = 2,      // ... hold all router logits
     TR_TOPK = 3,         // ... published the top-k
-    TR_H_HINT = 4,       // ... saw the h hint counter complete
-    TR_H_STAGED = 5,     // ... staged its quarter of h
-    TR_CTA_H_DONE = 6,   // the CTA's last worker finished its h-producing items
+    TR_HS_STAGED = 4,    // ... published h_shared
+    TR_HR_STAGED = 5,    // ... published h_routed
+    TR_CTA_HR_DONE = 6,  // the CTA's last worker finished its routed gate/up tasks
     TR_CTA_OUT = 7,      // the CTA's last worker finished the layer
     TRACE_SLOTS = 8,
     TRACE_CTAS = 256
@@ -192,6 +199,11 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         "l"(src), "r"(bytes), "r"(bar), "l"(pol)
         : "memory");
 }
+__device__ __forceinline__ void bulk_g2s_plain(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
@@ -232,6 +244,9 @@ __device__ __forceinline__ void st_relaxed_u64(void* p, unsigned long long v) {
 __device__ __forceinline__ void st_relaxed_v2u64(void* p, unsigned long long a, unsigned long long b) {
     asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1,%2};" ::"l"(p), "l"(a), "l"(b) : "memory");
 }
+__device__ __forceinline__ void st_relaxed_v2u32(void* p, uint32_t a, uint32_t b) {
+    asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
 __device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -265,61 +280,6 @@ __device__ __forceinline__ bool warp_wait_mbar(uint32_t bar, uint32_t parity, ui
     return __shfl_sync(FULL, (int)ok, 0) != 0;
 }
 
-// Pacing of a warp polling tagged data; gives up (error recorded) after TIMEOUT_NS.
-struct Poll {
-    uint64_t t0;
-    int rounds;
-    __device__ void start() {
-        t0 = gtimer();
-        rounds = 0;
-    }
-    // After a round: true = poll again, false = done (nothing pending) or give up.
-    __device__ bool again(bool pending_any, uint32_t* err, int lane) {
-        if (!pending_any) return false;
-        ++rounds;
-        int stop = 0;
-        if (lane == 0 && (rounds & 15) == 0) {
-            if (err_set(err)) {
-                stop = 1;
-            } else if (gtimer() - t0 > TIMEOUT_NS) {
-                atomicOr(err, ERR_TIMEOUT);
-                stop = 1;
-            }
-        }
-        __nanosleep(rounds < 8 ? 64 : 256);
-        return __shfl_sync(FULL, stop, 0) == 0;
-    }
-};
-
-// Wait (one warp) until the hint counter reaches target (modular u32 compare).
-// The counter only paces the polling of tagged data; it orders nothing.
-__device__ bool wait_hint(const uint32_t* cnt, uint32_t target, uint32_t* err, int lane) {
-    int st = 0;  // 0 waiting, 1 reached, 2 give up
-    if (lane == 0) {
-        const uint64_t t0 = gtimer();
-        for (uint32_t n = 0;; ++n) {
-            if ((int32_t)(ld_relaxed_u32(cnt) - target) >= 0) { st = 1; break; }
-            __nanosleep(HINT_SLEEP_NS);
-            if ((n & 15u) == 15u) {
-                if (err_set(err)) { st = 2; break; }
-                if (gtimer() - t0 > TIMEOUT_NS) { atomicOr(err, ERR_TIMEOUT); st = 2; break; }
-            }
-        }
-    }
-    return __shfl_sync(FULL, st, 0) == 1;
-}
-
-// A worker finished a phase of a layer: count it in the CTA; the CTA's last
-// worker bumps the grid-wide hint counter (relaxed, no fence).
-__device__ __forceinline__ void signal_phase(const Params& P, int l, int slot, uint32_t* cta_cnt, uint32_t* gcnt,
-                                             int lane) {
-    __syncwarp();
-    if (lane == 0 && (atomicAdd(cta_cnt, 1u) + 1u) % NWORK == 0) {
-        red_relaxed_add(gcnt, 1u);
-        trace_at(P, l, slot);
-    }
-    __syncwarp();
-}
 
 // ------------------------------------------------------------------ task lists
 
@@ -489,14 +449,14 @@ __device__ __forceinline__ void warp_sum4(float& a, float& b, float& c, float& d
 // sum_k W[k] n[k] over a bf16 row of K = H (16-byte chunk w covers n[8w..8w+7]).
 __device__ __forceinline__ float row_bf16(const unsigned char* row, const float* n, int lane) {
     const float4* n4 = reinterpret_cast<const float4*>(n);
-    unsigned long long acc[2] = {0ull, 0ull};
-#pragma unroll
+    unsigned long long acc = 0ull;
+#pragma unroll 1
     for (int m = 0; m < WPL; ++m) {
         const int w = lane + 32 * m;
         const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * w);
-        acc[m & 1] = dot8_bf16_2(v, n4[2 * w], n4[2 * w + 1], acc[m & 1]);
+        acc = dot8_bf16_2(v, n4[2 * w], n4[2 * w + 1], acc);
     }
-    return warp_sum(sum2(acc[0]) + sum2(acc[1]));
+    return warp_sum(sum2(acc));
 }
 
 // Four int4 rows of K = H at once (codes: 4 rows of HW words; sb: 4 rows of H/64
@@ -506,7 +466,7 @@ __device__ __forceinline__ float4 rows4_int4(const uint32_t* codes, const uint32
     const float4* n4 = reinterpret_cast<const float4*>(n);
     constexpr int SBW = GU_SB / 4;
     float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-#pragma unroll
+#pragma unroll 1
     for (int m = 0; m < WPL; ++m) {
         const int w = lane + 32 * m, g = w >> 3;
         const float4 na = n4[2 * w], nb = n4[2 * w + 1];
@@ -520,66 +480,135 @@ __device__ __forceinline__ float4 rows4_int4(const uint32_t* codes, const uint32
     return make_float4(a0, a1, a2, a3);
 }
 
-// ---- control warp 0: the layer input. Wait for every tagged output word of the
-// previous layer (or take the call's x), then publish x (bf16), r, n = r x and the
-// word sums of n.
-__device__ bool stage_x(const Params& P, int l, uint32_t prev_tag16, uint32_t hint_target, unsigned char* smem,
-                        int lane) {
-    uint16_t* xs = reinterpret_cast<uint16_t*>(smem + OFF_XS);
-    uint4* x4 = reinterpret_cast<uint4*>(xs);
-    constexpr int NCH = H / 4 / 32;   // 22 chunks of 4 tagged words per lane
-    if (l == 0) {
-        const uint4* s4 = reinterpret_cast<const uint4*>(P.x);
-#pragma unroll
-        for (int m = 0; m < WPL; ++m) x4[lane + 32 * m] = __ldcg(s4 + lane + 32 * m);
-    } else {
-        if (!wait_hint(P.layers[l - 1].cnt_out, hint_target, P.err, lane)) return false;
-        const uint32_t* src = P.layers[l - 1].xt;
-        uint32_t pend = (1u << NCH) - 1u;
-        Poll poll;
-        poll.start();
-        for (;;) {
-            // all loads of a round are issued before any is checked (one round trip per round)
-            constexpr int BATCH = 8;
-#pragma unroll
-            for (int m0 = 0; m0 < NCH; m0 += BATCH) {
-                const uint32_t pb = pend;
-                uint4 v[BATCH];
-#pragma unroll
-                for (int i = 0; i < BATCH; ++i)
-                    if (m0 + i < NCH && (pb >> (m0 + i) & 1u)) v[i] = ld_relaxed_v4(src + 4 * (lane + 32 * (m0 + i)));
-#pragma unroll
-                for (int i = 0; i < BATCH; ++i) {
-                    const int m = m0 + i;
-                    if (m < NCH && (pb >> m & 1u) && (v[i].x >> 16) == prev_tag16 && (v[i].y >> 16) == prev_tag16 &&
-                        (v[i].z >> 16) == prev_tag16 && (v[i].w >> 16) == prev_tag16) {
-                        reinterpret_cast<uint2*>(xs)[lane + 32 * m] = make_uint2(
-                            (v[i].x & 0xffffu) | (v[i].y << 16), (v[i].z & 0xffffu) | (v[i].w << 16));
-                        pend &= ~(1u << m);
-                    }
+// Wait (one warp) until the hint counter reaches target (modular u32 compare).
+// The counter only paces the reading of tagged data; it orders nothing.
+__device__ bool wait_hint(const uint32_t* cnt, uint32_t target, uint32_t* err, int lane) {
+    int st = 0;  // 1 reached, 2 give up
+    if (lane == 0) {
+        const uint64_t t0 = gtimer();
+        for (uint32_t n = 0;; ++n) {
+            if ((int32_t)(ld_relaxed_u32(cnt) - target) >= 0) {
+                st = 1;
+                break;
+            }
+            __nanosleep(HINT_SLEEP_NS);
+            if ((n & 63u) == 63u) {
+                if (err_set(err)) {
+                    st = 2;
+                    break;
+                }
+                if (gtimer() - t0 > TIMEOUT_NS) {
+                    atomicOr(err, ERR_TIMEOUT);
+                    st = 2;
+                    break;
                 }
             }
-            if (!poll.again(__any_sync(FULL, pend != 0), P.err, lane)) break;
         }
-        if (__any_sync(FULL, pend != 0)) return false;
-        if (lane == 0) trace_at(P, l, TR_X_READY);
+    }
+    return __shfl_sync(FULL, st, 0) == 1;
+}
+
+// A worker finished a phase of a layer: count it in the CTA; the CTA's last
+// worker bumps the grid-wide hint counter (relaxed, no fence).
+__device__ __forceinline__ void signal_phase(const Params& P, int l, int slot, uint32_t* cta_cnt, uint32_t* gcnt,
+                                             int lane) {
+    __syncwarp();
+    if (lane == 0 && (atomicAdd(cta_cnt, 1u) + 1u) % NWORK == 0) {
+        red_relaxed_add(gcnt, 1u);
+        if (slot >= 0) trace_at(P, l, slot);
     }
     __syncwarp();
-    const float eps = P.layers[l].eps;
-    float p = 0.0f;
-#pragma unroll 8
-    for (int k = lane; k < H; k += 32) {
-        const float v = bf2f(xs[k]);
-        p = fmaf(v, v, p);  // exact square: one rounding per term, as in the canonical sum
+}
+
+__device__ __forceinline__ uint32_t tag4_of(uint32_t epoch, int l) { return 1u + (epoch + (uint32_t)l) % 15u; }
+__device__ __forceinline__ uint32_t tagged_f(float v, uint32_t tag4) { return (__float_as_uint(v) & ~15u) | tag4; }
+__device__ __forceinline__ void ctrl_sync() { asm volatile("bar.sync %0, %1;" ::"n"(CTRL_BAR), "n"(NCTRL * 32) : "memory"); }
+
+// ---- control warps: bulk-copy a tagged block into shared memory and check it.
+// All four control warps call this with the same arguments; warp 0 issues the
+// copy, each warp checks its quarter with `check` (which returns the number of
+// stale words it saw and may unpack them), and the copy is repeated while any
+// word is stale. `loads` counts the uses of the load mbarrier.
+template <typename Check>
+__device__ bool ctrl_load(const Params& P, const void* src, uint32_t bytes, unsigned char* dst, uint32_t bar_load,
+                          int& loads, uint32_t* stale, int cw, int lane, Check check) {
+    const uint64_t t0 = gtimer();
+    for (int round = 0;; ++round) {
+        if (cw == 0 && lane == 0) {
+            stale[0] = 0u;
+            fence_proxy_async();  // the area was last read through the generic proxy
+            mbar_expect_tx(bar_load, bytes);
+            bulk_g2s_plain(smem_u32(dst), src, bytes, bar_load);
+        }
+        const bool got = warp_wait_mbar(bar_load, loads & 1, P.err, lane);
+        ++loads;
+        if (!got) {
+            if (lane == 0) atomicOr(&stale[1], 1u);
+        } else {
+            const uint32_t bad = check();
+            const uint32_t wbad = __reduce_add_sync(FULL, bad);
+            if (wbad && lane == 0) atomicAdd(&stale[0], wbad);
+        }
+        // only warp 0 decides a timeout, so that every control warp takes the same path
+        if (cw == 0 && lane == 0 && round > 16 && gtimer() - t0 > TIMEOUT_NS) {
+            atomicOr(&stale[1], 1u);
+            atomicOr(P.err, ERR_TIMEOUT);
+        }
+        ctrl_sync();
+        const uint32_t total = stale[0], abort_now = stale[1];
+        ctrl_sync();
+        if (abort_now) return false;
+        if (total == 0) return true;
+        if (round > 16) __nanosleep(256);
     }
-    p = warp_sum_canonical(p);
-    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(p, (float)H), eps)));
+}
+
+// The layer input: the tagged output of the previous layer (or the call's x)
+// -> x (bf16), r, n = r x and the word sums of n; all four control warps.
+__device__ bool stage_x(const Params& P, int l, uint32_t epoch, uint32_t hint_target, unsigned char* smem,
+                        uint32_t bar_load, int& loads, uint32_t* stale, int cw, int lane) {
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem + OFF_XS);
+    if (l == 0) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(P.x);
+        for (int c = cw * 32 + lane; c < H / 8; c += NCTRL * 32) reinterpret_cast<uint4*>(xs)[c] = __ldcg(s4 + c);
+    } else {
+        if (cw == 0 && !wait_hint(P.layers[l - 1].cnt_out, hint_target, P.err, lane) && lane == 0)
+            atomicOr(&stale[1], 1u);  // tells the other control warps to stop
+        ctrl_sync();
+        if (stale[1]) return false;
+        const uint32_t tag16 = (epoch * 64u + (uint32_t)(l - 1)) & 0xffffu;
+        unsigned char* land = smem + OFF_H;
+        auto check = [&]() -> uint32_t {
+            uint32_t bad = 0;
+            for (int c = cw * 32 + lane; c < H / 4; c += NCTRL * 32) {  // 4 tagged words per chunk
+                const uint4 v = reinterpret_cast<const uint4*>(land)[c];
+                bad += ((v.x >> 16) != tag16) + ((v.y >> 16) != tag16) + ((v.z >> 16) != tag16) +
+                       ((v.w >> 16) != tag16);
+                reinterpret_cast<uint2*>(xs)[c] = make_uint2((v.x & 0xffffu) | (v.y << 16), (v.z & 0xffffu) | (v.w << 16));
+            }
+            return bad;
+        };
+        if (!ctrl_load(P, P.layers[l - 1].xt, H * 4, land, bar_load, loads, stale, cw, lane, check)) return false;
+        if (cw == 0 && lane == 0) trace_at(P, l, TR_X_READY);
+    }
+    ctrl_sync();
+    float* rs = reinterpret_cast<float*>(smem + OFF_MISC);
+    if (cw == 0) {
+        float p = 0.0f;
+#pragma unroll 8
+        for (int k = lane; k < H; k += 32) {
+            const float v = bf2f(xs[k]);
+            p = fmaf(v, v, p);  // exact square: one rounding per term, as in the canonical sum
+        }
+        p = warp_sum_canonical(p);
+        if (lane == 0) rs[0] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(p, (float)H), P.layers[l].eps)));
+    }
+    ctrl_sync();
+    const float r = rs[0];
     float* n = reinterpret_cast<float*>(smem + OFF_N);
     float* sn = reinterpret_cast<float*>(smem + OFF_SN);
-#pragma unroll
-    for (int m = 0; m < WPL; ++m) {
-        const int w = lane + 32 * m;
-        const uint4 v = x4[w];
+    for (int w = cw * 32 + lane; w < HW; w += NCTRL * 32) {
+        const uint4 v = reinterpret_cast<const uint4*>(xs)[w];
         const float4 a = make_float4(__fmul_rn(r, bf_lo(v.x)), __fmul_rn(r, bf_hi(v.x)), __fmul_rn(r, bf_lo(v.y)),
                                      __fmul_rn(r, bf_hi(v.y)));
         const float4 b = make_float4(__fmul_rn(r, bf_lo(v.z)), __fmul_rn(r, bf_hi(v.z)), __fmul_rn(r, bf_lo(v.w)),
@@ -588,87 +617,69 @@ __device__ bool stage_x(const Params& P, int l, uint32_t prev_tag16, uint32_t hi
         reinterpret_cast<float4*>(n)[2 * w + 1] = b;
         sn[w] = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
     }
-    if (lane == 0) reinterpret_cast<float*>(smem + OFF_MISC)[0] = r;
-    __syncwarp();
+    ctrl_sync();
     return true;
 }
 
-// ---- control warp 0: the CTA's copy of the layer's top-k from the tagged logits.
+// Control warp 0: the CTA's copy of the layer's top-k from the tagged logits.
+// Each lane sorts its own candidates once (larger logit first, equal -> lower
+// index, NaN lowest, -0 == +0); each of the k rounds then takes the best lane
+// head with two warp reductions and the winning lane shifts its list.
 __device__ bool route_layer(const Params& P, int l, uint32_t tag, uint32_t epoch_x_e, unsigned char* smem, Route* rt,
-                            bool publish, int lane) {
+                            bool publish, uint32_t bar_load, int& loads, int lane) {
     const LayerDesc& D = P.layers[l];
-    float* zs = reinterpret_cast<float*>(smem + OFF_Z);
     if (!wait_hint(D.cnt_z, epoch_x_e, P.err, lane)) return false;
-    constexpr int NCH = MAX_E / 2 / 32;   // <= 4 chunks of 2 tagged logits per lane
-    const int nch = D.E / 2;
-    uint32_t pend = 0;
-#pragma unroll
-    for (int m = 0; m < NCH; ++m)
-        if (lane + 32 * m < nch) pend |= 1u << m;
-    Poll poll;
-    poll.start();
+    const unsigned long long* zt = reinterpret_cast<const unsigned long long*>(smem + OFF_Z);
+    const uint64_t t0 = gtimer();
     for (;;) {
-        const uint32_t pb = pend;
-        unsigned long long va[NCH], vb[NCH];
-#pragma unroll
-        for (int m = 0; m < NCH; ++m)
-            if (pb >> m & 1u) ld_relaxed_v2u64(D.zt + 2 * (lane + 32 * m), va[m], vb[m]);
-#pragma unroll
-        for (int m = 0; m < NCH; ++m) {
-            if ((pb >> m & 1u) && (uint32_t)(va[m] >> 32) == tag && (uint32_t)(vb[m] >> 32) == tag) {
-                const int ch = lane + 32 * m;
-                zs[2 * ch] = __uint_as_float((uint32_t)va[m]);
-                zs[2 * ch + 1] = __uint_as_float((uint32_t)vb[m]);
-                pend &= ~(1u << m);
-            }
+        if (lane == 0) {
+            fence_proxy_async();
+            mbar_expect_tx(bar_load, (uint32_t)D.E * 8);
+            bulk_g2s_plain(smem_u32(smem + OFF_Z), D.zt, (uint32_t)D.E * 8, bar_load);
         }
-        if (!poll.again(__any_sync(FULL, pend != 0), P.err, lane)) break;
+        if (!warp_wait_mbar(bar_load, loads & 1, P.err, lane)) return false;
+        ++loads;
+        int bad = 0;
+        for (int j = lane; j < D.E; j += 32) bad |= (uint32_t)(zt[j] >> 32) != tag;
+        if (!__any_sync(FULL, bad)) break;
+        __nanosleep(128);
+        if (gtimer() - t0 > TIMEOUT_NS) {
+            if (lane == 0) atomicOr(P.err, ERR_TIMEOUT);
+            return false;
+        }
     }
-    if (__any_sync(FULL, pend != 0)) return false;
     if (lane == 0) trace_at(P, l, TR_Z_READY);
-    __syncwarp();
-    const int s = l & 1;
-    // Top-k by rounds of two warp reductions: the largest remaining logit (as an
-    // order-preserving key, -0 == +0, NaN lowest), then the lowest index holding it.
-    constexpr int PER = MAX_E / 32;
-    uint32_t key[PER];
-    float val[PER];
-    uint32_t alive = 0;
-#pragma unroll
-    for (int m = 0; m < PER; ++m) {
-        const int j = lane + 32 * m;
-        val[m] = j < D.E ? zs[j] : 0.0f;
-        const float v = val[m] + 0.0f;  // -0 -> +0
+    // order-preserving keys in place of the tags (larger logit first, -0 == +0,
+    // NaN lowest but above "taken" = 0); every round takes the best remaining key
+    // and the lowest index holding it with two warp reductions
+    uint32_t* keys = reinterpret_cast<uint32_t*>(smem + OFF_Z) + 2 * MAX_E;  // after the tagged words
+    for (int j = lane; j < D.E; j += 32) {
+        const float v = __uint_as_float((uint32_t)zt[j]) + 0.0f;
         const uint32_t u = __float_as_uint(v);
-        key[m] = isnan(v) ? 0u : ((u & 0x80000000u) ? ~u : (u | 0x80000000u));
-        if (j < D.E) alive |= 1u << m;
+        keys[j] = isnan(v) ? 1u : ((u & 0x80000000u) ? ~u : (u | 0x80000000u));
     }
+    __syncwarp();
     float selz = 0.0f;
     int sel = -1;
+#pragma unroll 1
     for (int i = 0; i < K; ++i) {
         uint32_t bk = 0u;
         int bi = 0x7fffffff;
-#pragma unroll
-        for (int m = 0; m < PER; ++m) {
-            const int j = lane + 32 * m;
-            if ((alive >> m & 1u) && (key[m] > bk || (key[m] == bk && j < bi))) {
-                bk = key[m];
+#pragma unroll 1
+        for (int j = lane; j < D.E; j += 32) {
+            const uint32_t kj = keys[j];
+            if (kj > bk) {  // j increases: equal keys keep the lower index
+                bk = kj;
                 bi = j;
             }
         }
         const uint32_t kmax = __reduce_max_sync(FULL, bk);
-        const int imin = (int)__reduce_min_sync(FULL, (uint32_t)(bk == kmax ? bi : 0x7fffffff));
-        float vsel = 0.0f;
-#pragma unroll
-        for (int m = 0; m < PER; ++m)
-            if (lane + 32 * m == imin) {
-                vsel = val[m];
-                alive &= ~(1u << m);
-            }
-        vsel = __shfl_sync(FULL, vsel, imin & 31);
+        const int imin = (int)__reduce_min_sync(FULL, bk == kmax ? (uint32_t)bi : 0x7fffffffu);
+        if (lane == (imin & 31)) keys[imin] = 0u;
+        __syncwarp();
         if (lane == i) {
             sel = imin;
-            selz = vsel;
+            selz = __uint_as_float((uint32_t)zt[imin]);
         }
     }
     // softmax over the selected logits, summed in top-k order
@@ -680,25 +691,24 @@ __device__ bool route_layer(const Params& P, int l, uint32_t tag, uint32_t epoch
     const float ev = lane < K ? expf(__fsub_rn(selz, zmax)) : 0.0f;
     float esum = 0.0f;
     for (int i = 0; i < K; ++i) esum = __fadd_rn(esum, __shfl_sync(FULL, ev, i));
-    if (lane < K) {
-        rt->id[s][lane] = sel;
-        rt->w[s][lane] = __fdiv_rn(ev, esum);
-    }
-    __syncwarp();
+    const int s = l & 1;
     int bad = 0;
     if (lane < K) {
-        int e = rt->id[s][lane];
+        const float wv = __fdiv_rn(ev, esum);
+        rt->id[s][lane] = sel;
+        rt->w[s][lane] = wv;
+        int e = sel;
         bad = (unsigned)e >= (unsigned)D.E;
         if (bad) e = 0;  // never form an address from an out-of-range id
         if (D.slot_map) e = __ldcg(D.slot_map + e);
         rt->ep[s][lane] = D.ebase + (size_t)e * D.estride;
         if (publish) {
-            D.idx[lane] = rt->id[s][lane];
-            D.w[lane] = rt->w[s][lane];
+            D.idx[lane] = sel;
+            D.w[lane] = wv;
         }
     }
     if (publish)
-        for (int j = lane; j < D.E; j += 32) D.logits[j] = zs[j];
+        for (int j = lane; j < D.E; j += 32) D.logits[j] = __uint_as_float((uint32_t)zt[j]);
     if (__any_sync(FULL, bad)) {
         if (lane == 0) atomicOr(P.err, ERR_BAD_ID);
         return false;
@@ -707,64 +717,37 @@ __device__ bool route_layer(const Params& P, int l, uint32_t tag, uint32_t epoch
     return true;
 }
 
-// ---- control warps 0..3: quarter q of h (tagged fp32) -> shared memory, plus the
-// word sums of its h_routed part.
-__device__ bool stage_h(const Params& P, int l, uint32_t tag, uint32_t hint_target, uint32_t bar_hh,
-                        unsigned char* smem, int q, int lane) {
+// h_shared or h_routed (tagged fp32 words) -> shared memory, in place, checked by
+// the four control warps; for h_routed also the word sums of each 8-float word.
+__device__ bool stage_h(const Params& P, int l, uint32_t tag4, const uint32_t* hint, uint32_t hint_target,
+                        bool routed, unsigned char* smem, uint32_t bar_load, int& loads, uint32_t* stale, int cw,
+                        int lane) {
     const LayerDesc& D = P.layers[l];
-    // control warp 0 reads the hint counter; warps 1..3 sleep on an mbarrier until it is reached
-    if (q == 0) {
-        if (!wait_hint(D.cnt_h, hint_target, P.err, lane)) return false;
-        if (lane == 0) {
-            mbar_arrive(bar_hh);
-            trace_at(P, l, TR_H_HINT);
+    if (cw == 0 && !wait_hint(hint, hint_target, P.err, lane) && lane == 0) atomicOr(&stale[1], 1u);
+    ctrl_sync();
+    if (stale[1]) return false;
+    const int w0 = routed ? 0 : K * I, nw = routed ? K * I : S;  // in floats
+    uint32_t* h = reinterpret_cast<uint32_t*>(smem + OFF_H) + w0;
+    auto check = [&]() -> uint32_t {
+        uint32_t bad = 0;
+        for (int c = cw * 32 + lane; c < nw / 4; c += NCTRL * 32) {
+            const uint4 v = reinterpret_cast<const uint4*>(h)[c];
+            bad += ((v.x & 15u) != tag4) + ((v.y & 15u) != tag4) + ((v.z & 15u) != tag4) + ((v.w & 15u) != tag4);
         }
-    } else if (!warp_wait_mbar(bar_hh, l & 1, P.err, lane)) {
+        return bad;
+    };
+    if (!ctrl_load(P, D.ht + w0, (uint32_t)nw * 4, reinterpret_cast<unsigned char*>(h), bar_load, loads, stale, cw,
+                   lane, check))
         return false;
-    }
-    float* h = reinterpret_cast<float*>(smem + OFF_H);
-    float* sh = reinterpret_cast<float*>(smem + OFF_SH);
-    constexpr int NCHQ = H_QUARTER / 2;              // 968 chunks of 2 tagged words
-    constexpr int NCH = (NCHQ + 31) / 32;            // 31 per lane
-    const int w0 = q * H_QUARTER;
-    uint32_t pend = 0;
-#pragma unroll
-    for (int m = 0; m < NCH; ++m)
-        if (lane + 32 * m < NCHQ) pend |= 1u << m;
-    Poll poll;
-    poll.start();
-    for (;;) {
-        // all loads of a batch are issued before any is checked
-        constexpr int BATCH = 8;
-#pragma unroll
-        for (int m0 = 0; m0 < NCH; m0 += BATCH) {
-            const uint32_t pb = pend;
-            unsigned long long va[BATCH], vb[BATCH];
-#pragma unroll
-            for (int i = 0; i < BATCH; ++i)
-                if (m0 + i < NCH && (pb >> (m0 + i) & 1u))
-                    ld_relaxed_v2u64(D.ht + w0 + 2 * (lane + 32 * (m0 + i)), va[i], vb[i]);
-#pragma unroll
-            for (int i = 0; i < BATCH; ++i) {
-                const int m = m0 + i;
-                if (m < NCH && (pb >> m & 1u) && (uint32_t)(va[i] >> 32) == tag && (uint32_t)(vb[i] >> 32) == tag) {
-                    *reinterpret_cast<float2*>(h + w0 + 2 * (lane + 32 * m)) =
-                        make_float2(__uint_as_float((uint32_t)va[i]), __uint_as_float((uint32_t)vb[i]));
-                    pend &= ~(1u << m);
-                }
-            }
+    if (routed) {
+        float* sh = reinterpret_cast<float*>(smem + OFF_SH);
+        const float4* h4 = reinterpret_cast<const float4*>(h);
+        for (int w8 = cw * 32 + lane; w8 < K * I / 8; w8 += NCTRL * 32) {
+            const float4 a = h4[2 * w8], b = h4[2 * w8 + 1];
+            sh[w8] = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
         }
-        if (!poll.again(__any_sync(FULL, pend != 0), P.err, lane)) break;
     }
-    if (__any_sync(FULL, pend != 0)) return false;
-    __syncwarp();
-    // word sums of h_routed for the 8-float words of this quarter
-    for (int w8 = w0 / 8 + lane; w8 < (w0 + H_QUARTER) / 8 && w8 < K * I / 8; w8 += 32) {
-        const float4 a = reinterpret_cast<const float4*>(h)[2 * w8];
-        const float4 b = reinterpret_cast<const float4*>(h)[2 * w8 + 1];
-        sh[w8] = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
-    }
-    __syncwarp();
+    ctrl_sync();
     return true;
 }
 
@@ -776,84 +759,98 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
     const int G = gridDim.x;
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    const uint32_t bar_x = smem_u32(&bars[NWORK * NS]);
-    const uint32_t bar_k = smem_u32(&bars[NWORK * NS + 1]);
-    const uint32_t bar_h = smem_u32(&bars[NWORK * NS + 2]);
-    const uint32_t bar_hh = smem_u32(&bars[NWORK * NS + 3]);
+    const uint32_t bar_x = smem_u32(&bars[B_X]);
+    const uint32_t bar_k = smem_u32(&bars[B_K]);
+    const uint32_t bar_hs = smem_u32(&bars[B_HS]);
+    const uint32_t bar_hr = smem_u32(&bars[B_HR]);
+    const uint32_t bar_load = smem_u32(&bars[B_LOAD]);
     Route* rt = reinterpret_cast<Route*>(smem + OFF_RT);
     uint32_t* s_epoch = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 4);
-    uint32_t* cta_cnt = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 8);  // [0] h phase, [1] output phase
+    uint32_t* cta_cnt = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 8);  // [0] hs, [1] hr, [2] out
+    uint32_t* stale = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 20);   // [0] stale words, [1] abort, [2] loads
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NWORK * NS; ++s) mbar_init(smem_u32(&bars[s]), 1);
         mbar_init(bar_x, 1);
         mbar_init(bar_k, 1);
-        mbar_init(bar_h, NCTRL);
-        mbar_init(bar_hh, 1);
+        mbar_init(bar_hs, 1);
+        mbar_init(bar_hr, 1);
+        mbar_init(bar_load, 1);
         *s_epoch = ld_relaxed_u32(P.epoch);
-        cta_cnt[0] = 0;
-        cta_cnt[1] = 0;
+        cta_cnt[0] = cta_cnt[1] = cta_cnt[2] = 0;
+        stale[0] = stale[1] = stale[2] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
     const uint32_t epoch = *s_epoch;
-    const uint32_t hint_target = epoch * (uint32_t)G;   // every launch adds G to each hint counter
+    const uint32_t hint_target = epoch * (uint32_t)G;   // every launch adds G to each per-CTA hint counter
     const int E = P.layers[0].E;
 
     if (warp < NCTRL) {
         // ================================================= control warps
+        const int cw = warp;
+        int loads = 0;
         bool ok = true;
         for (int l = 0; l < P.L && ok; ++l) {
+            const LayerDesc& D = P.layers[l];
             const uint32_t tag = epoch * 64u + (uint32_t)l;
-            if (warp == 0) {
-                ok = stage_x(P, l, (tag - 1u) & 0xffffu, hint_target, smem, lane);
-                if (!ok) break;
-                if (lane == 0) {
-                    mbar_arrive(bar_x);
-                    trace_at(P, l, TR_X_STAGED);
-                }
-                ok = route_layer(P, l, tag, epoch * (uint32_t)E, smem, rt, blockIdx.x == 0, lane);
-                if (!ok) break;
-                if (lane == 0) {
+            const uint32_t tag4 = tag4_of(epoch, l);
+            if (!(ok = stage_x(P, l, epoch, hint_target, smem, bar_load, loads, stale, cw, lane))) break;
+            if (cw == 0 && lane == 0) {
+                mbar_arrive(bar_x);
+                trace_at(P, l, TR_X_STAGED);
+            }
+            int rok = 1;
+            if (cw == 0) {
+                rok = route_layer(P, l, tag, epoch * (uint32_t)E, smem, rt, blockIdx.x == 0, bar_load, loads, lane);
+                if (rok && lane == 0) {
                     mbar_arrive(bar_k);
                     trace_at(P, l, TR_TOPK);
                 }
+                if (!rok && lane == 0) atomicOr(&stale[1], 1u);
+                if (lane == 0) stale[2] = (uint32_t)loads;  // route_layer's copies: warp 0 tells the others
             }
-            ok = stage_h(P, l, tag, hint_target, bar_hh, smem, warp, lane);
-            if (!ok) break;
-            if (lane == 0) {
-                mbar_arrive(bar_h);
-                if (warp == 0) trace_at(P, l, TR_H_STAGED);
+            ctrl_sync();
+            if (stale[1]) {
+                ok = false;
+                break;
+            }
+            loads = (int)stale[2];
+            if (!(ok = stage_h(P, l, tag4, D.cnt_hs, hint_target, false, smem, bar_load, loads, stale, cw, lane))) break;
+            if (cw == 0 && lane == 0) {
+                mbar_arrive(bar_hs);
+                trace_at(P, l, TR_HS_STAGED);
+            }
+            if (!(ok = stage_h(P, l, tag4, D.cnt_hr, hint_target, true, smem, bar_load, loads, stale, cw, lane))) break;
+            if (cw == 0 && lane == 0) {
+                mbar_arrive(bar_hr);
+                trace_at(P, l, TR_HR_STAGED);
             }
         }
         // CTA 0 advances the epoch once the last layer's output is complete
         if (ok && blockIdx.x == 0 && warp == 0 && wait_hint(P.layers[P.L - 1].cnt_out, hint_target, P.err, lane)) {
             const uint32_t* src = P.layers[P.L - 1].xt;
             const uint32_t tag16 = (epoch * 64u + (uint32_t)(P.L - 1)) & 0xffffu;
-            constexpr int NCH = H / 4 / 32;
-            uint32_t pend = (1u << NCH) - 1u;
-            Poll poll;
-            poll.start();
+            const uint64_t t0 = gtimer();
             for (;;) {
-                constexpr int BATCH = 8;
-#pragma unroll
-                for (int m0 = 0; m0 < NCH; m0 += BATCH) {
-                    const uint32_t pb = pend;
-                    uint4 v[BATCH];
-#pragma unroll
-                    for (int i = 0; i < BATCH; ++i)
-                        if (m0 + i < NCH && (pb >> (m0 + i) & 1u)) v[i] = ld_relaxed_v4(src + 4 * (lane + 32 * (m0 + i)));
-#pragma unroll
-                    for (int i = 0; i < BATCH; ++i)
-                        if (m0 + i < NCH && (pb >> (m0 + i) & 1u) && (v[i].x >> 16) == tag16 &&
-                            (v[i].y >> 16) == tag16 && (v[i].z >> 16) == tag16 && (v[i].w >> 16) == tag16)
-                            pend &= ~(1u << (m0 + i));
+                int bad = 0;
+                for (int c = lane; c < H / 4; c += 32) {
+                    const uint4 v = ld_relaxed_v4(src + 4 * c);
+                    bad |= ((v.x >> 16) != tag16) | ((v.y >> 16) != tag16) | ((v.z >> 16) != tag16) |
+                           ((v.w >> 16) != tag16);
                 }
-                if (!poll.again(__any_sync(FULL, pend != 0), P.err, lane)) break;
+                if (!__any_sync(FULL, bad)) {
+                    // the epoch counts launches (mod 2^32): hint targets epoch * G stay consistent with the
+                    // counters, and a tag epoch * 64 + layer only repeats 2^26 launches later
+                    if (lane == 0) st_relaxed_u32(P.epoch, epoch + 1u);
+                    break;
+                }
+                __nanosleep(256);
+                if (gtimer() - t0 > TIMEOUT_NS) {
+                    if (lane == 0) atomicOr(P.err, ERR_TIMEOUT);
+                    break;
+                }
             }
-            // the epoch counts launches (mod 2^32): hint targets epoch * G stay consistent with the
-            // counters, and a tag epoch * 64 + layer only repeats 2^26 launches later
-            if (!__any_sync(FULL, pend != 0) && lane == 0) st_relaxed_u32(P.epoch, epoch + 1u);
         }
         return;
     }
@@ -881,7 +878,6 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
     const float* n_s = reinterpret_cast<const float*>(smem + OFF_N);
     const float* sn_s = reinterpret_cast<const float*>(smem + OFF_SN);
     float r = 0.0f;
-    int h_seen = 0;  // layers whose staged h this warp has seen (phases are observed in order)
 
     // Layers whose top-k this warp has seen published. The routing mbarrier is
     // tested one phase at a time, in order: a parity test of a later phase
@@ -914,6 +910,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
     for (int l = 0; l < P.L && ok; ++l) {
         const LayerDesc& D = P.layers[l];
         const uint32_t tag = epoch * 64u + (uint32_t)l;
+        const uint32_t tag4 = tag4_of(epoch, l);
         const uint32_t tag16 = tag & 0xffffu;
         if (P.prefetch && lane == 0) prefetch_layer(c, l + 1 < P.L ? l + 1 : 0);
         try_issue();
@@ -921,15 +918,28 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
         r = reinterpret_cast<const float*>(smem + OFF_MISC)[0];
         const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem + OFF_XS);
         uint16_t* pout = l == P.L - 1 ? P.out : nullptr;
-        bool h_ready = false, h_signalled = false;
+        bool hs_sig = false, hr_sig = false, hs_ready = false, hr_ready = false;
         while (con.l == l) {
-            if (con.kind == T_DOWN && !h_ready) {
-                signal_phase(P, l, TR_CTA_H_DONE, &cta_cnt[0], D.cnt_h, lane);
-                h_signalled = true;
-                try_issue();
-                if (!(ok = warp_wait_mbar(bar_h, l & 1, P.err, lane))) break;
-                h_seen = l + 1;
-                h_ready = true;
+            // phase signals when the consume pointer leaves a kind of task
+            if (!hs_sig && con.kind > T_SGU) {
+                signal_phase(P, l, -1, &cta_cnt[0], D.cnt_hs, lane);
+                hs_sig = true;
+            }
+            if (!hr_sig && con.kind > T_RGU) {
+                signal_phase(P, l, TR_CTA_HR_DONE, &cta_cnt[1], D.cnt_hr, lane);
+                hr_sig = true;
+            }
+            if (con.kind == T_DOWN) {
+                if (con.sub < 2 && !hs_ready) {
+                    try_issue();
+                    if (!(ok = warp_wait_mbar(bar_hs, l & 1, P.err, lane))) break;
+                    hs_ready = true;
+                }
+                if (con.sub == 2 && !hr_ready) {
+                    try_issue();
+                    if (!(ok = warp_wait_mbar(bar_hr, l & 1, P.err, lane))) break;
+                    hr_ready = true;
+                }
             }
             // make sure the item is in flight, then wait for it
             try_issue();
@@ -954,7 +964,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
             if (con.kind == T_ROUTER) {
                 const uint16_t* wrow = reinterpret_cast<const uint16_t*>(st);
                 float d = 0.0f;
-#pragma unroll 8
+#pragma unroll 4
                 for (int k = lane; k < H; k += 32) d = fmaf(bf2f(wrow[k]), bf2f(xs[k]), d);  // exact products
                 d = warp_sum_canonical(d);
                 float z = __fmul_rn(r, d);
@@ -968,7 +978,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
                 if (con.sub == 0) {
                     carry0 = v;
                 } else if (lane == 0) {
-                    st_relaxed_u64(D.ht + K * I + (con.t - D.E), tag64(tag, gelu_tanh(carry0) * v));
+                    st_relaxed_u32(D.ht + K * I + (con.t - D.E), tagged_f(gelu_tanh(carry0) * v, tag4));
                 }
             } else if (con.kind == T_RGU) {
                 const int u = con.t - D.E - N_SGU;
@@ -977,34 +987,31 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
                 const uint32_t* sb = reinterpret_cast<const uint32_t*>(st + 4 * GU_ROW);
                 const float4 gu = rows4_int4(codes, sb, n_s, sn_s, lane);  // gate p0, up p0, gate p0+1, up p0+1
                 if (lane == 0)
-                    st_relaxed_v2u64(D.ht + (size_t)i * I + p0, tag64(tag, gelu_tanh(gu.x) * gu.y),
-                                     tag64(tag, gelu_tanh(gu.z) * gu.w));
+                    st_relaxed_v2u32(D.ht + (size_t)i * I + p0, tagged_f(gelu_tanh(gu.x) * gu.y, tag4),
+                                     tagged_f(gelu_tanh(gu.z) * gu.w, tag4));
             } else {
                 const int j0 = 2 * (con.t - D.E - N_SGU - N_RGU);
                 const float* hsh = reinterpret_cast<const float*>(smem + OFF_H) + K * I;
                 if (con.sub < 2) {
                     // shared down row j0 + sub (bf16, K = S): chunks ch = lane + 32 t, t < 9
-                    unsigned long long ac[2] = {0ull, 0ull};
-#pragma unroll
-                    for (int t = 0; t < (S / 8 + 31) / 32; ++t) {
-                        const int ch = lane + 32 * t;
-                        if (ch < S / 8) {
-                            const uint4 v = *reinterpret_cast<const uint4*>(st + 16 * ch);
-                            const float4 h0 = *reinterpret_cast<const float4*>(hsh + 8 * ch);
-                            const float4 h1 = *reinterpret_cast<const float4*>(hsh + 8 * ch + 4);
-                            ac[t & 1] = dot8_bf16_2(v, h0, h1, ac[t & 1]);
-                        }
+                    unsigned long long ac = 0ull;
+#pragma unroll 1
+                    for (int ch = lane; ch < S / 8; ch += 32) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(st + 16 * ch);
+                        const float4 h0 = *reinterpret_cast<const float4*>(hsh + 8 * ch);
+                        const float4 h1 = *reinterpret_cast<const float4*>(hsh + 8 * ch + 4);
+                        ac = dot8_bf16_2(v, h0, h1, ac);
                     }
-                    const float acc = warp_sum(sum2(ac[0]) + sum2(ac[1]));
+                    const float acc = warp_sum(sum2(ac));
                     if (con.sub == 0) carry0 = acc;
                     else carry1 = acc;
                 } else {
                     // the 8 experts' down rows j0, j0 + 1 (int4, K = I), weighted
                     const float* hr = reinterpret_cast<const float*>(smem + OFF_H);
                     const float* sh = reinterpret_cast<const float*>(smem + OFF_SH);
-                    float y0 = 0.0f, y1 = 0.0f, z0 = 0.0f, z1 = 0.0f;
+                    float y0 = 0.0f, y1 = 0.0f;
                     const int sbrow = j0 & 3;
-#pragma unroll
+#pragma unroll 1
                     for (int i = 0; i < K; ++i) {
                         const uint32_t* codes = reinterpret_cast<const uint32_t*>(st + i * 2 * D_ROW);
                         const uint32_t* sb = reinterpret_cast<const uint32_t*>(st + DN_SB_OFF + i * 4 * D_SB) +
@@ -1023,16 +1030,9 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
                             }
                         }
                         const float wi = rt->w[l & 1][i];
-                        if (i & 1) {
-                            z0 = fmaf(wi, p0, z0);
-                            z1 = fmaf(wi, p1, z1);
-                        } else {
-                            y0 = fmaf(wi, p0, y0);
-                            y1 = fmaf(wi, p1, y1);
-                        }
+                        y0 = fmaf(wi, p0, y0);
+                        y1 = fmaf(wi, p1, y1);
                     }
-                    y0 += z0;
-                    y1 += z1;
                     float dummy0 = 0.0f, dummy1 = 0.0f;
                     warp_sum4(y0, y1, dummy0, dummy1);
                     if (lane == 0) {
@@ -1051,19 +1051,18 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
             it_next(con, c);
         }
         if (!ok) break;
-        if (!h_signalled) signal_phase(P, l, TR_CTA_H_DONE, &cta_cnt[0], D.cnt_h, lane);
-        // observe this layer's routing and h phases even without items that needed them,
-        // so that later parity tests never run two phases behind
+        if (!hs_sig) signal_phase(P, l, -1, &cta_cnt[0], D.cnt_hs, lane);
+        if (!hr_sig) signal_phase(P, l, TR_CTA_HR_DONE, &cta_cnt[1], D.cnt_hr, lane);
+        // observe this layer's routing and h phases even without items that needed
+        // them, so that later parity tests never run two phases behind
         try_issue();
         if (!topk_known(l)) {
             if (!(ok = warp_wait_mbar(bar_k, l & 1, P.err, lane))) break;
             k_seen = l + 1;
         }
-        if (h_seen <= l) {
-            if (!(ok = warp_wait_mbar(bar_h, l & 1, P.err, lane))) break;
-            h_seen = l + 1;
-        }
-        signal_phase(P, l, TR_CTA_OUT, &cta_cnt[1], D.cnt_out, lane);
+        if (!hs_ready && !(ok = warp_wait_mbar(bar_hs, l & 1, P.err, lane))) break;
+        if (!hr_ready && !(ok = warp_wait_mbar(bar_hr, l & 1, P.err, lane))) break;
+        signal_phase(P, l, TR_CTA_OUT, &cta_cnt[2], D.cnt_out, lane);
     }
 
     if (!ok && lane == 0) {
@@ -1102,7 +1101,7 @@ namespace {
 
 struct StackCarve {
     size_t err, epoch, descs, layers0, per_layer, total;
-    size_t cnt_z, cnt_h, cnt_out, zt, ht, xt, logits, idx, w, act;
+    size_t cnt_z, cnt_hs, cnt_hr, cnt_out, zt, ht, xt, logits, idx, w, act;
 };
 
 StackCarve stack_carve(int L, int E) {
@@ -1115,10 +1114,11 @@ StackCarve stack_carve(int L, int E) {
     // per-layer block
     size_t p = 0;
     c.cnt_z = p; p += 128;
-    c.cnt_h = p; p += 128;
+    c.cnt_hs = p; p += 128;
+    c.cnt_hr = p; p += 128;
     c.cnt_out = p; p += 128;
     c.zt = p; p += align_up((size_t)E * 8, 128);
-    c.ht = p; p += align_up((size_t)fused::H_FLOATS * 8, 128);
+    c.ht = p; p += align_up((size_t)fused::H_FLOATS * 4, 128);
     c.xt = p; p += align_up((size_t)fused::H * 4, 128);
     c.logits = p; p += align_up((size_t)E * 4, 128);
     c.idx = p; p += 128;
@@ -1214,10 +1214,11 @@ tf_status tf_stack_create(tf_layer* const* layers, int L, const float* const* lo
         D.slot_map = d.experts.slot_of_expert;
         D.bias = logit_bias ? logit_bias[l] : nullptr;
         D.cnt_z = reinterpret_cast<uint32_t*>(base + sc.cnt_z);
-        D.cnt_h = reinterpret_cast<uint32_t*>(base + sc.cnt_h);
+        D.cnt_hs = reinterpret_cast<uint32_t*>(base + sc.cnt_hs);
+        D.cnt_hr = reinterpret_cast<uint32_t*>(base + sc.cnt_hr);
         D.cnt_out = reinterpret_cast<uint32_t*>(base + sc.cnt_out);
         D.zt = reinterpret_cast<unsigned long long*>(base + sc.zt);
-        D.ht = reinterpret_cast<unsigned long long*>(base + sc.ht);
+        D.ht = reinterpret_cast<uint32_t*>(base + sc.ht);
         D.xt = reinterpret_cast<uint32_t*>(base + sc.xt);
         D.logits = reinterpret_cast<float*>(base + sc.logits);
         D.idx = reinterpret_cast<int32_t*>(base + sc.idx);
