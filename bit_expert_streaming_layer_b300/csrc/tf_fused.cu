@@ -89,7 +89,8 @@ static_assert((K * I) % (8 * NCTRL) == 0 && S % (8 * NCTRL) == 0, "control warps
 // shared-memory layout
 constexpr int OFF_RING = 0;
 constexpr int OFF_XS = OFF_RING + NWORK * NS * STAGE;   // bf16 x [H]
-constexpr int OFF_N = OFF_XS + H * 2;                    // fp32 n [H]
+constexpr int OFF_N = OFF_XS + H * 2;                    // fp32 n in two halves per word: n[8w..8w+3] at
+                                                         // float4 w, n[8w+4..8w+7] at float4 HW + w
 constexpr int OFF_SN = OFF_N + H * 4;                    // fp32 word sums of n [HW]
 constexpr int OFF_H = OFF_SN + HW * 4;                   // tagged fp32 h_routed [K*I], h_shared [S]; also the
                                                          // landing zone of the tagged layer input
@@ -100,11 +101,11 @@ constexpr int RT_BYTES = 2 * (K * 8 + K * 4 + K * 4);
 constexpr int OFF_BAR = OFF_RT + RT_BYTES;               // mbarriers
 enum { B_X = NWORK * NS, B_K, B_HS, B_HR, B_LOAD, N_BAR };
 constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;            // r, epoch, CTA phase counters, stale count
-constexpr size_t SMEM_BYTES = OFF_MISC + 32;
+constexpr int MAX_L = 64;                                // layers (tags are epoch * 64 + layer)
+constexpr int OFF_DESC = OFF_MISC + 32;                  // copies of the layer descriptors [MAX_L]
 static_assert(H * 4 <= H_FLOATS * 4, "the tagged layer input fits the h area");
 static_assert(OFF_H % 16 == 0 && OFF_N % 16 == 0 && OFF_RT % 16 == 0 && OFF_BAR % 8 == 0 && OFF_Z % 16 == 0,
               "alignment");
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
 struct LayerDesc {
     const uint16_t* Wr;
@@ -131,6 +132,10 @@ struct LayerDesc {
     unsigned long long off_gu_sb, off_d_codes, off_d_sb;
 };
 
+constexpr size_t SMEM_BYTES = OFF_DESC + MAX_L * sizeof(LayerDesc);
+static_assert(sizeof(LayerDesc) % 8 == 0 && OFF_DESC % 8 == 0, "descriptor copies move 8-byte words");
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory with the descriptors");
+
 struct Params {
     const LayerDesc* layers;
     int L;
@@ -153,11 +158,23 @@ enum {
     TR_HR_STAGED = 5,    // ... published h_routed
     TR_CTA_HR_DONE = 6,  // the CTA's last worker finished its routed gate/up tasks
     TR_CTA_OUT = 7,      // the CTA's last worker finished the layer
-    TRACE_SLOTS = 8,
+    TR_W_SGU_DONE = 8,   // worker 0 finished its shared gate/up items
+    TR_W_RGU_READY = 9,  // ... had the data of its first routed gate/up item
+    TR_W_RGU_DONE = 10,  // ... finished its routed gate/up items
+    TR_W_DS_DONE = 11,   // ... finished its shared-down items
+    TR_W_RD_READY = 12,  // ... had the data of its routed-down item
+    TR_W_DONE = 13,      // ... finished the layer
+    TRACE_SLOTS = 16,
     TRACE_CTAS = 256
 };
 
 enum { T_ROUTER = 0, T_SGU = 1, T_RGU = 2, T_DOWN = 3 };
+
+// The CTA's shared-memory copy of layer l's descriptor (made at kernel start).
+extern __shared__ __align__(128) unsigned char g_smem[];
+__device__ __forceinline__ const LayerDesc& LD(int l) {
+    return reinterpret_cast<const LayerDesc*>(g_smem + OFF_DESC)[l];
+}
 enum { ERR_TIMEOUT = 1, ERR_BAD_ID = 2 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -339,7 +356,7 @@ static_assert(sizeof(Route) <= RT_BYTES, "routing cache");
 
 // Lane 0 enqueues the copies of one item into a stage.
 __device__ void issue_item(const Ctx& c, const It& it, const Route* rt, uint32_t dst, uint32_t bar, uint64_t pol) {
-    const LayerDesc& D = c.P->layers[it.l];
+    const LayerDesc& D = LD(it.l);
     fence_proxy_async();  // the stage's previous contents were read through the generic proxy
     if (it.kind == T_ROUTER) {
         mbar_expect_tx(bar, ROW_BF);
@@ -375,7 +392,7 @@ __device__ void issue_item(const Ctx& c, const It& it, const Route* rt, uint32_t
 
 // L2 prefetch of the data-independent weights of worker gw's tasks in layer l.
 __device__ void prefetch_layer(const Ctx& c, int l) {
-    const LayerDesc& D = c.P->layers[l];
+    const LayerDesc& D = LD(l);
     for (int t = first_task(c.gw, l, c.NTL, c.NW); t < c.NTL; t += c.NW) {
         const int kind = task_kind(t, c.E);
         if (kind == T_ROUTER) {
@@ -446,7 +463,8 @@ __device__ __forceinline__ void warp_sum4(float& a, float& b, float& c, float& d
     }
 }
 
-// sum_k W[k] n[k] over a bf16 row of K = H (16-byte chunk w covers n[8w..8w+7]).
+// sum_k W[k] n[k] over a bf16 row of K = H (16-byte chunk w covers n[8w..8w+7],
+// held in shared memory as the float4s w and HW + w).
 __device__ __forceinline__ float row_bf16(const unsigned char* row, const float* n, int lane) {
     const float4* n4 = reinterpret_cast<const float4*>(n);
     unsigned long long acc = 0ull;
@@ -454,7 +472,7 @@ __device__ __forceinline__ float row_bf16(const unsigned char* row, const float*
     for (int m = 0; m < WPL; ++m) {
         const int w = lane + 32 * m;
         const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * w);
-        acc = dot8_bf16_2(v, n4[2 * w], n4[2 * w + 1], acc);
+        acc = dot8_bf16_2(v, n4[w], n4[HW + w], acc);
     }
     return warp_sum(sum2(acc));
 }
@@ -466,10 +484,10 @@ __device__ __forceinline__ float4 rows4_int4(const uint32_t* codes, const uint32
     const float4* n4 = reinterpret_cast<const float4*>(n);
     constexpr int SBW = GU_SB / 4;
     float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-#pragma unroll 1
+#pragma unroll 2
     for (int m = 0; m < WPL; ++m) {
         const int w = lane + 32 * m, g = w >> 3;
-        const float4 na = n4[2 * w], nb = n4[2 * w + 1];
+        const float4 na = n4[w], nb = n4[HW + w];
         const float S = sn[w];
         a0 = word_affine(codes[w], sb[g], na, nb, S, a0);
         a1 = word_affine(codes[HW + w], sb[SBW + g], na, nb, S, a1);
@@ -572,7 +590,7 @@ __device__ bool stage_x(const Params& P, int l, uint32_t epoch, uint32_t hint_ta
         const uint4* s4 = reinterpret_cast<const uint4*>(P.x);
         for (int c = cw * 32 + lane; c < H / 8; c += NCTRL * 32) reinterpret_cast<uint4*>(xs)[c] = __ldcg(s4 + c);
     } else {
-        if (cw == 0 && !wait_hint(P.layers[l - 1].cnt_out, hint_target, P.err, lane) && lane == 0)
+        if (cw == 0 && !wait_hint(LD(l - 1).cnt_out, hint_target, P.err, lane) && lane == 0)
             atomicOr(&stale[1], 1u);  // tells the other control warps to stop
         ctrl_sync();
         if (stale[1]) return false;
@@ -588,7 +606,7 @@ __device__ bool stage_x(const Params& P, int l, uint32_t epoch, uint32_t hint_ta
             }
             return bad;
         };
-        if (!ctrl_load(P, P.layers[l - 1].xt, H * 4, land, bar_load, loads, stale, cw, lane, check)) return false;
+        if (!ctrl_load(P, LD(l - 1).xt, H * 4, land, bar_load, loads, stale, cw, lane, check)) return false;
         if (cw == 0 && lane == 0) trace_at(P, l, TR_X_READY);
     }
     ctrl_sync();
@@ -601,7 +619,7 @@ __device__ bool stage_x(const Params& P, int l, uint32_t epoch, uint32_t hint_ta
             p = fmaf(v, v, p);  // exact square: one rounding per term, as in the canonical sum
         }
         p = warp_sum_canonical(p);
-        if (lane == 0) rs[0] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(p, (float)H), P.layers[l].eps)));
+        if (lane == 0) rs[0] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(p, (float)H), LD(l).eps)));
     }
     ctrl_sync();
     const float r = rs[0];
@@ -613,8 +631,8 @@ __device__ bool stage_x(const Params& P, int l, uint32_t epoch, uint32_t hint_ta
                                      __fmul_rn(r, bf_hi(v.y)));
         const float4 b = make_float4(__fmul_rn(r, bf_lo(v.z)), __fmul_rn(r, bf_hi(v.z)), __fmul_rn(r, bf_lo(v.w)),
                                      __fmul_rn(r, bf_hi(v.w)));
-        reinterpret_cast<float4*>(n)[2 * w] = a;
-        reinterpret_cast<float4*>(n)[2 * w + 1] = b;
+        reinterpret_cast<float4*>(n)[w] = a;
+        reinterpret_cast<float4*>(n)[HW + w] = b;
         sn[w] = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
     }
     ctrl_sync();
@@ -627,7 +645,7 @@ __device__ bool stage_x(const Params& P, int l, uint32_t epoch, uint32_t hint_ta
 // head with two warp reductions and the winning lane shifts its list.
 __device__ bool route_layer(const Params& P, int l, uint32_t tag, uint32_t epoch_x_e, unsigned char* smem, Route* rt,
                             bool publish, uint32_t bar_load, int& loads, int lane) {
-    const LayerDesc& D = P.layers[l];
+    const LayerDesc& D = LD(l);
     if (!wait_hint(D.cnt_z, epoch_x_e, P.err, lane)) return false;
     const unsigned long long* zt = reinterpret_cast<const unsigned long long*>(smem + OFF_Z);
     const uint64_t t0 = gtimer();
@@ -722,7 +740,7 @@ __device__ bool route_layer(const Params& P, int l, uint32_t tag, uint32_t epoch
 __device__ bool stage_h(const Params& P, int l, uint32_t tag4, const uint32_t* hint, uint32_t hint_target,
                         bool routed, unsigned char* smem, uint32_t bar_load, int& loads, uint32_t* stale, int cw,
                         int lane) {
-    const LayerDesc& D = P.layers[l];
+    const LayerDesc& D = LD(l);
     if (cw == 0 && !wait_hint(hint, hint_target, P.err, lane) && lane == 0) atomicOr(&stale[1], 1u);
     ctrl_sync();
     if (stale[1]) return false;
@@ -754,7 +772,7 @@ __device__ bool stage_h(const Params& P, int l, uint32_t tag4, const uint32_t* h
 // ------------------------------------------------------------------ the kernel
 
 __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
-    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char* smem = g_smem;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int G = gridDim.x;
 
@@ -781,10 +799,15 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
         stale[0] = stale[1] = stale[2] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    {  // the layer descriptors, copied once
+        const unsigned long long* src = reinterpret_cast<const unsigned long long*>(P.layers);
+        unsigned long long* dst = reinterpret_cast<unsigned long long*>(smem + OFF_DESC);
+        for (int i = threadIdx.x; i < P.L * (int)(sizeof(LayerDesc) / 8); i += blockDim.x) dst[i] = __ldg(src + i);
+    }
     __syncthreads();
     const uint32_t epoch = *s_epoch;
     const uint32_t hint_target = epoch * (uint32_t)G;   // every launch adds G to each per-CTA hint counter
-    const int E = P.layers[0].E;
+    const int E = LD(0).E;
 
     if (warp < NCTRL) {
         // ================================================= control warps
@@ -792,7 +815,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
         int loads = 0;
         bool ok = true;
         for (int l = 0; l < P.L && ok; ++l) {
-            const LayerDesc& D = P.layers[l];
+            const LayerDesc& D = LD(l);
             const uint32_t tag = epoch * 64u + (uint32_t)l;
             const uint32_t tag4 = tag4_of(epoch, l);
             if (!(ok = stage_x(P, l, epoch, hint_target, smem, bar_load, loads, stale, cw, lane))) break;
@@ -828,8 +851,8 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
             }
         }
         // CTA 0 advances the epoch once the last layer's output is complete
-        if (ok && blockIdx.x == 0 && warp == 0 && wait_hint(P.layers[P.L - 1].cnt_out, hint_target, P.err, lane)) {
-            const uint32_t* src = P.layers[P.L - 1].xt;
+        if (ok && blockIdx.x == 0 && warp == 0 && wait_hint(LD(P.L - 1).cnt_out, hint_target, P.err, lane)) {
+            const uint32_t* src = LD(P.L - 1).xt;
             const uint32_t tag16 = (epoch * 64u + (uint32_t)(P.L - 1)) & 0xffffu;
             const uint64_t t0 = gtimer();
             for (;;) {
@@ -868,6 +891,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
     const uint32_t ring_u32 = smem_u32(ring);
     const uint32_t bar0 = smem_u32(&bars[wk * NS]);
     const uint64_t pol = evict_first_policy();
+    const bool w0t = P.trace && wk == 0 && lane == 0;
 
     It iss, con;
     it_begin_layer(iss, c, 0);
@@ -908,7 +932,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
 
     if (P.prefetch && lane == 0) prefetch_layer(c, 0);
     for (int l = 0; l < P.L && ok; ++l) {
-        const LayerDesc& D = P.layers[l];
+        const LayerDesc& D = LD(l);
         const uint32_t tag = epoch * 64u + (uint32_t)l;
         const uint32_t tag4 = tag4_of(epoch, l);
         const uint32_t tag16 = tag & 0xffffu;
@@ -919,6 +943,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
         const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem + OFF_XS);
         uint16_t* pout = l == P.L - 1 ? P.out : nullptr;
         bool hs_sig = false, hr_sig = false, hs_ready = false, hr_ready = false;
+        bool t_rgu = false, t_sgu = false, t_rg2 = false, t_ds = false;
         while (con.l == l) {
             // phase signals when the consume pointer leaves a kind of task
             if (!hs_sig && con.kind > T_SGU) {
@@ -961,6 +986,17 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
             const int slot = n_con % NS;
             if (!(ok = warp_wait_mbar(bar0 + 8 * slot, (n_con / NS) & 1, P.err, lane))) break;
             const unsigned char* st = ring + slot * STAGE;
+            if (w0t) {
+                if (con.kind == T_RGU && !t_rgu) trace_at(P, l, TR_W_RGU_READY);
+                if (con.kind == T_DOWN && con.sub == 2) trace_at(P, l, TR_W_RD_READY);
+                if (con.kind > T_SGU && !t_sgu) trace_at(P, l, TR_W_SGU_DONE);
+                if (con.kind > T_RGU && !t_rg2) trace_at(P, l, TR_W_RGU_DONE);
+                if (con.kind == T_DOWN && con.sub == 2 && !t_ds) trace_at(P, l, TR_W_DS_DONE);
+            }
+            t_rgu |= con.kind == T_RGU;
+            t_sgu |= con.kind > T_SGU;
+            t_rg2 |= con.kind > T_RGU;
+            t_ds |= con.kind == T_DOWN && con.sub == 2;
             if (con.kind == T_ROUTER) {
                 const uint16_t* wrow = reinterpret_cast<const uint16_t*>(st);
                 float d = 0.0f;
@@ -993,7 +1029,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
                 const int j0 = 2 * (con.t - D.E - N_SGU - N_RGU);
                 const float* hsh = reinterpret_cast<const float*>(smem + OFF_H) + K * I;
                 if (con.sub < 2) {
-                    // shared down row j0 + sub (bf16, K = S): chunks ch = lane + 32 t, t < 9
+                    // shared down row j0 + sub (bf16, K = S)
                     unsigned long long ac = 0ull;
 #pragma unroll 1
                     for (int ch = lane; ch < S / 8; ch += 32) {
@@ -1063,6 +1099,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
         if (!hs_ready && !(ok = warp_wait_mbar(bar_hs, l & 1, P.err, lane))) break;
         if (!hr_ready && !(ok = warp_wait_mbar(bar_hr, l & 1, P.err, lane))) break;
         signal_phase(P, l, TR_CTA_OUT, &cta_cnt[2], D.cnt_out, lane);
+        if (w0t) trace_at(P, l, TR_W_DONE);
     }
 
     if (!ok && lane == 0) {
@@ -1145,7 +1182,7 @@ cudaError_t stack_reset(tf_stack* s, cudaStream_t st) {
 extern "C" {
 
 size_t tf_stack_workspace_bytes(int L, int E) {
-    if (L < 1 || E < fused::K || E > TF_MAX_E) return 0;
+    if (L < 1 || L > fused::MAX_L || E < fused::K || E > TF_MAX_E) return 0;
     return stack_carve(L, E).total;
 }
 
@@ -1155,6 +1192,7 @@ tf_status tf_stack_create(tf_layer* const* layers, int L, const float* const* lo
     if (!out) return fail(TF_ERR_INVALID_ARG, "%s: out is NULL", fn);
     *out = nullptr;
     if (!layers || L < 1) return fail(TF_ERR_INVALID_ARG, "%s: no layers", fn);
+    if (L > fused::MAX_L) return fail(TF_ERR_NOT_SUPPORTED, "%s: at most %d layers (L=%d)", fn, fused::MAX_L, L);
     std::vector<tf_layer_desc> ds((size_t)L);
     for (int l = 0; l < L; ++l) {
         if (!layers[l]) return fail(TF_ERR_INVALID_ARG, "%s: layer %d is NULL", fn, l);
@@ -1248,7 +1286,7 @@ tf_status tf_stack_set_prefetch(tf_stack* s, int on) {
 
 tf_status tf_stack_set_trace(tf_stack* s, void* buffer, size_t bytes) {
     if (!s) return fail(TF_ERR_INVALID_ARG, "tf_stack_set_trace: NULL");
-    const size_t need = (size_t)s->L * fused::TRACE_CTAS * fused::TRACE_SLOTS * 8;
+    const size_t need = (size_t)s->L * fused::TRACE_CTAS * fused::TRACE_SLOTS * 8;  // L x 256 x 16 stamps
     if (buffer && bytes < need) return fail(TF_ERR_INVALID_ARG, "tf_stack_set_trace: the buffer needs %zu bytes", need);
     if (buffer && s->grid > fused::TRACE_CTAS)
         return fail(TF_ERR_NOT_SUPPORTED, "tf_stack_set_trace: more than %d CTAs", fused::TRACE_CTAS);

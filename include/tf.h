@@ -370,13 +370,16 @@ tf_status tf_stack_create(tf_layer* const* layers, int L, const float* const* lo
 /* L2 prefetch of the next layer's data-independent weights (router, shared
  * expert) while a layer runs: on (1) or off (0, the default). */
 tf_status tf_stack_set_prefetch(tf_stack* s, int on);
-/* Phase trace for measurement: with a device buffer of L * 256 * 8 uint64 set,
- * each step writes, for layer l and CTA c, at buffer[(256 l + c) * 8 + slot],
- * the %globaltimer (ns) at which the CTA's first control warp 0 saw the whole
- * layer input, 1 published x and n, 2 saw all router logits, 3 published the
- * top-k, 4 saw the h counter complete, 5 staged its part of h; 6 the CTA's last
- * worker warp finished its h-producing tasks, 7 its layer work. NULL turns
- * tracing off. */
+/* Phase trace for measurement: with a device buffer of L * 256 * 16 uint64 set,
+ * each step writes, for layer l and CTA c, at buffer[(256 l + c) * 16 + slot],
+ * the %globaltimer (ns) at which the CTA's control warps 0 held the whole layer
+ * input, 1 published x and n, 2 held all router logits, 3 published the top-k,
+ * 4 published h_shared, 5 published h_routed; at which 6 the CTA's last worker
+ * finished its routed gate/up tasks, 7 its layer work; and at which the CTA's
+ * first worker warp 8 finished its shared gate/up items, 9 had its first routed
+ * gate/up data, 10 finished its routed gate/up items, 11 finished its shared-down
+ * items, 12 had its routed-down data, 13 finished the layer. NULL turns tracing
+ * off. */
 tf_status tf_stack_set_trace(tf_stack* s, void* buffer, size_t bytes);
 /* out = stack(x) for one token; x, out device bf16 [H], 16-byte aligned, out != x. */
 tf_status tf_stack_step(tf_stack* s, const void* x, void* out, void* stream);
