@@ -8,6 +8,14 @@ the stack output fed back as the next input. One step = one token through all
 30 layers. Prints one JSON line (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode|prefill|streaming|batched]
+
+--workload prefill times the 4096-token grouped layer (tcgen05 GEMMs);
+--workload streaming runs the decode stack with the experts in pinned host
+memory behind the 16-slot-per-layer LFU cache and reports the hit rate, the
+bytes fetched per token, the copy stall and the host-link bandwidth;
+--workload batched runs the stack with 64 tokens per step through the grouped
+tcgen05 path (routed and shared experts).
 
 --impl reference times the CPU oracle (the plain single-threaded C reference
 of the same layer) on the host cores, on a bounded sample of the same
@@ -236,6 +244,310 @@ def run_ours(args, rank, world):
     return ms, prof, clocks, gpu_launches, e2e_s, e2e_steps
 
 
+# ------------------------------------------------------------------ streamed experts (LFU cache, host store)
+
+STREAM_SEED, STREAM_ZIPF, STREAM_SLOTS = 2, 1.1, 16
+STREAM_ALPHA = 0.35    # Zipf bias scale that puts the LFU hit rate in the 60-70 % band
+STREAM_METRIC = "MoE decode tok/s with experts streamed from pinned host memory through a 16-slot LFU cache (1 B300)"
+STREAM_WORKLOAD = ("30-layer MoE-only decode stack, batch 1, a fresh x ~ N(0,1) per step (the next token's input); "
+                   "experts (12.9 GB, 3,840 x 3.36 MB) in "
+                   "pinned host memory, a 16-slot-per-layer LFU cache in HBM (1.61 GB), misses copied by "
+                   "cudaMemcpyAsync on a copy stream overlapped with the shared expert; router logits biased by "
+                   "Zipf(1.1) popularity (alpha %.2f) over a seeded per-layer rank->expert map, and with probability "
+                   "0.5 per (step, layer) +30 on the previous step's 8 ids; seed 2")
+
+
+def h2d_probe(dev, copy_stream, n_slots=32, reps=5):
+    """Pinned host -> device copy bandwidth in GB/s: n_slots expert blobs, one copy each."""
+    import torch
+    import bit_expert_streaming_layer_b300 as B
+    slot = B.tf_expert_slot_bytes(H, I)
+    src = torch.empty(n_slots * slot, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(n_slots * slot, dtype=torch.uint8, device=dev)
+    best = 0.0
+    with torch.cuda.stream(copy_stream):
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(copy_stream)
+            for i in range(n_slots):
+                dst[i * slot:(i + 1) * slot].copy_(src[i * slot:(i + 1) * slot], non_blocking=True)
+            e1.record(copy_stream)
+            copy_stream.synchronize()
+            best = max(best, n_slots * slot / (e0.elapsed_time(e1) / 1000.0) / 1e9)
+    return best
+
+
+def run_streaming(args):
+    import torch
+    import bit_expert_streaming_layer_b300 as B
+    import workload as W
+    from workload.model import SyntheticStack, hidden_tensor
+
+    seed, alpha = STREAM_SEED, args.alpha
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stack = SyntheticStack(seed, L, H=H, I=I, E=E, k=K_ACT, S=S, resident=False, n_slots=STREAM_SLOTS, device=dev)
+    zipf_h = np.stack([W.zipf_bias(seed, l, E, STREAM_ZIPF, alpha)[0] for l in range(L)])
+    zipf_d = torch.from_numpy(zipf_h).to(dev)
+    bias_h = torch.empty(L, E, dtype=torch.float32, pin_memory=True)
+    bias_hn = bias_h.numpy()
+    bias_d = torch.empty(L, E, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    copy_stream = torch.cuda.Stream(dev)
+    probe = h2d_probe(dev, copy_stream)
+    # one fresh input per step: a fed-back output settles on a fixed point whose routing never changes
+    n_inputs = args.warmup + args.steps + min(args.steps, 32) + min(args.steps, 64)
+    xs = torch.stack([hidden_tensor(seed, t, 1, H, device=dev)[0] for t in range(n_inputs)])
+    bufs = [torch.empty(H, dtype=torch.bfloat16, device=dev) for _ in range(5)]   # 0-1 outputs, 2-3 scratch, 4 input
+    prev = [None] * L
+    tot = {"hits": 0, "misses": 0, "bytes": 0, "stall_ms": 0.0, "copy_ms": 0.0, "shared_ms": 0.0, "tokens": 0}
+
+    def token(step, src, dst, measure=0):
+        x = src
+        for l in range(L):
+            if prev[l] is not None and W.coin(seed, l, step):
+                bias_hn[l] = zipf_h[l]
+                bias_hn[l, prev[l]] += 30.0
+                bias_d[l].copy_(bias_h[l], non_blocking=True)
+                bias = bias_d[l]
+            else:
+                bias = zipf_d[l]
+            y = dst if l == L - 1 else bufs[2 + l % 2]
+            st = B.tf_layer_step(stack.layers[l], stack.cache, l, step, stack.store, x, y, 1, bias, 0, stream,
+                                 copy_stream, measure)
+            prev[l] = np.array(st.ids[:K_ACT], dtype=np.int64)
+            tot["hits"] += st.hits
+            tot["misses"] += st.misses
+            tot["bytes"] += st.bytes_fetched
+            tot["stall_ms"] += st.stall_ms
+            tot["copy_ms"] += st.copy_ms
+            tot["shared_ms"] += st.shared_ms
+            x = y
+        tot["tokens"] += 1
+
+    step = 0
+    for _ in range(args.warmup):
+        token(step, xs[step], bufs[0])
+        step += 1
+    torch.cuda.synchronize()
+    for k in tot:
+        tot[k] = 0
+    sampler = ClockSampler(0)
+    sampler.start()
+    B.tf_profile_begin(min(args.steps, 8) * 4 * L)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        token(step, xs[step], bufs[step % 2])
+        step += 1
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    prof = B.tf_profile_end()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    timed = dict(tot)
+    assert not torch.isnan(bufs[(step - 1) % 2].float()).any(), "NaN in the stack output"
+
+    # stall and copy times: the call synchronises each layer to read its events, so these steps are not timed
+    meas_steps = min(args.steps, 32)
+    for k in tot:
+        tot[k] = 0
+    for _ in range(meas_steps):
+        token(step, xs[step], bufs[0], measure=1)
+        step += 1
+    meas = dict(tot)
+
+    # end to end: the input from pinned host memory and the output back, every step
+    hy = torch.empty(H, dtype=torch.bfloat16, pin_memory=True)
+    hxs = xs.cpu().pin_memory()
+    e2e_steps = min(args.steps, 64)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        bufs[4].copy_(hxs[step], non_blocking=True)
+        token(step, bufs[4], bufs[0])
+        hy.copy_(bufs[0], non_blocking=True)
+        stream.synchronize()
+        step += 1
+    e2e_s = time.perf_counter() - t0
+    stack.close()
+
+    n = args.steps
+    lookups = timed["hits"] + timed["misses"]
+    fetch_gbs = timed["bytes"] / (ms / 1000.0) / 1e9
+    launches = sum(v[1] for v in prof.values())
+    line = {
+        "metric": STREAM_METRIC, "value": round(n / (ms / 1000.0), 2), "unit": "tok/s", "n_gpus": 1, "steps": n,
+        "warmup": args.warmup, "ms_per_step": round(ms / n, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": STREAM_WORKLOAD % alpha, "layers": L, "slots_per_layer": STREAM_SLOTS,
+                   "zipf_s": STREAM_ZIPF, "zipf_alpha": alpha, "repeat_p": 0.5, "repeat_bonus": 30.0,
+                   "l2": "no flush: every step streams 1.1 GB of resident shared/router weights plus the cached "
+                         "experts, far above the 126 MB L2"},
+        "hit_rate": round(timed["hits"] / max(1, lookups), 4),
+        "bytes_fetched_per_token": int(timed["bytes"] / n),
+        "roofline": {"bound": "host_link", "achieved": round(fetch_gbs, 2), "peak": round(probe, 2), "unit": "GB/s",
+                     "frac": round(fetch_gbs / probe, 4),
+                     "peak_source": "pinned host->device copy probe in the same run (32 x 3.36 MB)", "traffic": None},
+        "stall_us_per_token": round(meas["stall_ms"] * 1000.0 / max(1, meas["tokens"]), 1),
+        "copy_gbs_during_fills": round(meas["bytes"] / max(1e-9, meas["copy_ms"] / 1000.0) / 1e9, 2),
+        "shared_branch_us_per_token": round(meas["shared_ms"] * 1000.0 / max(1, meas["tokens"]), 1),
+        "measured_steps_for_stall": meas_steps,
+        "kernels": {k: {"event_ms_total": round(v[0], 4), "launches": int(v[1])} for k, v in prof.items() if v[1]},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_steps / e2e_s, 2), "unit": "tok/s", "h2d_bytes_per_step": H * 2,
+                "d2h_bytes_per_step": H * 2},
+    }
+    if not args.no_cpu_baseline:
+        base = oracle_baseline(args.oracle_layers)
+        line["cpu_baseline"] = {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------ batched decode (64 tokens per step)
+
+BATCH_T, BATCH_SEED = 64, 3
+BATCH_METRIC = "batched MoE decode tok/s, 64 tokens per step (1 B300)"
+BATCH_WORKLOAD = ("30-layer MoE-only stack, 64 tokens per step (x ~ N(0,1) [64, 2816] at step 0, the outputs fed back), "
+                  "uniform routing (no bias), H=2816, 128 experts of I=704 (int4 g64, fp16 scale+bias), top-8; routed "
+                  "experts by grouped dequant-to-bf16 tcgen05 GEMMs, the bf16 shared expert 2816->2112->2816 by the "
+                  "same GEMM kernel; all experts resident in HBM; seed 3")
+PAYLOAD = 3 * (I * H // 2 + I * (H // 64) * 4)       # 3,345,408 B per expert
+# kernels behind one profiling bracket of a batched layer step: rms, histogram, positions, inverse init, two
+# gathers and the shared plan; four GEMMs
+BATCH_KERNELS_PER_BRACKET = {"router": 1, "permute": 7, "gemm": 4, "combine": 1}
+
+
+def batched_cpu_baseline(seed, x_bits, n_tokens=2):
+    """The oracle (bf16-operand reading, with the shared expert) on n_tokens tokens of layer 0: routing, 8 experts
+    and the shared expert; tok/s over 30 layers."""
+    import oracle as O
+    import workload as W
+    O.build()
+    shared = W.shared_weights(seed, 0, H, S)
+    Wr = W.router_weights(seed, 0, E, H)
+    elapsed = 0.0
+    for t in range(n_tokens):
+        idx = O.route(x_bits[t], Wr, None, K_ACT)[2]
+        experts = W.experts_parallel(seed, 0, idx, H, I)   # generation is not timed
+        t0 = time.perf_counter()
+        r, _, idx, w = O.route(x_bits[t], Wr, None, K_ACT)
+        O.layer_combine(x_bits[t], r, experts, w, shared, bf16_ops=True)
+        elapsed += time.perf_counter() - t0
+    return {"value": n_tokens / (elapsed * L), "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "sample": "%d tokens of layer 0 at step 0 (router, 8 experts and the shared expert each), single-threaded "
+                      "fp32 C oracle in its bf16-operand reading; tok/s = tokens / (30 x their layer time)" % n_tokens}
+
+
+def run_batched(args):
+    import torch
+    import bit_expert_streaming_layer_b300 as B
+    from workload.model import SyntheticStack, bf16_bits, hidden_tensor
+
+    seed, T = BATCH_SEED, BATCH_T
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stack = SyntheticStack(seed, L, H=H, I=I, E=E, k=K_ACT, S=S, resident=True, T_max=T, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    x0 = hidden_tensor(seed, 0, T, H, device=dev)
+    bufs = [torch.empty(T, H, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    bufs[0].copy_(x0)
+
+    def step(src, dst):
+        x = src
+        for l in range(L):
+            y = dst if l == L - 1 else bufs[2 + l % 2]
+            B.tf_layer_step(stack.layers[l], None, l, 0, None, x, y, T, None, 0, stream)
+            x = y
+
+    cur, nxt = 0, 1
+    for _ in range(args.warmup):
+        step(bufs[cur], bufs[nxt])
+        cur, nxt = nxt, cur
+    torch.cuda.synchronize()
+    sampler = ClockSampler(0)
+    sampler.start()
+    prof_steps = min(args.steps, 8)
+    prof_cap = prof_steps * L           # timed brackets per kind: one per layer of the first prof_steps steps
+    B.tf_profile_begin(prof_cap)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(bufs[cur], bufs[nxt])
+        cur, nxt = nxt, cur
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    prof = B.tf_profile_end()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    assert not torch.isnan(bufs[cur].float()).any(), "NaN in the stack output"
+
+    # census (untimed): distinct experts per layer on one more step -> algorithmic bytes
+    distinct = []
+    x = bufs[cur]
+    for l in range(L):
+        y = bufs[2 + l % 2]
+        B.tf_layer_step(stack.layers[l], None, l, 0, None, x, y, T, None, 0, stream)
+        idx = stack.layers[l].routing_tensors(T)[0]
+        distinct.append(int(torch.unique(idx).numel()))
+        x = y
+    torch.cuda.synchronize()
+    layer_bytes = [d * PAYLOAD + SHARED_GU + SHARED_D for d in distinct]
+    step_bytes = sum(layer_bytes) + L * ROUTER
+
+    # end to end: the 64 inputs from pinned host memory and the 64 outputs back, every step
+    hx = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
+    hy = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
+    hx.copy_(x0.cpu())
+    e2e_steps = min(args.steps, 32)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        bufs[0].copy_(hx, non_blocking=True)
+        step(bufs[0], bufs[1])
+        hy.copy_(bufs[1], non_blocking=True)
+        stream.synchronize()
+        hx.copy_(hy)
+    e2e_s = time.perf_counter() - t0
+    x_bits = bf16_bits(x0)
+    stack.close()
+
+    peak, peak_kind = peaks()
+    gemm_ms, gemm_n = prof["gemm"]
+    gemm_brackets = min(gemm_n, prof_cap)    # one bracket = the four GEMM launches of one layer
+    gemm_avg_s = gemm_ms / max(1, gemm_brackets) / 1000.0
+    mean_layer_bytes = sum(layer_bytes) / L
+    gemm_gbs = mean_layer_bytes / gemm_avg_s / 1e9
+    n = args.steps
+    line = {
+        "metric": BATCH_METRIC, "value": round(T * n / (ms / 1000.0), 1), "unit": "tok/s", "n_gpus": 1, "steps": n,
+        "warmup": args.warmup, "ms_per_step": round(ms / n, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": BATCH_WORKLOAD, "layers": L, "tokens_per_step": T,
+                   "l2": "no flush: each step streams about %.1f GB of weights, far above the 126 MB L2"
+                         % (step_bytes / 1e9)},
+        "distinct_experts_per_layer": round(sum(distinct) / L, 1),
+        "weight_bytes_per_step": step_bytes,
+        "weight_gbs": round(step_bytes / (ms / n / 1000.0) / 1e9, 1),
+        "roofline": {"bound": "hbm", "kernel": "gemm", "achieved": round(gemm_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gemm_gbs / peak, 4), "peak_source": peak_kind + " (hbm_gbs)",
+                     "bytes_per_launch": int(mean_layer_bytes),
+                     "launch": "the four GEMM launches of one layer (routed gate/up, down; shared gate/up, down)",
+                     "traffic": None},
+        "kernels": {k: {"event_ms_total": round(v[0], 4), "brackets": int(v[1]), "timed_brackets": min(int(v[1]), prof_cap),
+                        "avg_us": round(v[0] / max(1, min(v[1], prof_cap)) * 1000.0, 2)}
+                    for k, v in prof.items() if v[1]},
+        "gpu_launches": int(sum(v[1] * BATCH_KERNELS_PER_BRACKET.get(k, 1) for k, v in prof.items())),
+        "clocks": clocks,
+        "e2e": {"value": round(T * e2e_steps / e2e_s, 1), "unit": "tok/s", "h2d_bytes_per_step": T * H * 2,
+                "d2h_bytes_per_step": T * H * 2},
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = batched_cpu_baseline(seed, x_bits)
+    print(json.dumps(line))
+
+
 # ------------------------------------------------------------------ prefill-shaped layer (grouped path)
 
 PREFILL_T = 4096
@@ -365,8 +677,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefetch", action="store_true",
                     help="fused path: prefetch the next layer's shared weights into L2 (measured slower)")
-    ap.add_argument("--workload", choices=["decode", "prefill"], default="decode",
-                    help="decode: the 30-layer decode stack (the headline line); prefill: the 4096-token grouped layer")
+    ap.add_argument("--workload", choices=["decode", "prefill", "streaming", "batched"], default="decode",
+                    help="decode: the 30-layer decode stack (the headline line); prefill: the 4096-token grouped "
+                         "layer; streaming: the decode stack through the 16-slot LFU cache with a host store; "
+                         "batched: the stack with 64 tokens per step")
+    ap.add_argument("--alpha", type=float, default=STREAM_ALPHA,
+                    help="streaming: scale of the Zipf(1.1) router bias")
     ap.add_argument("--layers", type=int, default=L,
                     help="stack depth; the benchmark workload is 30, fewer only for small profiling captures")
     args = ap.parse_args()
@@ -396,6 +712,14 @@ def main():
     if args.workload == "prefill":
         if rank == 0:
             run_prefill(args)
+        return
+    if args.workload == "streaming":
+        if rank == 0:
+            run_streaming(args)
+        return
+    if args.workload == "batched":
+        if rank == 0:
+            run_batched(args)
         return
 
     if world > 1:

@@ -47,7 +47,8 @@ class LayerDesc(ctypes.Structure):
 
 class StepStats(ctypes.Structure):
     _fields_ = [("hits", ctypes.c_int32), ("misses", ctypes.c_int32), ("bytes_fetched", ctypes.c_uint64),
-                ("copy_ms", ctypes.c_float), ("shared_ms", ctypes.c_float), ("stall_ms", ctypes.c_float)]
+                ("copy_ms", ctypes.c_float), ("shared_ms", ctypes.c_float), ("stall_ms", ctypes.c_float),
+                ("ids", ctypes.c_int32 * TF_MAX_K)]
 
 
 # exported symbols and their C signatures (restype, argtypes)

@@ -98,6 +98,8 @@ struct tf_layer {
     ExpertLayout lay;
     char* ws = nullptr;
     size_t ws_bytes = 0;
+    char* grouped_ws = nullptr;      // T_max > 1 only
+    size_t grouped_bytes = 0;
     uint32_t* counters = nullptr;
     float* logits = nullptr;
     int32_t* idx = nullptr;
@@ -112,7 +114,7 @@ struct tf_layer {
 namespace {
 
 struct LayerCarve {
-    size_t counters, logits, idx, w, rms, h_routed, h_shared, total;
+    size_t counters, logits, idx, w, rms, h_routed, h_shared, grouped, grouped_bytes, total;
 };
 
 LayerCarve layer_carve(const tf_layer_desc* d, int T_max) {
@@ -125,6 +127,10 @@ LayerCarve layer_carve(const tf_layer_desc* d, int T_max) {
     c.rms = o;      o += align_up((size_t)T_max * 4, 256);
     c.h_routed = o; o += align_up((size_t)d->k * d->I * 4, 256);
     c.h_shared = o; o += align_up((size_t)(d->S > 0 ? d->S : 1) * 4, 256);
+    // T_max > 1: the grouped path's workspace (permutation, activations, h, y, shared-expert buffers)
+    c.grouped = o;
+    c.grouped_bytes = T_max > 1 ? grouped_workspace_bytes(T_max, d->H, d->I, d->E, d->k, d->S) : 0;
+    o += align_up(c.grouped_bytes, 256);
     c.total = o;
     return c;
 }
@@ -363,6 +369,8 @@ tf_status tf_layer_create(const tf_layer_desc* d, int T_max, void* workspace, si
     l->rms = reinterpret_cast<float*>(l->ws + c.rms);
     l->h_routed = reinterpret_cast<float*>(l->ws + c.h_routed);
     l->h_shared = reinterpret_cast<float*>(l->ws + c.h_shared);
+    l->grouped_ws = c.grouped_bytes ? l->ws + c.grouped : nullptr;
+    l->grouped_bytes = c.grouped_bytes;
     cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&l->h_idx), TF_MAX_K * sizeof(int32_t), cudaHostAllocDefault);
     if (e != cudaSuccess) {
         delete l;
@@ -464,8 +472,36 @@ tf_status tf_layer_step(tf_layer* l, tf_expert_cache* cache, int layer, int64_t 
         if (!h_expert_store) return fail(TF_ERR_INVALID_ARG, "%s: a cached step needs the pinned expert store", fn);
         if (!copy_stream) return fail(TF_ERR_INVALID_ARG, "%s: a cached step needs a copy stream", fn);
     }
-    if (T != 1) return fail(TF_ERR_NOT_SUPPORTED, "%s: T > 1 goes through tf_moe_ffn_grouped", fn);
     if (stats) std::memset(stats, 0, sizeof(*stats));
+    if (T > 1) {
+        // batched tokens: router for all T, then the grouped routed experts and shared expert (tcgen05 GEMMs)
+        clear_error();
+        cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
+        int e = launch_router_topk(static_cast<const uint16_t*>(x), T, d.H, static_cast<const uint16_t*>(d.W_r), d.E,
+                                   logit_bias, bias_stride, d.k, l->idx, l->w, l->logits, l->rms, l->counters, d.eps,
+                                   cs);
+        if (e) return cuda_status(e, fn);
+        GroupedArgs a;
+        std::memset(&a, 0, sizeof(a));
+        a.x = x;
+        a.out = out;
+        a.T = T;
+        a.table = &d.experts;
+        a.E = d.E;
+        a.k = d.k;
+        a.H = d.H;
+        a.I = d.I;
+        a.idx = l->idx;
+        a.w = l->w;
+        a.Wsg = d.W_sg;
+        a.Wsu = d.W_su;
+        a.Wsd = d.W_sd;
+        a.S = d.S;
+        a.eps = d.eps;
+        a.ws = l->grouped_ws;
+        a.ws_bytes = l->grouped_bytes;
+        return grouped_run(a, cs, fn);
+    }
     clear_error();
     cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
     if (measure && stats) {
@@ -540,6 +576,7 @@ tf_status tf_layer_step(tf_layer* l, tf_expert_cache* cache, int layer, int64_t 
     if (!e) e = launch_down(p, 1, d.S > 0, cs);
     if (e) return cuda_status(e, fn);
     if (stats) {
+        std::memcpy(stats->ids, ids, (size_t)k * 4);
         stats->misses = na;
         stats->hits = k - na;
         stats->bytes_fetched = bytes;

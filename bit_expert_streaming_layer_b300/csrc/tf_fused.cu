@@ -164,6 +164,8 @@ enum {
     TR_W_DS_DONE = 11,   // ... finished its shared-down items
     TR_W_RD_READY = 12,  // ... had the data of its routed-down item
     TR_W_DONE = 13,      // ... finished the layer
+    TR_W_RGU1_END = 14,  // ... finished computing its first routed gate/up item
+    TR_W_RGU_END = 15,   // ... finished computing its last routed gate/up item
     TRACE_SLOTS = 16,
     TRACE_CTAS = 256
 };
@@ -943,7 +945,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
         const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem + OFF_XS);
         uint16_t* pout = l == P.L - 1 ? P.out : nullptr;
         bool hs_sig = false, hr_sig = false, hs_ready = false, hr_ready = false;
-        bool t_rgu = false, t_sgu = false, t_rg2 = false, t_ds = false;
+        bool t_rgu = false, t_sgu = false, t_rg2 = false, t_ds = false, t_rg1 = false;
         while (con.l == l) {
             // phase signals when the consume pointer leaves a kind of task
             if (!hs_sig && con.kind > T_SGU) {
@@ -1025,6 +1027,11 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
                 if (lane == 0)
                     st_relaxed_v2u32(D.ht + (size_t)i * I + p0, tagged_f(gelu_tanh(gu.x) * gu.y, tag4),
                                      tagged_f(gelu_tanh(gu.z) * gu.w, tag4));
+                if (w0t) {
+                    if (!t_rg1) trace_at(P, l, TR_W_RGU1_END);
+                    trace_at(P, l, TR_W_RGU_END);
+                    t_rg1 = true;
+                }
             } else {
                 const int j0 = 2 * (con.t - D.E - N_SGU - N_RGU);
                 const float* hsh = reinterpret_cast<const float*>(smem + OFF_H) + K * I;

@@ -22,6 +22,12 @@
 //   warps 8..15 dequant: codes -> bf16 = RN(s q + b) into the SW128 A tile
 // Numerics (the configuration's "dequant-to-bf16 GEMMs with fp32 accumulate"):
 // n, the dequantised weights and h are bf16; products accumulate in fp32.
+//
+// The same kernel runs the bf16 shared expert of a batched layer (a_bf16 = 1):
+// the producer loads the weight tiles by TMA straight into the SW128 A stages
+// and the dequant warps stay idle. For the shared gate/up the tile interleaves
+// 8-row boxes of the gate and up matrices (rows 16i..16i+7 gate, 16i+8..16i+15
+// up), so a GELU pair sits in lanes m and m ^ 8 of one epilogue warp.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -87,6 +93,8 @@ struct GemmParams {
     float* yout;
     int ldo;                    // row length of the output (I or H)
     uint32_t* err;
+    int a_bf16;                 // 1: bf16 weight matrices by TMA (tmA, and tmA2 for the up rows); 0: int4 codes
+    int pair_log2;              // gate/up: the up row of tile row m is m ^ (1 << pair_log2)
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -253,7 +261,8 @@ __device__ __forceinline__ uint4 dequant8(uint32_t q, float s, float b) {
 }
 
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-    k_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
+    k_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmA2, GemmParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -271,7 +280,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             mbar_init(bar(BAR_CE + i), N_DQ_WARPS);
         }
         for (int i = 0; i < NA; ++i) {
-            mbar_init(bar(BAR_AF + i), N_DQ_WARPS);
+            mbar_init(bar(BAR_AF + i), p.a_bf16 ? 1 : N_DQ_WARPS);  // TMA bytes, or the dequant warps
             mbar_init(bar(BAR_AE + i), 1);
         }
         for (int i = 0; i < NBST; ++i) {
@@ -299,25 +308,45 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (warp == 0) {
         // ================================================ TMA producer
         if (lane == 0) {
-            int ci = 0, bi = 0, it_local = 0;
+            int ci = 0, bi = 0, ai = 0, it_local = 0;
             bool ok = true;
             for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
                 const Item it = decode_item(p, w);
                 const int sbi = it_local & 1;
-                if (!(ok = wait_bar(bar(BAR_SE + sbi), ((it_local >> 1) & 1) ^ 1, abort_flag, p.err))) break;
-                const uint32_t sb_bytes = (uint32_t)(BM * gpr * 4);
-                mbar_expect_tx(bar(BAR_SF + sbi), sb_bytes);
-                bulk_g2s(smem_u32(smem + OFF_SB + sbi * SB_MAX),
-                         p.ebase + (size_t)it.e * p.estride + p.off_sb + (size_t)it.mt * BM * gpr * 4, sb_bytes,
-                         bar(BAR_SF + sbi));
+                if (!p.a_bf16) {
+                    if (!(ok = wait_bar(bar(BAR_SE + sbi), ((it_local >> 1) & 1) ^ 1, abort_flag, p.err))) break;
+                    const uint32_t sb_bytes = (uint32_t)(BM * gpr * 4);
+                    mbar_expect_tx(bar(BAR_SF + sbi), sb_bytes);
+                    bulk_g2s(smem_u32(smem + OFF_SB + sbi * SB_MAX),
+                             p.ebase + (size_t)it.e * p.estride + p.off_sb + (size_t)it.mt * BM * gpr * 4, sb_bytes,
+                             bar(BAR_SF + sbi));
+                }
                 const int nbox = (it.nrows + BOX_ROWS - 1) / BOX_ROWS;
                 for (int ks = 0; ks < KS; ++ks) {
-                    const int cs = ci % NCS;
-                    if (!(ok = wait_bar(bar(BAR_CE + cs), ((ci / NCS) & 1) ^ 1, abort_flag, p.err))) break;
-                    mbar_expect_tx(bar(BAR_CF + cs), C_BYTES);
-                    tma_load_3d(smem_u32(smem + OFF_C + cs * C_BYTES), &tmA, ks * (BK / 2), it.mt * BM, it.e,
-                                bar(BAR_CF + cs));
-                    ++ci;
+                    if (p.a_bf16) {
+                        const int as = ai % NA;
+                        if (!(ok = wait_bar(bar(BAR_AE + as), ((ai / NA) & 1) ^ 1, abort_flag, p.err))) break;
+                        mbar_expect_tx(bar(BAR_AF + as), A_BYTES);
+                        const uint32_t dst = smem_u32(smem + OFF_A + as * A_BYTES);
+                        if (p.mode == 0) {
+                            // 8 gate rows, then the same 8 up rows, per 16-row band (1 KB boxes keep the SW128 atoms)
+                            for (int g = 0; g < BM / 16; ++g) {
+                                tma_load_2d(dst + g * 2048, &tmA, ks * BK, it.mt * (BM / 2) + g * 8, bar(BAR_AF + as));
+                                tma_load_2d(dst + g * 2048 + 1024, &tmA2, ks * BK, it.mt * (BM / 2) + g * 8,
+                                            bar(BAR_AF + as));
+                            }
+                        } else {
+                            tma_load_2d(dst, &tmA, ks * BK, it.mt * BM, bar(BAR_AF + as));
+                        }
+                        ++ai;
+                    } else {
+                        const int cs = ci % NCS;
+                        if (!(ok = wait_bar(bar(BAR_CE + cs), ((ci / NCS) & 1) ^ 1, abort_flag, p.err))) break;
+                        mbar_expect_tx(bar(BAR_CF + cs), C_BYTES);
+                        tma_load_3d(smem_u32(smem + OFF_C + cs * C_BYTES), &tmA, ks * (BK / 2), it.mt * BM, it.e,
+                                    bar(BAR_CF + cs));
+                        ++ci;
+                    }
                     const int bs = bi % NBST;
                     if (!(ok = wait_bar(bar(BAR_BE + bs), ((bi / NBST) & 1) ^ 1, abort_flag, p.err))) break;
                     mbar_expect_tx(bar(BAR_BF + bs), (uint32_t)(nbox * BOX_ROWS * BK * 2));
@@ -332,6 +361,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 if (j >= 0) wait_bar(bar(BAR_CF + j % NCS), (j / NCS) & 1, abort_flag, p.err);
             for (int j = bi - NBST; j < bi; ++j)
                 if (j >= 0) wait_bar(bar(BAR_BF + j % NBST), (j / NBST) & 1, abort_flag, p.err);
+            for (int j = ai - NA; j < ai; ++j)
+                if (j >= 0) wait_bar(bar(BAR_AF + j % NA), (j / NA) & 1, abort_flag, p.err);
         }
     } else if (warp == 1) {
         // ================================================ MMA issuer
@@ -382,14 +413,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * NB);
             const int nchunks = (it.nrows + 7) / 8;
             if (p.mode == 0) {
-                const int j = (it.mt * BM + m) >> 1;  // h column (gate row 2j, up row 2j+1)
-                const bool up = m & 1;
+                // h column of this row pair: 2^ps gate rows then their 2^ps up rows, repeated
+                const int ps = p.pair_log2;
+                const int j = it.mt * (BM / 2) + ((m >> (ps + 1)) << ps) + (m & ((1 << ps) - 1));
+                const bool up = (m >> ps) & 1;
                 for (int c = 0; c < nchunks; ++c) {
                     float v[8];
                     tc_ld8(tbase + (uint32_t)(c * 8), v);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const float other = __shfl_xor_sync(FULL, v[i], 1);
+                        const float other = __shfl_xor_sync(FULL, v[i], 1 << ps);
                         const float g = up ? other : v[i], u = up ? v[i] : other;
                         const int n = c * 8 + i;
                         if ((i & 1) == (int)up && n < it.nrows) {
@@ -414,7 +447,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(BAR_DE + ab));
         }
-    } else if (warp >= 8) {
+    } else if (warp >= 8 && !p.a_bf16) {
         // ================================================ dequant
         const int t = threadIdx.x - 8 * 32;  // 0..255
         const int r = t >> 1, hf = t & 1;    // weight row in the tile, half of the 64-code group
@@ -565,6 +598,21 @@ __global__ void k_group_inv_init(const int32_t* __restrict__ idx, int P, int E, 
     if (p < P && (unsigned)__ldg(idx + p) >= (unsigned)E) inv[p] = -1;
 }
 
+// Work plan of the shared expert: one "expert" holding all T tokens in order.
+__global__ void k_shared_plan(int T, int mt_gu, int mt_d, int32_t* counts, int32_t* offsets, int32_t* tiles_gu,
+                              int32_t* tiles_d) {
+    if (threadIdx.x == 0) {
+        const int nb = (T + NB - 1) / NB;
+        counts[0] = T;
+        offsets[0] = 0;
+        offsets[1] = T;
+        tiles_gu[0] = 0;
+        tiles_gu[1] = nb * mt_gu;
+        tiles_d[0] = 0;
+        tiles_d[1] = nb * mt_d;
+    }
+}
+
 // r_t = 1/sqrt(mean(x_t^2) + eps) in the canonical order, one warp per token.
 __global__ void k_group_rms(const uint16_t* __restrict__ x, int T, int H, float eps, float* rms) {
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -574,13 +622,14 @@ __global__ void k_group_rms(const uint16_t* __restrict__ x, int T, int H, float 
     if (lane == 0) rms[t] = r;
 }
 
-// Row pos of the permuted activations: bf16(r_t * x_t), t = perm[pos] / k.
+// Row pos of the permuted activations: bf16(r_t * x_t), t = perm[pos] / k
+// (perm NULL: t = pos, the rows in token order).
 __global__ void k_group_gather(const uint16_t* __restrict__ x, const float* __restrict__ rms,
                                const int32_t* __restrict__ perm, int P, int k, int H, uint16_t* xp) {
     const int pos = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (pos >= P) return;
-    const int t = __ldg(perm + pos) / k;
+    const int t = perm ? __ldg(perm + pos) / k : pos;
     const float r = __ldg(rms + t);
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
     uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)pos * H);
@@ -595,8 +644,10 @@ __global__ void k_group_gather(const uint16_t* __restrict__ x, const float* __re
     }
 }
 
-// out[t] = bf16(x[t] + sum_i w[t,i] y[inv[t k + i]]), summed in top-k order.
+// out[t] = bf16(x[t] + delta), delta = ys[t] + sum_i w[t,i] y[inv[t k + i]],
+// the shared term first (ys NULL: none), then the routed terms in top-k order.
 __global__ void k_group_combine(const uint16_t* __restrict__ x, const float* __restrict__ y,
+                                const float* __restrict__ ys,
                                 const int32_t* __restrict__ inv, const float* __restrict__ w, int k, int H,
                                 const uint32_t* err, uint16_t* out, float* delta) {
     const int t = blockIdx.x;
@@ -615,7 +666,7 @@ __global__ void k_group_combine(const uint16_t* __restrict__ x, const float* __r
     }
     __syncthreads();
     for (int j = threadIdx.x * 4; j < H; j += blockDim.x * 4) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 acc = ys ? __ldg(reinterpret_cast<const float4*>(ys + (size_t)t * H + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int i = 0; i < k; ++i) {
             if (rows[i] < 0) continue;
             const float4 v = __ldg(reinterpret_cast<const float4*>(y + (size_t)rows[i] * H + j));
@@ -636,10 +687,12 @@ __global__ void k_group_combine(const uint16_t* __restrict__ x, const float* __r
 // ------------------------------------------------------------------ host
 
 struct Carve {
-    size_t err, counts, offsets, tiles_gu, tiles_d, perm, inv, rms, xp, hb, y, total;
+    size_t err, counts, offsets, tiles_gu, tiles_d, perm, inv, rms, xp, hb, y;
+    size_t s_plan, xn, hs, ys;  // shared expert (S > 0): plan arrays, n in token order, h, y
+    size_t total;
 };
 
-Carve carve(int T, int H, int I, int E, int k) {
+Carve carve(int T, int H, int I, int E, int k, int S) {
     Carve c;
     const size_t P = (size_t)T * k;
     size_t o = 0;
@@ -654,6 +707,13 @@ Carve carve(int T, int H, int I, int E, int k) {
     c.xp = o; o += align_up(P * H * 2, 256);
     c.hb = o; o += align_up(P * I * 2, 256);
     c.y = o; o += align_up(P * H * 4, 256);
+    c.s_plan = c.xn = c.hs = c.ys = 0;
+    if (S > 0) {
+        c.s_plan = o; o += 256;  // counts[1], offsets[2], tiles_gu[2], tiles_d[2]
+        c.xn = o; o += align_up((size_t)T * H * 2, 256);
+        c.hs = o; o += align_up((size_t)T * S * 2, 256);
+        c.ys = o; o += align_up((size_t)T * H * 4, 256);
+    }
     c.total = o;
     return c;
 }
@@ -684,46 +744,53 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, 
     return r == CUDA_SUCCESS;
 }
 
-}  // namespace grouped
-}  // namespace tf
-
-using namespace tf;
-
-extern "C" {
-
-size_t tf_moe_grouped_workspace_bytes(int T, int H, int I, int E, int k) {
-    if (T < 1 || H < 64 || I < 64 || E < 1 || E > TF_MAX_E || k < 1 || k > TF_MAX_K) return 0;
-    return grouped::carve(T, H, I, E, k).total;
+// Row-major bf16 [rows, cols] as a 2-D SW128 map with boxes of 64 columns (128 bytes) x box_rows rows.
+bool encode_rows(CUtensorMap* m, const void* base, int cols, int rows, int box_rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t str[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {BK, (cuuint32_t)box_rows};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-tf_status tf_moe_ffn_grouped(const void* x, void* out, int T, const tf_expert_table* table, int E, const int32_t* idx,
-                             const float* w, int k, int H, int I, float* delta, int32_t* perm_out, int32_t* counts_out,
-                             void* workspace, size_t ws_bytes, void* stream) {
+}  // namespace grouped
+
+size_t grouped_workspace_bytes(int T, int H, int I, int E, int k, int S) {
+    if (T < 1 || H < 64 || I < 64 || E < 1 || E > TF_MAX_E || k < 1 || k > TF_MAX_K || S < 0) return 0;
+    return grouped::carve(T, H, I, E, k, S).total;
+}
+
+tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     using namespace grouped;
-    const char* fn = "tf_moe_ffn_grouped";
-    if (!x || !out || !table || !idx || !w || !workspace) return fail(TF_ERR_INVALID_ARG, "%s: null pointer", fn);
-    if (x == out) return fail(TF_ERR_INVALID_ARG, "%s: out must not alias x", fn);
+    const int T = a.T, H = a.H, I = a.I, E = a.E, k = a.k, S = a.S;
+    const tf_expert_table* table = a.table;
+    if (!a.x || !a.out || !table || !a.idx || !a.w || !a.ws) return fail(TF_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (a.x == a.out) return fail(TF_ERR_INVALID_ARG, "%s: out must not alias x", fn);
     if (T < 1) return fail(TF_ERR_INVALID_ARG, "%s: T=%d", fn, T);
     if (H % 128 || I % 64 || H > 2816 || H < 128 || I < 64)
         return fail(TF_ERR_INVALID_ARG, "%s: H must be a multiple of 128 (<= 2816) and I a multiple of 64 (H=%d I=%d)",
                     fn, H, I);
     if (E < 1 || E > TF_MAX_E || k < 1 || k > TF_MAX_K || k > E)
         return fail(TF_ERR_INVALID_ARG, "%s: E=%d k=%d out of range", fn, E, k);
+    if (S < 0 || S % 64 || (S > 0 && (!a.Wsg || !a.Wsu || !a.Wsd)))
+        return fail(TF_ERR_INVALID_ARG, "%s: the shared expert needs S a multiple of 64 and three weights (S=%d)", fn,
+                    S);
+    if (S > 0 && (!aligned16(a.Wsg) || !aligned16(a.Wsu) || !aligned16(a.Wsd)))
+        return fail(TF_ERR_INVALID_ARG, "%s: shared weights must be 16-byte aligned", fn);
     if (!table->base || !aligned16(table->base) || table->stride % 16)
         return fail(TF_ERR_INVALID_ARG, "%s: expert table base and stride must be 16-byte aligned", fn);
     if (table->slot_of_expert)
         return fail(TF_ERR_NOT_SUPPORTED, "%s: the grouped path takes a resident expert table (no slot map)", fn);
-    if (!aligned16(x) || !aligned16(out) || (delta && !aligned16(delta)))
+    if (!aligned16(a.x) || !aligned16(a.out) || (a.delta && !aligned16(a.delta)))
         return fail(TF_ERR_INVALID_ARG, "%s: x, out and delta must be 16-byte aligned", fn);
     if ((size_t)T * k > (size_t)INT32_MAX / 4) return fail(TF_ERR_INVALID_ARG, "%s: T*k too large", fn);
-    const Carve c = carve(T, H, I, E, k);
-    if (ws_bytes < c.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    const Carve c = carve(T, H, I, E, k, S);
+    if (a.ws_bytes < c.total || (reinterpret_cast<uintptr_t>(a.ws) & 255))
         return fail(TF_ERR_INVALID_ARG, "%s: workspace misaligned or smaller than %zu bytes", fn, c.total);
     ExpertLayout lay;
     expert_layout(H, I, &lay);
     if (table->stride < lay.payload) return fail(TF_ERR_INVALID_ARG, "%s: expert stride below the payload size", fn);
 
-    char* ws = static_cast<char*>(workspace);
+    char* ws = static_cast<char*>(a.ws);
     uint32_t* err = reinterpret_cast<uint32_t*>(ws + c.err);
     int32_t* counts = reinterpret_cast<int32_t*>(ws + c.counts);
     int32_t* offsets = reinterpret_cast<int32_t*>(ws + c.offsets);
@@ -735,6 +802,10 @@ tf_status tf_moe_ffn_grouped(const void* x, void* out, int T, const tf_expert_ta
     uint16_t* xp = reinterpret_cast<uint16_t*>(ws + c.xp);
     uint16_t* hb = reinterpret_cast<uint16_t*>(ws + c.hb);
     float* y = reinterpret_cast<float*>(ws + c.y);
+    int32_t* s_plan = S > 0 ? reinterpret_cast<int32_t*>(ws + c.s_plan) : nullptr;
+    uint16_t* xn = S > 0 ? reinterpret_cast<uint16_t*>(ws + c.xn) : nullptr;
+    uint16_t* hs = S > 0 ? reinterpret_cast<uint16_t*>(ws + c.hs) : nullptr;
+    float* ys = S > 0 ? reinterpret_cast<float*>(ws + c.ys) : nullptr;
     const int P = T * k;
 
     // tensor maps: codes of every expert (3-D), permuted activations and h (2-D, SW128)
@@ -756,19 +827,16 @@ tf_status tf_moe_ffn_grouped(const void* x, void* out, int T, const tf_expert_ta
                     CU_TENSOR_MAP_SWIZZLE_NONE))
             return fail(TF_ERR_CUDA, "%s: tensor map of the down codes", fn);
     }
-    {
-        cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)P};
-        cuuint64_t str[1] = {(cuuint64_t)H * 2};
-        cuuint32_t box[2] = {BK, BOX_ROWS};
-        if (!encode(&tmB_gu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xp, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
-            return fail(TF_ERR_CUDA, "%s: tensor map of the permuted activations", fn);
-    }
-    {
-        cuuint64_t dims[2] = {(cuuint64_t)I, (cuuint64_t)P};
-        cuuint64_t str[1] = {(cuuint64_t)I * 2};
-        cuuint32_t box[2] = {BK, BOX_ROWS};
-        if (!encode(&tmB_d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, hb, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
-            return fail(TF_ERR_CUDA, "%s: tensor map of h", fn);
+    if (!encode_rows(&tmB_gu, xp, H, P, BOX_ROWS))
+        return fail(TF_ERR_CUDA, "%s: tensor map of the permuted activations", fn);
+    if (!encode_rows(&tmB_d, hb, I, P, BOX_ROWS)) return fail(TF_ERR_CUDA, "%s: tensor map of h", fn);
+    // shared expert: bf16 weights as SW128 row boxes (8 rows for the interleaved gate/up tile, 128 for down)
+    CUtensorMap tmS_g, tmS_u, tmS_d, tmS_xn, tmS_h;
+    if (S > 0) {
+        if (!encode_rows(&tmS_g, a.Wsg, H, S, 8) || !encode_rows(&tmS_u, a.Wsu, H, S, 8) ||
+            !encode_rows(&tmS_d, a.Wsd, S, H, BM) || !encode_rows(&tmS_xn, xn, H, T, BOX_ROWS) ||
+            !encode_rows(&tmS_h, hs, S, T, BOX_ROWS))
+            return fail(TF_ERR_CUDA, "%s: tensor maps of the shared expert", fn);
     }
     static bool attr_set = false;
     if (!attr_set) {
@@ -783,12 +851,17 @@ tf_status tf_moe_ffn_grouped(const void* x, void* out, int T, const tf_expert_ta
     clear_error();
 
     const int mt_gu = 2 * I / BM, mt_d = H / BM;
+    const uint16_t* x16 = static_cast<const uint16_t*>(a.x);
     prof_before(TF_KERNEL_PERMUTE, stream);
-    k_group_rms<<<(T + 7) / 8, 256, 0, st>>>(static_cast<const uint16_t*>(x), T, H, 1e-6f, rms);
-    k_group_hist<<<1, 1024, 0, st>>>(idx, P, E, mt_gu, mt_d, counts, offsets, tiles_gu, tiles_d);
-    k_group_pos<<<E, 1024, 0, st>>>(idx, P, offsets, perm, inv);
-    k_group_inv_init<<<(P + 255) / 256, 256, 0, st>>>(idx, P, E, inv);
-    k_group_gather<<<(P + 7) / 8, 256, 0, st>>>(static_cast<const uint16_t*>(x), rms, perm, P, k, H, xp);
+    k_group_rms<<<(T + 7) / 8, 256, 0, st>>>(x16, T, H, a.eps, rms);
+    k_group_hist<<<1, 1024, 0, st>>>(a.idx, P, E, mt_gu, mt_d, counts, offsets, tiles_gu, tiles_d);
+    k_group_pos<<<E, 1024, 0, st>>>(a.idx, P, offsets, perm, inv);
+    k_group_inv_init<<<(P + 255) / 256, 256, 0, st>>>(a.idx, P, E, inv);
+    k_group_gather<<<(P + 7) / 8, 256, 0, st>>>(x16, rms, perm, P, k, H, xp);
+    if (S > 0) {
+        k_group_gather<<<(T + 7) / 8, 256, 0, st>>>(x16, rms, nullptr, T, 1, H, xn);
+        k_shared_plan<<<1, 32, 0, st>>>(T, 2 * S / BM, H / BM, s_plan, s_plan + 1, s_plan + 3, s_plan + 5);
+    }
     prof_after(TF_KERNEL_PERMUTE, stream);
     if (cudaError_t e = cudaGetLastError()) return cuda_status(e, fn);
 
@@ -809,7 +882,7 @@ tf_status tf_moe_ffn_grouped(const void* x, void* out, int T, const tf_expert_ta
     gp.mode = 0;
     gp.hout = hb;
     gp.ldo = I;
-    k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmA_gu, tmB_gu, gp);
+    k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmA_gu, tmB_gu, tmA_gu, gp);
     gp.off_sb = lay.d_sb;
     gp.K = I;
     gp.MT = mt_d;
@@ -818,17 +891,74 @@ tf_status tf_moe_ffn_grouped(const void* x, void* out, int T, const tf_expert_ta
     gp.hout = nullptr;
     gp.yout = y;
     gp.ldo = H;
-    k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmA_d, tmB_d, gp);
+    k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmA_d, tmB_d, tmA_d, gp);
+    if (S > 0) {
+        GemmParams sp;
+        std::memset(&sp, 0, sizeof(sp));
+        sp.E = 1;
+        sp.counts = s_plan;
+        sp.offsets = s_plan + 1;
+        sp.err = err;
+        sp.a_bf16 = 1;
+        sp.pair_log2 = 3;
+        sp.K = H;
+        sp.MT = 2 * S / BM;
+        sp.tiles = s_plan + 3;
+        sp.mode = 0;
+        sp.hout = hs;
+        sp.ldo = S;
+        k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmS_g, tmS_xn, tmS_u, sp);
+        sp.K = S;
+        sp.MT = H / BM;
+        sp.tiles = s_plan + 5;
+        sp.mode = 1;
+        sp.hout = nullptr;
+        sp.yout = ys;
+        sp.ldo = H;
+        k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmS_d, tmS_h, tmS_d, sp);
+    }
     prof_after(TF_KERNEL_GEMM, stream);
     if (cudaError_t e = cudaGetLastError()) return cuda_status(e, fn);
 
     prof_before(TF_KERNEL_COMBINE, stream);
-    k_group_combine<<<T, 256, 0, st>>>(static_cast<const uint16_t*>(x), y, inv, w, k, H, err,
-                                       static_cast<uint16_t*>(out), delta);
+    k_group_combine<<<T, 256, 0, st>>>(x16, y, ys, inv, a.w, k, H, err, static_cast<uint16_t*>(a.out), a.delta);
     prof_after(TF_KERNEL_COMBINE, stream);
-    if (perm_out) cudaMemcpyAsync(perm_out, perm, (size_t)P * 4, cudaMemcpyDeviceToDevice, st);
-    if (counts_out) cudaMemcpyAsync(counts_out, counts, (size_t)E * 4, cudaMemcpyDeviceToDevice, st);
+    if (a.perm_out) cudaMemcpyAsync(a.perm_out, perm, (size_t)P * 4, cudaMemcpyDeviceToDevice, st);
+    if (a.counts_out) cudaMemcpyAsync(a.counts_out, counts, (size_t)E * 4, cudaMemcpyDeviceToDevice, st);
     return cuda_status(cudaGetLastError(), fn);
+}
+
+}  // namespace tf
+
+extern "C" {
+
+size_t tf_moe_grouped_workspace_bytes(int T, int H, int I, int E, int k) {
+    return tf::grouped_workspace_bytes(T, H, I, E, k, 0);
+}
+
+tf_status tf_moe_ffn_grouped(const void* x, void* out, int T, const tf_expert_table* table, int E, const int32_t* idx,
+                             const float* w, int k, int H, int I, float* delta, int32_t* perm_out, int32_t* counts_out,
+                             void* workspace, size_t ws_bytes, void* stream) {
+    tf::GroupedArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.x = x;
+    a.out = out;
+    a.T = T;
+    a.table = table;
+    a.E = E;
+    a.k = k;
+    a.H = H;
+    a.I = I;
+    a.idx = idx;
+    a.w = w;
+    a.delta = delta;
+    a.perm_out = perm_out;
+    a.counts_out = counts_out;
+    a.S = 0;
+    a.eps = 1e-6f;
+    a.ws = workspace;
+    a.ws_bytes = ws_bytes;
+    return tf::grouped_run(a, stream, "tf_moe_ffn_grouped");
 }
 
 }  // extern "C"

@@ -80,6 +80,31 @@ int launch_down(const DecodeParams& p, int with_routed, int with_shared, void* s
 int launch_dequant(const char* blob, int H, int I, int matrix, int as_bf16, void* out,
                    size_t off_sb, size_t off_codes, void* stream);
 
+// The grouped (batched / prefill) layer of tf_grouped.cu: routed experts by
+// tcgen05 GEMMs over the token x expert permutation and, when S > 0, the bf16
+// shared expert by the same GEMM kernel with TMA-loaded weights.
+struct GroupedArgs {
+    const void* x;                 // bf16 [T, H]
+    void* out;                     // bf16 [T, H]
+    int T;
+    const tf_expert_table* table;  // resident experts
+    int E, k, H, I;
+    const int32_t* idx;            // device [T, k]
+    const float* w;                // device [T, k]
+    float* delta;                  // nullable fp32 [T, H]
+    int32_t* perm_out;             // nullable [T*k]
+    int32_t* counts_out;           // nullable [E]
+    const void* Wsg;               // bf16 [S, H]; S = 0: no shared expert
+    const void* Wsu;               // bf16 [S, H]
+    const void* Wsd;               // bf16 [H, S]
+    int S;
+    float eps;
+    void* ws;
+    size_t ws_bytes;
+};
+size_t grouped_workspace_bytes(int T, int H, int I, int E, int k, int S);
+tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn);
+
 }  // namespace tf
 
 // Per-layer LFU metadata (host). Defined here so the layer step can reach the

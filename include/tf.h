@@ -309,11 +309,19 @@ typedef struct {
     float copy_ms;                 /* copy-stream time of the miss fills (measure = 1 only) */
     float shared_ms;               /* compute-stream time of the shared-expert branch (measure = 1) */
     float stall_ms;                /* max(0, copies end - shared branch end) (measure = 1) */
+    int32_t ids[TF_MAX_K];         /* the k selected experts in top-k order (cached step only; the
+                                      host reads them anyway to decide the copies) */
 } tf_step_stats;
 
 /*
  * out = layer(x). T tokens (T = 1 with a cache). logit_bias as in tf_router_topk.
  * Without a cache all work is enqueued on compute_stream and the call returns.
+ * T > 1 (at most the handle's T_max; batched decode or prefill): the router for
+ * all T tokens, then the grouped path of tf_moe_ffn_grouped (same requirements:
+ * H a multiple of 128 up to 2816, I a multiple of 64) with the shared expert
+ * (S a multiple of 64) run by the same tcgen05 GEMM kernel on its bf16
+ * weights; out = bf16(x + shared + sum_i w_i y_i), each operand of the GEMMs
+ * rounded to bf16 as in tf_moe_ffn_grouped. stats stay zero for T > 1.
  * With a cache (T = 1), the call enqueues the router and the shared branch,
  * waits on the host for the k selected ids (one small device->host copy: the
  * CPU decides the I/O), updates the LFU metadata for layer `layer` at `step`,
@@ -378,7 +386,8 @@ tf_status tf_stack_set_prefetch(tf_stack* s, int on);
  * finished its routed gate/up tasks, 7 its layer work; and at which the CTA's
  * first worker warp 8 finished its shared gate/up items, 9 had its first routed
  * gate/up data, 10 finished its routed gate/up items, 11 finished its shared-down
- * items, 12 had its routed-down data, 13 finished the layer. NULL turns tracing
+ * items, 12 had its routed-down data, 13 finished the layer, 14 finished
+ * computing its first routed gate/up item, 15 its last. NULL turns tracing
  * off. */
 tf_status tf_stack_set_trace(tf_stack* s, void* buffer, size_t bytes);
 /* out = stack(x) for one token; x, out device bf16 [H], 16-byte aligned, out != x. */

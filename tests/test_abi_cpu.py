@@ -142,6 +142,11 @@ def test_workspace_sizes():
     assert B.tf_moe_decode_workspace_bytes(2816, 704, 8) == 8 * 704 * 4
     d = B.layer_desc(2816, 704, 128, 8, 2112, 16, 16, 16, 16, B.ExpertTable(16, 16, None))
     assert B.tf_layer_workspace_bytes(d, 1) > 8 * 704 * 4 + 2112 * 4
+    # a handle for batched steps also holds the grouped path's buffers and the shared expert's n, h and y
+    T = 64
+    w64 = B.tf_layer_workspace_bytes(d, T)
+    assert w64 >= B.tf_layer_workspace_bytes(d, 1) + B.tf_moe_grouped_workspace_bytes(T, H, I, E, k) + \
+        T * H * 2 + T * 2112 * 2 + T * H * 4
 
 
 # ------------------------------------------------------------- LFU metadata

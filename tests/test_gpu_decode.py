@@ -265,6 +265,7 @@ def test_cached_step_traces_and_outputs(cfg, L, slots, steps):
             ev = lfu.step(step, l, ids)
             want += ev
             assert st.hits + st.misses == k and st.misses == sum(1 for e in ev if not e[3])
+            assert list(st.ids[:k]) == ids.tolist()
             assert st.bytes_fetched == st.misses * cached.payload
             # the cached path computes the same bits as the resident one
             assert torch.equal(out_c.view(torch.int16), out_r.view(torch.int16))
