@@ -247,14 +247,16 @@ def run_ours(args, rank, world):
 # ------------------------------------------------------------------ streamed experts (LFU cache, host store)
 
 STREAM_SEED, STREAM_ZIPF, STREAM_SLOTS = 2, 1.1, 16
-STREAM_ALPHA = 0.35    # Zipf bias scale that puts the LFU hit rate in the 60-70 % band
+STREAM_ALPHA = 0.1     # Zipf bias scale
+STREAM_NOISE = 1.5     # sigma of the per-(step, layer) router-logit noise (the token-dependent part of the logits)
 STREAM_METRIC = "MoE decode tok/s with experts streamed from pinned host memory through a 16-slot LFU cache (1 B300)"
 STREAM_WORKLOAD = ("30-layer MoE-only decode stack, batch 1, a fresh x ~ N(0,1) per step (the next token's input); "
                    "experts (12.9 GB, 3,840 x 3.36 MB) in "
                    "pinned host memory, a 16-slot-per-layer LFU cache in HBM (1.61 GB), misses copied by "
-                   "cudaMemcpyAsync on a copy stream overlapped with the shared expert; router logits biased by "
-                   "Zipf(1.1) popularity (alpha %.2f) over a seeded per-layer rank->expert map, and with probability "
-                   "0.5 per (step, layer) +30 on the previous step's 8 ids; seed 2")
+                   "cudaMemcpyAsync on a copy stream overlapped with the shared expert; router logit bias = Zipf(1.1) "
+                   "popularity (alpha %.2f) over a seeded per-layer rank->expert map + N(0, %.2f) noise per (step, layer) "
+                   "(the synthetic weights route every token alike beyond layer 0) + 30 on the previous step's 8 ids "
+                   "with probability 0.5 per (step, layer); seed 2")
 
 
 def h2d_probe(dev, copy_stream, n_slots=32, reps=5):
@@ -283,12 +285,11 @@ def run_streaming(args):
     import workload as W
     from workload.model import SyntheticStack, hidden_tensor
 
-    seed, alpha = STREAM_SEED, args.alpha
+    seed, alpha, sigma = STREAM_SEED, args.alpha, args.noise
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stack = SyntheticStack(seed, L, H=H, I=I, E=E, k=K_ACT, S=S, resident=False, n_slots=STREAM_SLOTS, device=dev)
     zipf_h = np.stack([W.zipf_bias(seed, l, E, STREAM_ZIPF, alpha)[0] for l in range(L)])
-    zipf_d = torch.from_numpy(zipf_h).to(dev)
     bias_h = torch.empty(L, E, dtype=torch.float32, pin_memory=True)
     bias_hn = bias_h.numpy()
     bias_d = torch.empty(L, E, dtype=torch.float32, device=dev)
@@ -298,6 +299,7 @@ def run_streaming(args):
     # one fresh input per step: a fed-back output settles on a fixed point whose routing never changes
     n_inputs = args.warmup + args.steps + min(args.steps, 32) + min(args.steps, 64)
     xs = torch.stack([hidden_tensor(seed, t, 1, H, device=dev)[0] for t in range(n_inputs)])
+    noise = np.stack([np.stack([W.route_noise(seed, l, t, E, sigma) for l in range(L)]) for t in range(n_inputs)])
     bufs = [torch.empty(H, dtype=torch.bfloat16, device=dev) for _ in range(5)]   # 0-1 outputs, 2-3 scratch, 4 input
     prev = [None] * L
     tot = {"hits": 0, "misses": 0, "bytes": 0, "stall_ms": 0.0, "copy_ms": 0.0, "shared_ms": 0.0, "tokens": 0}
@@ -305,13 +307,11 @@ def run_streaming(args):
     def token(step, src, dst, measure=0):
         x = src
         for l in range(L):
+            bias_hn[l] = zipf_h[l] + noise[step, l]
             if prev[l] is not None and W.coin(seed, l, step):
-                bias_hn[l] = zipf_h[l]
                 bias_hn[l, prev[l]] += 30.0
-                bias_d[l].copy_(bias_h[l], non_blocking=True)
-                bias = bias_d[l]
-            else:
-                bias = zipf_d[l]
+            bias_d[l].copy_(bias_h[l], non_blocking=True)
+            bias = bias_d[l]
             y = dst if l == L - 1 else bufs[2 + l % 2]
             st = B.tf_layer_step(stack.layers[l], stack.cache, l, step, stack.store, x, y, 1, bias, 0, stream,
                                  copy_stream, measure)
@@ -380,8 +380,9 @@ def run_streaming(args):
         "metric": STREAM_METRIC, "value": round(n / (ms / 1000.0), 2), "unit": "tok/s", "n_gpus": 1, "steps": n,
         "warmup": args.warmup, "ms_per_step": round(ms / n, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": STREAM_WORKLOAD % alpha, "layers": L, "slots_per_layer": STREAM_SLOTS,
-                   "zipf_s": STREAM_ZIPF, "zipf_alpha": alpha, "repeat_p": 0.5, "repeat_bonus": 30.0,
+        "config": {"workload": STREAM_WORKLOAD % (alpha, sigma), "layers": L, "slots_per_layer": STREAM_SLOTS,
+                   "zipf_s": STREAM_ZIPF, "zipf_alpha": alpha, "logit_noise_sigma": sigma, "repeat_p": 0.5,
+                   "repeat_bonus": 30.0,
                    "l2": "no flush: every step streams 1.1 GB of resident shared/router weights plus the cached "
                          "experts, far above the 126 MB L2"},
         "hit_rate": round(timed["hits"] / max(1, lookups), 4),
@@ -683,6 +684,8 @@ def main():
                          "batched: the stack with 64 tokens per step")
     ap.add_argument("--alpha", type=float, default=STREAM_ALPHA,
                     help="streaming: scale of the Zipf(1.1) router bias")
+    ap.add_argument("--noise", type=float, default=STREAM_NOISE,
+                    help="streaming: sigma of the per-(step, layer) router-logit noise")
     ap.add_argument("--layers", type=int, default=L,
                     help="stack depth; the benchmark workload is 30, fewer only for small profiling captures")
     args = ap.parse_args()

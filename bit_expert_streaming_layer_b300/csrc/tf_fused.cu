@@ -202,6 +202,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 // Blocking test: the thread sleeps until the phase completes or about ns elapse.
+// Non-blocking test of a phase (try_wait may suspend the thread for a while).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ bool mbar_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
     uint32_t ok;
     asm volatile(
@@ -280,7 +290,7 @@ __device__ __forceinline__ bool err_set(const uint32_t* err) { return *(volatile
 
 // Bounded wait on an mbarrier phase (one lane); false (error recorded) on timeout or when another CTA failed.
 __device__ bool wait_mbar(uint32_t bar, uint32_t parity, uint32_t* err) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = gtimer();
     for (uint32_t n = 1;; ++n) {
         if (mbar_wait_hint(bar, parity, SUSPEND_NS)) return true;
@@ -356,9 +366,44 @@ struct Route {
 };
 static_assert(sizeof(Route) <= RT_BYTES, "routing cache");
 
-// Lane 0 enqueues the copies of one item into a stage.
-__device__ void issue_item(const Ctx& c, const It& it, const Route* rt, uint32_t dst, uint32_t bar, uint64_t pol) {
+// The warp enqueues the copies of one item into a stage: lane 0 announces the
+// bytes on the stage's mbarrier, then one lane per copy issues it (an item's
+// copies leave in parallel instead of one after another).
+__device__ void issue_item(const Ctx& c, const It& it, const Route* rt, uint32_t dst, uint32_t bar, uint64_t pol,
+                           int lane) {
     const LayerDesc& D = LD(it.l);
+    if (it.kind == T_DOWN && it.sub == 2) {
+        if (lane == 0) mbar_expect_tx(bar, DN_BYTES);
+        __syncwarp();
+        if (lane < 2 * K) {
+            fence_proxy_async();  // the stage's previous contents were read through the generic proxy
+            const int j0 = 2 * (it.t - D.E - N_SGU - N_RGU);
+            const int i = lane & (K - 1);
+            const char* ep = rt->ep[it.l & 1][i];
+            if (lane < K)
+                bulk_g2s(dst + i * 2 * D_ROW, ep + D.off_d_codes + (size_t)j0 * D_ROW, 2 * D_ROW, bar, pol);
+            else
+                bulk_g2s(dst + DN_SB_OFF + i * 4 * D_SB, ep + D.off_d_sb + (size_t)(j0 & ~3) * D_SB, 4 * D_SB, bar,
+                         pol);
+        }
+        return;
+    }
+    if (it.kind == T_RGU) {
+        if (lane == 0) mbar_expect_tx(bar, RGU_BYTES);
+        __syncwarp();
+        if (lane < 2) {
+            fence_proxy_async();
+            const int u = it.t - D.E - N_SGU;
+            const int i = u / RGU_PER_EXPERT, p0 = 2 * (u % RGU_PER_EXPERT);
+            const char* ep = rt->ep[it.l & 1][i];
+            if (lane == 0)
+                bulk_g2s(dst, ep + (size_t)2 * p0 * GU_ROW, 4 * GU_ROW, bar, pol);
+            else
+                bulk_g2s(dst + 4 * GU_ROW, ep + D.off_gu_sb + (size_t)2 * p0 * GU_SB, 4 * GU_SB, bar, pol);
+        }
+        return;
+    }
+    if (lane != 0) return;
     fence_proxy_async();  // the stage's previous contents were read through the generic proxy
     if (it.kind == T_ROUTER) {
         mbar_expect_tx(bar, ROW_BF);
@@ -367,28 +412,10 @@ __device__ void issue_item(const Ctx& c, const It& it, const Route* rt, uint32_t
         const int j = it.t - D.E;
         mbar_expect_tx(bar, ROW_BF);
         bulk_g2s(dst, (it.sub == 0 ? D.Wsg : D.Wsu) + (size_t)j * H, ROW_BF, bar, pol);
-    } else if (it.kind == T_RGU) {
-        const int u = it.t - D.E - N_SGU;
-        const int i = u / RGU_PER_EXPERT, p0 = 2 * (u % RGU_PER_EXPERT);
-        const char* ep = rt->ep[it.l & 1][i];
-        mbar_expect_tx(bar, RGU_BYTES);
-        bulk_g2s(dst, ep + (size_t)2 * p0 * GU_ROW, 4 * GU_ROW, bar, pol);
-        bulk_g2s(dst + 4 * GU_ROW, ep + D.off_gu_sb + (size_t)2 * p0 * GU_SB, 4 * GU_SB, bar, pol);
     } else {
         const int j0 = 2 * (it.t - D.E - N_SGU - N_RGU);
-        if (it.sub < 2) {
-            mbar_expect_tx(bar, SROW_BF);
-            bulk_g2s(dst, D.Wsd + (size_t)(j0 + it.sub) * S, SROW_BF, bar, pol);
-        } else {
-            mbar_expect_tx(bar, DN_BYTES);
-#pragma unroll
-            for (int i = 0; i < K; ++i) {
-                const char* ep = rt->ep[it.l & 1][i];
-                bulk_g2s(dst + i * 2 * D_ROW, ep + D.off_d_codes + (size_t)j0 * D_ROW, 2 * D_ROW, bar, pol);
-                bulk_g2s(dst + DN_SB_OFF + i * 4 * D_SB, ep + D.off_d_sb + (size_t)(j0 & ~3) * D_SB, 4 * D_SB, bar,
-                         pol);
-            }
-        }
+        mbar_expect_tx(bar, SROW_BF);
+        bulk_g2s(dst, D.Wsd + (size_t)(j0 + it.sub) * S, SROW_BF, bar, pol);
     }
 }
 
@@ -669,34 +696,39 @@ __device__ bool route_layer(const Params& P, int l, uint32_t tag, uint32_t epoch
         }
     }
     if (lane == 0) trace_at(P, l, TR_Z_READY);
-    // order-preserving keys in place of the tags (larger logit first, -0 == +0,
-    // NaN lowest but above "taken" = 0); every round takes the best remaining key
-    // and the lowest index holding it with two warp reductions
-    uint32_t* keys = reinterpret_cast<uint32_t*>(smem + OFF_Z) + 2 * MAX_E;  // after the tagged words
-    for (int j = lane; j < D.E; j += 32) {
-        const float v = __uint_as_float((uint32_t)zt[j]) + 0.0f;
-        const uint32_t u = __float_as_uint(v);
-        keys[j] = isnan(v) ? 1u : ((u & 0x80000000u) ? ~u : (u | 0x80000000u));
+    // order-preserving keys (larger logit first, -0 == +0, NaN lowest but above
+    // "taken" = 0), held in registers (key m of a lane is expert lane + 32 m);
+    // every round takes the best remaining key and the lowest index holding it
+    // with two warp reductions
+    constexpr int KPL = MAX_E / 32;
+    uint32_t key[KPL];
+#pragma unroll
+    for (int m = 0; m < KPL; ++m) {
+        const int j = lane + 32 * m;
+        key[m] = 0u;
+        if (j < D.E) {
+            const float v = __uint_as_float((uint32_t)zt[j]) + 0.0f;
+            const uint32_t u = __float_as_uint(v);
+            key[m] = isnan(v) ? 1u : ((u & 0x80000000u) ? ~u : (u | 0x80000000u));
+        }
     }
-    __syncwarp();
     float selz = 0.0f;
     int sel = -1;
 #pragma unroll 1
     for (int i = 0; i < K; ++i) {
-        uint32_t bk = 0u;
-        int bi = 0x7fffffff;
-#pragma unroll 1
-        for (int j = lane; j < D.E; j += 32) {
-            const uint32_t kj = keys[j];
-            if (kj > bk) {  // j increases: equal keys keep the lower index
-                bk = kj;
-                bi = j;
+        uint32_t bk = key[0];
+        int bm = 0;
+#pragma unroll
+        for (int m = 1; m < KPL; ++m)
+            if (key[m] > bk) {  // m increases: equal keys keep the lower index
+                bk = key[m];
+                bm = m;
             }
-        }
         const uint32_t kmax = __reduce_max_sync(FULL, bk);
-        const int imin = (int)__reduce_min_sync(FULL, bk == kmax ? (uint32_t)bi : 0x7fffffffu);
-        if (lane == (imin & 31)) keys[imin] = 0u;
-        __syncwarp();
+        const int imin = (int)__reduce_min_sync(FULL, bk == kmax ? (uint32_t)(lane + 32 * bm) : 0x7fffffffu);
+#pragma unroll
+        for (int m = 0; m < KPL; ++m)  // a select per register (a value test keeps the array out of local memory)
+            key[m] = (key[m] == kmax && lane + 32 * m == imin) ? 0u : key[m];
         if (lane == i) {
             sel = imin;
             selz = __uint_as_float((uint32_t)zt[imin]);
@@ -912,7 +944,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
     auto topk_known = [&](int lt) -> bool {
         while (k_seen <= lt) {
             int rdy = 0;
-            if (lane == 0) rdy = mbar_try_wait(bar_k, k_seen & 1);
+            if (lane == 0) rdy = mbar_test_wait(bar_k, k_seen & 1);
             if (!__shfl_sync(FULL, rdy, 0)) return false;
             ++k_seen;
         }
@@ -922,10 +954,8 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
     auto try_issue = [&]() {
         while (n_iss < n_con + NS && iss.l < P.L) {
             if (it_needs_topk(iss) && !topk_known(iss.l)) break;
-            if (lane == 0) {
-                const int slot = n_iss % NS;
-                issue_item(c, iss, rt, ring_u32 + slot * STAGE, bar0 + 8 * slot, pol);
-            }
+            const int slot = n_iss % NS;
+            issue_item(c, iss, rt, ring_u32 + slot * STAGE, bar0 + 8 * slot, pol, lane);
             ++n_iss;
             it_next(iss, c);
         }
@@ -1002,7 +1032,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
             if (con.kind == T_ROUTER) {
                 const uint16_t* wrow = reinterpret_cast<const uint16_t*>(st);
                 float d = 0.0f;
-#pragma unroll 4
+#pragma unroll 8
                 for (int k = lane; k < H; k += 32) d = fmaf(bf2f(wrow[k]), bf2f(xs[k]), d);  // exact products
                 d = warp_sum_canonical(d);
                 float z = __fmul_rn(r, d);

@@ -32,6 +32,7 @@ T_B = 5          # expert fp16 biases
 T_SH = 6         # shared-expert bf16 weights (matrix 0 gate, 1 up, 2 down)
 T_ZIPF = 7       # Zipf rank -> expert permutation
 T_COIN = 8       # per-(step, layer) coin of the repeat-previous-top-k workload
+T_NOISE = 9      # per-(step, layer) router-logit noise of the streaming workload
 
 GATE, UP, DOWN = 0, 1, 2
 GROUP = 64
@@ -126,6 +127,13 @@ def zipf_bias(seed: int, layer: int, E: int, s: float, alpha: float = 1.0):
 def coin(seed: int, layer: int, step: int) -> bool:
     """Fair coin for (step, layer) of the repeat-previous-top-k workload."""
     return lib().wl_unif53(key(seed, T_COIN, layer), step) < 0.5
+
+
+def route_noise(seed: int, layer: int, step: int, E: int, sigma: float) -> np.ndarray:
+    """N(0, sigma) per expert for (step, layer), as float32 (bf16-rounded values): the token-dependent part of the
+    router logits in the streaming workload."""
+    bits = normal_bf16(key(seed, T_NOISE, layer, step), E, sigma)
+    return (bits.astype(np.uint32) << 16).view(np.float32)
 
 
 def hidden(seed: int, step: int, T: int, H: int) -> np.ndarray:
