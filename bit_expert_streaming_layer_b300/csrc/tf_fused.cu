@@ -96,7 +96,10 @@ constexpr int OFF_H = OFF_SN + HW * 4;                   // tagged fp32 h_routed
                                                          // landing zone of the tagged layer input
 constexpr int OFF_SH = OFF_H + H_FLOATS * 4;             // fp32 word sums of h_routed [K*I/8]
 constexpr int OFF_Z = OFF_SH + (K * I / 8) * 4;          // tagged logits [MAX_E] (64-bit words), then top-k keys [MAX_E]
-constexpr int OFF_RT = OFF_Z + MAX_E * 12;               // routing cache [2 layers]: expert ptrs, weights, ids
+constexpr int HG = H / 32;                               // 32-value blocks of n
+constexpr int DIG_WORDS = 28;                            // per block: 4 words x 6 digit words, scale, sum, pad
+constexpr int OFF_DIG = OFF_Z + MAX_E * 12;              // n as byte digits for the integer dot products [HG]
+constexpr int OFF_RT = OFF_DIG + HG * DIG_WORDS * 4;     // routing cache [2 layers]: expert ptrs, weights, ids
 constexpr int RT_BYTES = 2 * (K * 8 + K * 4 + K * 4);
 constexpr int OFF_BAR = OFF_RT + RT_BYTES;               // mbarriers
 enum { B_X = NWORK * NS, B_K, B_HS, B_HR, B_LOAD, N_BAR };
@@ -104,6 +107,7 @@ constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;            // r, epoch, CTA phase 
 constexpr int MAX_L = 64;                                // layers (tags are epoch * 64 + layer)
 constexpr int OFF_DESC = OFF_MISC + 32;                  // copies of the layer descriptors [MAX_L]
 static_assert(H * 4 <= H_FLOATS * 4, "the tagged layer input fits the h area");
+static_assert(OFF_DIG % 16 == 0 && HG % 8 == 0, "digit blocks");
 static_assert(OFF_H % 16 == 0 && OFF_N % 16 == 0 && OFF_RT % 16 == 0 && OFF_BAR % 8 == 0 && OFF_Z % 16 == 0,
               "alignment");
 
@@ -506,25 +510,57 @@ __device__ __forceinline__ float row_bf16(const unsigned char* row, const float*
     return warp_sum(sum2(acc));
 }
 
-// Four int4 rows of K = H at once (codes: 4 rows of HW words; sb: 4 rows of H/64
-// words): lane sums over the words w = lane + 32 m, then four warp reductions.
-__device__ __forceinline__ float4 rows4_int4(const uint32_t* codes, const uint32_t* sb, const float* n,
-                                             const float* sn, int lane) {
-    const float4* n4 = reinterpret_cast<const float4*>(n);
-    constexpr int SBW = GU_SB / 4;
-    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+// Byte dot products: acc + sum_i a.byte_i * b.byte_i, bytes unsigned (uu) or a signed (su).
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_su(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// One word of 8 codes against the digits of its 8 values of n: exact integer sums per digit.
+__device__ __forceinline__ void word_digits(uint32_t q, uint32_t lo0, uint32_t hi0, uint32_t lo1, uint32_t hi1,
+                                            uint32_t lo2, uint32_t hi2, int& s0, int& s1, int& s2) {
+    const uint32_t lo = q & 0x0f0f0f0fu, hi = (q >> 4) & 0x0f0f0f0fu;  // codes of columns 0,2,4,6 / 1,3,5,7
+    s0 = dp4a_uu(hi0, hi, dp4a_uu(lo0, lo, s0));
+    s1 = dp4a_uu(hi1, hi, dp4a_uu(lo1, lo, s1));
+    s2 = dp4a_su(hi2, hi, dp4a_su(lo2, lo, s2));
+}
+
+// Four int4 rows of K = H at once (the stage holds 4 rows of codes, then 4 rows
+// of {s,b}): lane = (row lane & 3, block lane >> 2, + 8 per step). Per 32-value
+// block the codes meet the digits of n in integer arithmetic (exact), then
+// s * (scale * sum q n_int) + b * sum n in fp32; the four lanes of a block read
+// the same digits.
+__device__ __forceinline__ float4 rows4_int4(const unsigned char* st, const uint32_t* dig, int lane) {
+    const int r = lane & 3, hb = lane >> 2;
+    const unsigned char* crow = st + r * GU_ROW;
+    const uint32_t* sbrow = reinterpret_cast<const uint32_t*>(st + 4 * GU_ROW) + r * (GU_SB / 4);
+    float acc = 0.0f;
 #pragma unroll 2
-    for (int m = 0; m < WPL; ++m) {
-        const int w = lane + 32 * m, g = w >> 3;
-        const float4 na = n4[w], nb = n4[HW + w];
-        const float S = sn[w];
-        a0 = word_affine(codes[w], sb[g], na, nb, S, a0);
-        a1 = word_affine(codes[HW + w], sb[SBW + g], na, nb, S, a1);
-        a2 = word_affine(codes[2 * HW + w], sb[2 * SBW + g], na, nb, S, a2);
-        a3 = word_affine(codes[3 * HW + w], sb[3 * SBW + g], na, nb, S, a3);
+    for (int m = 0; m < HG / 8; ++m) {
+        const int hg = hb + 8 * m;
+        const uint4 q = *reinterpret_cast<const uint4*>(crow + 16 * hg);
+        const uint4* dp = reinterpret_cast<const uint4*>(dig + hg * DIG_WORDS);
+        const uint4 d0 = dp[0], d1 = dp[1], d2 = dp[2], d3 = dp[3], d4 = dp[4], d5 = dp[5];
+        const float2 meta = *reinterpret_cast<const float2*>(dig + hg * DIG_WORDS + 24);
+        int s0 = 0, s1 = 0, s2 = 0;
+        word_digits(q.x, d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, s0, s1, s2);
+        word_digits(q.y, d1.z, d1.w, d2.x, d2.y, d2.z, d2.w, s0, s1, s2);
+        word_digits(q.z, d3.x, d3.y, d3.z, d3.w, d4.x, d4.y, s0, s1, s2);
+        word_digits(q.w, d4.z, d4.w, d5.x, d5.y, d5.z, d5.w, s0, s1, s2);
+        const float pq = fmaf((float)s2, 65536.0f, fmaf((float)s1, 256.0f, (float)s0)) * meta.x;
+        const uint32_t sbw = sbrow[hg >> 1];
+        acc = fmaf(h2f(sbw & 0xffffu), pq, fmaf(h2f(sbw >> 16), meta.y, acc));
     }
-    warp_sum4(a0, a1, a2, a3);
-    return make_float4(a0, a1, a2, a3);
+    acc += __shfl_xor_sync(FULL, acc, 4);
+    acc += __shfl_xor_sync(FULL, acc, 8);
+    acc += __shfl_xor_sync(FULL, acc, 16);
+    return make_float4(__shfl_sync(FULL, acc, 0), __shfl_sync(FULL, acc, 1), __shfl_sync(FULL, acc, 2),
+                       __shfl_sync(FULL, acc, 3));
 }
 
 // Wait (one warp) until the hint counter reaches target (modular u32 compare).
@@ -668,10 +704,63 @@ __device__ bool stage_x(const Params& P, int l, uint32_t epoch, uint32_t hint_ta
     return true;
 }
 
+// n for the integer dot products of the routed gate/up rows (control warps 1..3
+// while warp 0 routes): per block of 32 values a shared power-of-two scale puts
+// the largest |n| in [2^22, 2^23); each value becomes a 24-bit integer, split
+// into three byte digits (two unsigned, the top one signed), packed four to a
+// word in the order of the code bytes of a word of codes (columns 0,2,4,6 and
+// 1,3,5,7). Per block: 4 words x {lo0, hi0, lo1, hi1, lo2, hi2}, the inverse
+// scale and the block's sum of n.
+__device__ void stage_digits(unsigned char* smem, int t, int nt) {
+    const float4* n4 = reinterpret_cast<const float4*>(smem + OFF_N);
+    const float* sn = reinterpret_cast<const float*>(smem + OFF_SN);
+    uint32_t* dig = reinterpret_cast<uint32_t*>(smem + OFF_DIG);
+    for (int hg = t; hg < HG; hg += nt) {
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 a = n4[4 * hg + j], b = n4[HW + 4 * hg + j];
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+        }
+        float up = 0.0f, down = 0.0f;  // a block below 2^-100 counts as zero
+        if (m >= 7.8886e-31f) {
+            const int e = (int)((__float_as_uint(m) >> 23) & 0xffu) - 127;  // m in [2^e, 2^(e+1))
+            up = __uint_as_float((uint32_t)(127 + 22 - e) << 23);
+            down = __uint_as_float((uint32_t)(127 + e - 22) << 23);
+        }
+        uint32_t* d = dig + hg * DIG_WORDS;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 a = n4[4 * hg + j], b = n4[HW + 4 * hg + j];
+            const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            uint32_t lo0 = 0, lo1 = 0, lo2 = 0, hi0 = 0, hi1 = 0, hi2 = 0;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int q = __float2int_rn(v[c] * up);  // |q| < 2^23; v * up is exact
+                const int sh = 8 * (c >> 1);
+                const uint32_t b0 = (uint32_t)(q & 0xff) << sh, b1 = (uint32_t)((q >> 8) & 0xff) << sh,
+                               b2 = (uint32_t)((q >> 16) & 0xff) << sh;
+                if (c & 1) {
+                    hi0 |= b0;
+                    hi1 |= b1;
+                    hi2 |= b2;
+                } else {
+                    lo0 |= b0;
+                    lo1 |= b1;
+                    lo2 |= b2;
+                }
+            }
+            reinterpret_cast<uint2*>(d + 6 * j)[0] = make_uint2(lo0, hi0);
+            reinterpret_cast<uint2*>(d + 6 * j)[1] = make_uint2(lo1, hi1);
+            reinterpret_cast<uint2*>(d + 6 * j)[2] = make_uint2(lo2, hi2);
+        }
+        d[24] = __float_as_uint(down);
+        d[25] = __float_as_uint((sn[4 * hg] + sn[4 * hg + 1]) + (sn[4 * hg + 2] + sn[4 * hg + 3]));
+    }
+}
+
 // Control warp 0: the CTA's copy of the layer's top-k from the tagged logits.
-// Each lane sorts its own candidates once (larger logit first, equal -> lower
-// index, NaN lowest, -0 == +0); each of the k rounds then takes the best lane
-// head with two warp reductions and the winning lane shifts its list.
 __device__ bool route_layer(const Params& P, int l, uint32_t tag, uint32_t epoch_x_e, unsigned char* smem, Route* rt,
                             bool publish, uint32_t bar_load, int& loads, int lane) {
     const LayerDesc& D = LD(l);
@@ -858,8 +947,12 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
                 trace_at(P, l, TR_X_STAGED);
             }
             int rok = 1;
-            if (cw == 0) {
+            if (cw == 0)
                 rok = route_layer(P, l, tag, epoch * (uint32_t)E, smem, rt, blockIdx.x == 0, bar_load, loads, lane);
+            else
+                stage_digits(smem, (cw - 1) * 32 + lane, (NCTRL - 1) * 32);
+            ctrl_sync();  // the digits are complete before the top-k (which the routed gate/up items wait for)
+            if (cw == 0) {
                 if (rok && lane == 0) {
                     mbar_arrive(bar_k);
                     trace_at(P, l, TR_TOPK);
@@ -934,7 +1027,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
     bool ok = true;
     float carry0 = 0.0f, carry1 = 0.0f;  // partial results carried between the items of a task
     const float* n_s = reinterpret_cast<const float*>(smem + OFF_N);
-    const float* sn_s = reinterpret_cast<const float*>(smem + OFF_SN);
+    const uint32_t* dig_s = reinterpret_cast<const uint32_t*>(smem + OFF_DIG);
     float r = 0.0f;
 
     // Layers whose top-k this warp has seen published. The routing mbarrier is
@@ -1051,9 +1144,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
             } else if (con.kind == T_RGU) {
                 const int u = con.t - D.E - N_SGU;
                 const int i = u / RGU_PER_EXPERT, p0 = 2 * (u % RGU_PER_EXPERT);
-                const uint32_t* codes = reinterpret_cast<const uint32_t*>(st);
-                const uint32_t* sb = reinterpret_cast<const uint32_t*>(st + 4 * GU_ROW);
-                const float4 gu = rows4_int4(codes, sb, n_s, sn_s, lane);  // gate p0, up p0, gate p0+1, up p0+1
+                const float4 gu = rows4_int4(st, dig_s, lane);  // gate p0, up p0, gate p0+1, up p0+1
                 if (lane == 0)
                     st_relaxed_v2u32(D.ht + (size_t)i * I + p0, tagged_f(gelu_tanh(gu.x) * gu.y, tag4),
                                      tagged_f(gelu_tanh(gu.z) * gu.w, tag4));
