@@ -69,7 +69,6 @@ constexpr int GU_ROW = H / 2;              // 1408: int4 gate/up row
 constexpr int GU_SB = (H / 64) * 4;        // 176: its {s,b} pairs
 constexpr int D_ROW = I / 2;               // 352: int4 down row
 constexpr int D_SB = (I / 64) * 4;         // 44: its {s,b} pairs
-constexpr int D_WORDS = I / 8;             // 88 words per down row
 constexpr int N_SGU = S;                   // tasks of one shared row pair
 constexpr int N_RGU = K * I / 2;           // tasks of two routed row pairs
 constexpr int RGU_PER_EXPERT = I / 2;      // 352
@@ -94,11 +93,10 @@ constexpr int OFF_N = OFF_XS + H * 2;                    // fp32 n in two halves
 constexpr int OFF_SN = OFF_N + H * 4;                    // fp32 word sums of n [HW]
 constexpr int OFF_H = OFF_SN + HW * 4;                   // tagged fp32 h_routed [K*I], h_shared [S]; also the
                                                          // landing zone of the tagged layer input
-constexpr int OFF_SH = OFF_H + H_FLOATS * 4;             // fp32 word sums of h_routed [K*I/8]
-constexpr int OFF_Z = OFF_SH + (K * I / 8) * 4;          // tagged logits [MAX_E] (64-bit words), then top-k keys [MAX_E]
+constexpr int OFF_Z = OFF_H + H_FLOATS * 4;              // tagged logits [MAX_E] (64-bit words)
 constexpr int HG = H / 32;                               // 32-value blocks of n
 constexpr int DIG_WORDS = 28;                            // per block: 4 words x 6 digit words, scale, sum, pad
-constexpr int OFF_DIG = OFF_Z + MAX_E * 12;              // n as byte digits for the integer dot products [HG]
+constexpr int OFF_DIG = OFF_Z + MAX_E * 8;               // n as byte digits for the integer dot products [HG]
 constexpr int OFF_RT = OFF_DIG + HG * DIG_WORDS * 4;     // routing cache [2 layers]: expert ptrs, weights, ids
 constexpr int RT_BYTES = 2 * (K * 8 + K * 4 + K * 4);
 constexpr int OFF_BAR = OFF_RT + RT_BYTES;               // mbarriers
@@ -107,7 +105,9 @@ constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;            // r, epoch, CTA phase 
 constexpr int MAX_L = 64;                                // layers (tags are epoch * 64 + layer)
 constexpr int OFF_DESC = OFF_MISC + 32;                  // copies of the layer descriptors [MAX_L]
 static_assert(H * 4 <= H_FLOATS * 4, "the tagged layer input fits the h area");
-static_assert(OFF_DIG % 16 == 0 && HG % 8 == 0, "digit blocks");
+constexpr int HB = K * I / 32;                           // 32-value blocks of h_routed (22 per expert)
+static_assert(OFF_DIG % 16 == 0 && HG % 8 == 0 && I % 32 == 0, "digit blocks");
+static_assert(DIG_WORDS <= 32, "a digit block is no larger than the 32 fp32 values it replaces (in-place staging)");
 static_assert(OFF_H % 16 == 0 && OFF_N % 16 == 0 && OFF_RT % 16 == 0 && OFF_BAR % 8 == 0 && OFF_Z % 16 == 0,
               "alignment");
 
@@ -457,22 +457,6 @@ __device__ __forceinline__ float sum2(unsigned long long v) {
 __device__ __forceinline__ void fma2(unsigned long long& acc, unsigned long long a, unsigned long long b) {
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
 }
-// Byte b of x as the fp32 value 128 + x.byte_b (bytes hold one code 0..15): the
-// byte lands in mantissa bits 16..23 under the exponent of 128.0f.
-template <int B>
-__device__ __forceinline__ float byte128(uint32_t x) {
-    return __uint_as_float(__byte_perm(x, 0x43000000u, 0x7054u | (B << 8)));
-}
-// sum_p (128 + q_p) n_p over the 8 codes of one word (code p in bits 4p..4p+3).
-__device__ __forceinline__ float dot8_q128_2(uint32_t q, float4 a, float4 b) {
-    const uint32_t lo = q & 0x0f0f0f0fu, hi = (q >> 4) & 0x0f0f0f0fu;  // codes 0,2,4,6 / 1,3,5,7
-    unsigned long long acc = 0ull;
-    fma2(acc, pk2(byte128<0>(lo), byte128<0>(hi)), pk2(a.x, a.y));
-    fma2(acc, pk2(byte128<1>(lo), byte128<1>(hi)), pk2(a.z, a.w));
-    fma2(acc, pk2(byte128<2>(lo), byte128<2>(hi)), pk2(b.x, b.y));
-    fma2(acc, pk2(byte128<3>(lo), byte128<3>(hi)), pk2(b.z, b.w));
-    return sum2(acc);
-}
 // acc + sum over 8 bf16 weights (one 16-byte chunk) times n, packed FMA.
 __device__ __forceinline__ unsigned long long dot8_bf16_2(uint4 w, float4 a, float4 b, unsigned long long acc) {
     fma2(acc, pk2(bf_lo(w.x), bf_hi(w.x)), pk2(a.x, a.y));
@@ -481,21 +465,6 @@ __device__ __forceinline__ unsigned long long dot8_bf16_2(uint4 w, float4 a, flo
     fma2(acc, pk2(bf_lo(w.w), bf_hi(w.w)), pk2(b.z, b.w));
     return acc;
 }
-// acc + sum_p (s q_p + b) v_p = acc + s (P - 128 S) + b S for one word of codes.
-__device__ __forceinline__ float word_affine(uint32_t q, uint32_t sbw, float4 a, float4 b, float S, float acc) {
-    const float P = dot8_q128_2(q, a, b);
-    return fmaf(h2f(sbw & 0xffffu), fmaf(-128.0f, S, P), fmaf(h2f(sbw >> 16), S, acc));
-}
-__device__ __forceinline__ void warp_sum4(float& a, float& b, float& c, float& d) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-        a += __shfl_xor_sync(FULL, a, o);
-        b += __shfl_xor_sync(FULL, b, o);
-        c += __shfl_xor_sync(FULL, c, o);
-        d += __shfl_xor_sync(FULL, d, o);
-    }
-}
-
 // sum_k W[k] n[k] over a bf16 row of K = H (16-byte chunk w covers n[8w..8w+7],
 // held in shared memory as the float4s w and HW + w).
 __device__ __forceinline__ float row_bf16(const unsigned char* row, const float* n, int lane) {
@@ -704,59 +673,102 @@ __device__ bool stage_x(const Params& P, int l, uint32_t epoch, uint32_t hint_ta
     return true;
 }
 
-// n for the integer dot products of the routed gate/up rows (control warps 1..3
-// while warp 0 routes): per block of 32 values a shared power-of-two scale puts
-// the largest |n| in [2^22, 2^23); each value becomes a 24-bit integer, split
-// into three byte digits (two unsigned, the top one signed), packed four to a
-// word in the order of the code bytes of a word of codes (columns 0,2,4,6 and
-// 1,3,5,7). Per block: 4 words x {lo0, hi0, lo1, hi1, lo2, hi2}, the inverse
-// scale and the block's sum of n.
+// A block of 32 values (v[8 j + c] = column 8 j + c) for the integer dot
+// products: a shared power-of-two scale puts the largest |v| in [2^22, 2^23);
+// each value becomes a 24-bit integer, split into three byte digits (two
+// unsigned, the top one signed), packed four to a word in the order of the code
+// bytes of a word of codes (columns 0,2,4,6 and 1,3,5,7). Written: per word j
+// {lo0, hi0, lo1, hi1, lo2, hi2} at d[6 j], then the inverse scale and the sum
+// of the block.
+__device__ __forceinline__ void block_digits(const float (&v)[32], uint32_t* d) {
+    float m = 0.0f, sum = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float ws = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            m = fmaxf(m, fabsf(v[8 * j + c]));
+            ws += v[8 * j + c];
+        }
+        sum += ws;
+    }
+    float up = 0.0f, down = 0.0f;  // a block below 2^-100 counts as zero
+    if (m >= 7.8886e-31f) {
+        const int e = (int)((__float_as_uint(m) >> 23) & 0xffu) - 127;  // m in [2^e, 2^(e+1))
+        up = __uint_as_float((uint32_t)(127 + 22 - e) << 23);
+        down = __uint_as_float((uint32_t)(127 + e - 22) << 23);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t lo0 = 0, lo1 = 0, lo2 = 0, hi0 = 0, hi1 = 0, hi2 = 0;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int q = __float2int_rn(v[8 * j + c] * up);  // |q| < 2^23; v * up is exact
+            const int sh = 8 * (c >> 1);
+            const uint32_t b0 = (uint32_t)(q & 0xff) << sh, b1 = (uint32_t)((q >> 8) & 0xff) << sh,
+                           b2 = (uint32_t)((q >> 16) & 0xff) << sh;
+            if (c & 1) {
+                hi0 |= b0;
+                hi1 |= b1;
+                hi2 |= b2;
+            } else {
+                lo0 |= b0;
+                lo1 |= b1;
+                lo2 |= b2;
+            }
+        }
+        reinterpret_cast<uint2*>(d + 6 * j)[0] = make_uint2(lo0, hi0);
+        reinterpret_cast<uint2*>(d + 6 * j)[1] = make_uint2(lo1, hi1);
+        reinterpret_cast<uint2*>(d + 6 * j)[2] = make_uint2(lo2, hi2);
+    }
+    d[24] = __float_as_uint(down);
+    d[25] = __float_as_uint(sum);
+}
+
+// n as digit blocks for the routed gate/up rows (control warps 1..3 while warp 0 routes).
 __device__ void stage_digits(unsigned char* smem, int t, int nt) {
     const float4* n4 = reinterpret_cast<const float4*>(smem + OFF_N);
-    const float* sn = reinterpret_cast<const float*>(smem + OFF_SN);
     uint32_t* dig = reinterpret_cast<uint32_t*>(smem + OFF_DIG);
     for (int hg = t; hg < HG; hg += nt) {
-        float m = 0.0f;
+        float v[32];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const float4 a = n4[4 * hg + j], b = n4[HW + 4 * hg + j];
-            m = fmaxf(m, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
-            m = fmaxf(m, fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+            v[8 * j + 0] = a.x;
+            v[8 * j + 1] = a.y;
+            v[8 * j + 2] = a.z;
+            v[8 * j + 3] = a.w;
+            v[8 * j + 4] = b.x;
+            v[8 * j + 5] = b.y;
+            v[8 * j + 6] = b.z;
+            v[8 * j + 7] = b.w;
         }
-        float up = 0.0f, down = 0.0f;  // a block below 2^-100 counts as zero
-        if (m >= 7.8886e-31f) {
-            const int e = (int)((__float_as_uint(m) >> 23) & 0xffu) - 127;  // m in [2^e, 2^(e+1))
-            up = __uint_as_float((uint32_t)(127 + 22 - e) << 23);
-            down = __uint_as_float((uint32_t)(127 + e - 22) << 23);
-        }
-        uint32_t* d = dig + hg * DIG_WORDS;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float4 a = n4[4 * hg + j], b = n4[HW + 4 * hg + j];
-            const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            uint32_t lo0 = 0, lo1 = 0, lo2 = 0, hi0 = 0, hi1 = 0, hi2 = 0;
+        block_digits(v, dig + hg * DIG_WORDS);
+    }
+}
+
+// h_routed (fp32, in the h area) -> digit blocks in place, all four control
+// warps: block b's digits (112 bytes at 112 b) only cover fp32 blocks <= b, and
+// each round reads all its blocks before any of its digits are written.
+__device__ void digits_in_place(unsigned char* smem, int t) {
+    const float4* h4 = reinterpret_cast<const float4*>(smem + OFF_H);
+    uint32_t* dig = reinterpret_cast<uint32_t*>(smem + OFF_H);
+    for (int b0 = 0; b0 < HB; b0 += NCTRL * 32) {
+        const int b = b0 + t;
+        float v[32];
+        if (b < HB) {
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                const int q = __float2int_rn(v[c] * up);  // |q| < 2^23; v * up is exact
-                const int sh = 8 * (c >> 1);
-                const uint32_t b0 = (uint32_t)(q & 0xff) << sh, b1 = (uint32_t)((q >> 8) & 0xff) << sh,
-                               b2 = (uint32_t)((q >> 16) & 0xff) << sh;
-                if (c & 1) {
-                    hi0 |= b0;
-                    hi1 |= b1;
-                    hi2 |= b2;
-                } else {
-                    lo0 |= b0;
-                    lo1 |= b1;
-                    lo2 |= b2;
-                }
+                const float4 a = h4[8 * b + c];
+                v[4 * c + 0] = a.x;
+                v[4 * c + 1] = a.y;
+                v[4 * c + 2] = a.z;
+                v[4 * c + 3] = a.w;
             }
-            reinterpret_cast<uint2*>(d + 6 * j)[0] = make_uint2(lo0, hi0);
-            reinterpret_cast<uint2*>(d + 6 * j)[1] = make_uint2(lo1, hi1);
-            reinterpret_cast<uint2*>(d + 6 * j)[2] = make_uint2(lo2, hi2);
         }
-        d[24] = __float_as_uint(down);
-        d[25] = __float_as_uint((sn[4 * hg] + sn[4 * hg + 1]) + (sn[4 * hg + 2] + sn[4 * hg + 3]));
+        ctrl_sync();
+        if (b < HB) block_digits(v, dig + b * DIG_WORDS);
+        ctrl_sync();
     }
 }
 
@@ -880,14 +892,7 @@ __device__ bool stage_h(const Params& P, int l, uint32_t tag4, const uint32_t* h
     if (!ctrl_load(P, D.ht + w0, (uint32_t)nw * 4, reinterpret_cast<unsigned char*>(h), bar_load, loads, stale, cw,
                    lane, check))
         return false;
-    if (routed) {
-        float* sh = reinterpret_cast<float*>(smem + OFF_SH);
-        const float4* h4 = reinterpret_cast<const float4*>(h);
-        for (int w8 = cw * 32 + lane; w8 < K * I / 8; w8 += NCTRL * 32) {
-            const float4 a = h4[2 * w8], b = h4[2 * w8 + 1];
-            sh[w8] = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
-        }
-    }
+    if (routed) digits_in_place(smem, cw * 32 + lane);
     ctrl_sync();
     return true;
 }
@@ -1170,35 +1175,36 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
                     if (con.sub == 0) carry0 = acc;
                     else carry1 = acc;
                 } else {
-                    // the 8 experts' down rows j0, j0 + 1 (int4, K = I), weighted
-                    const float* hr = reinterpret_cast<const float*>(smem + OFF_H);
-                    const float* sh = reinterpret_cast<const float*>(smem + OFF_SH);
-                    float y0 = 0.0f, y1 = 0.0f;
-                    const int sbrow = j0 & 3;
+                    // the 8 experts' down rows j0, j0 + 1 (int4, K = I) against the digit blocks of
+                    // h_routed: lane = (row lane & 1, expert (lane >> 1) & 7, block (lane >> 4) + 2 m)
+                    const uint32_t* dh = reinterpret_cast<const uint32_t*>(smem + OFF_H);
+                    const int jr = lane & 1, i = (lane >> 1) & (K - 1);
+                    const unsigned char* crow = st + i * 2 * D_ROW + jr * D_ROW;
+                    const uint32_t* sbrow = reinterpret_cast<const uint32_t*>(st + DN_SB_OFF + i * 4 * D_SB) +
+                                            ((j0 & 3) + jr) * (D_SB / 4);
+                    float acc = 0.0f;
 #pragma unroll 1
-                    for (int i = 0; i < K; ++i) {
-                        const uint32_t* codes = reinterpret_cast<const uint32_t*>(st + i * 2 * D_ROW);
-                        const uint32_t* sb = reinterpret_cast<const uint32_t*>(st + DN_SB_OFF + i * 4 * D_SB) +
-                                             sbrow * (D_SB / 4);
-                        const float* hi = hr + i * I;
-                        float p0 = 0.0f, p1 = 0.0f;
-#pragma unroll
-                        for (int t = 0; t < (D_WORDS + 31) / 32; ++t) {
-                            const int w = lane + 32 * t;
-                            if (w < D_WORDS) {
-                                const float4 ha = *reinterpret_cast<const float4*>(hi + 8 * w);
-                                const float4 hb = *reinterpret_cast<const float4*>(hi + 8 * w + 4);
-                                const float sw = sh[i * D_WORDS + w];
-                                p0 = word_affine(codes[w], sb[w >> 3], ha, hb, sw, p0);
-                                p1 = word_affine(codes[D_WORDS + w], sb[D_SB / 4 + (w >> 3)], ha, hb, sw, p1);
-                            }
-                        }
-                        const float wi = rt->w[l & 1][i];
-                        y0 = fmaf(wi, p0, y0);
-                        y1 = fmaf(wi, p1, y1);
+                    for (int b = lane >> 4; b < I / 32; b += 2) {
+                        const uint4 q = *reinterpret_cast<const uint4*>(crow + 16 * b);
+                        const uint32_t* db = dh + (i * (I / 32) + b) * DIG_WORDS;
+                        const uint4* dp = reinterpret_cast<const uint4*>(db);
+                        const uint4 d0 = dp[0], d1 = dp[1], d2 = dp[2], d3 = dp[3], d4 = dp[4], d5 = dp[5];
+                        const float2 meta = *reinterpret_cast<const float2*>(db + 24);
+                        int s0 = 0, s1 = 0, s2 = 0;
+                        word_digits(q.x, d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, s0, s1, s2);
+                        word_digits(q.y, d1.z, d1.w, d2.x, d2.y, d2.z, d2.w, s0, s1, s2);
+                        word_digits(q.z, d3.x, d3.y, d3.z, d3.w, d4.x, d4.y, s0, s1, s2);
+                        word_digits(q.w, d4.z, d4.w, d5.x, d5.y, d5.z, d5.w, s0, s1, s2);
+                        const float pq = fmaf((float)s2, 65536.0f, fmaf((float)s1, 256.0f, (float)s0)) * meta.x;
+                        const uint32_t sbw = sbrow[b >> 1];
+                        acc = fmaf(h2f(sbw & 0xffffu), pq, fmaf(h2f(sbw >> 16), meta.y, acc));
                     }
-                    float dummy0 = 0.0f, dummy1 = 0.0f;
-                    warp_sum4(y0, y1, dummy0, dummy1);
+                    acc += __shfl_xor_sync(FULL, acc, 16);     // both halves of the blocks: y of (row, expert)
+                    acc *= rt->w[l & 1][i];                    // routing weight
+                    acc += __shfl_xor_sync(FULL, acc, 2);      // sum over the experts
+                    acc += __shfl_xor_sync(FULL, acc, 4);
+                    acc += __shfl_xor_sync(FULL, acc, 8);
+                    const float y0 = __shfl_sync(FULL, acc, 0), y1 = __shfl_sync(FULL, acc, 1);
                     if (lane == 0) {
                         const uint32_t o0 = f2bf(bf2f(xs[j0]) + (carry0 + y0));
                         const uint32_t o1 = f2bf(bf2f(xs[j0 + 1]) + (carry1 + y1));
