@@ -72,6 +72,22 @@ def set_layers(n_layers: int) -> None:
 set_layers(L)
 
 
+# DRAM traffic of the fused kernel from an ncu capture of a 4-layer stack of the same kernel (read + write bytes,
+# scaled by 30/4 to the 30-layer launch); reported only while the kernel source is the one that was captured
+FUSED_TRAFFIC = {"src_sha256": "e835eeda4635a233d811f1189d8adf86443b3cc7a2ab4b25769e93b057e477c8",
+                 "bytes_per_layer": (252826880 + 3527936) / 4}
+
+
+def fused_traffic(n_layers):
+    import hashlib
+    src = os.path.join(ROOT, "bit_expert_streaming_layer_b300", "csrc", "tf_fused.cu")
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return int(FUSED_TRAFFIC["bytes_per_layer"] * n_layers) if h == FUSED_TRAFFIC["src_sha256"] else None
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -764,7 +780,8 @@ def main():
         "weight_frac_of_peak": round(WEIGHTS_PER_TOKEN * args.steps / (ms / 1000.0) / 1e9 / peak, 4),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind + " (hbm_gbs)",
-                     "bytes_per_launch": BYTES[dom], "traffic": None},
+                     "bytes_per_launch": BYTES[dom],
+                     "traffic": fused_traffic(L) if (dom == "layer" and args.path == "fused") else None},
         "kernels": per_kernel,
         "gpu_launches": int(launches),
         "clocks": clocks,
