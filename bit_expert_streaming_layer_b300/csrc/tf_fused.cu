@@ -100,7 +100,7 @@ constexpr int OFF_DIG = OFF_Z + MAX_E * 8;               // n as byte digits for
 constexpr int OFF_RT = OFF_DIG + HG * DIG_WORDS * 4;     // routing cache [2 layers]: expert ptrs, weights, ids
 constexpr int RT_BYTES = 2 * (K * 8 + K * 4 + K * 4);
 constexpr int OFF_BAR = OFF_RT + RT_BYTES;               // mbarriers
-enum { B_X = NWORK * NS, B_K, B_HS, B_HR, B_LOAD, N_BAR };
+enum { B_X = NWORK * NS, B_XS, B_K, B_HS, B_HR, B_LOAD, N_BAR };  // B_XS: raw x staged; B_X: r and n too
 constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;            // r, epoch, CTA phase counters, stale count
 constexpr int MAX_L = 64;                                // layers (tags are epoch * 64 + layer)
 constexpr int OFF_DESC = OFF_MISC + 32;                  // copies of the layer descriptors [MAX_L]
@@ -618,7 +618,7 @@ __device__ bool ctrl_load(const Params& P, const void* src, uint32_t bytes, unsi
 // The layer input: the tagged output of the previous layer (or the call's x)
 // -> x (bf16), r, n = r x and the word sums of n; all four control warps.
 __device__ bool stage_x(const Params& P, int l, uint32_t epoch, uint32_t hint_target, unsigned char* smem,
-                        uint32_t bar_load, int& loads, uint32_t* stale, int cw, int lane) {
+                        uint32_t bar_load, uint32_t bar_xs, int& loads, uint32_t* stale, int cw, int lane) {
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem + OFF_XS);
     if (l == 0) {
         const uint4* s4 = reinterpret_cast<const uint4*>(P.x);
@@ -644,6 +644,7 @@ __device__ bool stage_x(const Params& P, int l, uint32_t epoch, uint32_t hint_ta
         if (cw == 0 && lane == 0) trace_at(P, l, TR_X_READY);
     }
     ctrl_sync();
+    if (cw == 0 && lane == 0) mbar_arrive(bar_xs);  // the router rows need only x (r is applied after the dot)
     float* rs = reinterpret_cast<float*>(smem + OFF_MISC);
     if (cw == 0) {
         float p = 0.0f;
@@ -906,6 +907,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     const uint32_t bar_x = smem_u32(&bars[B_X]);
+    const uint32_t bar_xs = smem_u32(&bars[B_XS]);
     const uint32_t bar_k = smem_u32(&bars[B_K]);
     const uint32_t bar_hs = smem_u32(&bars[B_HS]);
     const uint32_t bar_hr = smem_u32(&bars[B_HR]);
@@ -918,6 +920,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < NWORK * NS; ++s) mbar_init(smem_u32(&bars[s]), 1);
         mbar_init(bar_x, 1);
+        mbar_init(bar_xs, 1);
         mbar_init(bar_k, 1);
         mbar_init(bar_hs, 1);
         mbar_init(bar_hr, 1);
@@ -946,7 +949,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
             const LayerDesc& D = LD(l);
             const uint32_t tag = epoch * 64u + (uint32_t)l;
             const uint32_t tag4 = tag4_of(epoch, l);
-            if (!(ok = stage_x(P, l, epoch, hint_target, smem, bar_load, loads, stale, cw, lane))) break;
+            if (!(ok = stage_x(P, l, epoch, hint_target, smem, bar_load, bar_xs, loads, stale, cw, lane))) break;
             if (cw == 0 && lane == 0) {
                 mbar_arrive(bar_x);
                 trace_at(P, l, TR_X_STAGED);
@@ -1068,8 +1071,8 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
         const uint32_t tag16 = tag & 0xffffu;
         if (P.prefetch && lane == 0) prefetch_layer(c, l + 1 < P.L ? l + 1 : 0);
         try_issue();
-        if (!(ok = warp_wait_mbar(bar_x, l & 1, P.err, lane))) break;
-        r = reinterpret_cast<const float*>(smem + OFF_MISC)[0];
+        if (!(ok = warp_wait_mbar(bar_xs, l & 1, P.err, lane))) break;
+        bool n_ready = false;  // r and n of this layer (the second x phase) observed
         const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem + OFF_XS);
         uint16_t* pout = l == P.L - 1 ? P.out : nullptr;
         bool hs_sig = false, hr_sig = false, hs_ready = false, hr_ready = false;
@@ -1133,6 +1136,11 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
 #pragma unroll 8
                 for (int k = lane; k < H; k += 32) d = fmaf(bf2f(wrow[k]), bf2f(xs[k]), d);  // exact products
                 d = warp_sum_canonical(d);
+                if (!n_ready) {
+                    if (!(ok = warp_wait_mbar(bar_x, l & 1, P.err, lane))) break;
+                    n_ready = true;
+                    r = reinterpret_cast<const float*>(smem + OFF_MISC)[0];
+                }
                 float z = __fmul_rn(r, d);
                 if (D.bias) z = __fadd_rn(z, D.bias[con.t]);
                 if (lane == 0) {
@@ -1140,6 +1148,11 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
                     red_relaxed_add(D.cnt_z, 1u);
                 }
             } else if (con.kind == T_SGU) {
+                if (!n_ready) {
+                    if (!(ok = warp_wait_mbar(bar_x, l & 1, P.err, lane))) break;
+                    n_ready = true;
+                    r = reinterpret_cast<const float*>(smem + OFF_MISC)[0];
+                }
                 const float v = row_bf16(st, n_s, lane);
                 if (con.sub == 0) {
                     carry0 = v;
@@ -1226,6 +1239,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
         // observe this layer's routing and h phases even without items that needed
         // them, so that later parity tests never run two phases behind
         try_issue();
+        if (!n_ready && !(ok = warp_wait_mbar(bar_x, l & 1, P.err, lane))) break;
         if (!topk_known(l)) {
             if (!(ok = warp_wait_mbar(bar_k, l & 1, P.err, lane))) break;
             k_seen = l + 1;
