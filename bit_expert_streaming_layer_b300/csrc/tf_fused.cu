@@ -674,6 +674,17 @@ __device__ bool stage_x(const Params& P, int l, uint32_t epoch, uint32_t hint_ta
     return true;
 }
 
+// Bytes 0, 1 and 2 of four integers a, b, c, d gathered as (a_k, b_k, c_k, d_k), k = 0, 1, 2.
+__device__ __forceinline__ void digit_words(int a, int b, int c, int d, uint32_t& w0, uint32_t& w1, uint32_t& w2) {
+    const uint32_t t0 = __byte_perm((uint32_t)a, (uint32_t)b, 0x5140u);  // a0 b0 a1 b1
+    const uint32_t t1 = __byte_perm((uint32_t)c, (uint32_t)d, 0x5140u);  // c0 d0 c1 d1
+    const uint32_t t2 = __byte_perm((uint32_t)a, (uint32_t)b, 0x7362u);  // a2 b2 a3 b3
+    const uint32_t t3 = __byte_perm((uint32_t)c, (uint32_t)d, 0x7362u);  // c2 d2 c3 d3
+    w0 = __byte_perm(t0, t1, 0x5410u);
+    w1 = __byte_perm(t0, t1, 0x7632u);
+    w2 = __byte_perm(t2, t3, 0x5410u);
+}
+
 // A block of 32 values (v[8 j + c] = column 8 j + c) for the integer dot
 // products: a shared power-of-two scale puts the largest |v| in [2^22, 2^23);
 // each value becomes a 24-bit integer, split into three byte digits (two
@@ -701,23 +712,14 @@ __device__ __forceinline__ void block_digits(const float (&v)[32], uint32_t* d) 
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        uint32_t lo0 = 0, lo1 = 0, lo2 = 0, hi0 = 0, hi1 = 0, hi2 = 0;
+        int q[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const int q = __float2int_rn(v[8 * j + c] * up);  // |q| < 2^23; v * up is exact
-            const int sh = 8 * (c >> 1);
-            const uint32_t b0 = (uint32_t)(q & 0xff) << sh, b1 = (uint32_t)((q >> 8) & 0xff) << sh,
-                           b2 = (uint32_t)((q >> 16) & 0xff) << sh;
-            if (c & 1) {
-                hi0 |= b0;
-                hi1 |= b1;
-                hi2 |= b2;
-            } else {
-                lo0 |= b0;
-                lo1 |= b1;
-                lo2 |= b2;
-            }
-        }
+        for (int c = 0; c < 8; ++c) q[c] = __float2int_rn(v[8 * j + c] * up);  // |q| < 2^23; v * up is exact
+        // byte k of the four integers of columns 0,2,4,6 (then 1,3,5,7) gathered into one word: a 4x4
+        // byte transpose (digit 2 = byte 2 is the signed top digit in two's complement)
+        uint32_t lo0, lo1, lo2, hi0, hi1, hi2;
+        digit_words(q[0], q[2], q[4], q[6], lo0, lo1, lo2);
+        digit_words(q[1], q[3], q[5], q[7], hi0, hi1, hi2);
         reinterpret_cast<uint2*>(d + 6 * j)[0] = make_uint2(lo0, hi0);
         reinterpret_cast<uint2*>(d + 6 * j)[1] = make_uint2(lo1, hi1);
         reinterpret_cast<uint2*>(d + 6 * j)[2] = make_uint2(lo2, hi2);
