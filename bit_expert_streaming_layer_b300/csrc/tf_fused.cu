@@ -777,7 +777,7 @@ __device__ void digits_in_place(unsigned char* smem, int t) {
 
 // Control warp 0: the CTA's copy of the layer's top-k from the tagged logits.
 __device__ bool route_layer(const Params& P, int l, uint32_t tag, uint32_t epoch_x_e, unsigned char* smem, Route* rt,
-                            bool publish, uint32_t bar_load, int& loads, int lane) {
+                            uint32_t bar_load, int& loads, int lane, int& sel, float& selz) {
     const LayerDesc& D = LD(l);
     if (!wait_hint(D.cnt_z, epoch_x_e, P.err, lane)) return false;
     const unsigned long long* zt = reinterpret_cast<const unsigned long long*>(smem + OFF_Z);
@@ -816,8 +816,8 @@ __device__ bool route_layer(const Params& P, int l, uint32_t tag, uint32_t epoch
             key[m] = isnan(v) ? 1u : ((u & 0x80000000u) ? ~u : (u | 0x80000000u));
         }
     }
-    float selz = 0.0f;
-    int sel = -1;
+    selz = 0.0f;
+    sel = -1;
 #pragma unroll 1
     for (int i = 0; i < K; ++i) {
         uint32_t bk = key[0];
@@ -838,7 +838,32 @@ __device__ bool route_layer(const Params& P, int l, uint32_t tag, uint32_t epoch
             selz = __uint_as_float((uint32_t)zt[imin]);
         }
     }
-    // softmax over the selected logits, summed in top-k order
+    // the selected experts' addresses: all the routed copies need (the weights come later)
+    const int s = l & 1;
+    int bad = 0;
+    if (lane < K) {
+        rt->id[s][lane] = sel;
+        int e = sel;
+        bad = (unsigned)e >= (unsigned)D.E;
+        if (bad) e = 0;  // never form an address from an out-of-range id
+        if (D.slot_map) e = __ldcg(D.slot_map + e);
+        rt->ep[s][lane] = D.ebase + (size_t)e * D.estride;
+    }
+    if (__any_sync(FULL, bad)) {
+        if (lane == 0) atomicOr(P.err, ERR_BAD_ID);
+        return false;
+    }
+    __syncwarp();
+    return true;
+}
+
+// Control warp 0, after the top-k is released: the routing weights (softmax
+// over the selected logits, summed in top-k order), read by the routed-down
+// items only after the later h_routed phase; CTA 0 also publishes the routing.
+__device__ void route_weights(const Params& P, int l, unsigned char* smem, Route* rt, bool publish, int lane, int sel,
+                              float selz) {
+    const LayerDesc& D = LD(l);
+    const unsigned long long* zt = reinterpret_cast<const unsigned long long*>(smem + OFF_Z);
     float zmax = __shfl_sync(FULL, selz, 0);
     for (int i = 1; i < K; ++i) {
         const float zi = __shfl_sync(FULL, selz, i);
@@ -847,17 +872,9 @@ __device__ bool route_layer(const Params& P, int l, uint32_t tag, uint32_t epoch
     const float ev = lane < K ? expf(__fsub_rn(selz, zmax)) : 0.0f;
     float esum = 0.0f;
     for (int i = 0; i < K; ++i) esum = __fadd_rn(esum, __shfl_sync(FULL, ev, i));
-    const int s = l & 1;
-    int bad = 0;
     if (lane < K) {
         const float wv = __fdiv_rn(ev, esum);
-        rt->id[s][lane] = sel;
-        rt->w[s][lane] = wv;
-        int e = sel;
-        bad = (unsigned)e >= (unsigned)D.E;
-        if (bad) e = 0;  // never form an address from an out-of-range id
-        if (D.slot_map) e = __ldcg(D.slot_map + e);
-        rt->ep[s][lane] = D.ebase + (size_t)e * D.estride;
+        rt->w[l & 1][lane] = wv;
         if (publish) {
             D.idx[lane] = sel;
             D.w[lane] = wv;
@@ -865,12 +882,7 @@ __device__ bool route_layer(const Params& P, int l, uint32_t tag, uint32_t epoch
     }
     if (publish)
         for (int j = lane; j < D.E; j += 32) D.logits[j] = __uint_as_float((uint32_t)zt[j]);
-    if (__any_sync(FULL, bad)) {
-        if (lane == 0) atomicOr(P.err, ERR_BAD_ID);
-        return false;
-    }
     __syncwarp();
-    return true;
 }
 
 // h_shared or h_routed (tagged fp32 words) -> shared memory, in place, checked by
@@ -956,9 +968,9 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
                 mbar_arrive(bar_x);
                 trace_at(P, l, TR_X_STAGED);
             }
-            int rok = 1;
-            if (cw == 0)
-                rok = route_layer(P, l, tag, epoch * (uint32_t)E, smem, rt, blockIdx.x == 0, bar_load, loads, lane);
+            int rok = 1, sel = -1;
+            float selz = 0.0f;
+            if (cw == 0) rok = route_layer(P, l, tag, epoch * (uint32_t)E, smem, rt, bar_load, loads, lane, sel, selz);
             else
                 stage_digits(smem, (cw - 1) * 32 + lane, (NCTRL - 1) * 32);
             ctrl_sync();  // the digits are complete before the top-k (which the routed gate/up items wait for)
@@ -969,6 +981,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
                 }
                 if (!rok && lane == 0) atomicOr(&stale[1], 1u);
                 if (lane == 0) stale[2] = (uint32_t)loads;  // route_layer's copies: warp 0 tells the others
+                if (rok) route_weights(P, l, smem, rt, blockIdx.x == 0, lane, sel, selz);
             }
             ctrl_sync();
             if (stale[1]) {
