@@ -74,8 +74,8 @@ set_layers(L)
 
 # DRAM traffic of the fused kernel from an ncu capture of a 4-layer stack of the same kernel (read + write bytes,
 # scaled by 30/4 to the 30-layer launch); reported only while the kernel source is the one that was captured
-FUSED_TRAFFIC = {"src_sha256": "af067d461d963f1286ee35dceda3ec46ee010fed03eae4012e3ec6a59ef41046",
-                 "bytes_per_layer": (252820736 + 3096832) / 4}
+FUSED_TRAFFIC = {"src_sha256": "3105add69ba4a817f148375bc35e1cc03a345e9496aff34734dbe1c36f59867b",
+                 "bytes_per_layer": (252823296 + 3504640) / 4}
 
 
 def fused_traffic(n_layers):
