@@ -7,8 +7,8 @@
 // shared-expert branch beside them. What differs is how it is fed on B300.
 //
 // Work. Ten worker warps per CTA each own a two-stage shared-memory ring,
-// filled by cp.async.bulk copies that the warp's lane 0 issues ahead of use
-// (completion on per-stage mbarriers). A layer is cut into tasks, dealt
+// filled by cp.async.bulk copies that the warp issues ahead of use, one lane
+// per copy (completion on per-stage mbarriers). A layer is cut into tasks, dealt
 // round-robin over all worker warps of the grid (continuing from layer to
 // layer):
 //   router : one row of W_r (bf16), fixed-order dot product -> one logit
@@ -21,6 +21,18 @@
 // Because the shared-down rows only need h_shared, which is complete long
 // before h_routed, they are computed while the routed gate/up work finishes,
 // and the routed-down copies are already in flight when h_routed is ready.
+//
+// Arithmetic. Router and shared rows: fp32 FMA of the bf16 weights. Routed
+// rows (int4): integer dot products (dp4a) of the codes against n or h_routed
+// held as 24-bit block fixed point (one power-of-two scale per 32 values) in
+// byte digits, exact per block, then the group affine in fp32. The control
+// warps build the digits: n's while warp 0 selects the top-8, h_routed's in
+// place when it is staged.
+//
+// The layer input is released in two phases: the raw x (enough for the
+// router rows, which apply the RMS scale after their dot products), then r
+// and n (for the shared gate/up rows). The top-8 is released as soon as the
+// selected experts' addresses are known; the softmax weights follow.
 //
 // Synchronisation. Every value that crosses CTAs is published as a word that
 // carries its own tag, and a reader checks the tags of the words it needs:
@@ -162,11 +174,11 @@ enum {
     TR_HR_STAGED = 5,    // ... published h_routed
     TR_CTA_HR_DONE = 6,  // the CTA's last worker finished its routed gate/up tasks
     TR_CTA_OUT = 7,      // the CTA's last worker finished the layer
-    TR_W_SGU_DONE = 8,   // worker 0 finished its shared gate/up items
+    TR_W_SGU_DONE = 8,   // worker 0 had the data of its first item after its shared gate/up items
     TR_W_RGU_READY = 9,  // ... had the data of its first routed gate/up item
-    TR_W_RGU_DONE = 10,  // ... finished its routed gate/up items
-    TR_W_DS_DONE = 11,   // ... finished its shared-down items
-    TR_W_RD_READY = 12,  // ... had the data of its routed-down item
+    TR_W_RGU_DONE = 10,  // ... had the data of its first item after its routed gate/up items
+    TR_W_DS_DONE = 11,   // ... had the data of its first routed-down item (after its shared-down rows)
+    TR_W_RD_READY = 12,  // ... had the data of its last routed-down item
     TR_W_DONE = 13,      // ... finished the layer
     TR_W_RGU1_END = 14,  // ... finished computing its first routed gate/up item
     TR_W_RGU_END = 15,   // ... finished computing its last routed gate/up item
@@ -616,7 +628,8 @@ __device__ bool ctrl_load(const Params& P, const void* src, uint32_t bytes, unsi
 }
 
 // The layer input: the tagged output of the previous layer (or the call's x)
-// -> x (bf16), r, n = r x and the word sums of n; all four control warps.
+// -> x (bf16; released to the router rows), then r, n = r x and the word sums
+// of n; all four control warps.
 __device__ bool stage_x(const Params& P, int l, uint32_t epoch, uint32_t hint_target, unsigned char* smem,
                         uint32_t bar_load, uint32_t bar_xs, int& loads, uint32_t* stale, int cw, int lane) {
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem + OFF_XS);
@@ -886,7 +899,7 @@ __device__ void route_weights(const Params& P, int l, unsigned char* smem, Route
 }
 
 // h_shared or h_routed (tagged fp32 words) -> shared memory, in place, checked by
-// the four control warps; for h_routed also the word sums of each 8-float word.
+// the four control warps; h_routed is then turned into digit blocks in place.
 __device__ bool stage_h(const Params& P, int l, uint32_t tag4, const uint32_t* hint, uint32_t hint_target,
                         bool routed, unsigned char* smem, uint32_t bar_load, int& loads, uint32_t* stale, int cw,
                         int lane) {

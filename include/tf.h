@@ -370,6 +370,10 @@ tf_status tf_stack_decode(tf_layer* const* layers, int L, const void* x, void* o
  * Device-side waits are bounded (2 s); when one runs out the kernel records it
  * and returns early. tf_stack_check synchronises the stream, reports that as
  * TF_ERR_TIMEOUT and re-initialises the workspace.
+ * Numerics: router logits and the top-k are bit-identical to tf_router_topk;
+ * the routed experts' dot products take n and h_routed as 24-bit fixed point
+ * with one power-of-two scale per 32 values (integer sums, exact per block),
+ * so the outputs differ from tf_stack_decode only by rounding.
  */
 typedef struct tf_stack tf_stack;
 size_t tf_stack_workspace_bytes(int L, int E);
@@ -384,11 +388,11 @@ tf_status tf_stack_set_prefetch(tf_stack* s, int on);
  * input, 1 published x and n, 2 held all router logits, 3 published the top-k,
  * 4 published h_shared, 5 published h_routed; at which 6 the CTA's last worker
  * finished its routed gate/up tasks, 7 its layer work; and at which the CTA's
- * first worker warp 8 finished its shared gate/up items, 9 had its first routed
- * gate/up data, 10 finished its routed gate/up items, 11 finished its shared-down
- * items, 12 had its routed-down data, 13 finished the layer, 14 finished
- * computing its first routed gate/up item, 15 its last. NULL turns tracing
- * off. */
+ * first worker warp had the data of 8 its first item after its shared gate/up
+ * items, 9 its first routed gate/up item, 10 its first item after its routed
+ * gate/up items, 11 its first routed-down item, 12 its last routed-down item,
+ * and 13 finished the layer, 14 finished computing its first routed gate/up
+ * item, 15 its last. NULL turns tracing off. */
 tf_status tf_stack_set_trace(tf_stack* s, void* buffer, size_t bytes);
 /* out = stack(x) for one token; x, out device bf16 [H], 16-byte aligned, out != x. */
 tf_status tf_stack_step(tf_stack* s, const void* x, void* out, void* stream);
