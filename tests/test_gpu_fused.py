@@ -25,8 +25,9 @@ def _view(ptr, shape, typestr):
     return B.device_view(ptr, shape, typestr)
 
 
-def _check_layer(seed, l, x_bits, out_bits, idx_g, w_g, logits_g, bias=None):
-    H, I, E, k, S = FULL["H"], FULL["I"], FULL["E"], FULL["k"], FULL["S"]
+def _check_layer(seed, l, x_bits, out_bits, idx_g, w_g, logits_g, bias=None, E=None):
+    H, I, k, S = FULL["H"], FULL["I"], FULL["k"], FULL["S"]
+    E = FULL["E"] if E is None else E
     r, z, idx, w = O.route(x_bits, W.router_weights(seed, l, E, H), bias, k)
     assert np.array_equal(logits_g.view(np.uint32), z.view(np.uint32)), "router logits differ"
     assert idx_g.tolist() == idx.tolist()
@@ -112,4 +113,33 @@ def test_fused_stack_rejects_other_shapes():
     with pytest.raises(B.TFError) as e:
         B.Stack(st.layers, ws)
     assert e.value.status == B.TF_ERR_NOT_SUPPORTED
+    st.close()
+
+
+@pytest.mark.parametrize("E", [256, 8], ids=["E256_max", "E8_min"])
+def test_fused_stack_expert_count_limits(E):
+    """The largest expert count the fused kernel takes (8 top-k keys per lane) and
+    the smallest (the top-8 is every expert), teacher-forced over two steps."""
+    seed, L, H = 13, 2, FULL["H"]
+    cfg = dict(FULL, E=E)
+    st = SyntheticStack(seed, L, **cfg)
+    ws = torch.zeros(B.tf_stack_workspace_bytes(L, E), dtype=torch.uint8, device=DEV)
+    fs = B.Stack(st.layers, ws)
+    x = hidden_tensor(seed, 0, 1, H)[0]
+    for step in range(2):
+        out = torch.full((H,), float("nan"), dtype=torch.bfloat16, device=DEV)
+        B.tf_stack_step(fs, x, out)
+        B.tf_stack_check(fs)
+        xin = bf16_bits(x)
+        for l in range(L):
+            pi, pw, pl, pa = fs.layer_buffers(l)
+            y = out if l == L - 1 else _view(pa, (H,), "<i2").view(torch.bfloat16)
+            yb = bf16_bits(y)
+            idx_g = _view(pi, (FULL["k"],), "<i4").cpu().numpy()
+            w_g = _view(pw, (FULL["k"],), "<f4").cpu().numpy()
+            lg = _view(pl, (E,), "<f4").cpu().numpy()
+            _check_layer(seed, l, xin, yb, idx_g, w_g, lg, None, E=E)
+            xin = yb
+        x = out
+    fs.close()
     st.close()
