@@ -443,8 +443,8 @@ BATCH_WORKLOAD = ("30-layer MoE-only stack, 64 tokens per step (x ~ N(0,1) [64, 
                   "same GEMM kernel; all experts resident in HBM; seed 3")
 PAYLOAD = 3 * (I * H // 2 + I * (H // 64) * 4)       # 3,345,408 B per expert
 # kernels behind one profiling bracket of a batched layer step: rms, histogram, positions, inverse init, two
-# gathers and the shared plan; four GEMMs
-BATCH_KERNELS_PER_BRACKET = {"router": 1, "permute": 7, "gemm": 4, "combine": 1}
+# gathers and the shared plan; four GEMMs and the two split-K sums of the shared expert (64 tokens fit one tile)
+BATCH_KERNELS_PER_BRACKET = {"router": 1, "permute": 7, "gemm": 6, "combine": 1}
 
 
 def batched_cpu_baseline(seed, x_bits, n_tokens=2):

@@ -95,6 +95,9 @@ struct GemmParams {
     uint32_t* err;
     int a_bf16;                 // 1: bf16 weight matrices by TMA (tmA, and tmA2 for the up rows); 0: int4 codes
     int pair_log2;              // gate/up: the up row of tile row m is m ^ (1 << pair_log2)
+    int ksplit;                 // K split into ksplit items per tile (> 1: raw fp32 partial sums go to part)
+    float* part;                // [ksplit][ntok][mrows] partial sums (ksplit > 1)
+    int ntok, mrows;
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -219,7 +222,7 @@ __device__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort
 // Work item w -> (expert, token block, weight tile), weight tiles fastest so that
 // consecutive items share their token rows in L2.
 struct Item {
-    int e, row0, nrows, mt;
+    int e, row0, nrows, mt, kc;  // kc: which K chunk (split K)
 };
 __device__ __forceinline__ Item decode_item(const GemmParams& p, int w) {
     int lo = 0, hi = p.E;  // largest e with tiles[e] <= w
@@ -230,7 +233,9 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int w) {
     }
     Item it;
     it.e = lo;
-    const int local = w - __ldg(p.tiles + lo);
+    const int local0 = w - __ldg(p.tiles + lo);
+    it.kc = local0 % p.ksplit;
+    const int local = local0 / p.ksplit;
     const int nb = local / p.MT;
     it.mt = local - nb * p.MT;
     it.row0 = __ldg(p.offsets + lo) + nb * NB;
@@ -270,7 +275,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC + 4);
-    const int KS = p.K / BK;
+    const int KS = p.K / BK / p.ksplit;  // K stages per item
     const int total = __ldg(p.tiles + p.E);
     const int gpr = p.K / 64;  // quant groups per weight row
 
@@ -322,6 +327,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                              bar(BAR_SF + sbi));
                 }
                 const int nbox = (it.nrows + BOX_ROWS - 1) / BOX_ROWS;
+                const int ks0 = it.kc * KS;
                 for (int ks = 0; ks < KS; ++ks) {
                     if (p.a_bf16) {
                         const int as = ai % NA;
@@ -331,19 +337,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         if (p.mode == 0) {
                             // 8 gate rows, then the same 8 up rows, per 16-row band (1 KB boxes keep the SW128 atoms)
                             for (int g = 0; g < BM / 16; ++g) {
-                                tma_load_2d(dst + g * 2048, &tmA, ks * BK, it.mt * (BM / 2) + g * 8, bar(BAR_AF + as));
-                                tma_load_2d(dst + g * 2048 + 1024, &tmA2, ks * BK, it.mt * (BM / 2) + g * 8,
+                                tma_load_2d(dst + g * 2048, &tmA, (ks0 + ks) * BK, it.mt * (BM / 2) + g * 8,
+                                            bar(BAR_AF + as));
+                                tma_load_2d(dst + g * 2048 + 1024, &tmA2, (ks0 + ks) * BK, it.mt * (BM / 2) + g * 8,
                                             bar(BAR_AF + as));
                             }
                         } else {
-                            tma_load_2d(dst, &tmA, ks * BK, it.mt * BM, bar(BAR_AF + as));
+                            tma_load_2d(dst, &tmA, (ks0 + ks) * BK, it.mt * BM, bar(BAR_AF + as));
                         }
                         ++ai;
                     } else {
                         const int cs = ci % NCS;
                         if (!(ok = wait_bar(bar(BAR_CE + cs), ((ci / NCS) & 1) ^ 1, abort_flag, p.err))) break;
                         mbar_expect_tx(bar(BAR_CF + cs), C_BYTES);
-                        tma_load_3d(smem_u32(smem + OFF_C + cs * C_BYTES), &tmA, ks * (BK / 2), it.mt * BM, it.e,
+                        tma_load_3d(smem_u32(smem + OFF_C + cs * C_BYTES), &tmA, (ks0 + ks) * (BK / 2), it.mt * BM, it.e,
                                     bar(BAR_CF + cs));
                         ++ci;
                     }
@@ -351,7 +358,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     if (!(ok = wait_bar(bar(BAR_BE + bs), ((bi / NBST) & 1) ^ 1, abort_flag, p.err))) break;
                     mbar_expect_tx(bar(BAR_BF + bs), (uint32_t)(nbox * BOX_ROWS * BK * 2));
                     for (int r = 0; r < nbox; ++r)
-                        tma_load_2d(smem_u32(smem + OFF_B + bs * B_BYTES + r * BOX_ROWS * BK * 2), &tmB, ks * BK,
+                        tma_load_2d(smem_u32(smem + OFF_B + bs * B_BYTES + r * BOX_ROWS * BK * 2), &tmB, (ks0 + ks) * BK,
                                     it.row0 + r * BOX_ROWS, bar(BAR_BF + bs));
                     ++bi;
                 }
@@ -412,7 +419,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * NB);
             const int nchunks = (it.nrows + 7) / 8;
-            if (p.mode == 0) {
+            if (p.ksplit > 1) {
+                // raw partial sums of this K chunk, token-major so that the warp's rows are contiguous
+                const int row = it.mt * BM + m;
+                for (int c = 0; c < nchunks; ++c) {
+                    float v[8];
+                    tc_ld8(tbase + (uint32_t)(c * 8), v);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int n = c * 8 + i;
+                        if (n < it.nrows) p.part[((size_t)it.kc * p.ntok + it.row0 + n) * p.mrows + row] = v[i];
+                    }
+                }
+            } else if (p.mode == 0) {
                 // h column of this row pair: 2^ps gate rows then their 2^ps up rows, repeated
                 const int ps = p.pair_log2;
                 const int j = it.mt * (BM / 2) + ((m >> (ps + 1)) << ps) + (m & ((1 << ps) - 1));
@@ -599,18 +618,46 @@ __global__ void k_group_inv_init(const int32_t* __restrict__ idx, int P, int E, 
 }
 
 // Work plan of the shared expert: one "expert" holding all T tokens in order.
-__global__ void k_shared_plan(int T, int mt_gu, int mt_d, int32_t* counts, int32_t* offsets, int32_t* tiles_gu,
-                              int32_t* tiles_d) {
+__global__ void k_shared_plan(int T, int mt_gu, int mt_d, int ks_gu, int ks_d, int32_t* counts, int32_t* offsets,
+                              int32_t* tiles_gu, int32_t* tiles_d) {
     if (threadIdx.x == 0) {
         const int nb = (T + NB - 1) / NB;
         counts[0] = T;
         offsets[0] = 0;
         offsets[1] = T;
         tiles_gu[0] = 0;
-        tiles_gu[1] = nb * mt_gu;
+        tiles_gu[1] = nb * mt_gu * ks_gu;
         tiles_d[0] = 0;
-        tiles_d[1] = nb * mt_d;
+        tiles_d[1] = nb * mt_d * ks_d;
     }
+}
+
+// Split-K shared gate/up: h[t][j] = bf16(gelu(g) u), g and u summed over the K
+// chunks in order (gate row of column j and its up row 8 rows further, per the
+// 8-row interleave of the tiles).
+__global__ void k_shared_gu_combine(const float* __restrict__ part, int ks, int T, int S, uint16_t* hs) {
+    const int t = blockIdx.y;
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= S) return;
+    const int jj = j & 63;
+    const int rg = (j >> 6) * BM + (jj >> 3) * 16 + (jj & 7);
+    float g = 0.0f, u = 0.0f;
+    for (int c = 0; c < ks; ++c) {
+        const float* pr = part + ((size_t)c * T + t) * (2 * S);
+        g += pr[rg];
+        u += pr[rg + 8];
+    }
+    hs[(size_t)t * S + j] = f2bf(gelu_tanh(g) * u);
+}
+
+// Split-K shared down: ys[t][i] = sum of the K chunks in order.
+__global__ void k_shared_down_combine(const float* __restrict__ part, int ks, int T, int H, float* ys) {
+    const int t = blockIdx.y;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= H) return;
+    float y = 0.0f;
+    for (int c = 0; c < ks; ++c) y += part[((size_t)c * T + t) * H + i];
+    ys[(size_t)t * H + i] = y;
 }
 
 // r_t = 1/sqrt(mean(x_t^2) + eps) in the canonical order, one warp per token.
@@ -688,7 +735,7 @@ __global__ void k_group_combine(const uint16_t* __restrict__ x, const float* __r
 
 struct Carve {
     size_t err, counts, offsets, tiles_gu, tiles_d, perm, inv, rms, xp, hb, y;
-    size_t s_plan, xn, hs, ys;  // shared expert (S > 0): plan arrays, n in token order, h, y
+    size_t s_plan, xn, hs, ys, spart;  // shared expert (S > 0): plan arrays, n in token order, h, y, split-K sums
     size_t total;
 };
 
@@ -707,12 +754,16 @@ Carve carve(int T, int H, int I, int E, int k, int S) {
     c.xp = o; o += align_up(P * H * 2, 256);
     c.hb = o; o += align_up(P * I * 2, 256);
     c.y = o; o += align_up(P * H * 4, 256);
-    c.s_plan = c.xn = c.hs = c.ys = 0;
+    c.s_plan = c.xn = c.hs = c.ys = c.spart = 0;
     if (S > 0) {
         c.s_plan = o; o += 256;  // counts[1], offsets[2], tiles_gu[2], tiles_d[2]
         c.xn = o; o += align_up((size_t)T * H * 2, 256);
         c.hs = o; o += align_up((size_t)T * S * 2, 256);
         c.ys = o; o += align_up((size_t)T * H * 4, 256);
+        // split-K partial sums, used while the tokens fit one 256-row tile (at most 4 chunks)
+        const size_t tk = (size_t)(T < NB ? T : NB);
+        const size_t rows = (size_t)(2 * S > H ? 2 * S : H);
+        c.spart = o; o += align_up(4 * tk * rows * 4, 256);
     }
     c.total = o;
     return c;
@@ -858,9 +909,21 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     k_group_pos<<<E, 1024, 0, st>>>(a.idx, P, offsets, perm, inv);
     k_group_inv_init<<<(P + 255) / 256, 256, 0, st>>>(a.idx, P, E, inv);
     k_group_gather<<<(P + 7) / 8, 256, 0, st>>>(x16, rms, perm, P, k, H, xp);
+    // the shared expert has few weight tiles (2S/128 and H/128); while the tokens fit one tile row, split K
+    // so that more SMs stream its weights (chunks of at least 4 stages)
+    auto split_of = [](int kstages) {
+        for (int c : {4, 3, 2})
+            if (kstages % c == 0 && kstages / c >= 4) return c;
+        return 1;
+    };
+    const bool one_block = T <= NB;
+    const int ks_gu = (S > 0 && one_block) ? split_of(H / BK) : 1;
+    const int ks_d = (S > 0 && one_block) ? split_of(S / BK) : 1;
+    float* spart = S > 0 ? reinterpret_cast<float*>(ws + c.spart) : nullptr;
     if (S > 0) {
         k_group_gather<<<(T + 7) / 8, 256, 0, st>>>(x16, rms, nullptr, T, 1, H, xn);
-        k_shared_plan<<<1, 32, 0, st>>>(T, 2 * S / BM, H / BM, s_plan, s_plan + 1, s_plan + 3, s_plan + 5);
+        k_shared_plan<<<1, 32, 0, st>>>(T, 2 * S / BM, H / BM, ks_gu, ks_d, s_plan, s_plan + 1, s_plan + 3,
+                                        s_plan + 5);
     }
     prof_after(TF_KERNEL_PERMUTE, stream);
     if (cudaError_t e = cudaGetLastError()) return cuda_status(e, fn);
@@ -873,6 +936,7 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     gp.counts = counts;
     gp.offsets = offsets;
     gp.err = err;
+    gp.ksplit = 1;
 
     prof_before(TF_KERNEL_GEMM, stream);
     gp.off_sb = lay.gu_sb;
@@ -901,13 +965,18 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
         sp.err = err;
         sp.a_bf16 = 1;
         sp.pair_log2 = 3;
+        sp.ntok = T;
+        sp.part = spart;
         sp.K = H;
         sp.MT = 2 * S / BM;
         sp.tiles = s_plan + 3;
         sp.mode = 0;
         sp.hout = hs;
         sp.ldo = S;
+        sp.ksplit = ks_gu;
+        sp.mrows = 2 * S;
         k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmS_g, tmS_xn, tmS_u, sp);
+        if (ks_gu > 1) k_shared_gu_combine<<<dim3((S + 255) / 256, T), 256, 0, st>>>(spart, ks_gu, T, S, hs);
         sp.K = S;
         sp.MT = H / BM;
         sp.tiles = s_plan + 5;
@@ -915,7 +984,10 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
         sp.hout = nullptr;
         sp.yout = ys;
         sp.ldo = H;
+        sp.ksplit = ks_d;
+        sp.mrows = H;
         k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmS_d, tmS_h, tmS_d, sp);
+        if (ks_d > 1) k_shared_down_combine<<<dim3((H + 255) / 256, T), 256, 0, st>>>(spart, ks_d, T, H, ys);
     }
     prof_after(TF_KERNEL_GEMM, stream);
     if (cudaError_t e = cudaGetLastError()) return cuda_status(e, fn);
