@@ -249,17 +249,42 @@ template <int B>
 __device__ __forceinline__ float byte128(uint32_t x) {
     return __uint_as_float(__byte_perm(x, 0x43000000u, 0x7054u | (B << 8)));
 }
-// Eight codes of one word -> eight bf16 weights RN(fl(s q + b)) packed in a uint4.
+// Packed fp32 pairs (sm_100+ two-wide add and FMA; each lane is the IEEE operation).
+__device__ __forceinline__ unsigned long long pk2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpk2(unsigned long long v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// Eight codes of one word -> eight bf16 weights RN(fl(s q + b)) packed in a uint4:
+// (128 + q) - 128 is exact, s q is exact, so each weight takes one fp32 rounding,
+// then one to bf16. Columns 2j and 2j+1 share a packed pair.
 __device__ __forceinline__ uint4 dequant8(uint32_t q, float s, float b) {
     const uint32_t lo = q & 0x0f0f0f0fu, hi = (q >> 4) & 0x0f0f0f0fu;  // codes 0,2,4,6 / 1,3,5,7
+    const unsigned long long S2 = pk2(s, s), B2 = pk2(b, b), M2 = pk2(-128.0f, -128.0f);
+    const unsigned long long q0 = add2(pk2(byte128<0>(lo), byte128<0>(hi)), M2);
+    const unsigned long long q1 = add2(pk2(byte128<1>(lo), byte128<1>(hi)), M2);
+    const unsigned long long q2 = add2(pk2(byte128<2>(lo), byte128<2>(hi)), M2);
+    const unsigned long long q3 = add2(pk2(byte128<3>(lo), byte128<3>(hi)), M2);
+    const unsigned long long w[4] = {fma2(S2, q0, B2), fma2(S2, q1, B2), fma2(S2, q2, B2), fma2(S2, q3, B2)};
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const float qe = (j == 0 ? byte128<0>(lo) : j == 1 ? byte128<1>(lo) : j == 2 ? byte128<2>(lo) : byte128<3>(lo)) -
-                         128.0f;  // exact
-        const float qo = (j == 0 ? byte128<0>(hi) : j == 1 ? byte128<1>(hi) : j == 2 ? byte128<2>(hi) : byte128<3>(hi)) -
-                         128.0f;
-        const __nv_bfloat162 v = __floats2bfloat162_rn(fmaf(s, qe, b), fmaf(s, qo, b));  // s q exact: one rounding each
+        float a, c;
+        unpk2(w[j], a, c);
+        const __nv_bfloat162 v = __floats2bfloat162_rn(a, c);
         o[j] = *reinterpret_cast<const uint32_t*>(&v);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
