@@ -482,31 +482,58 @@ def run_batched(args):
     bufs = [torch.empty(T, H, dtype=torch.bfloat16, device=dev) for _ in range(4)]
     bufs[0].copy_(x0)
 
-    def step(src, dst):
+    def step(src, dst, st):
         x = src
         for l in range(L):
             y = dst if l == L - 1 else bufs[2 + l % 2]
-            B.tf_layer_step(stack.layers[l], None, l, 0, None, x, y, T, None, 0, stream)
+            B.tf_layer_step(stack.layers[l], None, l, 0, None, x, y, T, None, 0, st)
             x = y
 
     cur, nxt = 0, 1
     for _ in range(args.warmup):
-        step(bufs[cur], bufs[nxt])
+        step(bufs[cur], bufs[nxt], stream)
         cur, nxt = nxt, cur
     torch.cuda.synchronize()
+    # per-kernel times: a few plain steps with every launch bracketed by events
+    prof_steps = min(args.steps, 8)
+    prof_cap = prof_steps * L           # timed brackets per kind: one per layer of each profiled step
+    B.tf_profile_begin(prof_cap)
+    for _ in range(prof_steps):
+        step(bufs[cur], bufs[nxt], stream)
+        cur, nxt = nxt, cur
+    torch.cuda.synchronize()
+    prof = B.tf_profile_end()
+    # the step as two CUDA graphs (one per direction of the ping-pong buffers): a batched layer step
+    # enqueues no host synchronisation, so the whole 30-layer step is captured once and replayed
+    graphs = None
+    if not args.no_graph:
+        try:
+            cap = torch.cuda.Stream(dev)
+            graphs = [torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()]
+            for i in range(2):
+                with torch.cuda.graph(graphs[i], stream=cap):
+                    step(bufs[i], bufs[1 - i], torch.cuda.current_stream(dev))
+            torch.cuda.synchronize()
+            bufs[0].copy_(x0)
+            for i in range(2):       # first replays upload the graphs: keep them out of the timed region
+                graphs[i].replay()
+            torch.cuda.synchronize()
+        except RuntimeError as e:
+            print("CUDA graph capture failed (%s); timing plain launches" % e, file=sys.stderr)
+            graphs = None
+    cur, nxt = 0, 1
     sampler = ClockSampler(0)
     sampler.start()
-    prof_steps = min(args.steps, 8)
-    prof_cap = prof_steps * L           # timed brackets per kind: one per layer of the first prof_steps steps
-    B.tf_profile_begin(prof_cap)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(args.steps):
-        step(bufs[cur], bufs[nxt])
+        if graphs is not None:
+            graphs[cur].replay()
+        else:
+            step(bufs[cur], bufs[nxt], stream)
         cur, nxt = nxt, cur
     ev1.record(stream)
     torch.cuda.synchronize()
-    prof = B.tf_profile_end()
     clocks = sampler.stop()
     ms = ev0.elapsed_time(ev1)
     assert not torch.isnan(bufs[cur].float()).any(), "NaN in the stack output"
@@ -533,7 +560,10 @@ def run_batched(args):
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         bufs[0].copy_(hx, non_blocking=True)
-        step(bufs[0], bufs[1])
+        if graphs is not None:
+            graphs[0].replay()
+        else:
+            step(bufs[0], bufs[1], stream)
         hy.copy_(bufs[1], non_blocking=True)
         stream.synchronize()
         hx.copy_(hy)
@@ -552,7 +582,7 @@ def run_batched(args):
         "metric": BATCH_METRIC, "value": round(T * n / (ms / 1000.0), 1), "unit": "tok/s", "n_gpus": 1, "steps": n,
         "warmup": args.warmup, "ms_per_step": round(ms / n, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": BATCH_WORKLOAD, "layers": L, "tokens_per_step": T,
+        "config": {"workload": BATCH_WORKLOAD, "layers": L, "tokens_per_step": T, "cuda_graph": graphs is not None,
                    "l2": "no flush: each step streams about %.1f GB of weights, far above the 126 MB L2"
                          % (step_bytes / 1e9)},
         "distinct_experts_per_layer": round(sum(distinct) / L, 1),
@@ -566,7 +596,7 @@ def run_batched(args):
         "kernels": {k: {"event_ms_total": round(v[0], 4), "brackets": int(v[1]), "timed_brackets": min(int(v[1]), prof_cap),
                         "avg_us": round(v[0] / max(1, min(v[1], prof_cap)) * 1000.0, 2)}
                     for k, v in prof.items() if v[1]},
-        "gpu_launches": int(sum(v[1] * BATCH_KERNELS_PER_BRACKET.get(k, 1) for k, v in prof.items())),
+        "gpu_launches": int(n * L * sum(BATCH_KERNELS_PER_BRACKET.values())),   # kernels of the timed steps
         "clocks": clocks,
         "e2e": {"value": round(T * e2e_steps / e2e_s, 1), "unit": "tok/s", "h2d_bytes_per_step": T * H * 2,
                 "d2h_bytes_per_step": T * H * 2},
@@ -711,6 +741,8 @@ def main():
                          "batched: the stack with 64 tokens per step")
     ap.add_argument("--alpha", type=float, default=STREAM_ALPHA,
                     help="streaming: scale of the Zipf(1.1) router bias")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="batched: time plain launches instead of replaying the step as a CUDA graph")
     ap.add_argument("--noise", type=float, default=STREAM_NOISE,
                     help="streaming: sigma of the per-(step, layer) router-logit noise")
     ap.add_argument("--layers", type=int, default=L,
