@@ -102,7 +102,7 @@ constexpr int OFF_RING = 0;
 constexpr int OFF_XS = OFF_RING + NWORK * NS * STAGE;   // bf16 x [H]
 constexpr int OFF_N = OFF_XS + H * 2;                    // fp32 n in two halves per word: n[8w..8w+3] at
                                                          // float4 w, n[8w+4..8w+7] at float4 HW + w
-constexpr int OFF_SN = OFF_N + H * 4;                    // fp32 word sums of n [HW]
+constexpr int OFF_SN = OFF_N + H * 4;                    // fp32 word sums of n [HW] (written, no longer read)
 constexpr int OFF_H = OFF_SN + HW * 4;                   // tagged fp32 h_routed [K*I], h_shared [S]; also the
                                                          // landing zone of the tagged layer input
 constexpr int OFF_Z = OFF_H + H_FLOATS * 4;              // tagged logits [MAX_E] (64-bit words)
