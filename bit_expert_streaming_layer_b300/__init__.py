@@ -58,6 +58,7 @@ SIGNATURES = {
     "tf_last_error": (ctypes.c_char_p, []),
     "tf_status_string": (ctypes.c_char_p, [_S]),
     "tf_version": (ctypes.c_char_p, []),
+    "tf_struct_bytes": (_sz, [_i32]),
     "tf_expert_payload_bytes": (_sz, [_i32, _i32]),
     "tf_expert_slot_bytes": (_sz, [_i32, _i32]),
     "tf_expert_offsets": (_S, [_i32, _i32, _vp]),

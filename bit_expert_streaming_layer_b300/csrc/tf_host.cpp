@@ -69,6 +69,16 @@ const char* tf_status_string(tf_status s) {
 
 const char* tf_version(void) { return "tf-b300 0.1 (sm_103a)"; }
 
+size_t tf_struct_bytes(int which) {
+    switch (which) {
+        case 0: return sizeof(tf_expert_table);
+        case 1: return sizeof(tf_layer_desc);
+        case 2: return sizeof(tf_step_stats);
+        case 3: return sizeof(tf_cache_event);
+        default: return 0;
+    }
+}
+
 size_t tf_expert_payload_bytes(int H, int I) {
     ExpertLayout L;
     return expert_layout(H, I, &L) ? L.payload : 0;

@@ -314,6 +314,13 @@ typedef struct {
 } tf_step_stats;
 
 /*
+ * Size in bytes of a structure of this ABI, for bindings to check their own
+ * layout against the library's: which = 0 tf_expert_table, 1 tf_layer_desc,
+ * 2 tf_step_stats, 3 tf_cache_event; 0 for any other value.
+ */
+size_t tf_struct_bytes(int which);
+
+/*
  * out = layer(x). T tokens (T = 1 with a cache). logit_bias as in tf_router_topk.
  * Without a cache all work is enqueued on compute_stream and the call returns.
  * T > 1 (at most the handle's T_max; batched decode or prefill): the router for

@@ -33,6 +33,13 @@ def test_library_loads_and_exports_every_declared_symbol():
     assert set(B.SIGNATURES) == set(names)
 
 
+def test_binding_structures_match_the_library_layout():
+    L = B.lib()
+    for which, cls in enumerate([B.ExpertTable, B.LayerDesc, B.StepStats, B.CacheEvent]):
+        assert L.tf_struct_bytes(which) == ctypes.sizeof(cls), cls.__name__
+    assert L.tf_struct_bytes(4) == 0
+
+
 def test_version_and_status_strings():
     assert b"sm_103a" in B.lib().tf_version()
     assert B.lib().tf_status_string(1) == b"TF_ERR_INVALID_ARG"
