@@ -276,6 +276,7 @@ def run_ours(args, rank, world):
 STREAM_SEED, STREAM_ZIPF, STREAM_SLOTS = 2, 1.1, 16
 STREAM_ALPHA = 0.1     # Zipf bias scale
 STREAM_NOISE = 1.5     # sigma of the per-(step, layer) router-logit noise (the token-dependent part of the logits)
+SWEEP_WARMUP, SWEEP_STEPS = 16, 96   # per point of the slot-count sweep
 STREAM_METRIC = "MoE decode tok/s with experts streamed from pinned host memory through a 16-slot LFU cache (1 B300)"
 STREAM_WORKLOAD = ("30-layer MoE-only decode stack, batch 1, a fresh x ~ N(0,1) per step (the next token's input); "
                    "experts (12.9 GB, 3,840 x 3.36 MB) in "
@@ -324,14 +325,17 @@ def run_streaming(args):
     copy_stream = torch.cuda.Stream(dev)
     probe = h2d_probe(dev, copy_stream)
     # one fresh input per step: a fed-back output settles on a fixed point whose routing never changes
-    n_inputs = args.warmup + args.steps + min(args.steps, 32) + min(args.steps, 64)
+    sweep = [int(v) for v in args.slot_sweep.split(",") if v.strip()] if args.slot_sweep else []
+    n_inputs = args.warmup + args.steps + min(args.steps, 32) + min(args.steps, 64) + \
+        len(sweep) * (SWEEP_WARMUP + SWEEP_STEPS)
     xs = torch.stack([hidden_tensor(seed, t, 1, H, device=dev)[0] for t in range(n_inputs)])
     noise = np.stack([np.stack([W.route_noise(seed, l, t, E, sigma) for l in range(L)]) for t in range(n_inputs)])
     bufs = [torch.empty(H, dtype=torch.bfloat16, device=dev) for _ in range(5)]   # 0-1 outputs, 2-3 scratch, 4 input
     prev = [None] * L
     tot = {"hits": 0, "misses": 0, "bytes": 0, "stall_ms": 0.0, "copy_ms": 0.0, "shared_ms": 0.0, "tokens": 0}
 
-    def token(step, src, dst, measure=0):
+    def token(step, src, dst, measure=0, cache=None):
+        cache = cache if cache is not None else stack.cache
         x = src
         for l in range(L):
             bias_hn[l] = zipf_h[l] + noise[step, l]
@@ -340,7 +344,7 @@ def run_streaming(args):
             bias_d[l].copy_(bias_h[l], non_blocking=True)
             bias = bias_d[l]
             y = dst if l == L - 1 else bufs[2 + l % 2]
-            st = B.tf_layer_step(stack.layers[l], stack.cache, l, step, stack.store, x, y, 1, bias, 0, stream,
+            st = B.tf_layer_step(stack.layers[l], cache, l, step, stack.store, x, y, 1, bias, 0, stream,
                                  copy_stream, measure)
             prev[l] = np.array(st.ids[:K_ACT], dtype=np.int64)
             tot["hits"] += st.hits
@@ -397,6 +401,37 @@ def run_streaming(args):
         stream.synchronize()
         step += 1
     e2e_s = time.perf_counter() - t0
+
+    # slot-count sweep: the same workload through caches of other sizes (one device pool sized for the largest,
+    # a fresh LFU cache per point, cold start then SWEEP_WARMUP steps before SWEEP_STEPS timed ones)
+    sweep_out = []
+    if sweep:
+        pool = torch.zeros(L * max(sweep) * stack.slot, dtype=torch.uint8, device=dev)
+        for n_slots in sweep:
+            cache = B.ExpertCache(L, n_slots, E, stack.slot, pool)
+            for l in range(L):
+                prev[l] = None
+            for _ in range(SWEEP_WARMUP):
+                token(step, xs[step], bufs[0], cache=cache)
+                step += 1
+            torch.cuda.synchronize()
+            for k in tot:
+                tot[k] = 0
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(SWEEP_STEPS):
+                token(step, xs[step], bufs[step % 2], cache=cache)
+                step += 1
+            e1.record(stream)
+            torch.cuda.synchronize()
+            sms = e0.elapsed_time(e1)
+            sweep_out.append({"slots_per_layer": n_slots, "steps": SWEEP_STEPS,
+                              "tok_s": round(SWEEP_STEPS / (sms / 1000.0), 2),
+                              "hit_rate": round(tot["hits"] / max(1, tot["hits"] + tot["misses"]), 4),
+                              "bytes_fetched_per_token": int(tot["bytes"] / SWEEP_STEPS),
+                              "slot_pool_gb": round(L * n_slots * stack.slot / 1e9, 2)})
+            cache.close()
+        del pool
     stack.close()
 
     n = args.steps
@@ -427,6 +462,8 @@ def run_streaming(args):
         "e2e": {"value": round(e2e_steps / e2e_s, 2), "unit": "tok/s", "h2d_bytes_per_step": H * 2,
                 "d2h_bytes_per_step": H * 2},
     }
+    if sweep_out:
+        line["slot_sweep"] = sweep_out
     if not args.no_cpu_baseline:
         base = oracle_baseline(args.oracle_layers)
         line["cpu_baseline"] = {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")}
@@ -743,6 +780,8 @@ def main():
                     help="streaming: scale of the Zipf(1.1) router bias")
     ap.add_argument("--no-graph", action="store_true",
                     help="batched: time plain launches instead of replaying the step as a CUDA graph")
+    ap.add_argument("--slot-sweep", default="",
+                    help="streaming: also measure these slot counts per layer, e.g. 8,32,64")
     ap.add_argument("--noise", type=float, default=STREAM_NOISE,
                     help="streaming: sigma of the per-(step, layer) router-logit noise")
     ap.add_argument("--layers", type=int, default=L,
