@@ -337,6 +337,120 @@ def test_shared_ffn_closed_form():
     assert np.allclose(y, want, rtol=1e-12, atol=1e-12)
 
 
+def _rn_bf16(v) -> np.float64:
+    """fp32(v) rounded to the nearest bf16 (ties to even), by exhaustive comparison of the two neighbours."""
+    f = np.float32(v)
+    return np.float64(W.bf16_to_f32(np.array([_nearest_bf16_bruteforce(f)], np.uint16))[0])
+
+
+def _gelu64(v):
+    return 0.5 * v * (1 + math.tanh(math.sqrt(2 / math.pi) * (v + 0.044715 * v ** 3)))
+
+
+def _spread_input(rng, n):
+    """Values of magnitude in [1/8, 4) whose fp32 form is almost never a bf16 value: rounding them to bf16
+    changes them, and every bf16 value of this range is a multiple of 2^-10, so sums of up to 2^10 of them
+    are exact in fp64 (and in fp32)."""
+    mag = 2.0 ** rng.uniform(-3, 2, n)
+    return np.where(rng.random(n) < 0.5, -mag, mag).astype(np.float32).astype(np.float64)
+
+
+def _bf16_branch_variants(n, pi, sigma, wg=1.0, wu=1.0):
+    """Closed forms of y = Wd (gelu(Wg n) * (Wu n)) for gate rows e_pi(j) * wg, up rows all wu, down rows
+    e_sigma(j) (exact weights), in the bf16-operand reading and in the readings a slip would produce."""
+    nb = np.array([_rn_bf16(v) for v in n])
+    out = {}
+    for name, nn, round_h, round_gu in (("bf16 n and h", nb, True, False), ("fp32 n", n, True, False),
+                                        ("no h rounding", nb, False, False), ("g, u rounded", nb, False, True)):
+        U = wu * nn.sum()
+        h = []
+        for j in range(len(pi)):
+            g = wg * nn[pi[j]]
+            u = U
+            if round_gu:
+                g, u = _rn_bf16(g), _rn_bf16(u)
+            v = _gelu64(g) * u
+            h.append(_rn_bf16(v) if round_h else v)
+        out[name] = np.array([h[sigma[j]] for j in range(len(sigma))])
+    return out
+
+
+def _assert_only_reading(y, variants, want="bf16 n and h"):
+    assert np.array_equal(y, variants[want])
+    for name, v in variants.items():
+        if name != want:
+            assert not np.allclose(y, v, rtol=1e-6, atol=0), name   # the pin tells the readings apart
+
+
+def test_expert_ffn_bf16_operands_closed_form():
+    """The dequant-to-bf16 reading of a routed expert (bf16_ops = 1): n, every dequantised weight and h
+    are rounded to bf16 before their products. Gate = permutation, up = all-ones rows, down = another
+    permutation (weights exact in bf16), n not representable in bf16:
+        y_j = bf16(gelu(bf16(n_a)) * sum_k bf16(n_k)),   a = pi(sigma(j)).
+    Keeping n in fp32, dropping the rounding of h, or rounding g and u instead of h all fail."""
+    Hs, Is = 256, 128
+    rng = np.random.default_rng(17)
+    pi = rng.permutation(Hs)[:Is]
+    sigma = rng.integers(0, Is, Hs)
+    qg = np.zeros((Is, Hs), np.uint8)
+    qg[np.arange(Is), pi] = 1
+    qd = np.zeros((Hs, Is), np.uint8)
+    qd[np.arange(Hs), sigma] = 1
+    one, zero = _const_f16(1.0, (Is, Hs // 64)), _const_f16(0.0, (Is, Hs // 64))
+    ex = {"gate": (qg, one, zero),
+          "up": (np.zeros((Is, Hs), np.uint8), _const_f16(0.5, (Is, Hs // 64)), one),
+          "down": (qd, _const_f16(1.0, (Hs, Is // 64)), _const_f16(0.0, (Hs, Is // 64)))}
+    n = _spread_input(rng, Hs)
+    y = O.expert_ffn(n, ex, bf16_ops=True, bits=64)
+    _assert_only_reading(y, _bf16_branch_variants(n, pi, sigma))
+    # the fp32 reading of the same expert keeps every operand as it is
+    assert np.allclose(O.expert_ffn(n, ex, bf16_ops=False, bits=64),
+                       [_gelu64(n[pi[sigma[j]]]) * n.sum() for j in range(Hs)], rtol=1e-12, atol=0)
+
+
+def test_expert_ffn_bf16_rounds_the_dequantised_weights():
+    """The gate weight s q (code 3, bias 0) is not a bf16 value. In the bf16 reading the gate row holds
+    bf16(s q) at its permuted column, so g_j = bf16(s q) bf16(n_a); keeping the fp32 weight gives s q."""
+    Hs, Is = 192, 64
+    rng = np.random.default_rng(18)
+    pi = rng.permutation(Hs)[:Is]
+    sigma = rng.integers(0, Is, Hs)
+    s16 = np.float16(0.0131)
+    w_exact = np.float64(np.float32(s16)) * 3                  # s q is exact in fp32
+    w_bf16 = _rn_bf16(w_exact)
+    assert w_bf16 != w_exact
+    qg = np.zeros((Is, Hs), np.uint8)
+    qg[np.arange(Is), pi] = 3
+    qd = (np.arange(Is)[None, :] == sigma[:, None]).astype(np.uint8)
+    ex = {"gate": (qg, _const_f16(float(s16), (Is, Hs // 64)), _const_f16(0.0, (Is, Hs // 64))),
+          "up": (np.zeros((Is, Hs), np.uint8), _const_f16(0.5, (Is, Hs // 64)), _const_f16(1.0, (Is, Hs // 64))),
+          "down": (qd, _const_f16(1.0, (Hs, Is // 64)), _const_f16(0.0, (Hs, Is // 64)))}
+    n = _spread_input(rng, Hs)
+    y = O.expert_ffn(n, ex, bf16_ops=True, bits=64)
+    assert np.array_equal(y, _bf16_branch_variants(n, pi, sigma, wg=w_bf16)["bf16 n and h"])
+    assert not np.allclose(y, _bf16_branch_variants(n, pi, sigma, wg=w_exact)["bf16 n and h"], rtol=1e-6, atol=0)
+
+
+def test_shared_ffn_bf16_operands_closed_form():
+    """The bf16-operand reading of the shared expert (weights already bf16): n and h rounded to bf16.
+    Gate = permutation, up = all-twos rows, down = permutation:
+        y_j = bf16(gelu(bf16(n_a)) * 2 sum_k bf16(n_k))."""
+    Hs, Ss = 192, 96
+    rng = np.random.default_rng(19)
+    pi = rng.permutation(Hs)[:Ss]
+    sigma = rng.integers(0, Ss, Hs)
+    one = np.float32(1.0).view(np.uint32) >> 16
+    two = np.float32(2.0).view(np.uint32) >> 16
+    Wg = np.zeros((Ss, Hs), np.uint16)
+    Wg[np.arange(Ss), pi] = one
+    Wu = np.full((Ss, Hs), two, np.uint16)
+    Wd = np.zeros((Hs, Ss), np.uint16)
+    Wd[np.arange(Hs), sigma] = one
+    n = _spread_input(rng, Hs)
+    y = O.shared_ffn(n, Wg, Wu, Wd, bf16_ops=True, bits=64)
+    _assert_only_reading(y, _bf16_branch_variants(n, pi, sigma, wu=2.0))
+
+
 def test_layer_combine_weighted_sum_closed_form():
     """delta = shared + sum_i w_i y_i with per-expert closed forms, out = bf16(x + delta)."""
     Hs, Is, Ss, k = 128, 64, 64, 3
