@@ -4,9 +4,12 @@ CPU oracle, through the C ABI.
 T tokens go through the router, the grouped routed experts and the bf16 shared
 expert, both on the tcgen05 GEMM kernel. The oracle is the per-token decode
 layer with the shared expert, in its bf16-operand reading (n, every weight and
-h rounded to bf16, fp32 accumulation). Checked per token: the RMS scale, the
-router logits and top-k ids bit for bit, the weights to a few ulp, and the
-output and its update within the contract tolerance. Small shapes check every
+h rounded to bf16, fp32 accumulation) and in its plain fp32 reading (the
+contract). Checked per token: the RMS scale, the router logits and top-k ids
+bit for bit, the weights to a few ulp, and the output and its update within
+the contract tolerance against both readings. The layer step exposes no fp32
+update, so the update is out - x, allowed the bf16 output's own rounding
+(1.5 ulp of out, see parity.delta_rel_err). Small shapes check every
 token; the model's shape with 64 tokens (the batched-decode workload) checks
 sampled tokens.
 """
@@ -57,13 +60,19 @@ def _check(seed, cfg, st, x_bits, out_bits, route, tokens):
         for e in idx:
             if int(e) not in cache:
                 cache[int(e)] = W.expert(seed, 0, int(e), H, I)
-        out_o, delta_o = O.layer_combine(x_bits[t], r, [cache[int(e)] for e in idx], w, shared, bf16_ops=True)
+        ex = [cache[int(e)] for e in idx]
+        out_o, delta_o = O.layer_combine(x_bits[t], r, ex, w, shared, bf16_ops=True)
         got = bf16_to_f64(out_bits[t])
         assert not np.isnan(got).any(), t
         assert max_rel_err(got, bf16_to_f64(out_o)) <= CONTRACT_TOL, t
         err = delta_rel_err(out_bits[t], x_bits[t], delta_o)
         assert err <= CONTRACT_TOL, (t, err)
         worst = max(worst, err)
+        # the contract as written: the bf16 tensor-core path against the plain fp32 oracle
+        out_f, delta_f = O.layer_combine(x_bits[t], r, ex, w, shared, bf16_ops=False)
+        assert max_rel_err(got, bf16_to_f64(out_f)) <= CONTRACT_TOL, t
+        err_f = delta_rel_err(out_bits[t], x_bits[t], delta_f)
+        assert err_f <= CONTRACT_TOL, (t, err_f)
     return worst
 
 

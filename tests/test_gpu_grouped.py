@@ -1,9 +1,11 @@
 """GPU parity of the grouped (batched / prefill) routed-expert path,
 tf_moe_ffn_grouped, against the CPU oracle, through the C ABI.
 
-The oracle is the per-token decode layer in its dequant-to-bf16 reading (n,
-every dequantised weight and h rounded to bf16, fp32 accumulation), looped
-over tokens. Checked:
+The oracle is the per-token decode layer, looped over tokens, in two readings:
+its dequant-to-bf16 reading (n, every dequantised weight and h rounded to
+bf16, fp32 accumulation; the kernel's own roundings) and its plain fp32
+reading (the contract: the bf16 tensor-core path within 1e-2 of the fp32
+oracle). Checked:
   - the permutation and the per-expert counts exactly (a stable sort by expert
     of the (token, rank) pairs, and the histogram of the ids);
   - every token's output and update within the contract tolerance, on all
@@ -67,7 +69,11 @@ def _check_permutation(idx, perm, counts, E):
     assert np.array_equal(perm, np.argsort(idx.ravel(), kind="stable").astype(np.int32))
 
 
-def _check_tokens(seed, x_bits, idx, w, out_bits, delta, tokens, H, I):
+def _check_tokens(seed, x_bits, idx, w, out_bits, delta, tokens, H, I, worst_fp32=None):
+    """Per token: output and update within the contract against the oracle's bf16-operand reading and
+    against its plain fp32 reading; returns the worst update error of the former (worst_fp32[0] gets the
+    worst of the latter)."""
+    worst_fp32 = worst_fp32 if worst_fp32 is not None else [0.0]
     cache = {}
     worst = 0.0
     for t in tokens:
@@ -75,14 +81,22 @@ def _check_tokens(seed, x_bits, idx, w, out_bits, delta, tokens, H, I):
             if int(e) not in cache:
                 cache[int(e)] = W.expert(seed, 0, int(e), H, I)
         r = O.rms_scale(x_bits[t])
-        out_o, delta_o = O.layer_combine(x_bits[t], r, [cache[int(e)] for e in idx[t]], w[t], None, bf16_ops=True)
+        ex = [cache[int(e)] for e in idx[t]]
         got_o = bf16_to_f64(out_bits[t])
         assert not np.isnan(got_o).any() and not np.isnan(delta[t]).any(), t
+        # the bf16-operand reading (the kernel's own roundings): tight
+        out_o, delta_o = O.layer_combine(x_bits[t], r, ex, w[t], None, bf16_ops=True)
         e_out = max_rel_err(got_o, bf16_to_f64(out_o))
         e_delta = max_rel_err(delta[t], delta_o)
         assert e_out <= CONTRACT_TOL, (t, e_out)
         assert e_delta <= CONTRACT_TOL, (t, e_delta)
         worst = max(worst, e_delta)
+        # the contract as written: the bf16 tensor-core path against the plain fp32 oracle
+        out_f, delta_f = O.layer_combine(x_bits[t], r, ex, w[t], None, bf16_ops=False)
+        assert max_rel_err(got_o, bf16_to_f64(out_f)) <= CONTRACT_TOL, t
+        e_f = max_rel_err(delta[t], delta_f)
+        assert e_f <= CONTRACT_TOL, (t, e_f)
+        worst_fp32[0] = max(worst_fp32[0], e_f)
     return worst
 
 
@@ -101,8 +115,10 @@ def test_grouped_small_all_tokens(H, I, E, k, T, zipf_s, skip):
     _check_permutation(idx, perm, counts, E)
     for e in skip:
         assert counts[e] == 0
-    worst = _check_tokens(seed, x_bits, idx, w, out, delta, range(T), H, I)
+    worst_fp32 = [0.0]
+    worst = _check_tokens(seed, x_bits, idx, w, out, delta, range(T), H, I, worst_fp32)
     assert worst < 5e-3
+    assert worst_fp32[0] < CONTRACT_TOL
 
 
 def _sampled_tokens(idx, counts, n, seed):
