@@ -31,7 +31,8 @@ _STATUS = {0: "TF_OK", 1: "TF_ERR_INVALID_ARG", 2: "TF_ERR_CUDA", 3: "TF_ERR_OOM
 
 
 class ExpertTable(ctypes.Structure):
-    _fields_ = [("base", ctypes.c_void_p), ("stride", ctypes.c_size_t), ("slot_of_expert", ctypes.c_void_p)]
+    _fields_ = [("base", ctypes.c_void_p), ("stride", ctypes.c_size_t), ("slot_of_expert", ctypes.c_void_p),
+                ("n_experts", ctypes.c_int32), ("n_slots", ctypes.c_int32)]
 
 
 class CacheEvent(ctypes.Structure):
@@ -209,8 +210,10 @@ def tf_dequant_expert(blob, H, I, matrix, as_bf16, out, stream=None) -> None:
            "tf_dequant_expert")
 
 
-def expert_table(base, stride: int, slot_of_expert=None) -> ExpertTable:
-    return ExpertTable(_ptr(base), stride, _ptr(slot_of_expert))
+def expert_table(base, stride: int, slot_of_expert=None, n_experts: int = 0, n_slots: int = 0) -> ExpertTable:
+    """Expert e at base + (slot_of_expert[e] if a map is given else e) * stride; ids valid in [0, n_experts)
+    (0: the layer's E where a layer descriptor carries the table), map entries in [0, n_slots)."""
+    return ExpertTable(_ptr(base), stride, _ptr(slot_of_expert), n_experts, n_slots)
 
 
 # ----------------------------------------------------------------- MoE FFN

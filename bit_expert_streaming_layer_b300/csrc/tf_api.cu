@@ -19,6 +19,19 @@ tf_status cuda_status(int err, const char* what) {
 
 static int g_copy_countdown = 0;  // failure injection for the miss-fill engine (0 = off)
 
+int smem_limit_once(const void* kernel, int bytes) {
+    static std::mutex mu;
+    static std::vector<std::pair<const void*, int>> done;  // (kernel, device) pairs already raised
+    int dev = 0;
+    if (cudaError_t e = cudaGetDevice(&dev)) return (int)e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const auto& d : done)
+        if (d.first == kernel && d.second == dev) return 0;
+    if (cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) return (int)e;
+    done.emplace_back(kernel, dev);
+    return 0;
+}
+
 // ------------------------------------------------------------- profiling
 struct Prof {
     bool on = false;
@@ -55,6 +68,9 @@ static tf_status check_table(const tf_expert_table* t, const char* fn) {
     if (!t || !t->base) return fail(TF_ERR_INVALID_ARG, "%s: expert table or its base is NULL", fn);
     if (!aligned16(t->base) || t->stride % 16)
         return fail(TF_ERR_INVALID_ARG, "%s: expert base and stride must be 16-byte aligned", fn);
+    if (t->n_experts < 1) return fail(TF_ERR_INVALID_ARG, "%s: the table's n_experts must be >= 1", fn);
+    if (t->slot_of_expert && t->n_slots < 1)
+        return fail(TF_ERR_INVALID_ARG, "%s: a table with a slot map needs n_slots >= 1", fn);
     return TF_OK;
 }
 
@@ -66,6 +82,8 @@ static ExpertRef table_ref(const tf_expert_table* t, const int32_t* idx) {
     r.slot_map = t->slot_of_expert;
     r.idx = idx;
     r.use_ptrs = 0;
+    r.n_experts = t->n_experts;
+    r.n_slots = t->n_slots;
     return r;
 }
 
@@ -146,6 +164,11 @@ tf_status check_desc(const tf_layer_desc* d, const char* fn) {
                      !aligned16(d->W_sd)))
         return fail(TF_ERR_INVALID_ARG, "%s: shared-expert weights NULL or misaligned", fn);
     if (!(d->eps >= 0.0f)) return fail(TF_ERR_INVALID_ARG, "%s: eps must be >= 0", fn);
+    if (d->experts.n_experts != 0 && d->experts.n_experts != d->E)
+        return fail(TF_ERR_INVALID_ARG, "%s: the expert table's n_experts (%d) is not E (%d)", fn,
+                    d->experts.n_experts, d->E);
+    if (d->experts.slot_of_expert && d->experts.n_slots < 1)
+        return fail(TF_ERR_INVALID_ARG, "%s: a table with a slot map needs n_slots >= 1", fn);
     return TF_OK;
 }
 
@@ -358,6 +381,7 @@ tf_status tf_layer_create(const tf_layer_desc* d, int T_max, void* workspace, si
     tf_layer* l = new (std::nothrow) tf_layer();
     if (!l) return fail(TF_ERR_OOM, "%s: out of host memory", fn);
     l->d = *d;
+    if (l->d.experts.n_experts == 0) l->d.experts.n_experts = d->E;  // 0 stands for the descriptor's E
     l->T_max = T_max;
     expert_layout(d->H, d->I, &l->lay);
     l->ws = static_cast<char*>(workspace);

@@ -152,6 +152,11 @@ __global__ void __launch_bounds__(GU_WARPS * 32) k_gateup(DecodeParams p, int u0
         if (u < routed_units) {
             const int i = u / I, j = u - (u / I) * I;
             const char* blob = expert_ptr(p.ex, i);
+            dst = p.h_routed + (size_t)i * I + j;
+            if (!blob) {  // out-of-range expert id: no load, the output becomes NaN
+                if (lane == 0) *dst = qnan();
+                continue;
+            }
             const char* gq = blob + (size_t)(2 * j) * (H / 2);
             const char* uq = gq + H / 2;
             const uint32_t* gsb = reinterpret_cast<const uint32_t*>(blob + p.off_gu_sb + (size_t)(2 * j) * (H / 64) * 4);
@@ -189,7 +194,6 @@ __global__ void __launch_bounds__(GU_WARPS * 32) k_gateup(DecodeParams p, int u0
                     }
                 }
             }
-            dst = p.h_routed + (size_t)i * I + j;
         } else {
             const int j = u - routed_units;
             const char* gw = reinterpret_cast<const char*>(p.Wsg + (size_t)j * H);
@@ -251,11 +255,22 @@ __global__ void __launch_bounds__(DN_WARPS * 32) k_down(DecodeParams p, int with
             for (int t = threadIdx.x; t < S / 4; t += blockDim.x) ds[t] = __ldcg(gs + t);
         }
     }
+    __shared__ int s_bad;
+    if (threadIdx.x == 0) s_bad = 0;
+    __syncthreads();
     if (threadIdx.x < kr) {
         s_w[threadIdx.x] = p.w[threadIdx.x];
         s_ptr[threadIdx.x] = expert_ptr(p.ex, threadIdx.x);
+        if (!s_ptr[threadIdx.x]) s_bad = 1;
     }
     __syncthreads();
+    if (s_bad) {  // an out-of-range expert id: no load through it; the outputs become NaN
+        for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < H; j += gridDim.x * blockDim.x) {
+            p.out[j] = 0x7fc0u;
+            if (p.delta) p.delta[j] = qnan();
+        }
+        return;
+    }
     for (int c = threadIdx.x; c < kr * (I / 32); c += blockDim.x) {
         float s = 0.0f;
 #pragma unroll
@@ -352,11 +367,7 @@ int launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* Wr, int 
                        uint32_t* counters, float eps, void* stream) {
     dim3 grid((E + RT_WARPS - 1) / RT_WARPS, T);
     const size_t smem = (size_t)(RT_WARPS + 1) * H * 2;
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_router_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        attr = true;
-    }
+    if (int e = smem_limit_once((const void*)k_router_topk, 200 * 1024)) return e;
     prof_before(TF_KERNEL_ROUTER, stream);
     k_router_topk<<<grid, RT_WARPS * 32, smem, (cudaStream_t)stream>>>(x, H, Wr, E, bias, bias_stride, k, idx, w,
                                                                     logits, rms, counters, eps);
@@ -378,11 +389,7 @@ static int sm_count() {
 int launch_gateup(const DecodeParams& p, int u0, int u1, void* stream) {
     if (u1 <= u0) return 0;
     const size_t smem = (size_t)p.H * 4 + (size_t)(p.H / 32) * 4;
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-        attr = true;
-    }
+    if (int e = smem_limit_once((const void*)k_gateup, 64 * 1024)) return e;
     const int units = u1 - u0;
     int grid = (units + GU_WARPS - 1) / GU_WARPS;
     const int cap = sm_count() * 4;
@@ -396,11 +403,7 @@ int launch_gateup(const DecodeParams& p, int u0, int u1, void* stream) {
 int launch_down(const DecodeParams& p, int with_routed, int with_shared, void* stream) {
     const int kr = with_routed ? p.k : 0;
     const size_t smem = ((size_t)down_hs_offset(kr, p.I) + (with_shared ? (size_t)p.S : 0)) * 4;
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_down, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        attr = true;
-    }
+    if (int e = smem_limit_once((const void*)k_down, 200 * 1024)) return e;
     int grid = (p.H + DN_WARPS - 1) / DN_WARPS;
     const int cap = sm_count() * 2;
     if (grid > cap) grid = cap;

@@ -117,12 +117,20 @@ __device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib) {
     return ia < ib;
 }
 
+// Address of the i-th selected expert, or NULL when its id (or its slot) is out
+// of range: an invalid id is never turned into an address.
 __device__ __forceinline__ const char* expert_ptr(const ExpertRef& r, int i) {
     if (r.use_ptrs) return r.ptr[i];
     int e = r.idx[i];
-    if (r.slot_map) e = r.slot_map[e];
+    if ((unsigned)e >= (unsigned)r.n_experts) return nullptr;
+    if (r.slot_map) {
+        e = r.slot_map[e];
+        if ((unsigned)e >= (unsigned)r.n_slots) return nullptr;
+    }
     return r.base + (size_t)e * r.stride;
 }
+
+__device__ __forceinline__ float qnan() { return __int_as_float(0x7fc00000); }
 
 // ---------------------------------------------------- top-k of one token
 // Warp 0 of a CTA: the k best of z[0..E) (larger first, ties -> lower index,

@@ -145,6 +145,8 @@ struct LayerDesc {
     uint32_t* cnt_out;        // CTAs whose output rows are done (+= gridDim per launch)
     int E;
     float eps;
+    int n_slots;              // with slot_map: its entries are valid in [0, n_slots)
+    int pad_;
     unsigned long long off_gu_sb, off_d_codes, off_d_sb;
 };
 
@@ -847,7 +849,13 @@ __device__ bool route_layer(const Params& P, int l, uint32_t tag, uint32_t epoch
         int e = sel;
         bad = (unsigned)e >= (unsigned)D.E;
         if (bad) e = 0;  // never form an address from an out-of-range id
-        if (D.slot_map) e = __ldcg(D.slot_map + e);
+        if (D.slot_map) {
+            e = __ldcg(D.slot_map + e);
+            if ((unsigned)e >= (unsigned)D.n_slots) {
+                bad = 1;
+                e = 0;
+            }
+        }
         rt->ep[s][lane] = D.ebase + (size_t)e * D.estride;
     }
     if (__any_sync(FULL, bad)) {
@@ -1427,6 +1435,7 @@ tf_status tf_stack_create(tf_layer* const* layers, int L, const float* const* lo
         D.act_out = reinterpret_cast<uint16_t*>(base + sc.act);
         D.E = E;
         D.eps = d.eps;
+        D.n_slots = d.experts.n_slots;
         D.off_gu_sb = lay.gu_sb;
         D.off_d_codes = lay.d_codes;
         D.off_d_sb = lay.d_sb;

@@ -856,6 +856,9 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
         return fail(TF_ERR_INVALID_ARG, "%s: expert table base and stride must be 16-byte aligned", fn);
     if (table->slot_of_expert)
         return fail(TF_ERR_NOT_SUPPORTED, "%s: the grouped path takes a resident expert table (no slot map)", fn);
+    if (table->n_experts != 0 && table->n_experts != E)
+        return fail(TF_ERR_INVALID_ARG, "%s: the expert table's n_experts (%d) is not E (%d)", fn, table->n_experts,
+                    E);
     if (!aligned16(a.x) || !aligned16(a.out) || (a.delta && !aligned16(a.delta)))
         return fail(TF_ERR_INVALID_ARG, "%s: x, out and delta must be 16-byte aligned", fn);
     if ((size_t)T * k > (size_t)INT32_MAX / 4) return fail(TF_ERR_INVALID_ARG, "%s: T*k too large", fn);
@@ -914,12 +917,7 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
             !encode_rows(&tmS_h, hs, S, T, BOX_ROWS))
             return fail(TF_ERR_CUDA, "%s: tensor maps of the shared expert", fn);
     }
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_group_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GEMM_SMEM);
-        if (e != cudaSuccess) return cuda_status(e, fn);
-        attr_set = true;
-    }
+    if (int e = smem_limit_once((const void*)k_group_gemm, (int)GEMM_SMEM)) return cuda_status(e, fn);
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -43,6 +43,8 @@ struct ExpertRef {
     const int32_t* slot_map;     // nullable
     const int32_t* idx;          // device [k]
     int use_ptrs;
+    int n_experts;               // ids valid in [0, n_experts)
+    int n_slots;                 // slot_map entries valid in [0, n_slots)
 };
 
 struct DecodeParams {
@@ -64,6 +66,10 @@ struct DecodeParams {
 
 // Descriptor a layer handle was created with (tf_api.cu).
 void layer_desc_of(const tf_layer* l, tf_layer_desc* out);
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device); thread-safe. Returns a cudaError_t.
+int smem_limit_once(const void* kernel, int bytes);
 
 // Event bracketing of launches while profiling is on (tf_api.cu).
 void prof_before(int kind, void* stream);

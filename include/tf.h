@@ -148,13 +148,23 @@ tf_status tf_router_topk(const void* x, int T, int H, const void* W_r, int E, co
 /*
  * Where the packed experts live in device memory. Expert e is at
  *   base + (slot_of_expert ? slot_of_expert[e] : e) * stride
- * (slot_of_expert is a device int32 [E] map, NULL for a resident array).
- * base and stride must be 16-byte aligned.
+ * (slot_of_expert is a device int32 [n_experts] map, NULL for a resident
+ * array). base and stride must be 16-byte aligned.
+ *   n_experts  expert ids are valid in [0, n_experts). The kernels read the ids
+ *              (and the map) on the device; an id outside that range, or a map
+ *              entry outside [0, n_slots), is never turned into an address: the
+ *              call's outputs become NaN instead (the error is seen in the data,
+ *              since the call returns before the kernels run).
+ *   n_slots    with slot_of_expert: the number of slots at base (map entries
+ *              are valid in [0, n_slots)); ignored without a map.
+ * In a tf_layer_desc, n_experts = 0 stands for the descriptor's E.
  */
 typedef struct {
     const void* base;
     size_t stride;
     const int32_t* slot_of_expert;
+    int32_t n_experts;
+    int32_t n_slots;
 } tf_expert_table;
 
 /* Dequantise one matrix (0 gate, 1 up, 2 down) of a packed device expert to a
@@ -168,6 +178,7 @@ tf_status tf_dequant_expert(const void* blob, int H, int I, int matrix, int as_b
 /*
  * Routed-expert FFN of one token with the weighted combine into the residual:
  *   out = x + sum_i w[i] * E_idx[i](RMSNorm(x))      (i in top-k order)
+ * table->n_experts >= 1 is required; an id outside it makes out (and delta) NaN.
  * HN page "Show HN: ...", section "Abordagem tecnica (MoE + streaming por
  * SSD)": only a small subset of experts is active per token; devtrends page,
  * section "Sem dependencias do llama.cpp e MLX": fused 4-bit GEMV and MoE kernels.

@@ -115,8 +115,19 @@ def test_device_entry_points_reject_bad_arguments_before_launch():
     assert L.tf_router_topk(8, 1, 100, 8, 128, None, 0, 8, 8, 8, None, None, 8, 1 << 20, None) == 1
     t = B.ExpertTable(8, 3, None)     # stride not a multiple of 16
     assert L.tf_moe_ffn_decode(8, 8, ctypes.byref(t), 8, 8, 8, 2816, 704, None, 8, 1 << 20, None) == 1
-    t = B.ExpertTable(16, 16, None)
+    t = B.ExpertTable(16, 16, None, 128)
     assert L.tf_moe_ffn_decode(8, 8, ctypes.byref(t), 8, 8, 8, 2816, 704, None, 8, 16, None) == 1  # small ws
+    assert b"workspace" in L.tf_last_error()
+    # the id range must be given: the kernels check every id against it before forming an address
+    t = B.ExpertTable(16, 16, None, 0)
+    assert L.tf_moe_ffn_decode(8, 8, ctypes.byref(t), 8, 8, 8, 2816, 704, None, 8, 1 << 20, None) == 1
+    assert b"n_experts" in L.tf_last_error()
+    assert L.tf_moe_ffn_decode_noalloc(8, 8, ctypes.byref(t), 8, 8, 8, 2816, 704, None, None) == 1
+    t = B.ExpertTable(16, 16, 256, 128, 0)   # a slot map without its slot count
+    assert L.tf_moe_ffn_decode(8, 8, ctypes.byref(t), 8, 8, 8, 2816, 704, None, 8, 1 << 20, None) == 1
+    assert b"n_slots" in L.tf_last_error()
+    d = B.layer_desc(2816, 704, 128, 8, 2112, 16, 16, 16, 16, B.ExpertTable(16, 16, None, 64))
+    assert B.tf_layer_workspace_bytes(d, 1) == 0          # the table's id range is not the layer's E
     d = B.layer_desc(2816, 704, 128, 8, 2112, 16)   # shared weights missing
     assert B.tf_layer_workspace_bytes(d, 1) == 0
     h = ctypes.c_void_p()
@@ -137,6 +148,10 @@ def test_device_entry_points_reject_bad_arguments_before_launch():
     tm = B.ExpertTable(256, 3358720, 512)   # a slot map: the grouped path takes resident experts only
     assert grouped(256, 512, 4, ctypes.byref(tm), 128, 256, 256, 8, 2816, 704, None, None, None, 256, ws,
                    None) == 5
+    te = B.ExpertTable(256, 3358720, None, 64)   # the table's id range is not E
+    assert grouped(256, 512, 4, ctypes.byref(te), 128, 256, 256, 8, 2816, 704, None, None, None, 256, ws,
+                   None) == 1
+    assert b"n_experts" in L.tf_last_error()
 
 
 def test_workspace_sizes():

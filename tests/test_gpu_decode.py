@@ -129,7 +129,7 @@ def test_moe_ffn_decode_parity(cfg):
     Wr = W.router_weights(seed, 0, E, H)
     r, z, idx, w = O.route(xb, Wr, None, k)
     d_exp, slot = _device_experts(seed, 0, idx, E, H, I)
-    table = B.expert_table(d_exp, slot)
+    table = B.expert_table(d_exp, slot, n_experts=E)
     d_idx = torch.from_numpy(idx).to(DEV)
     d_w = torch.from_numpy(w.astype(np.float32)).to(DEV)
     ws = torch.zeros(B.tf_moe_decode_workspace_bytes(H, I, k), dtype=torch.uint8, device=DEV)
@@ -152,6 +152,35 @@ def test_moe_ffn_decode_parity(cfg):
     B.tf_moe_ffn_decode(x2, x2, table, d_idx, d_w, k, H, I, None, ws, ws.numel())
     torch.cuda.synchronize()
     assert torch.equal(x2.view(torch.int16), out.view(torch.int16))
+
+
+def test_moe_ffn_decode_out_of_range_ids_give_nan_without_a_read():
+    """An id outside the table's range (or a slot-map entry outside its slots) is never turned into an
+    address: the output and the update become NaN. The ids are checked on the device before any load."""
+    H, I, E, k = 512, 256, 8, 4
+    seed = 23
+    d_exp, slot = _device_experts(seed, 0, np.arange(E), E, H, I)
+    x = hidden_tensor(seed, 0, 1, H)[0]
+    ws = torch.zeros(B.tf_moe_decode_workspace_bytes(H, I, k), dtype=torch.uint8, device=DEV)
+    d_w = torch.full((k,), 0.25, dtype=torch.float32, device=DEV)
+    smap = torch.tensor([0, 1, 2, 3, 4, 5, 6, 99], dtype=torch.int32, device=DEV)   # expert 7 -> slot 99
+    cases = [(B.expert_table(d_exp, slot, n_experts=E), [0, 1, E, 2]),
+             (B.expert_table(d_exp, slot, n_experts=E), [0, -1, 1, 2]),
+             (B.expert_table(d_exp, slot, smap, n_experts=E, n_slots=E), [0, 1, 7, 2])]
+    for table, ids in cases:
+        d_idx = torch.tensor(ids, dtype=torch.int32, device=DEV)
+        out, delta = nan_bf16(H), nan_f32(H)
+        out.zero_()
+        delta.zero_()
+        B.tf_moe_ffn_decode(x, out, table, d_idx, d_w, k, H, I, delta, ws, ws.numel())
+        torch.cuda.synchronize()
+        assert torch.isnan(out.float()).all() and torch.isnan(delta).all(), ids
+    # the same ids in range give finite outputs
+    d_idx = torch.tensor([0, 1, 6, 2], dtype=torch.int32, device=DEV)
+    out, delta = nan_bf16(H), nan_f32(H)
+    B.tf_moe_ffn_decode(x, out, cases[2][0], d_idx, d_w, k, H, I, delta, ws, ws.numel())
+    torch.cuda.synchronize()
+    assert not torch.isnan(out.float()).any() and not torch.isnan(delta).any()
 
 
 # ------------------------------------------------------------- layer step
