@@ -72,31 +72,69 @@ def set_layers(n_layers: int) -> None:
 set_layers(L)
 
 
-# DRAM traffic of the fused kernel from an ncu capture of a 4-layer stack of the same kernel (read + write bytes,
-# scaled by 30/4 to the 30-layer launch); reported only while the kernel's code (its source without // comments
-# and blank lines) is the one that was captured
-FUSED_TRAFFIC = {"code_sha256": "5d4901950c408e13a5fdd9a2e26efdf8d9559195a838dc8b8b8989e09da49e7d",
-                 "bytes_per_layer": (252804352 + 4017152) / 4}
+# DRAM traffic of the fused kernel taken from an ncu capture (not measured in this run): read + write bytes of a
+# 4-layer stack of the same kernel, scaled by 30/4 to the 30-layer launch. Reported only while the kernel's code
+# (its source and the headers it includes, without // comments and blank lines, plus the nvcc flags) is the one
+# that was captured; null otherwise.
+FUSED_TRAFFIC = {"code_sha256": None, "bytes_per_layer": None, "capture": None}
+FUSED_SOURCES = ("tf_fused.cu", "tf_device.cuh", "tf_internal.h")
 
 
-def code_hash(path):
+def code_hash(paths, extra=""):
     import hashlib
     lines = []
-    for ln in open(path).read().splitlines():
-        i = ln.find("//")
-        ln = (ln[:i] if i >= 0 else ln).rstrip()
-        if ln:
-            lines.append(ln)
+    for path in paths:
+        for ln in open(path).read().splitlines():
+            i = ln.find("//")
+            ln = (ln[:i] if i >= 0 else ln).rstrip()
+            if ln:
+                lines.append(ln)
+    lines.append(extra)
     return hashlib.sha256("\n".join(lines).encode()).hexdigest()
 
 
+def fused_code_hash():
+    from bit_expert_streaming_layer_b300 import build as kb
+    csrc = os.path.join(ROOT, "bit_expert_streaming_layer_b300", "csrc")
+    paths = [os.path.join(csrc, f) for f in FUSED_SOURCES] + [os.path.join(ROOT, "include", "tf.h")]
+    return code_hash(paths, " ".join(kb.ARCH + kb.COMMON[:4]))
+
+
 def fused_traffic(n_layers):
-    src = os.path.join(ROOT, "bit_expert_streaming_layer_b300", "csrc", "tf_fused.cu")
+    if FUSED_TRAFFIC["code_sha256"] is None:
+        return None
     try:
-        h = code_hash(src)
+        h = fused_code_hash()
     except OSError:
         return None
     return int(FUSED_TRAFFIC["bytes_per_layer"] * n_layers) if h == FUSED_TRAFFIC["code_sha256"] else None
+
+
+def spread(ms_list):
+    """Median, p10 and p90 of per-step times (ms)."""
+    a = np.asarray(ms_list, np.float64)
+    return {"median_ms": round(float(np.median(a)), 5), "p10_ms": round(float(np.percentile(a, 10)), 5),
+            "p90_ms": round(float(np.percentile(a, 90)), 5), "n": int(a.size)}
+
+
+def host_info():
+    """CPU model and core count of this host, GPU name."""
+    model = ""
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    info = {"nproc": os.cpu_count(), "cpu_model": model}
+    try:
+        import torch
+        if torch.cuda.is_available():
+            info["gpu"] = torch.cuda.get_device_name(0)
+    except Exception:
+        pass
+    return info
 
 
 def peaks():
@@ -162,6 +200,20 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ oracle baseline
 
+def _oracle_layer(O, W, x, l, mt, shared=None):
+    """One layer of the decode stack on the oracle: (output bits, seconds of oracle time). Weight generation is
+    not timed."""
+    Wr = W.router_weights(SEED, l, E, H)
+    shared = shared if shared is not None else W.shared_weights(SEED, l, H, S)
+    t0 = time.perf_counter()
+    r, z, idx, w = O.route(x, Wr, mt=mt)
+    el = time.perf_counter() - t0
+    experts = W.experts_parallel(SEED, l, idx, H, I)
+    t0 = time.perf_counter()
+    out, _ = O.layer_combine(x, r, experts, w, shared, mt=mt)
+    return out, el + time.perf_counter() - t0
+
+
 def oracle_baseline(n_layers: int = 6):
     """Time the CPU oracle on a bounded sample: the first n_layers of step 0 of the stack
     (routing + 8 experts + shared expert + combine), single thread. Returns tok/s for 30 layers."""
@@ -169,22 +221,46 @@ def oracle_baseline(n_layers: int = 6):
     import workload as W
     O.build()
     x = W.hidden(SEED, 0, 1, H)[0]
-    elapsed = 0.0
+    elapsed, outs = 0.0, []
     for l in range(n_layers):
-        Wr = W.router_weights(SEED, l, E, H)
-        shared = W.shared_weights(SEED, l, H, S)
-        t0 = time.perf_counter()
-        r, z, idx, w = O.route(x, Wr)
-        elapsed += time.perf_counter() - t0
-        experts = W.experts_parallel(SEED, l, idx, H, I)      # generation is not timed
-        t0 = time.perf_counter()
-        x, _ = O.layer_combine(x, r, experts, w, shared)
-        elapsed += time.perf_counter() - t0
+        x, dt = _oracle_layer(O, W, x, l, False)
+        outs.append(x)
+        elapsed += dt
     per_layer = elapsed / n_layers
     return {"value": 1.0 / (per_layer * L), "unit": "tok/s", "cores": 1, "kind": "oracle",
             "sample": "%d of the 30 layers of one decode step (step 0, seed %d), single-threaded fp32 C oracle; "
                       "tok/s = 1 / (30 x mean layer time); weight generation not timed" % (n_layers, SEED),
-            "seconds": elapsed}
+            "seconds": elapsed, "outputs": outs}
+
+
+def oracle_baseline_all_cores(ref_outputs):
+    """The same oracle with OpenMP over its independent output rows, on all host cores, for one whole decode
+    step (all layers of step 0); the layers the single-threaded sample covered must come out bit-identical."""
+    import oracle as O
+    import workload as W
+    from concurrent.futures import ThreadPoolExecutor
+    O.build()
+    with ThreadPoolExecutor(min(32, os.cpu_count() or 1)) as ex:    # generation, not timed
+        shared = list(ex.map(lambda l: W.shared_weights(SEED, l, H, S), range(L)))
+    x = W.hidden(SEED, 0, 1, H)[0]
+    elapsed = 0.0
+    for l in range(L):
+        x, dt = _oracle_layer(O, W, x, l, True, shared[l])
+        elapsed += dt
+        if l < len(ref_outputs):
+            assert np.array_equal(x, ref_outputs[l]), "the all-cores oracle differs from the single-threaded one"
+    return {"value": 1.0 / elapsed, "unit": "tok/s", "cores": O.threads(True), "kind": "oracle",
+            "sample": "one whole decode step (all %d layers of step 0, seed %d), the fp32 C oracle with OpenMP "
+                      "over its output rows (per-row sums unchanged; outputs bit-identical to the single-threaded "
+                      "oracle on the layers both ran); weight generation not timed" % (L, SEED),
+            "bit_identical_layers": len(ref_outputs), "seconds": round(elapsed, 3)}
+
+
+def cpu_baselines(n_layers):
+    one = oracle_baseline(n_layers)
+    allc = oracle_baseline_all_cores(one["outputs"])
+    return ({k: one[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            {k: allc[k] for k in ("value", "unit", "cores", "kind", "sample", "bit_identical_layers")})
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -229,19 +305,20 @@ def run_ours(args, rank, world):
     sampler.start()
     prof_steps = min(args.steps, args.profile_steps)
     B.tf_profile_begin(prof_steps * (1 if args.path == "fused" else L))
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     torch.cuda.synchronize()
-    ev0.record(stream)
-    for _ in range(args.steps):
+    evs[0].record(stream)
+    for i in range(args.steps):
         step(cur, nxt)
         cur, nxt = nxt, cur
-    ev1.record(stream)
+        evs[i + 1].record(stream)
     torch.cuda.synchronize()
     prof = B.tf_profile_end()
     clocks = sampler.stop()
     if fused is not None:
         B.tf_stack_check(fused, stream)
-    ms = ev0.elapsed_time(ev1)
+    ms = evs[0].elapsed_time(evs[-1])
+    step_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
     if world > 1:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -268,7 +345,7 @@ def run_ours(args, rank, world):
         B.tf_stack_check(fused, stream)
         fused.close()
     stack.close()
-    return ms, prof, clocks, gpu_launches, e2e_s, e2e_steps
+    return ms, prof, clocks, gpu_launches, e2e_s, e2e_steps, step_ms
 
 
 # ------------------------------------------------------------------ streamed experts (LFU cache, host store)
@@ -464,6 +541,7 @@ def run_streaming(args):
     }
     if sweep_out:
         line["slot_sweep"] = sweep_out
+    line["host"] = host_info()
     if not args.no_cpu_baseline:
         base = oracle_baseline(args.oracle_layers)
         line["cpu_baseline"] = {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")}
@@ -758,6 +836,37 @@ def run_prefill(args):
     print(json.dumps(line))
 
 
+def run_reference(args):
+    """The CPU oracle, as it stands (single-threaded fp32 C), on the decode workload. One step of this arm is one
+    layer of the stack: step s runs layer s mod 30 on the previous step's output (the token's layers in order, the
+    last layer's output feeding the next token's first layer), so that W + K steps are a bounded sample that ends
+    in well under a minute. tok/s = 1 / (30 x the mean measured layer time)."""
+    import oracle as O
+    import workload as W
+    O.build()
+    x = W.hidden(SEED, 0, 1, H)[0]
+    times = []
+    for s in range(args.warmup + args.steps):
+        x, dt = _oracle_layer(O, W, x, s % L, False)
+        if s >= args.warmup:
+            times.append(dt)
+    layer_s = float(np.mean(times))
+    value = 1.0 / (L * layer_s)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(layer_s * 1000.0, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "layers": L,
+                       "step": "one layer of the 30-layer stack (1/30 of a token), outputs fed forward; "
+                               "tok/s = 1 / (30 x mean layer time); weight generation not timed"},
+            "step_time": spread([t * 1000.0 for t in times]),
+            "host": host_info(),
+            "cpu_baseline": {"value": round(value, 5), "unit": "tok/s", "cores": 1, "kind": "oracle",
+                             "sample": "%d layer steps after %d warm-up layer steps of the decode stack, seed %d, "
+                                       "single-threaded fp32 C oracle" % (args.steps, args.warmup, SEED)},
+            "e2e": {"value": round(value, 5), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -796,18 +905,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        steps_s = []
-        base = None
-        for _ in range(max(1, args.steps if args.steps <= 3 else 1)):
-            base = oracle_baseline(args.oracle_layers)
-            steps_s.append(base["seconds"])
-        line = {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": "tok/s", "n_gpus": args.gpus,
-                "steps": 1, "warmup": 0, "ms_per_step": 1000.0 / base["value"], "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-                "config": {"workload": WORKLOAD, "layers": L},
-                "cpu_baseline": {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")},
-                "e2e": {"value": base["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
+        run_reference(args)
         return
 
     if args.workload == "prefill":
@@ -829,7 +927,7 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
 
-    ms, prof, clocks, launches, e2e_s, e2e_steps = run_ours(args, rank, world)
+    ms, prof, clocks, launches, e2e_s, e2e_steps, step_ms = run_ours(args, rank, world)
     if rank != 0:
         return
     tok_s = world * args.steps / (ms / 1000.0)
@@ -865,14 +963,15 @@ def main():
                      "bytes_per_launch": BYTES[dom],
                      "traffic": fused_traffic(L) if (dom == "layer" and args.path == "fused") else None},
         "kernels": per_kernel,
+        "step_time": spread(step_ms),
         "gpu_launches": int(launches),
         "clocks": clocks,
+        "host": host_info(),
         "e2e": {"value": round(world * e2e_steps / e2e_s, 2), "unit": "tok/s", "h2d_bytes_per_step": H * 2,
                 "d2h_bytes_per_step": H * 2},
     }
     if world == 1 and not args.no_cpu_baseline:
-        base = oracle_baseline(args.oracle_layers)
-        line["cpu_baseline"] = {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        line["cpu_baseline"], line["cpu_baseline_all_cores"] = cpu_baselines(args.oracle_layers)
     print(json.dumps(line))
 
 

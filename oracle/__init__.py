@@ -6,7 +6,9 @@ binding) never does, and the oracle shares no code with it: both sides are fed
 by the seeded generators in ``workload/`` and nothing else.
 
 The arithmetic lives in ``oracle.c`` (plain single-threaded C, built twice:
-fp32 and fp64); this module only loads it and marshals numpy arrays.
+fp32 and fp64, and once more as fp32 with OpenMP over its independent output
+rows, which gives bit-identical results and is used only to time the oracle on
+all host cores); this module only loads it and marshals numpy arrays.
 
 Pins: every function here is checked in ``tests/test_oracle_*.py`` against
 closed forms, brute force, hand-written traces and the pages' fixed facts.
@@ -25,15 +27,17 @@ EPS = 1e-6
 K_ACTIVE = 8
 
 
-def _lib_path(bits: int) -> str:
-    return os.path.join(_HERE, "liboracle%d.so" % bits)
+def _lib_path(bits: int, mt: bool = False) -> str:
+    return os.path.join(_HERE, "liboracle%d%s.so" % (bits, "mt" if mt else ""))
 
 
 def build(force: bool = False) -> None:
-    """Compile the fp32 and fp64 oracles (-O2, no FMA contraction, no fast-math, SSE2)."""
-    for bits, defs in ((32, ["-DREAL=float", "-DREAL_IS_DOUBLE=0"]),
-                       (64, ["-DREAL=double", "-DREAL_IS_DOUBLE=1"])):
-        out = _lib_path(bits)
+    """Compile the fp32 and fp64 oracles (-O2, no FMA contraction, no fast-math, SSE2), and the fp32 oracle
+    once more with OpenMP over its independent output rows (bit-identical results, for timing on all cores)."""
+    for bits, mt, defs in ((32, False, ["-DREAL=float", "-DREAL_IS_DOUBLE=0"]),
+                           (64, False, ["-DREAL=double", "-DREAL_IS_DOUBLE=1"]),
+                           (32, True, ["-DREAL=float", "-DREAL_IS_DOUBLE=0", "-fopenmp"])):
+        out = _lib_path(bits, mt)
         if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(_SRC):
             tmp = out + ".tmp%d" % os.getpid()
             subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
@@ -53,10 +57,12 @@ class CacheEvent(ctypes.Structure):
 _libs: dict = {}
 
 
-def lib(bits: int = 32):
-    if bits not in _libs:
+def lib(bits: int = 32, mt: bool = False):
+    """The fp32 (bits = 32) or fp64 oracle; mt = True: the fp32 build whose row loops use all cores."""
+    key = (bits, mt)
+    if key not in _libs:
         build()
-        L = ctypes.CDLL(_lib_path(bits))
+        L = ctypes.CDLL(_lib_path(bits, mt))
         R = ctypes.c_float if bits == 32 else ctypes.c_double
         vp, i32 = ctypes.c_void_p, ctypes.c_int
         L.or_half_to_float.restype = ctypes.c_float
@@ -88,8 +94,14 @@ def lib(bits: int = 32):
         L.or_lfu_step.argtypes = [vp, i32, i32, vp, i32, ctypes.POINTER(CacheEvent)]
         L.or_lfu_state.argtypes = [vp, i32, vp, vp, vp]
         L.or_real_bytes.restype = i32
-        _libs[bits] = L
-    return _libs[bits]
+        L.or_threads.restype = i32
+        _libs[key] = L
+    return _libs[key]
+
+
+def threads(mt: bool = True) -> int:
+    """Threads the row loops of the oracle build use (1 for the plain build)."""
+    return lib(32, mt).or_threads()
 
 
 def _dt(bits):
@@ -172,7 +184,7 @@ def softmax_selected(z, idx, bits: int = 32) -> np.ndarray:
     return w
 
 
-def route(x, Wr, bias=None, k: int = K_ACTIVE, bits: int = 32, eps: float = EPS):
+def route(x, Wr, bias=None, k: int = K_ACTIVE, bits: int = 32, eps: float = EPS, mt: bool = False):
     """One token's routing -> (r, z[E], idx[k] best first, w[k])."""
     x, xp = _c(x, np.uint16)
     Wr, wp = _c(Wr, np.uint16)
@@ -185,7 +197,8 @@ def route(x, Wr, bias=None, k: int = K_ACTIVE, bits: int = 32, eps: float = EPS)
     z = np.empty(E, _dt(bits))
     idx = np.empty(k, np.int32)
     w = np.empty(k, _dt(bits))
-    lib(bits).or_route(xp, H, wp, E, bp, k, eps, ctypes.byref(r), z.ctypes.data, idx.ctypes.data, w.ctypes.data)
+    lib(bits, mt).or_route(xp, H, wp, E, bp, k, eps, ctypes.byref(r), z.ctypes.data, idx.ctypes.data,
+                           w.ctypes.data)
     return r.value, z, idx, w
 
 
@@ -225,7 +238,7 @@ def shared_ffn(n, Wg, Wu, Wd, bf16_ops: bool = False, bits: int = 32) -> np.ndar
     return y
 
 
-def layer_combine(x, r, experts: list, w, shared=None, bf16_ops: bool = False, bits: int = 32):
+def layer_combine(x, r, experts: list, w, shared=None, bf16_ops: bool = False, bits: int = 32, mt: bool = False):
     """out = bf16(x + delta), delta = shared + sum_i w_i y_i (experts given in top-k order).
 
     Returns (out bf16 bits [H], delta [H])."""
@@ -247,8 +260,8 @@ def layer_combine(x, r, experts: list, w, shared=None, bf16_ops: bool = False, b
         Wd, dp = _c(Wd, np.uint16)
     out = np.empty(H, np.uint16)
     delta = np.empty(H, _dt(bits))
-    lib(bits).or_layer_combine(xp, H, I, r, k, arr, wp, S, gp, up, dp, int(bf16_ops), out.ctypes.data,
-                               delta.ctypes.data)
+    lib(bits, mt).or_layer_combine(xp, H, I, r, k, arr, wp, S, gp, up, dp, int(bf16_ops), out.ctypes.data,
+                                   delta.ctypes.data)
     return out, delta
 
 

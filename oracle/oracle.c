@@ -34,6 +34,13 @@
  *  - 16-slot LFU expert cache per layer (devtrends page, "Qual e o principal
  *    truque da arquitetura": 16 slots, LFU). Reading: textbook LFU, see or_lfu_step.
  *
+ * Threads. The plain build is single-threaded. The same file is also built with
+ * -fopenmp (liboracle32mt.so), which only spreads the independent output rows
+ * of the router, the dequantisation and the matrix-vector products over the
+ * host's cores; each row is still summed by one thread in the order below, so
+ * that build's results are bit-identical to the single-threaded ones. It
+ * exists to time the oracle on all cores.
+ *
  * Canonical reduction order (used for sum x^2 and for the router dot products,
  * so that the top-8 selection is reproducible bit for bit): 32 partial sums,
  * partial l accumulating the terms k = l, l+32, l+64, ... in increasing k; then
@@ -139,16 +146,17 @@ void or_normalise(const uint16_t* x, int H, REAL r, REAL* n) {
 /* z_e = (r * d_e) + bias_e with d_e = sum_k Wr[e,k] x_k in canonical order. */
 void or_router_logits(const uint16_t* x, int H, const uint16_t* Wr, int E, const float* bias,
                       REAL r, REAL* z) {
-    REAL* t = (REAL*)malloc(sizeof(REAL) * (size_t)H);
+#pragma omp parallel for schedule(static)
     for (int e = 0; e < E; ++e) {
+        REAL* t = (REAL*)malloc(sizeof(REAL) * (size_t)H);
         for (int k = 0; k < H; ++k)
             t[k] = (REAL)or_bf16_to_float(Wr[(size_t)e * H + k]) * (REAL)or_bf16_to_float(x[k]);
         REAL d = canonical_sum(t, H);
         REAL v = r * d;
         if (bias) v = v + (REAL)bias[e];
         z[e] = v;
+        free(t);
     }
-    free(t);
 }
 
 /* a ranks before b: larger value first, equal values -> lower index; NaN below everything. */
@@ -202,6 +210,7 @@ REAL or_dequant(uint8_t q, uint16_t s, uint16_t b) {
 void or_dequant_matrix(const uint8_t* q, const uint16_t* s, const uint16_t* b, int R, int K,
                        int bf16_ops, REAL* W) {
     int G = K / OR_GROUP;
+#pragma omp parallel for schedule(static)
     for (int j = 0; j < R; ++j)
         for (int k = 0; k < K; ++k) {
             size_t gi = (size_t)j * G + (size_t)(k / OR_GROUP);
@@ -224,6 +233,7 @@ REAL or_gelu(REAL v) {
 
 /* y[R] = W[R,K] v[K], sequential in k. */
 static void matvec(const REAL* W, int R, int K, const REAL* v, REAL* y) {
+#pragma omp parallel for schedule(static)
     for (int j = 0; j < R; ++j) {
         REAL acc = (REAL)0;
         for (int k = 0; k < K; ++k) acc = acc + W[(size_t)j * K + k] * v[k];
@@ -422,3 +432,11 @@ void or_lfu_state(const or_lfu* c, int layer, int32_t* expert, int64_t* count, i
 }
 
 int or_real_bytes(void) { return (int)sizeof(REAL); }
+
+/* Threads the row loops may use: 1 in the plain build. */
+#ifdef _OPENMP
+#include <omp.h>
+int or_threads(void) { return omp_get_max_threads(); }
+#else
+int or_threads(void) { return 1; }
+#endif

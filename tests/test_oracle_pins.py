@@ -494,6 +494,25 @@ def test_fp32_oracle_bounded_by_fp64_oracle_full_layer():
     assert np.all(diff <= np.abs(W.bf16_to_f32(out64)) * 2.0 ** -7 + 1e-30)
 
 
+def test_all_cores_build_is_bit_identical():
+    """The OpenMP build only spreads independent rows over threads: its routing and layer output equal the
+    single-threaded oracle's bit for bit (full shapes, with the shared expert)."""
+    S = 2112
+    x = W.hidden(2, 0, 1, H)[0]
+    Wr = W.router_weights(2, 0, E, H)
+    r1, z1, i1, w1 = O.route(x, Wr)
+    r2, z2, i2, w2 = O.route(x, Wr, mt=True)
+    assert np.float32(r1).view(np.uint32) == np.float32(r2).view(np.uint32)
+    assert np.array_equal(z1.view(np.uint32), z2.view(np.uint32)) and np.array_equal(i1, i2)
+    assert np.array_equal(w1.view(np.uint32), w2.view(np.uint32))
+    experts = W.experts_parallel(2, 0, i1, H, I)
+    shared = W.shared_weights(2, 0, H, S)
+    o1, d1 = O.layer_combine(x, r1, experts, w1, shared)
+    o2, d2 = O.layer_combine(x, r1, experts, w1, shared, mt=True)
+    assert np.array_equal(o1, o2) and np.array_equal(d1.view(np.uint32), d2.view(np.uint32))
+    assert O.threads(False) == 1 and O.threads(True) >= 1
+
+
 def test_oracle_precisions():
     assert O.lib(32).or_real_bytes() == 4
     assert O.lib(64).or_real_bytes() == 8
