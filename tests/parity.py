@@ -5,6 +5,12 @@ oracle, read as max_i |a_i - r_i| / max_i |r_i| (per token), must be <= 1e-2.
 It is checked on the bf16 layer output and on the fp32 update delta = out - x
 (before rounding), since after the first layers the residual dominates out.
 
+Outputs are bf16 by the layer's format. Where a bf16 output is compared with
+the plain fp32 oracle across different arithmetic (the bf16 tensor-core path),
+it is compared with the oracle's exact x + delta, allowing the output's own
+rounding to bf16 (out_rel_err); where no fp32 update is exposed, out - x is
+compared with the oracle's delta allowing 1.5 ulp of out (delta_rel_err).
+
 The fp32 decode path is also held to a much tighter elementwise bound,
 max_i |a_i - r_i| / max(|r_i|, 1e-3 * rms(r)), which catches a wrong term that
 the normwise bound would hide.
@@ -49,3 +55,15 @@ def delta_rel_err(out_bits, x_bits, delta_ref) -> float:
     d = np.asarray(delta_ref, np.float64)
     excess = np.maximum(np.abs((o - x) - d) - 1.5 * bf16_ulp(o), 0.0)
     return float(np.max(excess) / max(np.max(np.abs(d)), 1e-30))
+
+
+def out_rel_err(out_bits, x_bits, delta_ref) -> float:
+    """Error of a bf16 layer output against the reference's exact output x + delta (before any rounding to
+    bf16), after allowing the output's own rounding to bf16 (half an ulp of out). Comparing two independently
+    rounded bf16 outputs instead would charge up to two ulps of quantisation (up to 1.6 % relative) to the
+    arithmetic being checked."""
+    o = bf16_to_f64(out_bits)
+    ref = bf16_to_f64(x_bits) + np.asarray(delta_ref, np.float64)
+    excess = np.maximum(np.abs(o - ref) - 0.5 * bf16_ulp(o), 0.0)
+    return float(np.max(excess) / max(np.max(np.abs(ref)), 1e-30))
+
