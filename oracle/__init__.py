@@ -71,6 +71,8 @@ def lib(bits: int = 32, mt: bool = False):
         L.or_bf16_to_float.argtypes = [ctypes.c_uint16]
         L.or_float_to_bf16.restype = ctypes.c_uint16
         L.or_float_to_bf16.argtypes = [ctypes.c_float]
+        L.or_float_to_half.restype = ctypes.c_uint16
+        L.or_float_to_half.argtypes = [ctypes.c_float]
         L.or_rms_scale.restype = R
         L.or_rms_scale.argtypes = [vp, i32, ctypes.c_double]
         L.or_normalise.argtypes = [vp, i32, R, vp]
@@ -82,8 +84,8 @@ def lib(bits: int = 32, mt: bool = False):
         L.or_dequant_matrix.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         L.or_gelu.restype = R
         L.or_gelu.argtypes = [R]
-        L.or_expert_ffn.argtypes = [vp, i32, i32, ctypes.POINTER(Expert), i32, vp]
-        L.or_shared_ffn.argtypes = [vp, i32, i32, vp, vp, vp, i32, vp]
+        L.or_expert_ffn.argtypes = [vp, i32, i32, ctypes.POINTER(Expert), i32, i32, R, vp]
+        L.or_shared_ffn.argtypes = [vp, i32, i32, vp, vp, vp, i32, R, vp]
         L.or_route.argtypes = [vp, i32, vp, i32, vp, i32, ctypes.c_double, ctypes.POINTER(R), vp, vp, vp]
         L.or_layer_combine.argtypes = [vp, i32, i32, R, i32, ctypes.POINTER(Expert), vp, i32, vp, vp, vp,
                                        i32, vp, vp]
@@ -123,6 +125,13 @@ def float_to_bf16(f: float) -> int:
     return lib().or_float_to_bf16(f)
 
 
+def float_to_half(f: float) -> int:
+    return lib().or_float_to_half(f)
+
+
+FMT = {"fp32": 0, "bf16": 1, "fp16": 2}   # operand formats of the FFN readings (rounding before products)
+
+
 def gelu(v: float, bits: int = 32) -> float:
     return lib(bits).or_gelu(v)
 
@@ -131,13 +140,13 @@ def dequant(q: int, s: int, b: int, bits: int = 32) -> float:
     return lib(bits).or_dequant(q, s, b)
 
 
-def dequant_matrix(q, s, b, bf16_ops: bool = False, bits: int = 32) -> np.ndarray:
+def dequant_matrix(q, s, b, fmt: str = "fp32", bits: int = 32) -> np.ndarray:
     R, K = q.shape
     q, qp = _c(q, np.uint8)
     s, sp = _c(s, np.uint16)
     b, bp = _c(b, np.uint16)
     W = np.empty((R, K), _dt(bits))
-    lib(bits).or_dequant_matrix(qp, sp, bp, R, K, int(bf16_ops), W.ctypes.data)
+    lib(bits).or_dequant_matrix(qp, sp, bp, R, K, FMT[fmt], W.ctypes.data)
     return W
 
 
@@ -216,30 +225,34 @@ def _expert_struct(ex: dict, keep: list) -> Expert:
     return st
 
 
-def expert_ffn(n, ex: dict, bf16_ops: bool = False, bits: int = 32) -> np.ndarray:
-    """y = Wd (gelu(Wg n) * (Wu n)) for one logical expert (see workload.expert)."""
+def expert_ffn(n, ex: dict, fmt: str = "fp32", bits: int = 32, in_scale: float = 1.0,
+               fmt_down: str | None = None) -> np.ndarray:
+    """y = Wd (gelu(c Wg n) * (c Wu n)), c = in_scale, for one logical expert (see workload.expert); fmt rounds
+    Wg, Wu and n, fmt_down (default: fmt) rounds Wd and h before their products."""
     n, np_ = _c(n, _dt(bits))
     I, H = ex["gate"][0].shape
     keep: list = []
     st = _expert_struct(ex, keep)
     y = np.empty(H, _dt(bits))
-    lib(bits).or_expert_ffn(np_, H, I, ctypes.byref(st), int(bf16_ops), y.ctypes.data)
+    lib(bits).or_expert_ffn(np_, H, I, ctypes.byref(st), FMT[fmt], FMT[fmt_down or fmt], in_scale, y.ctypes.data)
     return y
 
 
-def shared_ffn(n, Wg, Wu, Wd, bf16_ops: bool = False, bits: int = 32) -> np.ndarray:
+def shared_ffn(n, Wg, Wu, Wd, fmt: str = "fp32", bits: int = 32, in_scale: float = 1.0) -> np.ndarray:
     n, np_ = _c(n, _dt(bits))
     S, H = Wg.shape
     Wg, gp = _c(Wg, np.uint16)
     Wu, up = _c(Wu, np.uint16)
     Wd, dp = _c(Wd, np.uint16)
     y = np.empty(H, _dt(bits))
-    lib(bits).or_shared_ffn(np_, H, S, gp, up, dp, int(bf16_ops), y.ctypes.data)
+    lib(bits).or_shared_ffn(np_, H, S, gp, up, dp, FMT[fmt], in_scale, y.ctypes.data)
     return y
 
 
-def layer_combine(x, r, experts: list, w, shared=None, bf16_ops: bool = False, bits: int = 32, mt: bool = False):
-    """out = bf16(x + delta), delta = shared + sum_i w_i y_i (experts given in top-k order).
+def layer_combine(x, r, experts: list, w, shared=None, tc: bool = False, bits: int = 32, mt: bool = False):
+    """out = bf16(x + delta), delta = shared + sum_i w_i y_i (experts given in top-k order). tc = True is the
+    tensor-core reading (x fed as it is, r applied after the gate/up dot products; fp16 operands for the routed
+    experts' gate/up with x scaled by the power of two of r, bf16 for their down and for the shared expert).
 
     Returns (out bf16 bits [H], delta [H])."""
     x, xp = _c(x, np.uint16)
@@ -260,7 +273,7 @@ def layer_combine(x, r, experts: list, w, shared=None, bf16_ops: bool = False, b
         Wd, dp = _c(Wd, np.uint16)
     out = np.empty(H, np.uint16)
     delta = np.empty(H, _dt(bits))
-    lib(bits, mt).or_layer_combine(xp, H, I, r, k, arr, wp, S, gp, up, dp, int(bf16_ops), out.ctypes.data,
+    lib(bits, mt).or_layer_combine(xp, H, I, r, k, arr, wp, S, gp, up, dp, int(tc), out.ctypes.data,
                                    delta.ctypes.data)
     return out, delta
 

@@ -105,7 +105,49 @@ uint16_t or_float_to_bf16(float f) {
     return (uint16_t)upper;
 }
 
+/* fp32 -> IEEE binary16, round to nearest, ties to even (overflow -> inf, NaN kept). */
+uint16_t or_float_to_half(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    uint32_t sign = (u >> 16) & 0x8000u;
+    if (isnan(f)) return (uint16_t)(sign | 0x7E00u);
+    float a = fabsf(f);
+    if (a == 0.0f) return (uint16_t)sign;
+    if (a >= 65520.0f) return (uint16_t)(sign | 0x7C00u);     /* rounds past the largest finite value */
+    /* a = m * 2^e with the spacing of binary16 at a: 2^(e - 10) for normal values (e >= -14), 2^-24 below */
+    int e;
+    frexpf(a, &e);                                            /* a in [2^(e-1), 2^e) */
+    int q = e - 1 - 10;
+    if (q < -24) q = -24;
+    float steps = ldexpf(a, -q);                              /* exact: a / 2^q */
+    float fl = floorf(steps);
+    float rem = steps - fl;
+    uint32_t n = (uint32_t)fl;
+    if (rem > 0.5f || (rem == 0.5f && (n & 1u))) n += 1u;    /* n * 2^q is the rounded magnitude */
+    /* encode n * 2^q: subnormal when q = -24 and n < 1024 */
+    uint32_t bits;
+    if (q == -24 && n < 1024u) {
+        bits = n;
+    } else {
+        int ex = q + 25;                                       /* biased exponent of n * 2^q with n in [1024, 2048] */
+        if (n == 2048u) { n = 1024u; ex += 1; }
+        if (ex >= 31) return (uint16_t)(sign | 0x7C00u);
+        bits = ((uint32_t)ex << 10) | (n - 1024u);
+    }
+    return (uint16_t)(sign | bits);
+}
+
 static REAL to_bf16_real(REAL v) { return (REAL)or_bf16_to_float(or_float_to_bf16((float)v)); }
+static REAL to_f16_real(REAL v) { return (REAL)or_half_to_float(or_float_to_half((float)v)); }
+
+/* Operand formats of the tensor-core reading: values are rounded from fp32 to this format before
+ * their products (OR_FMT_NONE: kept as they are, the fp32 reading). */
+enum { OR_FMT_NONE = 0, OR_FMT_BF16 = 1, OR_FMT_F16 = 2 };
+static REAL to_fmt(REAL v, int fmt) {
+    if (fmt == OR_FMT_BF16) return to_bf16_real(v);
+    if (fmt == OR_FMT_F16) return to_f16_real(v);
+    return v;
+}
 
 /* ------------------------------------------------------- canonical reduction */
 
@@ -206,16 +248,16 @@ REAL or_dequant(uint8_t q, uint16_t s, uint16_t b) {
     return p + bv;
 }
 
-/* Dense [R, K] matrix from codes q[R][K] and s, b [R][K/64]; bf16_ops rounds each weight to bf16. */
+/* Dense [R, K] matrix from codes q[R][K] and s, b [R][K/64]; fmt rounds each weight (OR_FMT_*). */
 void or_dequant_matrix(const uint8_t* q, const uint16_t* s, const uint16_t* b, int R, int K,
-                       int bf16_ops, REAL* W) {
+                       int fmt, REAL* W) {
     int G = K / OR_GROUP;
 #pragma omp parallel for schedule(static)
     for (int j = 0; j < R; ++j)
         for (int k = 0; k < K; ++k) {
             size_t gi = (size_t)j * G + (size_t)(k / OR_GROUP);
             REAL w = or_dequant(q[(size_t)j * K + k], s[gi], b[gi]);
-            W[(size_t)j * K + k] = bf16_ops ? to_bf16_real(w) : w;
+            W[(size_t)j * K + k] = to_fmt(w, fmt);
         }
 }
 
@@ -248,12 +290,17 @@ typedef struct {
 } or_expert;
 
 /*
- * One routed expert on the normalised input n[H]:
- *   g = Wg n, u = Wu n, h = gelu(g) * u, y = Wd h.
- * bf16_ops = 1 is the dequant-to-bf16 tensor-core reading: n, every weight and
- * h are rounded to bf16 before their products (accumulation stays in REAL).
+ * One routed expert on the input v[H]:
+ *   g = c (Wg v), u = c (Wu v), h = gelu(g) * u, y = Wd h,   c = in_scale.
+ * The fp32 reading (formats OR_FMT_NONE) takes v = n (the normalised input) and
+ * c = 1. A tensor-core reading rounds the operands of each product before it
+ * (accumulation stays in REAL): Wg, Wu and v to fmt_gu, Wd and h to fmt_d (bf16
+ * or fp16); there the layer passes the raw layer input (see or_layer_combine)
+ * and applies the RMS scale to the two dot products after them, as the router
+ * applies it. Equal to the first form in real arithmetic.
  */
-void or_expert_ffn(const REAL* n, int H, int I, const or_expert* ex, int bf16_ops, REAL* y) {
+void or_expert_ffn(const REAL* v, int H, int I, const or_expert* ex, int fmt_gu, int fmt_d, REAL in_scale,
+                   REAL* y) {
     REAL* Wg = (REAL*)malloc(sizeof(REAL) * (size_t)I * H);
     REAL* Wu = (REAL*)malloc(sizeof(REAL) * (size_t)I * H);
     REAL* Wd = (REAL*)malloc(sizeof(REAL) * (size_t)H * I);
@@ -261,23 +308,27 @@ void or_expert_ffn(const REAL* n, int H, int I, const or_expert* ex, int bf16_op
     REAL* g = (REAL*)malloc(sizeof(REAL) * (size_t)I);
     REAL* u = (REAL*)malloc(sizeof(REAL) * (size_t)I);
     REAL* h = (REAL*)malloc(sizeof(REAL) * (size_t)I);
-    or_dequant_matrix(ex->q[0], ex->s[0], ex->b[0], I, H, bf16_ops, Wg);
-    or_dequant_matrix(ex->q[1], ex->s[1], ex->b[1], I, H, bf16_ops, Wu);
-    or_dequant_matrix(ex->q[2], ex->s[2], ex->b[2], H, I, bf16_ops, Wd);
-    for (int k = 0; k < H; ++k) nn[k] = bf16_ops ? to_bf16_real(n[k]) : n[k];
+    or_dequant_matrix(ex->q[0], ex->s[0], ex->b[0], I, H, fmt_gu, Wg);
+    or_dequant_matrix(ex->q[1], ex->s[1], ex->b[1], I, H, fmt_gu, Wu);
+    or_dequant_matrix(ex->q[2], ex->s[2], ex->b[2], H, I, fmt_d, Wd);
+    for (int k = 0; k < H; ++k) nn[k] = to_fmt(v[k], fmt_gu);
     matvec(Wg, I, H, nn, g);
     matvec(Wu, I, H, nn, u);
     for (int j = 0; j < I; ++j) {
+        g[j] = in_scale * g[j];
+        u[j] = in_scale * u[j];
         REAL hj = or_gelu(g[j]) * u[j];
-        h[j] = bf16_ops ? to_bf16_real(hj) : hj;
+        h[j] = to_fmt(hj, fmt_d);
     }
     matvec(Wd, H, I, h, y);
     free(Wg); free(Wu); free(Wd); free(nn); free(g); free(u); free(h);
 }
 
-/* Dense shared expert with bf16 weights: gate [S,H], up [S,H], down [H,S]. */
-void or_shared_ffn(const REAL* n, int H, int S, const uint16_t* Wg16, const uint16_t* Wu16,
-                   const uint16_t* Wd16, int bf16_ops, REAL* y) {
+/* Dense shared expert with bf16 weights: gate [S,H], up [S,H], down [H,S]; the
+ * input v, fmt (for v and h; the weights are bf16 already) and in_scale as for
+ * or_expert_ffn. */
+void or_shared_ffn(const REAL* v, int H, int S, const uint16_t* Wg16, const uint16_t* Wu16,
+                   const uint16_t* Wd16, int fmt, REAL in_scale, REAL* y) {
     REAL* Wg = (REAL*)malloc(sizeof(REAL) * (size_t)S * H);
     REAL* Wu = (REAL*)malloc(sizeof(REAL) * (size_t)S * H);
     REAL* Wd = (REAL*)malloc(sizeof(REAL) * (size_t)H * S);
@@ -290,12 +341,14 @@ void or_shared_ffn(const REAL* n, int H, int S, const uint16_t* Wg16, const uint
         Wu[i] = (REAL)or_bf16_to_float(Wu16[i]);
         Wd[i] = (REAL)or_bf16_to_float(Wd16[i]);
     }
-    for (int k = 0; k < H; ++k) nn[k] = bf16_ops ? to_bf16_real(n[k]) : n[k];
+    for (int k = 0; k < H; ++k) nn[k] = to_fmt(v[k], fmt);
     matvec(Wg, S, H, nn, g);
     matvec(Wu, S, H, nn, u);
     for (int j = 0; j < S; ++j) {
+        g[j] = in_scale * g[j];
+        u[j] = in_scale * u[j];
         REAL hj = or_gelu(g[j]) * u[j];
-        h[j] = bf16_ops ? to_bf16_real(hj) : hj;
+        h[j] = to_fmt(hj, fmt);
     }
     matvec(Wd, H, S, h, y);
     free(Wg); free(Wu); free(Wd); free(nn); free(g); free(u); free(h);
@@ -318,28 +371,52 @@ void or_route(const uint16_t* x, int H, const uint16_t* Wr, int E, const float* 
  * Combine for one token, given its routing (idx only selects which experts
  * the caller passed in ex[0..k)):
  *   delta_j = shared_j + sum_{i in top-k order} w_i * y_ij ;  out_j = bf16(x_j + delta_j).
- * Wsg may be NULL (no shared expert).
+ * Wsg may be NULL (no shared expert). The fp32 reading (tc = 0) feeds the FFNs
+ * n = r x. The tensor-core reading (tc = 1) feeds them the raw input and applies
+ * the scale after the gate and up dot products (see or_expert_ffn): the shared
+ * expert takes bf16 operands (its bf16 weights, x, h) with scale r; the routed
+ * experts take fp16 operands for gate/up (the dequantised weights and x p, where
+ * p = 2^e is the power of two with r = m 2^e, m in [1, 2): an exact scaling that
+ * keeps the fp16 operand near unit size whatever the size of x) with scale
+ * m = r / p, and bf16 operands for down (the dequantised weights and h, whose
+ * range fp16 does not always hold).
  */
 void or_layer_combine(const uint16_t* x, int H, int I, REAL r, int k, const or_expert* ex,
                       const REAL* w, int S, const uint16_t* Wsg, const uint16_t* Wsu,
-                      const uint16_t* Wsd, int bf16_ops, uint16_t* out, REAL* delta) {
+                      const uint16_t* Wsd, int tc, uint16_t* out, REAL* delta) {
     REAL* n = (REAL*)malloc(sizeof(REAL) * (size_t)H);
+    REAL* v = (REAL*)malloc(sizeof(REAL) * (size_t)H);
     REAL* y = (REAL*)malloc(sizeof(REAL) * (size_t)H);
-    or_normalise(x, H, r, n);
+    REAL in_scale = (REAL)1, routed_scale = (REAL)1;
+    if (tc) {
+        int e;
+        frexp((double)r, &e);                               /* r = m 2^(e-1), m in [1, 2) */
+        const REAL p = (REAL)ldexp(1.0, e - 1);
+        for (int j = 0; j < H; ++j) {
+            n[j] = (REAL)or_bf16_to_float(x[j]);
+            v[j] = n[j] * p;                                /* exact: a power of two */
+        }
+        in_scale = r;
+        routed_scale = r / p;                               /* exact: m */
+    } else {
+        or_normalise(x, H, r, n);
+        for (int j = 0; j < H; ++j) v[j] = n[j];
+    }
     for (int j = 0; j < H; ++j) delta[j] = (REAL)0;
     if (Wsg) {
-        or_shared_ffn(n, H, S, Wsg, Wsu, Wsd, bf16_ops, y);
+        or_shared_ffn(n, H, S, Wsg, Wsu, Wsd, tc ? OR_FMT_BF16 : OR_FMT_NONE, in_scale, y);
         for (int j = 0; j < H; ++j) delta[j] = y[j];
     }
     for (int i = 0; i < k; ++i) {
-        or_expert_ffn(n, H, I, &ex[i], bf16_ops, y);
+        or_expert_ffn(v, H, I, &ex[i], tc ? OR_FMT_F16 : OR_FMT_NONE, tc ? OR_FMT_BF16 : OR_FMT_NONE, routed_scale,
+                      y);
         for (int j = 0; j < H; ++j) delta[j] = delta[j] + w[i] * y[j];
     }
     for (int j = 0; j < H; ++j) {
         REAL o = (REAL)or_bf16_to_float(x[j]) + delta[j];
         out[j] = or_float_to_bf16((float)o);
     }
-    free(n); free(y);
+    free(n); free(v); free(y);
 }
 
 /* ------------------------------------------------------------ LFU simulator */

@@ -156,7 +156,10 @@ def test_dequant_matrix_layout_and_bf16_variant():
     R, K = 5, 192
     q, s, b = W.expert_matrix(3, 0, 0, 0, R, K)
     Wm = O.dequant_matrix(q, s, b)
-    Wb = O.dequant_matrix(q, s, b, bf16_ops=True)
+    Wb = O.dequant_matrix(q, s, b, fmt="bf16")
+    Wh = O.dequant_matrix(q, s, b, fmt="fp16")
+    # fp16 weights: numpy's own round-to-nearest-even conversion of the fp32 weight
+    assert np.array_equal(Wh, Wm.astype(np.float16).astype(np.float32))
     sf, bf = W.f16_to_f32(s), W.f16_to_f32(b)
     for j in range(R):
         for k in range(K):
@@ -343,6 +346,23 @@ def _rn_bf16(v) -> np.float64:
     return np.float64(W.bf16_to_f32(np.array([_nearest_bf16_bruteforce(f)], np.uint16))[0])
 
 
+def _rn_f16(v) -> np.float64:
+    """fp32(v) rounded to the nearest fp16 (ties to even), by numpy's conversion."""
+    return np.float64(np.float16(np.float32(v)))
+
+
+def test_float_to_half_round_nearest_even():
+    rng = np.random.default_rng(3)
+    vals = rng.standard_normal(20000).astype(np.float32) * (np.float32(10.0) ** rng.integers(-9, 5, 20000))
+    ties = (np.arange(1, 2048, dtype=np.float32) + np.float32(0.5)) * np.float32(2.0 ** -24)   # subnormal ties
+    ties2 = (np.arange(1024, 2048, dtype=np.float32) + np.float32(0.5)) * np.float32(2.0 ** -3)  # normal ties
+    edge = np.array([0.0, -0.0, 65504.0, 65519.99, 65520.0, -70000.0, 2.0 ** -25, 2.0 ** -24, 6.1e-5],
+                    np.float32)
+    with np.errstate(over="ignore"):
+        for v in np.concatenate([vals.astype(np.float32), ties, ties2, edge]):
+            assert O.float_to_half(float(v)) == int(np.float32(v).astype(np.float16).view(np.uint16)), v
+
+
 def _gelu64(v):
     return 0.5 * v * (1 + math.tanh(math.sqrt(2 / math.pi) * (v + 0.044715 * v ** 3)))
 
@@ -355,17 +375,19 @@ def _spread_input(rng, n):
     return np.where(rng.random(n) < 0.5, -mag, mag).astype(np.float32).astype(np.float64)
 
 
-def _bf16_branch_variants(n, pi, sigma, wg=1.0, wu=1.0):
-    """Closed forms of y = Wd (gelu(Wg n) * (Wu n)) for gate rows e_pi(j) * wg, up rows all wu, down rows
-    e_sigma(j) (exact weights), in the bf16-operand reading and in the readings a slip would produce."""
+def _bf16_branch_variants(n, pi, sigma, wg=1.0, wu=1.0, c=1.0, rnd=_rn_bf16):
+    """Closed forms of y = Wd (gelu(c Wg n) * (c Wu n)) for gate rows e_pi(j) * wg, up rows all wu, down rows
+    e_sigma(j) (exact weights), in a rounded-operand reading (rnd: bf16 or fp16) and in the readings a slip
+    would produce."""
+    _rn_bf16 = rnd
     nb = np.array([_rn_bf16(v) for v in n])
     out = {}
     for name, nn, round_h, round_gu in (("bf16 n and h", nb, True, False), ("fp32 n", n, True, False),
                                         ("no h rounding", nb, False, False), ("g, u rounded", nb, False, True)):
-        U = wu * nn.sum()
+        U = c * (wu * nn.sum())
         h = []
         for j in range(len(pi)):
-            g = wg * nn[pi[j]]
+            g = c * (wg * nn[pi[j]])
             u = U
             if round_gu:
                 g, u = _rn_bf16(g), _rn_bf16(u)
@@ -383,7 +405,7 @@ def _assert_only_reading(y, variants, want="bf16 n and h"):
 
 
 def test_expert_ffn_bf16_operands_closed_form():
-    """The dequant-to-bf16 reading of a routed expert (bf16_ops = 1): n, every dequantised weight and h
+    """The bf16 reading of an expert (fmt = "bf16"): n, every dequantised weight and h
     are rounded to bf16 before their products. Gate = permutation, up = all-ones rows, down = another
     permutation (weights exact in bf16), n not representable in bf16:
         y_j = bf16(gelu(bf16(n_a)) * sum_k bf16(n_k)),   a = pi(sigma(j)).
@@ -401,11 +423,107 @@ def test_expert_ffn_bf16_operands_closed_form():
           "up": (np.zeros((Is, Hs), np.uint8), _const_f16(0.5, (Is, Hs // 64)), one),
           "down": (qd, _const_f16(1.0, (Hs, Is // 64)), _const_f16(0.0, (Hs, Is // 64)))}
     n = _spread_input(rng, Hs)
-    y = O.expert_ffn(n, ex, bf16_ops=True, bits=64)
+    y = O.expert_ffn(n, ex, fmt="bf16", bits=64)
     _assert_only_reading(y, _bf16_branch_variants(n, pi, sigma))
     # the fp32 reading of the same expert keeps every operand as it is
-    assert np.allclose(O.expert_ffn(n, ex, bf16_ops=False, bits=64),
+    assert np.allclose(O.expert_ffn(n, ex, fmt="fp32", bits=64),
                        [_gelu64(n[pi[sigma[j]]]) * n.sum() for j in range(Hs)], rtol=1e-12, atol=0)
+
+
+def test_expert_ffn_bf16_scale_after_the_dot_products():
+    """The bf16 reading of a layer feeds the raw bf16 input x and applies the RMS scale c = r to g and u after
+    their dot products (before GELU): y_j = bf16(gelu(c bf16(v_a)) * c sum_k bf16(v_k)). A scale left out, or
+    applied to h instead of g and u, fails."""
+    Hs, Is = 256, 128
+    rng = np.random.default_rng(21)
+    pi = rng.permutation(Hs)[:Is]
+    sigma = rng.integers(0, Is, Hs)
+    qg = np.zeros((Is, Hs), np.uint8)
+    qg[np.arange(Is), pi] = 1
+    qd = (np.arange(Is)[None, :] == sigma[:, None]).astype(np.uint8)
+    one, zero = _const_f16(1.0, (Is, Hs // 64)), _const_f16(0.0, (Is, Hs // 64))
+    ex = {"gate": (qg, one, zero),
+          "up": (np.zeros((Is, Hs), np.uint8), _const_f16(0.5, (Is, Hs // 64)), one),
+          "down": (qd, _const_f16(1.0, (Hs, Is // 64)), _const_f16(0.0, (Hs, Is // 64)))}
+    v = _spread_input(rng, Hs)
+    c = 0.7317
+    y = O.expert_ffn(v, ex, fmt="bf16", bits=64, in_scale=c)
+    want = _bf16_branch_variants(v, pi, sigma, c=c)["bf16 n and h"]
+    assert np.array_equal(y, want)
+    assert not np.allclose(y, _bf16_branch_variants(v, pi, sigma)["bf16 n and h"], rtol=1e-6, atol=0)
+    h_scaled = np.array([_rn_bf16(c * c * _gelu64(_rn_bf16(v[pi[sigma[j]]])) * np.sum([_rn_bf16(t) for t in v]))
+                         for j in range(Hs)])
+    assert not np.allclose(y, h_scaled, rtol=1e-6, atol=0)
+
+
+def test_expert_ffn_fp16_operands_closed_form():
+    """The fp16 reading of a routed expert (the tensor-core reading of the routed GEMMs): v, every dequantised
+    weight and h rounded to fp16, the scale c after the dot products:
+        y_j = fp16(gelu(c fp16(v_a)) * c sum_k fp16(v_k)).
+    The bf16 rounding, or none, fails."""
+    Hs, Is = 256, 128
+    rng = np.random.default_rng(22)
+    pi = rng.permutation(Hs)[:Is]
+    sigma = rng.integers(0, Is, Hs)
+    qg = np.zeros((Is, Hs), np.uint8)
+    qg[np.arange(Is), pi] = 3
+    qd = (np.arange(Is)[None, :] == sigma[:, None]).astype(np.uint8)
+    s16 = np.float16(0.0131)
+    w_g = np.float64(np.float32(s16)) * 3
+    ex = {"gate": (qg, _const_f16(float(s16), (Is, Hs // 64)), _const_f16(0.0, (Is, Hs // 64))),
+          "up": (np.zeros((Is, Hs), np.uint8), _const_f16(0.5, (Is, Hs // 64)), _const_f16(1.0, (Is, Hs // 64))),
+          "down": (qd, _const_f16(1.0, (Hs, Is // 64)), _const_f16(0.0, (Hs, Is // 64)))}
+    v = _spread_input(rng, Hs) * 37.0          # values fp16 does not hold exactly either
+    c = 0.0613
+    y = O.expert_ffn(v, ex, fmt="fp16", bits=64, in_scale=c)
+    want = _bf16_branch_variants(v, pi, sigma, wg=_rn_f16(w_g), c=c, rnd=_rn_f16)
+    assert np.array_equal(y, want["bf16 n and h"])
+    for name in ("fp32 n", "no h rounding", "g, u rounded"):
+        assert not np.allclose(y, want[name], rtol=1e-7, atol=0), name
+    assert not np.allclose(y, _bf16_branch_variants(v, pi, sigma, wg=_rn_bf16(w_g), c=c)["bf16 n and h"],
+                           rtol=1e-6, atol=0)
+
+
+def test_layer_combine_tensor_core_reading_feeds_x_and_r():
+    """layer_combine's tensor-core reading is the shared FFN (bf16 operands, input x, scale r after the gate/up
+    dot products) and the routed FFNs (fp16 operands, input x p, scale r / p, p the power of two of r); its fp32
+    reading feeds n = r x with scale 1."""
+    Hs, Is, Ss, k = 192, 64, 128, 3
+    x = W.hidden(6, 0, 1, Hs)[0]
+    r = O.rms_scale(x, 64)
+    xf = W.bf16_to_f32(x).astype(np.float64)
+    experts = [W.expert(30 + i, 0, 0, Hs, Is) for i in range(k)]
+    Wg, Wu, Wd = W.shared_weights(6, 0, Hs, Ss)
+    w = np.array([0.5, 0.3, 0.2])
+    _, delta = O.layer_combine(x, r, experts, w, (Wg, Wu, Wd), tc=True, bits=64)
+    p = 2.0 ** math.floor(math.log2(r))
+    assert 1.0 <= r / p < 2.0
+    want = O.shared_ffn(xf, Wg, Wu, Wd, fmt="bf16", bits=64, in_scale=r)
+    for i in range(k):
+        want = want + w[i] * O.expert_ffn(xf * p, experts[i], fmt="fp16", fmt_down="bf16", bits=64, in_scale=r / p)
+    assert np.array_equal(delta, want)
+    alt = O.shared_ffn(xf, Wg, Wu, Wd, fmt="bf16", bits=64, in_scale=r)
+    for i in range(k):   # fp16 for the down products too: a different reading, which the pin tells apart
+        alt = alt + w[i] * O.expert_ffn(xf * p, experts[i], fmt="fp16", bits=64, in_scale=r / p)
+    assert not np.array_equal(delta, alt)
+    # the same layer with x scaled by 2^20: the fp16 operand x p is the same, the update scales with x
+    xb = (W.bf16_to_f32(x) * np.float32(2.0 ** 20)).view(np.uint32) >> 16
+    xb = xb.astype(np.uint16)
+    r2 = O.rms_scale(xb, 64)
+    _, d2 = O.layer_combine(xb, r2, experts, w, None, tc=True, bits=64)
+    _, d1 = O.layer_combine(x, r, experts, w, None, tc=True, bits=64)
+    assert np.all(np.isfinite(d2)) and np.allclose(d2, d1, rtol=1e-6, atol=0)
+    n = O.normalise(x, r, 64)
+    for fs, fe, xin, c in (("bf16", "fp16", n, 1.0), ("bf16", "bf16", xf, r), ("fp16", "fp16", xf, r)):
+        wrong = O.shared_ffn(xin, Wg, Wu, Wd, fmt=fs, bits=64, in_scale=c)
+        for i in range(k):
+            wrong = wrong + w[i] * O.expert_ffn(xin, experts[i], fmt=fe, bits=64, in_scale=c)
+        assert not np.array_equal(delta, wrong), (fs, fe)
+    _, delta32 = O.layer_combine(x, r, experts, w, (Wg, Wu, Wd), tc=False, bits=64)
+    want32 = O.shared_ffn(n, Wg, Wu, Wd, bits=64)
+    for i in range(k):
+        want32 = want32 + w[i] * O.expert_ffn(n, experts[i], bits=64)
+    assert np.array_equal(delta32, want32)
 
 
 def test_expert_ffn_bf16_rounds_the_dequantised_weights():
@@ -426,13 +544,13 @@ def test_expert_ffn_bf16_rounds_the_dequantised_weights():
           "up": (np.zeros((Is, Hs), np.uint8), _const_f16(0.5, (Is, Hs // 64)), _const_f16(1.0, (Is, Hs // 64))),
           "down": (qd, _const_f16(1.0, (Hs, Is // 64)), _const_f16(0.0, (Hs, Is // 64)))}
     n = _spread_input(rng, Hs)
-    y = O.expert_ffn(n, ex, bf16_ops=True, bits=64)
+    y = O.expert_ffn(n, ex, fmt="bf16", bits=64)
     assert np.array_equal(y, _bf16_branch_variants(n, pi, sigma, wg=w_bf16)["bf16 n and h"])
     assert not np.allclose(y, _bf16_branch_variants(n, pi, sigma, wg=w_exact)["bf16 n and h"], rtol=1e-6, atol=0)
 
 
 def test_shared_ffn_bf16_operands_closed_form():
-    """The bf16-operand reading of the shared expert (weights already bf16): n and h rounded to bf16.
+    """The bf16 reading of the shared expert (weights already bf16): n and h rounded to bf16.
     Gate = permutation, up = all-twos rows, down = permutation:
         y_j = bf16(gelu(bf16(n_a)) * 2 sum_k bf16(n_k))."""
     Hs, Ss = 192, 96
@@ -447,7 +565,7 @@ def test_shared_ffn_bf16_operands_closed_form():
     Wd = np.zeros((Hs, Ss), np.uint16)
     Wd[np.arange(Hs), sigma] = one
     n = _spread_input(rng, Hs)
-    y = O.shared_ffn(n, Wg, Wu, Wd, bf16_ops=True, bits=64)
+    y = O.shared_ffn(n, Wg, Wu, Wd, fmt="bf16", bits=64)
     _assert_only_reading(y, _bf16_branch_variants(n, pi, sigma, wu=2.0))
 
 
