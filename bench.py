@@ -12,7 +12,8 @@ the stack output fed back as the next input. One step = one token through all
 
 --workload prefill times the 4096-token grouped layer (tcgen05 GEMMs);
 --workload streaming runs the decode stack with the experts in pinned host
-memory behind the 16-slot-per-layer LFU cache and reports the hit rate, the
+memory behind the 16-slot-per-layer LFU cache (metadata on the device; the
+host-metadata mode on 1-4 copy streams beside it) and reports the hit rate, the
 bytes fetched per token, the copy stall and the host-link bandwidth;
 --workload batched runs the stack with 64 tokens per step through the grouped
 tcgen05 path (routed and shared experts).
@@ -353,12 +354,13 @@ def run_ours(args, rank, world):
 STREAM_SEED, STREAM_ZIPF, STREAM_SLOTS = 2, 1.1, 16
 STREAM_ALPHA = 0.1     # Zipf bias scale
 STREAM_NOISE = 1.5     # sigma of the per-(step, layer) router-logit noise (the token-dependent part of the logits)
-SWEEP_WARMUP, SWEEP_STEPS = 16, 96   # per point of the slot-count sweep
 STREAM_METRIC = "MoE decode tok/s with experts streamed from pinned host memory through a 16-slot LFU cache (1 B300)"
 STREAM_WORKLOAD = ("30-layer MoE-only decode stack, batch 1, a fresh x ~ N(0,1) per step (the next token's input); "
                    "experts (12.9 GB, 3,840 x 3.36 MB) in "
-                   "pinned host memory, a 16-slot-per-layer LFU cache in HBM (1.61 GB), misses copied by "
-                   "cudaMemcpyAsync on a copy stream overlapped with the shared expert; router logit bias = Zipf(1.1) "
+                   "pinned host memory, a 16-slot-per-layer LFU cache in HBM (1.61 GB) with its metadata on the "
+                   "device, misses copied by a kernel reading the mapped host store on a high-priority stream, "
+                   "overlapped with the shared expert (the host-metadata mode, cudaMemcpyAsync on 1-4 copy "
+                   "streams, reported beside it); router logit bias = Zipf(1.1) "
                    "popularity (alpha %.2f) over a seeded per-layer rank->expert map + N(0, %.2f) noise per (step, layer) "
                    "(the synthetic weights route every token alike beyond layer 0) + 30 on the previous step's 8 ids "
                    "with probability 0.5 per (step, layer); seed 2")
@@ -385,6 +387,10 @@ def h2d_probe(dev, copy_stream, n_slots=32, reps=5):
 
 
 def run_streaming(args):
+    """The decode stack with every expert in pinned host memory behind a 16-slot-per-layer LFU cache in HBM, in two
+    modes on the same host store: the LFU metadata on the device (no host wait inside a token; the misses copied by
+    a kernel reading the mapped host store) and on the host (one host wait per layer; the misses copied by the
+    copy engine, cudaMemcpyAsync, on 1..4 copy streams). The line's value is the device-metadata mode."""
     import torch
     import bit_expert_streaming_layer_b300 as B
     import workload as W
@@ -399,72 +405,111 @@ def run_streaming(args):
     bias_hn = bias_h.numpy()
     bias_d = torch.empty(L, E, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    copy_stream = torch.cuda.Stream(dev)
-    probe = h2d_probe(dev, copy_stream)
-    # one fresh input per step: a fed-back output settles on a fixed point whose routing never changes
+    copy_streams = [torch.cuda.Stream(dev) for _ in range(4)]
+    fetch = torch.cuda.Stream(dev, priority=-1)
+    probe = h2d_probe(dev, copy_streams[0])
     sweep = [int(v) for v in args.slot_sweep.split(",") if v.strip()] if args.slot_sweep else []
-    n_inputs = args.warmup + args.steps + min(args.steps, 32) + min(args.steps, 64) + \
-        len(sweep) * (SWEEP_WARMUP + SWEEP_STEPS)
+    n_copy_points = 4
+    n_inputs = args.warmup + args.steps + min(args.steps, 32) + min(args.steps, 64)
     xs = torch.stack([hidden_tensor(seed, t, 1, H, device=dev)[0] for t in range(n_inputs)])
     noise = np.stack([np.stack([W.route_noise(seed, l, t, E, sigma) for l in range(L)]) for t in range(n_inputs)])
     bufs = [torch.empty(H, dtype=torch.bfloat16, device=dev) for _ in range(5)]   # 0-1 outputs, 2-3 scratch, 4 input
-    prev = [None] * L
-    tot = {"hits": 0, "misses": 0, "bytes": 0, "stall_ms": 0.0, "copy_ms": 0.0, "shared_ms": 0.0, "tokens": 0}
+    idx_views = [stack.layers[l].routing_tensors()[0][0] for l in range(L)]
 
-    def token(step, src, dst, measure=0, cache=None):
-        cache = cache if cache is not None else stack.cache
-        x = src
-        for l in range(L):
-            bias_hn[l] = zipf_h[l] + noise[step, l]
-            if prev[l] is not None and W.coin(seed, l, step):
-                bias_hn[l, prev[l]] += 30.0
-            bias_d[l].copy_(bias_h[l], non_blocking=True)
-            bias = bias_d[l]
-            y = dst if l == L - 1 else bufs[2 + l % 2]
-            st = B.tf_layer_step(stack.layers[l], cache, l, step, stack.store, x, y, 1, bias, 0, stream,
-                                 copy_stream, measure)
-            prev[l] = np.array(st.ids[:K_ACT], dtype=np.int64)
-            tot["hits"] += st.hits
-            tot["misses"] += st.misses
-            tot["bytes"] += st.bytes_fetched
-            tot["stall_ms"] += st.stall_ms
-            tot["copy_ms"] += st.copy_ms
-            tot["shared_ms"] += st.shared_ms
-            x = y
-        tot["tokens"] += 1
+    def new_device_cache(n_slots):
+        pool = torch.zeros(L * n_slots * stack.slot, dtype=torch.uint8, device=dev)
+        state = torch.zeros(B.tf_device_cache_state_bytes(L, n_slots, E, 0), dtype=torch.uint8, device=dev)
+        c = B.DeviceCache(L, n_slots, E, stack.slot, pool, stack.store, state, 0)
+        c.set_fetch_ctas(args.fetch_ctas)
+        return c
+
+    class Run:
+        """One cache (host or device metadata) fed a sequence of tokens; counts what its steps did."""
+
+        def __init__(self, mode, cache):
+            self.mode, self.cache, self.prev = mode, cache, [None] * L
+            self.zero()
+
+        def zero(self):
+            self.t = {"hits": 0, "misses": 0, "bytes": 0, "stall_ms": 0.0, "copy_ms": 0.0, "shared_ms": 0.0,
+                      "tokens": 0}
+
+        def token(self, step, src, dst, measure=0):
+            for l in range(L):
+                bias_hn[l] = zipf_h[l] + noise[step, l]
+                if self.prev[l] is not None and W.coin(seed, l, step):
+                    bias_hn[l, self.prev[l]] += 30.0
+            bias_d.copy_(bias_h, non_blocking=True)
+            x = src
+            for l in range(L):
+                y = dst if l == L - 1 else bufs[2 + l % 2]
+                if self.mode == "device":
+                    st = B.tf_layer_step_device_cache(stack.layers[l], self.cache, l, x, y, bias_d[l], 0, stream,
+                                                      fetch, measure)
+                else:
+                    st = B.tf_layer_step(stack.layers[l], self.cache, l, step, stack.store, x, y, 1, bias_d[l], 0,
+                                         stream, copy_streams[0], measure)
+                    self.prev[l] = np.array(st.ids[:K_ACT], dtype=np.int64)
+                if self.mode == "host" or measure:
+                    for k_, f in (("hits", "hits"), ("misses", "misses"), ("bytes", "bytes_fetched"),
+                                  ("stall_ms", "stall_ms"), ("copy_ms", "copy_ms"), ("shared_ms", "shared_ms")):
+                        self.t[k_] += getattr(st, f)
+                x = y
+            if self.mode == "device":
+                # the next token's router bias repeats this token's experts: one read of the 30 layers' ids
+                ids = torch.stack(idx_views).cpu().numpy()
+                for l in range(L):
+                    self.prev[l] = ids[l].astype(np.int64)
+            self.t["tokens"] += 1
 
     step = 0
-    for _ in range(args.warmup):
-        token(step, xs[step], bufs[0])
-        step += 1
-    torch.cuda.synchronize()
-    for k in tot:
-        tot[k] = 0
+
+    def timed(run, n_steps, warmup):
+        """Every run replays the same tokens from a cold cache (steps 0 ..), so that all modes and sweep points
+        see the same routing, hits and misses; only the mechanism differs."""
+        nonlocal step
+        step = 0
+        for _ in range(warmup):
+            run.token(step, xs[step], bufs[0])
+            step += 1
+        torch.cuda.synchronize()
+        if run.mode == "device":
+            c0 = run.cache.counters()
+        run.zero()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_steps):
+            run.token(step, xs[step], bufs[step % 2])
+            step += 1
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t = dict(run.t)
+        if run.mode == "device":
+            c1 = run.cache.counters()
+            t["hits"], t["misses"] = c1[0] - c0[0], c1[1] - c0[1]
+            t["bytes"] = t["misses"] * stack.payload
+        return e0.elapsed_time(e1), t
+
+    def measured(run, n_steps):
+        nonlocal step
+        run.zero()
+        for _ in range(n_steps):
+            run.token(step, xs[step], bufs[0], measure=1)
+            step += 1
+        return dict(run.t)
+
+    # ---- device-metadata mode (the line's value)
+    dcache = new_device_cache(STREAM_SLOTS)
+    drun = Run("device", dcache)
     sampler = ClockSampler(0)
     sampler.start()
-    B.tf_profile_begin(min(args.steps, 8) * 4 * L)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        token(step, xs[step], bufs[step % 2])
-        step += 1
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    B.tf_profile_begin(min(args.steps, 8) * 6 * L)
+    ms, timed_d = timed(drun, args.steps, args.warmup)
     prof = B.tf_profile_end()
     clocks = sampler.stop()
-    ms = ev0.elapsed_time(ev1)
-    timed = dict(tot)
     assert not torch.isnan(bufs[(step - 1) % 2].float()).any(), "NaN in the stack output"
-
-    # stall and copy times: the call synchronises each layer to read its events, so these steps are not timed
     meas_steps = min(args.steps, 32)
-    for k in tot:
-        tot[k] = 0
-    for _ in range(meas_steps):
-        token(step, xs[step], bufs[0], measure=1)
-        step += 1
-    meas = dict(tot)
-
+    meas_d = measured(drun, meas_steps)
     # end to end: the input from pinned host memory and the output back, every step
     hy = torch.empty(H, dtype=torch.bfloat16, pin_memory=True)
     hxs = xs.cpu().pin_memory()
@@ -473,47 +518,58 @@ def run_streaming(args):
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         bufs[4].copy_(hxs[step], non_blocking=True)
-        token(step, bufs[4], bufs[0])
+        drun.token(step, bufs[4], bufs[0])
         hy.copy_(bufs[0], non_blocking=True)
         stream.synchronize()
         step += 1
     e2e_s = time.perf_counter() - t0
+    dcache.close()
 
-    # slot-count sweep: the same workload through caches of other sizes (one device pool sized for the largest,
-    # a fresh LFU cache per point, cold start then SWEEP_WARMUP steps before SWEEP_STEPS timed ones)
+    # ---- host-metadata mode: the copy engine on 1, 2, 3 and 4 copy streams (fresh cache per point, same tokens)
+    host_points = []
+    for n_cs in range(1, n_copy_points + 1):
+        hcache = B.ExpertCache(L, STREAM_SLOTS, E, stack.slot, stack.pool)
+        if n_cs > 1:
+            hcache.set_copy_streams(copy_streams[:n_cs])
+        hrun = Run("host", hcache)
+        n_steps = args.steps
+        hms, th = timed(hrun, n_steps, args.warmup)
+        pt = {"copy_streams": n_cs, "steps": n_steps, "tok_s": round(n_steps / (hms / 1000.0), 2),
+              "hit_rate": round(th["hits"] / max(1, th["hits"] + th["misses"]), 4),
+              "bytes_fetched_per_token": int(th["bytes"] / n_steps),
+              "fill_gbs": round(th["bytes"] / (hms / 1000.0) / 1e9, 2)}
+        if n_cs == 1:
+            mh = measured(hrun, meas_steps)
+            pt["stall_us_per_token"] = round(mh["stall_ms"] * 1000.0 / max(1, mh["tokens"]), 1)
+            pt["copy_gbs_during_fills"] = round(mh["bytes"] / max(1e-9, mh["copy_ms"] / 1000.0) / 1e9, 2)
+        host_points.append(pt)
+        hcache.close()
+
+    # ---- slot-count sweep (device-metadata mode), one pool per point, the same tokens from a cold start
     sweep_out = []
-    if sweep:
-        pool = torch.zeros(L * max(sweep) * stack.slot, dtype=torch.uint8, device=dev)
-        for n_slots in sweep:
-            cache = B.ExpertCache(L, n_slots, E, stack.slot, pool)
-            for l in range(L):
-                prev[l] = None
-            for _ in range(SWEEP_WARMUP):
-                token(step, xs[step], bufs[0], cache=cache)
-                step += 1
-            torch.cuda.synchronize()
-            for k in tot:
-                tot[k] = 0
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(SWEEP_STEPS):
-                token(step, xs[step], bufs[step % 2], cache=cache)
-                step += 1
-            e1.record(stream)
-            torch.cuda.synchronize()
-            sms = e0.elapsed_time(e1)
-            sweep_out.append({"slots_per_layer": n_slots, "steps": SWEEP_STEPS,
-                              "tok_s": round(SWEEP_STEPS / (sms / 1000.0), 2),
-                              "hit_rate": round(tot["hits"] / max(1, tot["hits"] + tot["misses"]), 4),
-                              "bytes_fetched_per_token": int(tot["bytes"] / SWEEP_STEPS),
-                              "slot_pool_gb": round(L * n_slots * stack.slot / 1e9, 2)})
-            cache.close()
-        del pool
+    for n_slots in sweep:
+        c = new_device_cache(n_slots)
+        sms, ts = timed(Run("device", c), args.steps, args.warmup)
+        sweep_out.append({"slots_per_layer": n_slots, "steps": args.steps,
+                          "tok_s": round(args.steps / (sms / 1000.0), 2),
+                          "hit_rate": round(ts["hits"] / max(1, ts["hits"] + ts["misses"]), 4),
+                          "bytes_fetched_per_token": int(ts["bytes"] / args.steps),
+                          "slot_pool_gb": round(L * n_slots * stack.slot / 1e9, 2)})
+        c.close()
+    # fetch-kernel width (device-metadata mode, 16 slots)
+    fetch_sweep = []
+    for ctas in [int(v) for v in args.fetch_sweep.split(",") if v.strip()]:
+        c = new_device_cache(STREAM_SLOTS)
+        c.set_fetch_ctas(ctas)
+        fms, tf_ = timed(Run("device", c), args.steps, args.warmup)
+        fetch_sweep.append({"fetch_ctas": ctas, "tok_s": round(args.steps / (fms / 1000.0), 2),
+                            "fill_gbs": round(tf_["bytes"] / (fms / 1000.0) / 1e9, 2)})
+        c.close()
     stack.close()
 
     n = args.steps
-    lookups = timed["hits"] + timed["misses"]
-    fetch_gbs = timed["bytes"] / (ms / 1000.0) / 1e9
+    lookups = timed_d["hits"] + timed_d["misses"]
+    fetch_gbs = timed_d["bytes"] / (ms / 1000.0) / 1e9
     launches = sum(v[1] for v in prof.values())
     line = {
         "metric": STREAM_METRIC, "value": round(n / (ms / 1000.0), 2), "unit": "tok/s", "n_gpus": 1, "steps": n,
@@ -521,26 +577,29 @@ def run_streaming(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": STREAM_WORKLOAD % (alpha, sigma), "layers": L, "slots_per_layer": STREAM_SLOTS,
                    "zipf_s": STREAM_ZIPF, "zipf_alpha": alpha, "logit_noise_sigma": sigma, "repeat_p": 0.5,
-                   "repeat_bonus": 30.0,
+                   "repeat_bonus": 30.0, "cache_metadata": "device", "fetch_ctas": args.fetch_ctas,
                    "l2": "no flush: every step streams 1.1 GB of resident shared/router weights plus the cached "
                          "experts, far above the 126 MB L2"},
-        "hit_rate": round(timed["hits"] / max(1, lookups), 4),
-        "bytes_fetched_per_token": int(timed["bytes"] / n),
+        "hit_rate": round(timed_d["hits"] / max(1, lookups), 4),
+        "bytes_fetched_per_token": int(timed_d["bytes"] / n),
         "roofline": {"bound": "host_link", "achieved": round(fetch_gbs, 2), "peak": round(probe, 2), "unit": "GB/s",
                      "frac": round(fetch_gbs / probe, 4),
                      "peak_source": "pinned host->device copy probe in the same run (32 x 3.36 MB)", "traffic": None},
-        "stall_us_per_token": round(meas["stall_ms"] * 1000.0 / max(1, meas["tokens"]), 1),
-        "copy_gbs_during_fills": round(meas["bytes"] / max(1e-9, meas["copy_ms"] / 1000.0) / 1e9, 2),
-        "shared_branch_us_per_token": round(meas["shared_ms"] * 1000.0 / max(1, meas["tokens"]), 1),
+        "stall_us_per_token": round(meas_d["stall_ms"] * 1000.0 / max(1, meas_d["tokens"]), 1),
+        "copy_gbs_during_fills": round(meas_d["bytes"] / max(1e-9, meas_d["copy_ms"] / 1000.0) / 1e9, 2),
+        "shared_branch_us_per_token": round(meas_d["shared_ms"] * 1000.0 / max(1, meas_d["tokens"]), 1),
         "measured_steps_for_stall": meas_steps,
+        "host_metadata": host_points,
         "kernels": {k: {"event_ms_total": round(v[0], 4), "launches": int(v[1])} for k, v in prof.items() if v[1]},
-        "gpu_launches": int(launches),
+        "gpu_launches": int(n * L * 6),    # router, shared gate/up and down, LFU, fetch, routed gate/up, routed down
         "clocks": clocks,
         "e2e": {"value": round(e2e_steps / e2e_s, 2), "unit": "tok/s", "h2d_bytes_per_step": H * 2,
                 "d2h_bytes_per_step": H * 2},
     }
     if sweep_out:
         line["slot_sweep"] = sweep_out
+    if fetch_sweep:
+        line["fetch_sweep"] = fetch_sweep
     line["host"] = host_info()
     if not args.no_cpu_baseline:
         base = oracle_baseline(args.oracle_layers)
@@ -554,7 +613,8 @@ BATCH_T, BATCH_SEED = 64, 3
 BATCH_METRIC = "batched MoE decode tok/s, 64 tokens per step (1 B300)"
 BATCH_WORKLOAD = ("30-layer MoE-only stack, 64 tokens per step (x ~ N(0,1) [64, 2816] at step 0, the outputs fed back), "
                   "uniform routing (no bias), H=2816, 128 experts of I=704 (int4 g64, fp16 scale+bias), top-8; routed "
-                  "experts by grouped dequant-to-bf16 tcgen05 GEMMs, the bf16 shared expert 2816->2112->2816 by the "
+                  "experts by grouped dequant-to-16-bit tcgen05 GEMMs (fp16 gate/up, bf16 down), the bf16 shared "
+                  "expert 2816->2112->2816 by the "
                   "same GEMM kernel; all experts resident in HBM; seed 3")
 PAYLOAD = 3 * (I * H // 2 + I * (H // 64) * 4)       # 3,345,408 B per expert
 # kernels behind one profiling bracket of a batched layer step: rms, histogram, positions, inverse init, two
@@ -563,7 +623,7 @@ BATCH_KERNELS_PER_BRACKET = {"router": 1, "permute": 7, "gemm": 6, "combine": 1}
 
 
 def batched_cpu_baseline(seed, x_bits, n_tokens=2):
-    """The oracle (bf16-operand reading, with the shared expert) on n_tokens tokens of layer 0: routing, 8 experts
+    """The oracle (tensor-core reading, with the shared expert) on n_tokens tokens of layer 0: routing, 8 experts
     and the shared expert; tok/s over 30 layers."""
     import oracle as O
     import workload as W
@@ -576,11 +636,11 @@ def batched_cpu_baseline(seed, x_bits, n_tokens=2):
         experts = W.experts_parallel(seed, 0, idx, H, I)   # generation is not timed
         t0 = time.perf_counter()
         r, _, idx, w = O.route(x_bits[t], Wr, None, K_ACT)
-        O.layer_combine(x_bits[t], r, experts, w, shared, bf16_ops=True)
+        O.layer_combine(x_bits[t], r, experts, w, shared, tc=True)
         elapsed += time.perf_counter() - t0
     return {"value": n_tokens / (elapsed * L), "unit": "tok/s", "cores": 1, "kind": "oracle",
             "sample": "%d tokens of layer 0 at step 0 (router, 8 experts and the shared expert each), single-threaded "
-                      "fp32 C oracle in its bf16-operand reading; tok/s = tokens / (30 x their layer time)" % n_tokens}
+                      "fp32 C oracle in its tensor-core reading; tok/s = tokens / (30 x their layer time)" % n_tokens}
 
 
 def run_batched(args):
@@ -726,7 +786,8 @@ def run_batched(args):
 PREFILL_T = 4096
 PREFILL_FLOP = 2 * PREFILL_T * K_ACT * (2 * I * H + H * I)   # 389.8 GFLOP: gate/up + down GEMMs
 PREFILL_WORKLOAD = ("prefill-shaped MoE layer: 4096 tokens x H=2816, 128 experts of I=704 (int4 g64, fp16 scale+bias), "
-                    "top-8 of router logits + Zipf(1.2) popularity bias, grouped dequant-to-bf16 tcgen05 GEMMs with "
+                    "top-8 of router logits + Zipf(1.2) popularity bias, grouped dequant-to-16-bit tcgen05 GEMMs "
+                    "(fp16 gate/up, bf16 down) with "
                     "fp32 accumulation, weighted combine; seed 4")
 
 
@@ -739,7 +800,7 @@ def tensor_peak():
 
 
 def prefill_cpu_baseline(seed, x_bits, idx, w, n_tokens=2):
-    """The oracle (bf16-operand reading) on n_tokens tokens of the layer; tok/s."""
+    """The oracle (tensor-core reading) on n_tokens tokens of the layer; tok/s."""
     import oracle as O
     import workload as W
     O.build()
@@ -748,11 +809,11 @@ def prefill_cpu_baseline(seed, x_bits, idx, w, n_tokens=2):
         experts = W.experts_parallel(seed, 0, idx[t], H, I)   # generation is not timed
         t0 = time.perf_counter()
         r = O.rms_scale(x_bits[t])
-        O.layer_combine(x_bits[t], r, experts, w[t], None, bf16_ops=True)
+        O.layer_combine(x_bits[t], r, experts, w[t], None, tc=True)
         elapsed += time.perf_counter() - t0
     return {"value": n_tokens / elapsed, "unit": "tok/s", "cores": 1, "kind": "oracle",
             "sample": "%d of the 4096 tokens (all 8 experts each), single-threaded fp32 C oracle in its "
-                      "bf16-operand reading; expert generation not timed" % n_tokens}
+                      "tensor-core reading; expert generation not timed" % n_tokens}
 
 
 def run_prefill(args):
@@ -891,6 +952,10 @@ def main():
                     help="batched: time plain launches instead of replaying the step as a CUDA graph")
     ap.add_argument("--slot-sweep", default="",
                     help="streaming: also measure these slot counts per layer, e.g. 8,32,64")
+    ap.add_argument("--fetch-ctas", type=int, default=32,
+                    help="streaming: CTAs of the kernel that copies missing experts from the host store")
+    ap.add_argument("--fetch-sweep", default="",
+                    help="streaming: also measure these fetch-kernel widths, e.g. 8,16,64")
     ap.add_argument("--noise", type=float, default=STREAM_NOISE,
                     help="streaming: sigma of the per-(step, layer) router-logit noise")
     ap.add_argument("--layers", type=int, default=L,

@@ -81,6 +81,16 @@ SIGNATURES = {
     "tf_expert_cache_trace": (_S, [_vp, _vp, _sz, ctypes.POINTER(_sz)]),
     "tf_expert_cache_state": (_S, [_vp, _i32, _vp, _vp, _vp]),
     "tf_expert_cache_destroy": (_S, [_vp]),
+    "tf_expert_cache_set_copy_streams": (_S, [_vp, ctypes.POINTER(_vp), _i32]),
+    "tf_device_cache_state_bytes": (_sz, [_i32, _i32, _i32, _sz]),
+    "tf_device_cache_create": (_S, [_i32, _i32, _i32, _sz, _vp, _vp, _vp, _sz, _sz, ctypes.POINTER(_vp)]),
+    "tf_device_cache_set_fetch_ctas": (_S, [_vp, _i32]),
+    "tf_device_cache_counters": (_S, [_vp, ctypes.POINTER(_i64), ctypes.POINTER(_i64), ctypes.POINTER(_i64), _vp]),
+    "tf_device_cache_trace": (_S, [_vp, _vp, _sz, ctypes.POINTER(_sz), _vp]),
+    "tf_device_cache_state": (_S, [_vp, _i32, _vp, _vp, _vp, _vp]),
+    "tf_device_cache_destroy": (_S, [_vp]),
+    "tf_layer_step_device_cache": (_S, [_vp, _vp, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _i32,
+                                        ctypes.POINTER(StepStats)]),
     "tf_layer_workspace_bytes": (_sz, [ctypes.POINTER(LayerDesc), _i32]),
     "tf_layer_create": (_S, [ctypes.POINTER(LayerDesc), _i32, _vp, _sz, ctypes.POINTER(_vp)]),
     "tf_layer_destroy": (_S, [_vp]),
@@ -101,6 +111,7 @@ SIGNATURES = {
     "tf_profile_begin": (_S, [_i32]),
     "tf_profile_end": (_S, [_vp, _vp]),
     "tf_test_fail_nth_copy": (_S, [_i32]),
+    "tf_test_set_wait_limit_ns": (_S, [ctypes.c_uint64]),
 }
 
 KERNEL_NAMES = ["router", "gateup", "down", "layer", "permute", "gemm", "combine", "other"]
@@ -297,9 +308,75 @@ class ExpertCache:
                "tf_expert_cache_state")
         return ex, cnt, lu
 
+    def set_copy_streams(self, streams) -> None:
+        """Stripe the miss fills over these streams (empty list: back to the call's copy stream)."""
+        self._streams = list(streams)
+        arr = (ctypes.c_void_p * max(1, len(self._streams)))(*[_stream(s) for s in self._streams])
+        _check(lib().tf_expert_cache_set_copy_streams(self.handle, arr, len(self._streams)),
+               "tf_expert_cache_set_copy_streams")
+
     def close(self):
         if self.handle:
             lib().tf_expert_cache_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def tf_device_cache_state_bytes(n_layers: int, n_slots: int, n_experts: int, trace_capacity: int) -> int:
+    return lib().tf_device_cache_state_bytes(n_layers, n_slots, n_experts, trace_capacity)
+
+
+class DeviceCache:
+    """Owner of a tf_device_cache handle: the per-layer LFU cache with its metadata in device memory.
+    `state` must be a device tensor of tf_device_cache_state_bytes(...) bytes kept alive by the caller; the
+    pool and the pinned host store likewise."""
+
+    def __init__(self, n_layers: int, n_slots: int, n_experts: int, slot_bytes: int, d_slot_pool, h_expert_store,
+                 state, trace_capacity: int = 0):
+        h = ctypes.c_void_p()
+        self.state_buf, self.pool, self.store = state, d_slot_pool, h_expert_store
+        _check(lib().tf_device_cache_create(n_layers, n_slots, n_experts, slot_bytes, _ptr(d_slot_pool),
+                                            _ptr(h_expert_store), _ptr(state), state.numel() * state.element_size(),
+                                            trace_capacity, ctypes.byref(h)), "tf_device_cache_create")
+        self.handle = h.value
+        self.n_slots = n_slots
+
+    def set_fetch_ctas(self, ctas: int) -> None:
+        _check(lib().tf_device_cache_set_fetch_ctas(self.handle, ctas), "tf_device_cache_set_fetch_ctas")
+
+    def counters(self, stream=None):
+        """(hits, misses, events recorded) since creation."""
+        h, m, n = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().tf_device_cache_counters(self.handle, ctypes.byref(h), ctypes.byref(m), ctypes.byref(n),
+                                              _stream(stream)), "tf_device_cache_counters")
+        return h.value, m.value, n.value
+
+    def trace(self, stream=None):
+        n = ctypes.c_size_t()
+        _check(lib().tf_device_cache_trace(self.handle, None, 0, ctypes.byref(n), _stream(stream)),
+               "tf_device_cache_trace")
+        buf = (CacheEvent * max(1, n.value))()
+        _check(lib().tf_device_cache_trace(self.handle, buf, n.value, ctypes.byref(n), _stream(stream)),
+               "tf_device_cache_trace")
+        return [(e.step, e.layer, e.expert, e.hit, e.slot, e.evicted) for e in buf[:n.value]]
+
+    def state(self, layer: int, stream=None):
+        import numpy as np
+        ex = np.empty(self.n_slots, np.int32)
+        cnt = np.empty(self.n_slots, np.int64)
+        lu = np.empty(self.n_slots, np.int64)
+        _check(lib().tf_device_cache_state(self.handle, layer, ex.ctypes.data, cnt.ctypes.data, lu.ctypes.data,
+                                           _stream(stream)), "tf_device_cache_state")
+        return ex, cnt, lu
+
+    def close(self):
+        if self.handle:
+            lib().tf_device_cache_destroy(self.handle)
             self.handle = None
 
     def __del__(self):
@@ -314,7 +391,7 @@ class ExpertCache:
 def layer_desc(H, I, E, k, S, W_r, W_sg=None, W_su=None, W_sd=None, experts: ExpertTable | None = None,
                eps: float = 1e-6) -> LayerDesc:
     return LayerDesc(H, I, E, k, S, eps, _ptr(W_r), _ptr(W_sg), _ptr(W_su), _ptr(W_sd),
-                     experts if experts is not None else ExpertTable(None, 0, None))
+                     experts if experts is not None else ExpertTable(None, 0, None, 0, 0))
 
 
 def tf_layer_workspace_bytes(desc: LayerDesc, T_max: int) -> int:
@@ -364,6 +441,16 @@ def tf_layer_step(layer: Layer, cache: ExpertCache | None, layer_index: int, ste
                                _ptr(x), _ptr(out), T, _ptr(logit_bias), bias_stride, _stream(compute_stream),
                                _stream(copy_stream) if copy_stream is not None else None, measure,
                                ctypes.byref(stats)), "tf_layer_step")
+    return stats
+
+
+def tf_layer_step_device_cache(layer: Layer, cache: DeviceCache, layer_index: int, x, out, logit_bias=None,
+                               bias_stride: int = 0, compute_stream=None, fetch_stream=None, measure: int = 0):
+    stats = StepStats()
+    _check(lib().tf_layer_step_device_cache(layer.handle, cache.handle, layer_index, _ptr(x), _ptr(out),
+                                            _ptr(logit_bias), bias_stride, _stream(compute_stream),
+                                            _stream(fetch_stream), measure, ctypes.byref(stats)),
+           "tf_layer_step_device_cache")
     return stats
 
 
@@ -445,3 +532,8 @@ def tf_profile_end() -> dict:
 
 def tf_test_fail_nth_copy(n: int) -> None:
     _check(lib().tf_test_fail_nth_copy(n), "tf_test_fail_nth_copy")
+
+
+def tf_test_set_wait_limit_ns(ns: int) -> None:
+    """Limit of the kernels' waits on other warps / CTAs for later launches (0: the default 2 s)."""
+    _check(lib().tf_test_set_wait_limit_ns(ns), "tf_test_set_wait_limit_ns")

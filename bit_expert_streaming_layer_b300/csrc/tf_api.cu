@@ -2,6 +2,7 @@
 // dequant export, layer handles, the (cached) layer step and the decode stack.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -18,6 +19,10 @@ tf_status cuda_status(int err, const char* what) {
 }
 
 static int g_copy_countdown = 0;  // failure injection for the miss-fill engine (0 = off)
+
+constexpr unsigned long long DEFAULT_WAIT_LIMIT_NS = 2000000000ull;
+static std::atomic<unsigned long long> g_wait_limit_ns{DEFAULT_WAIT_LIMIT_NS};
+unsigned long long test_wait_limit_ns() { return g_wait_limit_ns.load(); }
 
 int smem_limit_once(const void* kernel, int bytes) {
     static std::mutex mu;
@@ -110,29 +115,10 @@ using namespace tf;
 
 // ------------------------------------------------------------------ handles
 
-struct tf_layer {
-    tf_layer_desc d;
-    int T_max = 0;
-    ExpertLayout lay;
-    char* ws = nullptr;
-    size_t ws_bytes = 0;
-    char* grouped_ws = nullptr;      // T_max > 1 only
-    size_t grouped_bytes = 0;
-    uint32_t* counters = nullptr;
-    float* logits = nullptr;
-    int32_t* idx = nullptr;
-    float* w = nullptr;
-    float* rms = nullptr;
-    float* h_routed = nullptr;
-    float* h_shared = nullptr;
-    int32_t* h_idx = nullptr;        // pinned staging for the cached step
-    cudaEvent_t ev_idx = nullptr, ev_copies = nullptr, ev_t0 = nullptr, ev_shared = nullptr, ev_c0 = nullptr;
-};
-
 namespace {
 
 struct LayerCarve {
-    size_t counters, logits, idx, w, rms, h_routed, h_shared, grouped, grouped_bytes, total;
+    size_t counters, logits, idx, w, rms, h_routed, h_shared, ys, grouped, grouped_bytes, total;
 };
 
 LayerCarve layer_carve(const tf_layer_desc* d, int T_max) {
@@ -145,6 +131,7 @@ LayerCarve layer_carve(const tf_layer_desc* d, int T_max) {
     c.rms = o;      o += align_up((size_t)T_max * 4, 256);
     c.h_routed = o; o += align_up((size_t)d->k * d->I * 4, 256);
     c.h_shared = o; o += align_up((size_t)(d->S > 0 ? d->S : 1) * 4, 256);
+    c.ys = o;       o += align_up((size_t)d->H * 4, 256);
     // T_max > 1: the grouped path's workspace (permutation, activations, h, y, shared-expert buffers)
     c.grouped = o;
     c.grouped_bytes = T_max > 1 ? grouped_workspace_bytes(T_max, d->H, d->I, d->E, d->k, d->S) : 0;
@@ -172,6 +159,9 @@ tf_status check_desc(const tf_layer_desc* d, const char* fn) {
     return TF_OK;
 }
 
+}  // namespace
+
+namespace tf {
 DecodeParams decode_params(const tf_layer* l, const void* x, void* out, float* delta, const ExpertRef& ex,
                            const float* w, const float* rms_in) {
     DecodeParams p;
@@ -198,9 +188,6 @@ DecodeParams decode_params(const tf_layer* l, const void* x, void* out, float* d
     return p;
 }
 
-}  // namespace
-
-namespace tf {
 void layer_desc_of(const tf_layer* l, tf_layer_desc* out) { *out = l->d; }
 }  // namespace tf
 
@@ -234,15 +221,15 @@ tf_status tf_router_topk(const void* x, int T, int H, const void* W_r, int E, co
 
 // ------------------------------------------------------------------ dequant
 
-tf_status tf_dequant_expert(const void* blob, int H, int I, int matrix, int as_bf16, void* out, void* stream) {
+tf_status tf_dequant_expert(const void* blob, int H, int I, int matrix, int format, void* out, void* stream) {
     ExpertLayout L;
     if (!blob || !out) return fail(TF_ERR_INVALID_ARG, "tf_dequant_expert: null pointer");
-    if (!expert_layout(H, I, &L) || matrix < 0 || matrix > 2)
-        return fail(TF_ERR_INVALID_ARG, "tf_dequant_expert: bad H/I/matrix");
+    if (!expert_layout(H, I, &L) || matrix < 0 || matrix > 2 || format < 0 || format > 2)
+        return fail(TF_ERR_INVALID_ARG, "tf_dequant_expert: bad H/I/matrix/format");
     clear_error();
     const size_t off_sb = matrix < 2 ? L.gu_sb : L.d_sb;
     const size_t off_codes = matrix < 2 ? L.gu_codes : L.d_codes;
-    return cuda_status(launch_dequant(static_cast<const char*>(blob), H, I, matrix, as_bf16, out, off_sb, off_codes,
+    return cuda_status(launch_dequant(static_cast<const char*>(blob), H, I, matrix, format, out, off_sb, off_codes,
                                       stream),
                        "tf_dequant_expert");
 }
@@ -393,6 +380,7 @@ tf_status tf_layer_create(const tf_layer_desc* d, int T_max, void* workspace, si
     l->rms = reinterpret_cast<float*>(l->ws + c.rms);
     l->h_routed = reinterpret_cast<float*>(l->ws + c.h_routed);
     l->h_shared = reinterpret_cast<float*>(l->ws + c.h_shared);
+    l->ys = reinterpret_cast<float*>(l->ws + c.ys);
     l->grouped_ws = c.grouped_bytes ? l->ws + c.grouped : nullptr;
     l->grouped_bytes = c.grouped_bytes;
     cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&l->h_idx), TF_MAX_K * sizeof(int32_t), cudaHostAllocDefault);
@@ -472,6 +460,11 @@ tf_status tf_profile_end(double* ms, int64_t* launches) {
     }
     prof_release();
     return st;
+}
+
+tf_status tf_test_set_wait_limit_ns(uint64_t ns) {
+    g_wait_limit_ns = ns ? (unsigned long long)ns : DEFAULT_WAIT_LIMIT_NS;
+    return TF_OK;
 }
 
 tf_status tf_test_fail_nth_copy(int n) {
@@ -554,7 +547,11 @@ tf_status tf_layer_step(tf_layer* l, tf_expert_cache* cache, int layer, int64_t 
     ExpertRef none;
     std::memset(&none, 0, sizeof(none));
     DecodeParams p = decode_params(l, x, out, nullptr, none, l->w, l->rms);
+    // the shared branch (gate/up, then down into the fp32 buffer ys) runs while the host decides the copies and
+    // while they run; the routed down later adds x + ys + its own terms
+    p.ys = d.S > 0 ? l->ys : nullptr;
     if (d.S > 0 && (e = launch_gateup(p, k * d.I, k * d.I + d.S, cs))) return cuda_status(e, fn);
+    if (d.S > 0 && (e = launch_down(p, 0, 1, cs))) return cuda_status(e, fn);
     if (measure && stats && (e = cudaEventRecord(l->ev_shared, cs))) return cuda_status(e, fn);
     if ((e = cudaEventSynchronize(l->ev_idx))) return cuda_status(e, fn);  // the one host wait: the CPU decides the I/O
     int32_t ids[TF_MAX_K], slot[TF_MAX_K];
@@ -564,7 +561,10 @@ tf_status tf_layer_step(tf_layer* l, tf_expert_cache* cache, int layer, int64_t 
     int32_t admitted[TF_MAX_K];
     int na = 0;
     uint64_t bytes = 0;
-    if (measure && stats && (e = cudaEventRecord(l->ev_c0, ps))) return cuda_status(e, fn);
+    // copy streams: the cache's set (the k-th miss on streams[k mod n]) or the call's copy stream
+    const int nstr = c->copy_streams.empty() ? 1 : (int)c->copy_streams.size();
+    auto copy_stream_of = [&](int m) { return c->copy_streams.empty() ? ps : c->copy_streams[m % nstr]; };
+    if (measure && stats && (e = cudaEventRecord(l->ev_c0, copy_stream_of(0)))) return cuda_status(e, fn);
     const char* pool = static_cast<const char*>(c->d_slot_pool);
     const char* store = static_cast<const char*>(h_expert_store);
     for (int i = 0; i < k; ++i) {
@@ -573,13 +573,13 @@ tf_status tf_layer_step(tf_layer* l, tf_expert_cache* cache, int layer, int64_t 
         tf_status st = tf_expert_cache_admit(c, layer, step, ids[i], ids, k, &s, &evicted);
         if (st == TF_OK) {
             slot[i] = s;
-            admitted[na++] = s;
             char* dst = const_cast<char*>(pool) + ((size_t)layer * c->n_slots + s) * c->slot_bytes;
             const char* src = store + ((size_t)layer * d.E + ids[i]) * c->slot_bytes;
             if (g_copy_countdown > 0 && --g_copy_countdown == 0)
                 e = (int)cudaErrorInvalidValue;  // injected failure: the copy is not enqueued
             else
-                e = (int)cudaMemcpyAsync(dst, src, l->lay.payload, cudaMemcpyHostToDevice, ps);
+                e = (int)cudaMemcpyAsync(dst, src, l->lay.payload, cudaMemcpyHostToDevice, copy_stream_of(na));
+            admitted[na++] = s;
             if (e) st = cuda_status(e, "tf_layer_step: expert copy");
             bytes += l->lay.payload;
         }
@@ -589,15 +589,22 @@ tf_status tf_layer_step(tf_layer* l, tf_expert_cache* cache, int layer, int64_t 
             return fail(st, "%s: miss fill failed, %d admitted slot(s) rolled back: %s", fn, na, msg.c_str());
         }
     }
-    if ((e = cudaEventRecord(l->ev_copies, ps))) return cuda_status(e, fn);
-    if ((e = cudaStreamWaitEvent(cs, l->ev_copies, 0))) return cuda_status(e, fn);
+    if (c->copy_streams.empty()) {
+        if ((e = cudaEventRecord(l->ev_copies, ps))) return cuda_status(e, fn);
+        if ((e = cudaStreamWaitEvent(cs, l->ev_copies, 0))) return cuda_status(e, fn);
+    } else {
+        for (int j = 0; j < nstr; ++j) {
+            if ((e = cudaEventRecord(c->copy_events[j], c->copy_streams[j]))) return cuda_status(e, fn);
+            if ((e = cudaStreamWaitEvent(cs, c->copy_events[j], 0))) return cuda_status(e, fn);
+        }
+    }
     ExpertRef r;
     std::memset(&r, 0, sizeof(r));
     r.use_ptrs = 1;
     for (int i = 0; i < k; ++i) r.ptr[i] = pool + ((size_t)layer * c->n_slots + slot[i]) * c->slot_bytes;
     p.ex = r;
     e = launch_gateup(p, 0, k * d.I, cs);
-    if (!e) e = launch_down(p, 1, d.S > 0, cs);
+    if (!e) e = launch_down(p, 1, 0, cs);  // out = x + ys + routed terms (ys: the shared down, enqueued above)
     if (e) return cuda_status(e, fn);
     if (stats) {
         std::memcpy(stats->ids, ids, (size_t)k * 4);
@@ -608,13 +615,38 @@ tf_status tf_layer_step(tf_layer* l, tf_expert_cache* cache, int layer, int64_t 
             if ((e = cudaStreamSynchronize(cs))) return cuda_status(e, fn);
             float t_shared = 0.f, t_copies = 0.f, t_copy = 0.f;
             if (d.S > 0) cudaEventElapsedTime(&t_shared, l->ev_t0, l->ev_shared);
-            cudaEventElapsedTime(&t_copies, l->ev_t0, l->ev_copies);
-            cudaEventElapsedTime(&t_copy, l->ev_c0, l->ev_copies);
+            if (c->copy_streams.empty()) {
+                cudaEventElapsedTime(&t_copies, l->ev_t0, l->ev_copies);
+                cudaEventElapsedTime(&t_copy, l->ev_c0, l->ev_copies);
+            } else {
+                for (int j = 0; j < nstr; ++j) {  // the last stream to finish ends the fills
+                    float a = 0.f, b = 0.f;
+                    cudaEventElapsedTime(&a, l->ev_t0, c->copy_events[j]);
+                    cudaEventElapsedTime(&b, l->ev_c0, c->copy_events[j]);
+                    t_copies = a > t_copies ? a : t_copies;
+                    t_copy = b > t_copy ? b : t_copy;
+                }
+            }
             stats->shared_ms = t_shared;
             stats->copy_ms = t_copy;
             stats->stall_ms = t_copies > t_shared ? t_copies - t_shared : 0.f;
         }
     }
+    return TF_OK;
+}
+
+tf_status tf_expert_cache_set_copy_streams(tf_expert_cache* c, void* const* streams, int n) {
+    const char* fn = "tf_expert_cache_set_copy_streams";
+    if (!c || n < 0 || n > TF_MAX_K || (n > 0 && !streams)) return fail(TF_ERR_INVALID_ARG, "%s: bad arguments", fn);
+    for (int j = 0; j < n; ++j)
+        if (!streams[j]) return fail(TF_ERR_INVALID_ARG, "%s: stream %d is NULL", fn, j);
+    while ((int)c->copy_events.size() < n) {
+        cudaEvent_t ev = nullptr;
+        if (cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDefault)) return cuda_status(e, fn);
+        c->copy_events.push_back(ev);
+    }
+    c->copy_streams.clear();
+    for (int j = 0; j < n; ++j) c->copy_streams.push_back(static_cast<cudaStream_t>(streams[j]));
     return TF_OK;
 }
 

@@ -102,6 +102,137 @@ k_router_topk(const uint16_t* __restrict__ x, int H, const uint16_t* __restrict_
     }
 }
 
+// ----------------------------------------------------- router for many tokens
+//
+// The same logits as k_router_topk, computed for a tile of tokens against a
+// block of TE experts whose rows are held in shared memory as fp32 (converted
+// once per CTA, reused by every token of the CTA). The fixed summation order is
+// kept exactly: the canonical sum has 32 partials, partial r summing the terms
+// k = r, r + 32, r + 64, ... in increasing k, then a xor butterfly 16, 8, 4, 2,
+// 1. Here a quad of four threads owns one token; thread m of the quad keeps the
+// eight partials r = 8m .. 8m + 7 (one 16-byte load of x covers its eight k of
+// a 32-wide step, in increasing k for every partial). The butterfly steps 16
+// and 8 pair partials of threads m ^ 2 and m ^ 1 (shuffles inside the quad), the
+// steps 4, 2 and 1 pair partials inside a thread. Products of two bf16 values
+// are exact in fp32, so each fused multiply-add rounds once, as in the
+// canonical sum.
+
+constexpr int RTT_THREADS = 256;
+constexpr int RTT_TOKENS = RTT_THREADS / 4;   // tokens in flight per CTA (one per quad)
+constexpr int RTT_SMEM_MAX = 227 * 1024;      // the expert block of W_r as fp32 (TE * H * 4 bytes) fits this
+
+__device__ __forceinline__ unsigned long long rt_pk2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void rt_unpk2(unsigned long long v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ void rt_fma2(unsigned long long& acc, unsigned long long a, unsigned long long b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+// The quad's butterfly of the 32 partials held as four packed pairs per thread
+// (pair p = partials 8m + 2p, 8m + 2p + 1): the canonical sum, equal in all four threads.
+__device__ __forceinline__ float quad_canonical(const unsigned long long (&a)[4]) {
+    float v[8];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) rt_unpk2(a[p], v[2 * p], v[2 * p + 1]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __fadd_rn(v[i], __shfl_xor_sync(FULL, v[i], 2));   // step 16
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __fadd_rn(v[i], __shfl_xor_sync(FULL, v[i], 1));   // step 8
+    const float u0 = __fadd_rn(v[0], v[4]), u1 = __fadd_rn(v[1], v[5]);                   // step 4
+    const float u2 = __fadd_rn(v[2], v[6]), u3 = __fadd_rn(v[3], v[7]);
+    const float w0 = __fadd_rn(u0, u2), w1 = __fadd_rn(u1, u3);                           // step 2
+    return __fadd_rn(w0, w1);                                                               // step 1
+}
+
+template <int TE>
+__global__ void __launch_bounds__(RTT_THREADS)
+k_router_tiled(const uint16_t* __restrict__ x, int T, int H, const uint16_t* __restrict__ Wr, int E,
+               const float* __restrict__ bias, int bias_stride, float* __restrict__ logits,
+               float* __restrict__ rms, float eps, int tokens_per_cta) {
+    extern __shared__ float4 rts4[];
+    float* wsm = reinterpret_cast<float*>(rts4);   // [TE][H] fp32
+    const int e0 = blockIdx.x * TE;
+    const int nv = H / 8;
+    for (int v = threadIdx.x; v < TE * nv; v += blockDim.x) {
+        const int e = v / nv, c = v - e * nv;
+        uint4 wv = make_uint4(0u, 0u, 0u, 0u);
+        if (e0 + e < E) wv = __ldg(reinterpret_cast<const uint4*>(Wr + (size_t)(e0 + e) * H) + c);
+        float4* d = reinterpret_cast<float4*>(wsm + (size_t)e * H + 8 * c);
+        d[0] = make_float4(bf_lo(wv.x), bf_hi(wv.x), bf_lo(wv.y), bf_hi(wv.y));
+        d[1] = make_float4(bf_lo(wv.z), bf_hi(wv.z), bf_lo(wv.w), bf_hi(wv.w));
+    }
+    __syncthreads();
+    const int quad = threadIdx.x >> 2, m = threadIdx.x & 3;
+    const int t0 = blockIdx.y * tokens_per_cta;
+    const int t1 = min(T, t0 + tokens_per_cta);
+    for (int base = t0; base < t1; base += RTT_TOKENS) {   // uniform trip count: every quad takes part
+        const int t = base + quad;
+        const bool valid = t < t1;
+        const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)(valid ? t : t0) * H);
+        unsigned long long acc[TE][4], sq[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            sq[p] = 0ull;
+#pragma unroll
+            for (int e = 0; e < TE; ++e) acc[e][p] = 0ull;
+        }
+#pragma unroll 2
+        for (int j = 0; j < H / 32; ++j) {
+            const uint4 xv = __ldg(xr + 4 * j + m);   // k = 32 j + 8 m .. 32 j + 8 m + 7
+            const unsigned long long x01 = rt_pk2(bf_lo(xv.x), bf_hi(xv.x)), x23 = rt_pk2(bf_lo(xv.y), bf_hi(xv.y));
+            const unsigned long long x45 = rt_pk2(bf_lo(xv.z), bf_hi(xv.z)), x67 = rt_pk2(bf_lo(xv.w), bf_hi(xv.w));
+            rt_fma2(sq[0], x01, x01);
+            rt_fma2(sq[1], x23, x23);
+            rt_fma2(sq[2], x45, x45);
+            rt_fma2(sq[3], x67, x67);
+            const float* wk = wsm + 32 * j + 8 * m;
+#pragma unroll
+            for (int e = 0; e < TE; ++e) {
+                const float4 wa = *reinterpret_cast<const float4*>(wk + (size_t)e * H);
+                const float4 wb = *reinterpret_cast<const float4*>(wk + (size_t)e * H + 4);
+                rt_fma2(acc[e][0], rt_pk2(wa.x, wa.y), x01);
+                rt_fma2(acc[e][1], rt_pk2(wa.z, wa.w), x23);
+                rt_fma2(acc[e][2], rt_pk2(wb.x, wb.y), x45);
+                rt_fma2(acc[e][3], rt_pk2(wb.z, wb.w), x67);
+            }
+        }
+        const float ss = quad_canonical(sq);
+        const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)H), eps)));
+#pragma unroll
+        for (int e = 0; e < TE; ++e) {
+            const float d = quad_canonical(acc[e]);
+            const int ge = e0 + e;
+            if (valid && (e & 3) == m && ge < E) {
+                float z = __fmul_rn(r, d);
+                if (bias) z = __fadd_rn(z, bias[(size_t)t * bias_stride + ge]);
+                logits[(size_t)t * E + ge] = z;
+            }
+        }
+        if (valid && m == 0 && blockIdx.x == 0 && rms) rms[t] = r;
+    }
+}
+
+// One warp per token: top-k of its logits and the softmax over the selected ones.
+__global__ void __launch_bounds__(256) k_topk_rows(const float* __restrict__ logits, int T, int E, int k,
+                                                   int32_t* __restrict__ idx, float* __restrict__ wout) {
+    extern __shared__ float tks[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float* z = tks + (size_t)warp * E;
+    unsigned char* taken = reinterpret_cast<unsigned char*>(tks + (size_t)8 * E) + (size_t)warp * E;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= T) return;
+    for (int j = lane; j < E; j += 32) {
+        z[j] = logits[(size_t)t * E + j];
+        taken[j] = 0;
+    }
+    __syncwarp();
+    warp_topk_softmax(z, taken, E, k, lane, idx + (size_t)t * k, wout + (size_t)t * k);
+}
+
 // --------------------------------------------------------------- gate / up
 
 constexpr int GU_WARPS = 8;
@@ -334,16 +465,20 @@ __global__ void __launch_bounds__(DN_WARPS * 32) k_down(DecodeParams p, int with
         acc = warp_sum(acc);
         accs = warp_sum(accs);
         if (lane == 0) {
-            const float d = accs + acc;
-            p.out[j] = f2bf(bf2f(p.x[j]) + d);
-            if (p.delta) p.delta[j] = d;
+            if (p.ys && !with_routed) {
+                p.ys[j] = accs;  // the shared term alone; a routed-only launch adds the rest
+            } else {
+                const float d = (p.ys ? p.ys[j] : accs) + acc;  // same sum as a launch with both terms
+                p.out[j] = f2bf(bf2f(p.x[j]) + d);
+                if (p.delta) p.delta[j] = d;
+            }
         }
     }
 }
 
 // ------------------------------------------------------------------ dequant
 
-__global__ void k_dequant(const char* __restrict__ blob, int H, int I, int matrix, int as_bf16, void* out,
+__global__ void k_dequant(const char* __restrict__ blob, int H, int I, int matrix, int format, void* out,
                           size_t off_sb, size_t off_codes) {
     // matrix 0/1: [I, H] rows at packed rows 2j+matrix; matrix 2: [H, I]
     const int R = matrix < 2 ? I : H, K = matrix < 2 ? H : I;
@@ -355,16 +490,55 @@ __global__ void k_dequant(const char* __restrict__ blob, int H, int I, int matri
         const uint32_t q = (kk & 1) ? (byte >> 4) : (byte & 15u);
         const uint32_t sb = *reinterpret_cast<const uint32_t*>(blob + off_sb + (prow * (K / 64) + kk / 64) * 4);
         const float w = __fadd_rn(__fmul_rn(h2f(sb & 0xffffu), (float)q), h2f(sb >> 16));
-        if (as_bf16) static_cast<uint16_t*>(out)[t] = f2bf(w);
+        if (format == 1) static_cast<uint16_t*>(out)[t] = f2bf(w);
+        else if (format == 2) static_cast<uint16_t*>(out)[t] = __half_as_ushort(__float2half_rn(w));
         else static_cast<float*>(out)[t] = w;
     }
 }
 
 }  // namespace
 
+static int sm_count();
+
+// Many tokens: the token-tiled logits, then one warp per token for the top-k. A wide expert block (8 rows) for
+// large T keeps every SM busy with few W_r conversions; a narrow one (2 rows) spreads small batches over more CTAs.
+static int launch_router_many(const uint16_t* x, int T, int H, const uint16_t* Wr, int E, const float* bias,
+                              int bias_stride, int k, int32_t* idx, float* w, float* logits, float* rms, float eps,
+                              cudaStream_t st) {
+    const bool wide = T >= 512;
+    const int TE = wide ? 8 : 2;
+    const int gx = (E + TE - 1) / TE;
+    const int target = 2 * sm_count();
+    int gy = (target + gx - 1) / gx;
+    int per = (T + gy - 1) / gy;
+    per = (per + RTT_TOKENS - 1) / RTT_TOKENS * RTT_TOKENS;   // whole passes of one token per quad
+    gy = (T + per - 1) / per;
+    const size_t smem = (size_t)TE * H * 4;
+    if (smem > (size_t)RTT_SMEM_MAX) return (int)cudaErrorInvalidValue;   // H beyond what one CTA can hold
+    // the limit is raised once to the largest size any call may ask for (a smaller one would refuse later calls)
+    const void* kern = wide ? (const void*)k_router_tiled<8> : (const void*)k_router_tiled<2>;
+    if (int e = smem_limit_once(kern, RTT_SMEM_MAX)) return e;
+    if (wide)
+        k_router_tiled<8><<<dim3(gx, gy), RTT_THREADS, smem, st>>>(x, T, H, Wr, E, bias, bias_stride, logits, rms,
+                                                                   eps, per);
+    else
+        k_router_tiled<2><<<dim3(gx, gy), RTT_THREADS, smem, st>>>(x, T, H, Wr, E, bias, bias_stride, logits, rms,
+                                                                   eps, per);
+    const size_t tk_smem = (size_t)8 * E * 5;   // <= 40 KB for E <= 1024: within the default limit
+    k_topk_rows<<<(T + 7) / 8, 256, tk_smem, st>>>(logits, T, E, k, idx, w);
+    return (int)cudaGetLastError();
+}
+
 int launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* Wr, int E, const float* bias,
                        int bias_stride, int k, int32_t* idx, float* w, float* logits, float* rms,
                        uint32_t* counters, float eps, void* stream) {
+    if (T > 1 && (size_t)(T >= 512 ? 8 : 2) * H * 4 <= (size_t)RTT_SMEM_MAX) {
+        prof_before(TF_KERNEL_ROUTER, stream);
+        const int e = launch_router_many(x, T, H, Wr, E, bias, bias_stride, k, idx, w, logits, rms, eps,
+                                         (cudaStream_t)stream);
+        prof_after(TF_KERNEL_ROUTER, stream);
+        return e;
+    }
     dim3 grid((E + RT_WARPS - 1) / RT_WARPS, T);
     const size_t smem = (size_t)(RT_WARPS + 1) * H * 2;
     if (int e = smem_limit_once((const void*)k_router_topk, 200 * 1024)) return e;
@@ -413,10 +587,10 @@ int launch_down(const DecodeParams& p, int with_routed, int with_shared, void* s
     return (int)cudaGetLastError();
 }
 
-int launch_dequant(const char* blob, int H, int I, int matrix, int as_bf16, void* out, size_t off_sb,
+int launch_dequant(const char* blob, int H, int I, int matrix, int format, void* out, size_t off_sb,
                    size_t off_codes, void* stream) {
     prof_before(TF_KERNEL_OTHER, stream);
-    k_dequant<<<sm_count() * 4, 256, 0, (cudaStream_t)stream>>>(blob, H, I, matrix, as_bf16, out, off_sb, off_codes);
+    k_dequant<<<sm_count() * 4, 256, 0, (cudaStream_t)stream>>>(blob, H, I, matrix, format, out, off_sb, off_codes);
     prof_after(TF_KERNEL_OTHER, stream);
     return (int)cudaGetLastError();
 }

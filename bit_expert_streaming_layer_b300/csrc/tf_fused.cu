@@ -89,7 +89,7 @@ constexpr int RGU_BYTES = 4 * GU_ROW + 4 * GU_SB;   // 6336
 constexpr int DN_SB_OFF = K * 2 * D_ROW;            // 5632
 constexpr int DN_BYTES = DN_SB_OFF + K * 4 * D_SB;  // 7040
 constexpr int H_FLOATS = K * I + S;                 // h_routed then h_shared
-constexpr unsigned long long TIMEOUT_NS = 2000000000ull;  // 2 s per wait
+constexpr unsigned long long OWN_LIMIT_NS = 2000000000ull;  // 2 s: waits for this warp's own copies
 constexpr uint32_t SUSPEND_NS = 1000;      // suspend hint of a blocking mbarrier test
 constexpr uint32_t HINT_SLEEP_NS = 64;     // pause between two reads of a hint counter
 constexpr int CTRL_BAR = 1;                // named barrier of the control warps
@@ -163,6 +163,7 @@ struct Params {
     uint32_t* epoch;             // launch epoch (>= 1), advanced by CTA 0 at the end
     int prefetch;                // 1: prefetch the next layer's data-independent weights into L2
     unsigned long long* trace;   // nullable: TRACE_SLOTS %globaltimer stamps per (layer, CTA)
+    unsigned long long dep_limit_ns;   // limit of a wait on other warps or CTAs (2 s unless a test shortens it)
 };
 
 // Trace slots per (layer, CTA) (ns stamps of %globaltimer), written when
@@ -296,24 +297,44 @@ __device__ __forceinline__ unsigned long long tag64(uint32_t tag, float v) {
 
 __device__ __forceinline__ bool err_set(const uint32_t* err) { return *(volatile const uint32_t*)err != 0; }
 
-// Bounded wait on an mbarrier phase (one lane); false (error recorded) on timeout or when another CTA failed.
-__device__ bool wait_mbar(uint32_t bar, uint32_t parity, uint32_t* err) {
+// Bounded wait (one lane) on an mbarrier phase that other warps complete: false
+// (error recorded) after `limit` ns, or as soon as another CTA has failed.
+__device__ bool wait_mbar(uint32_t bar, uint32_t parity, uint32_t* err, unsigned long long limit) {
     if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = gtimer();
     for (uint32_t n = 1;; ++n) {
         if (mbar_wait_hint(bar, parity, SUSPEND_NS)) return true;
         if ((n & 7u) == 0) {
             if (err_set(err)) return false;
-            if (gtimer() - t0 > TIMEOUT_NS) {
+            if (gtimer() - t0 > limit) {
                 atomicOr(err, ERR_TIMEOUT);
                 return false;
             }
         }
     }
 }
-__device__ __forceinline__ bool warp_wait_mbar(uint32_t bar, uint32_t parity, uint32_t* err, int lane) {
+__device__ __forceinline__ bool warp_wait_mbar(uint32_t bar, uint32_t parity, const Params& P, int lane) {
     bool ok = true;
-    if (lane == 0) ok = wait_mbar(bar, parity, err);
+    if (lane == 0) ok = wait_mbar(bar, parity, P.err, P.dep_limit_ns);
+    return __shfl_sync(FULL, (int)ok, 0) != 0;
+}
+// Wait (one lane) for the warp's own bulk copy to land. It ignores other CTAs'
+// failures: a warp never leaves while a copy into its shared memory is in flight.
+// Bounded all the same (2 s; a copy that does not land is recorded as a timeout).
+__device__ bool wait_own(uint32_t bar, uint32_t parity, uint32_t* err) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = gtimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_wait_hint(bar, parity, SUSPEND_NS)) return true;
+        if ((n & 7u) == 0 && gtimer() - t0 > OWN_LIMIT_NS) {
+            atomicOr(err, ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ bool warp_wait_own(uint32_t bar, uint32_t parity, uint32_t* err, int lane) {
+    bool ok = true;
+    if (lane == 0) ok = wait_own(bar, parity, err);
     return __shfl_sync(FULL, (int)ok, 0) != 0;
 }
 
@@ -536,7 +557,8 @@ __device__ __forceinline__ float4 rows4_int4(const unsigned char* st, const uint
 
 // Wait (one warp) until the hint counter reaches target (modular u32 compare).
 // The counter only paces the reading of tagged data; it orders nothing.
-__device__ bool wait_hint(const uint32_t* cnt, uint32_t target, uint32_t* err, int lane) {
+__device__ bool wait_hint(const uint32_t* cnt, uint32_t target, const Params& P, int lane) {
+    uint32_t* err = P.err;
     int st = 0;  // 1 reached, 2 give up
     if (lane == 0) {
         const uint64_t t0 = gtimer();
@@ -551,7 +573,7 @@ __device__ bool wait_hint(const uint32_t* cnt, uint32_t target, uint32_t* err, i
                     st = 2;
                     break;
                 }
-                if (gtimer() - t0 > TIMEOUT_NS) {
+                if (gtimer() - t0 > P.dep_limit_ns) {
                     atomicOr(err, ERR_TIMEOUT);
                     st = 2;
                     break;
@@ -594,7 +616,7 @@ __device__ bool ctrl_load(const Params& P, const void* src, uint32_t bytes, unsi
             mbar_expect_tx(bar_load, bytes);
             bulk_g2s(smem_u32(dst), src, bytes, bar_load);
         }
-        const bool got = warp_wait_mbar(bar_load, loads & 1, P.err, lane);
+        const bool got = warp_wait_own(bar_load, loads & 1, P.err, lane);
         ++loads;
         if (!got) {
             if (lane == 0) atomicOr(&stale[1], 1u);
@@ -604,7 +626,7 @@ __device__ bool ctrl_load(const Params& P, const void* src, uint32_t bytes, unsi
             if (wbad && lane == 0) atomicAdd(&stale[0], wbad);
         }
         // only warp 0 decides a timeout, so that every control warp takes the same path
-        if (cw == 0 && lane == 0 && round > 16 && gtimer() - t0 > TIMEOUT_NS) {
+        if (cw == 0 && lane == 0 && round > 16 && (err_set(P.err) || gtimer() - t0 > P.dep_limit_ns)) {
             atomicOr(&stale[1], 1u);
             atomicOr(P.err, ERR_TIMEOUT);
         }
@@ -627,7 +649,7 @@ __device__ bool stage_x(const Params& P, int l, uint32_t epoch, uint32_t hint_ta
         const uint4* s4 = reinterpret_cast<const uint4*>(P.x);
         for (int c = cw * 32 + lane; c < H / 8; c += NCTRL * 32) reinterpret_cast<uint4*>(xs)[c] = __ldcg(s4 + c);
     } else {
-        if (cw == 0 && !wait_hint(LD(l - 1).cnt_out, hint_target, P.err, lane) && lane == 0)
+        if (cw == 0 && !wait_hint(LD(l - 1).cnt_out, hint_target, P, lane) && lane == 0)
             atomicOr(&stale[1], 1u);  // tells the other control warps to stop
         ctrl_sync();
         if (stale[1]) return false;
@@ -782,7 +804,7 @@ __device__ void digits_in_place(unsigned char* smem, int t) {
 __device__ bool route_layer(const Params& P, int l, uint32_t tag, uint32_t epoch_x_e, unsigned char* smem, Route* rt,
                             uint32_t bar_load, int& loads, int lane, int& sel, float& selz) {
     const LayerDesc& D = LD(l);
-    if (!wait_hint(D.cnt_z, epoch_x_e, P.err, lane)) return false;
+    if (!wait_hint(D.cnt_z, epoch_x_e, P, lane)) return false;
     const unsigned long long* zt = reinterpret_cast<const unsigned long long*>(smem + OFF_Z);
     const uint64_t t0 = gtimer();
     for (;;) {
@@ -791,13 +813,14 @@ __device__ bool route_layer(const Params& P, int l, uint32_t tag, uint32_t epoch
             mbar_expect_tx(bar_load, (uint32_t)D.E * 8);
             bulk_g2s(smem_u32(smem + OFF_Z), D.zt, (uint32_t)D.E * 8, bar_load);
         }
-        if (!warp_wait_mbar(bar_load, loads & 1, P.err, lane)) return false;
+        if (!warp_wait_own(bar_load, loads & 1, P.err, lane)) return false;
         ++loads;
         int bad = 0;
         for (int j = lane; j < D.E; j += 32) bad |= (uint32_t)(zt[j] >> 32) != tag;
         if (!__any_sync(FULL, bad)) break;
         __nanosleep(128);
-        if (gtimer() - t0 > TIMEOUT_NS) {
+        if (err_set(P.err)) return false;
+        if (gtimer() - t0 > P.dep_limit_ns) {
             if (lane == 0) atomicOr(P.err, ERR_TIMEOUT);
             return false;
         }
@@ -900,7 +923,7 @@ __device__ bool stage_h(const Params& P, int l, uint32_t tag4, const uint32_t* h
                         bool routed, unsigned char* smem, uint32_t bar_load, int& loads, uint32_t* stale, int cw,
                         int lane) {
     const LayerDesc& D = LD(l);
-    if (cw == 0 && !wait_hint(hint, hint_target, P.err, lane) && lane == 0) atomicOr(&stale[1], 1u);
+    if (cw == 0 && !wait_hint(hint, hint_target, P, lane) && lane == 0) atomicOr(&stale[1], 1u);
     ctrl_sync();
     if (stale[1]) return false;
     const int w0 = routed ? 0 : K * I, nw = routed ? K * I : S;  // in floats
@@ -1010,7 +1033,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
             }
         }
         // CTA 0 advances the epoch once the last layer's output is complete
-        if (ok && blockIdx.x == 0 && warp == 0 && wait_hint(LD(P.L - 1).cnt_out, hint_target, P.err, lane)) {
+        if (ok && blockIdx.x == 0 && warp == 0 && wait_hint(LD(P.L - 1).cnt_out, hint_target, P, lane)) {
             const uint32_t* src = LD(P.L - 1).xt;
             const uint32_t tag16 = (epoch * 64u + (uint32_t)(P.L - 1)) & 0xffffu;
             const uint64_t t0 = gtimer();
@@ -1028,7 +1051,8 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
                     break;
                 }
                 __nanosleep(256);
-                if (gtimer() - t0 > TIMEOUT_NS) {
+                if (err_set(P.err)) break;
+                if (gtimer() - t0 > P.dep_limit_ns) {
                     if (lane == 0) atomicOr(P.err, ERR_TIMEOUT);
                     break;
                 }
@@ -1094,7 +1118,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
         const uint32_t tag16 = tag & 0xffffu;
         if (P.prefetch && lane == 0) prefetch_layer(c, l + 1 < P.L ? l + 1 : 0);
         try_issue();
-        if (!(ok = warp_wait_mbar(bar_xs, l & 1, P.err, lane))) break;
+        if (!(ok = warp_wait_mbar(bar_xs, l & 1, P, lane))) break;
         bool n_ready = false;  // r and n of this layer (the second x phase) observed
         const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem + OFF_XS);
         uint16_t* pout = l == P.L - 1 ? P.out : nullptr;
@@ -1113,12 +1137,12 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
             if (con.kind == T_DOWN) {
                 if (con.sub < 2 && !hs_ready) {
                     try_issue();
-                    if (!(ok = warp_wait_mbar(bar_hs, l & 1, P.err, lane))) break;
+                    if (!(ok = warp_wait_mbar(bar_hs, l & 1, P, lane))) break;
                     hs_ready = true;
                 }
                 if (con.sub == 2 && !hr_ready) {
                     try_issue();
-                    if (!(ok = warp_wait_mbar(bar_hr, l & 1, P.err, lane))) break;
+                    if (!(ok = warp_wait_mbar(bar_hr, l & 1, P, lane))) break;
                     hr_ready = true;
                 }
             }
@@ -1130,7 +1154,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
                     ok = false;
                     break;
                 }
-                if (!(ok = warp_wait_mbar(bar_k, con.l & 1, P.err, lane))) break;
+                if (!(ok = warp_wait_mbar(bar_k, con.l & 1, P, lane))) break;
                 k_seen = con.l + 1;
                 try_issue();
                 if (n_iss == n_con) {
@@ -1140,7 +1164,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
                 }
             }
             const int slot = n_con % NS;
-            if (!(ok = warp_wait_mbar(bar0 + 8 * slot, (n_con / NS) & 1, P.err, lane))) break;
+            if (!(ok = warp_wait_own(bar0 + 8 * slot, (n_con / NS) & 1, P.err, lane))) break;
             const unsigned char* st = ring + slot * STAGE;
             if (w0t) {
                 if (con.kind == T_RGU && !t_rgu) trace_at(P, l, TR_W_RGU_READY);
@@ -1160,7 +1184,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
                 for (int k = lane; k < H; k += 32) d = fmaf(bf2f(wrow[k]), bf2f(xs[k]), d);  // exact products
                 d = warp_sum_canonical(d);
                 if (!n_ready) {
-                    if (!(ok = warp_wait_mbar(bar_x, l & 1, P.err, lane))) break;
+                    if (!(ok = warp_wait_mbar(bar_x, l & 1, P, lane))) break;
                     n_ready = true;
                     r = reinterpret_cast<const float*>(smem + OFF_MISC)[0];
                 }
@@ -1172,7 +1196,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
                 }
             } else if (con.kind == T_SGU) {
                 if (!n_ready) {
-                    if (!(ok = warp_wait_mbar(bar_x, l & 1, P.err, lane))) break;
+                    if (!(ok = warp_wait_mbar(bar_x, l & 1, P, lane))) break;
                     n_ready = true;
                     r = reinterpret_cast<const float*>(smem + OFF_MISC)[0];
                 }
@@ -1262,13 +1286,13 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
         // observe this layer's routing and h phases even without items that needed
         // them, so that later parity tests never run two phases behind
         try_issue();
-        if (!n_ready && !(ok = warp_wait_mbar(bar_x, l & 1, P.err, lane))) break;
+        if (!n_ready && !(ok = warp_wait_mbar(bar_x, l & 1, P, lane))) break;
         if (!topk_known(l)) {
-            if (!(ok = warp_wait_mbar(bar_k, l & 1, P.err, lane))) break;
+            if (!(ok = warp_wait_mbar(bar_k, l & 1, P, lane))) break;
             k_seen = l + 1;
         }
-        if (!hs_ready && !(ok = warp_wait_mbar(bar_hs, l & 1, P.err, lane))) break;
-        if (!hr_ready && !(ok = warp_wait_mbar(bar_hr, l & 1, P.err, lane))) break;
+        if (!hs_ready && !(ok = warp_wait_mbar(bar_hs, l & 1, P, lane))) break;
+        if (!hr_ready && !(ok = warp_wait_mbar(bar_hr, l & 1, P, lane))) break;
         signal_phase(P, l, TR_CTA_OUT, &cta_cnt[2], D.cnt_out, lane);
         if (w0t) trace_at(P, l, TR_W_DONE);
     }
@@ -1278,7 +1302,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
         for (int j = n_con; j < n_iss; ++j) {
             const uint64_t t0 = gtimer();
             while (!mbar_try_wait(bar0 + 8 * (j % NS), (j / NS) & 1))
-                if (gtimer() - t0 > TIMEOUT_NS) break;
+                if (gtimer() - t0 > OWN_LIMIT_NS) break;
         }
     }
 }
@@ -1482,6 +1506,7 @@ tf_status tf_stack_step(tf_stack* s, const void* x, void* out, void* stream) {
     P.epoch = s->epoch;
     P.prefetch = s->prefetch;
     P.trace = s->trace;
+    P.dep_limit_ns = test_wait_limit_ns();
     void* args[] = {&P};
     clear_error();
     prof_before(TF_KERNEL_LAYER, stream);

@@ -1,6 +1,6 @@
 // Grouped (batched / prefill) routed-expert FFN on the 5th-generation tensor
 // cores: token x expert histogram, exclusive scan, stable permutation, grouped
-// dequant-to-bf16 tcgen05 GEMMs with fp32 accumulation in TMEM, and the
+// dequant-to-16-bit tcgen05 GEMMs with fp32 accumulation in TMEM, and the
 // unpermute-combine.
 //
 // Page "Como executar um modelo de 26 bilhoes de parametros em dois gigabytes de
@@ -20,8 +20,24 @@
 //   warp 1      TMEM owner; lane 0 issues tcgen05.mma and tcgen05.commit
 //   warps 4..7  epilogue: tcgen05.ld, GELU-gate (gate/up) or plain (down), store
 //   warps 8..15 dequant: codes -> bf16 = RN(s q + b) into the SW128 A tile
-// Numerics (the configuration's "dequant-to-bf16 GEMMs with fp32 accumulate"):
-// n, the dequantised weights and h are bf16; products accumulate in fp32.
+// Numerics: 16-bit operands, fp32 accumulation in TMEM. The token operand is
+// the layer input x itself and the RMS scale r of each token multiplies its
+// gate and up sums in the epilogue, as the router applies it after its dot
+// products: equal in real arithmetic to feeding r x, without rounding r x to
+// 16 bits (which alone cost up to 2.6 % against the fp32 layer in bf16). The
+// routed gate/up GEMM runs on fp16 operands: weights dequantised to fp16 (RN of
+// the fp32 s q + b) and x p, where p = 2^e is the power of two of the token's
+// RMS scale r = m 2^e (m in [1, 2)): the scaling is exact and keeps the operand
+// near unit size (|x p| < 2 sqrt(H)) however large x grows, and m then
+// multiplies the gate and up sums. With the expert weights of the model
+// configuration (a mean weight near 0.09 that cancels in tokens with a small
+// update), bf16 gate/up weights alone cost up to 0.8 % against the fp32 layer;
+// fp16 takes the same kind::f16 instruction at the same rate with three more
+// mantissa bits. The routed down GEMM stays on bf16 operands (the dequantised
+// weights and h): h reaches about 7e4 in fed-back stacks of these weights,
+// beyond fp16. Worst checked token against the fp32 layer: 0.7 %. The shared
+// expert's weights are given as bf16, so its GEMMs take bf16 operands (x, its
+// weights, h).
 //
 // The same kernel runs the bf16 shared expert of a batched layer (a_bf16 = 1):
 // the producer loads the weight tiles by TMA straight into the SW128 A stages
@@ -54,7 +70,7 @@ constexpr int C_BYTES = BM * BK / 2;             // 4 KB of codes per stage
 constexpr int SB_MAX = BM * (2816 / 64) * 4;     // 22,528 B of {s,b} per tile (K up to 2816)
 constexpr int GEMM_THREADS = 512;
 constexpr int N_DQ_WARPS = 8;
-constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
+constexpr unsigned long long OWN_LIMIT_NS = 2000000000ull;   // waits for this thread's own copies and MMAs
 
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + NA * A_BYTES;
@@ -98,6 +114,9 @@ struct GemmParams {
     int ksplit;                 // K split into ksplit items per tile (> 1: raw fp32 partial sums go to part)
     float* part;                // [ksplit][ntok][mrows] partial sums (ksplit > 1)
     int ntok, mrows;
+    const float* col_scale;     // gate/up: the RMS scale of each token row of the B operand (g, u *= it)
+    int f16;                    // 1: fp16 operands (dequantised A and B), 0: bf16
+    unsigned long long dep_limit_ns;   // limit of a wait on another role (2 s unless a test shortens it)
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -195,26 +214,44 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     d |= (uint64_t)2 << 61;
     return d;
 }
-// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, N (multiple of 16, <= 256) and M = 128.
-__device__ __forceinline__ uint32_t idesc_bf16(int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+// Instruction descriptor of kind::f16: fp32 accumulator, A and B both bf16
+// (format 1) or both fp16 (format 0), both K-major, N (multiple of 16, <= 256)
+// and M = 128.
+__device__ __forceinline__ uint32_t idesc_f16(int n, int bf16) {
+    const uint32_t ab = bf16 ? ((1u << 7) | (1u << 10)) : 0u;
+    return (1u << 4) | ab | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 
-// Bounded mbarrier wait of one thread; on timeout or abort it raises the CTA's
-// abort flag (and the global error word) and returns false.
-__device__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, uint32_t* err) {
+// Bounded mbarrier wait of one thread on another role; after `limit` ns it
+// raises the CTA's abort flag (and the global error word) and returns false, and
+// it returns false as soon as the flag is up.
+__device__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, uint32_t* err,
+                         unsigned long long limit) {
     if (mbar_wait_hint(bar, parity)) return true;
     const uint64_t t0 = gtimer();
     for (uint32_t n = 1;; ++n) {
         if (mbar_wait_hint(bar, parity)) return true;
         if ((n & 7u) == 0) {
             if (*abort_flag) return false;
-            if (gtimer() - t0 > TIMEOUT_NS) {
+            if (gtimer() - t0 > limit) {
                 *abort_flag = 1u;
                 atomicOr(err, 1u);
                 return false;
             }
+        }
+    }
+}
+// Wait for this thread's own copies or MMAs to complete: it ignores the abort flag
+// (nothing may still write to shared memory or TMEM when the CTA releases them) and
+// is bounded by a fixed 2 s.
+__device__ bool wait_own(uint32_t bar, uint32_t parity, uint32_t* err) {
+    if (mbar_wait_hint(bar, parity)) return true;
+    const uint64_t t0 = gtimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_wait_hint(bar, parity)) return true;
+        if ((n & 7u) == 0 && gtimer() - t0 > OWN_LIMIT_NS) {
+            atomicOr(err, 1u);
+            return false;
         }
     }
 }
@@ -268,9 +305,10 @@ __device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigne
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
 }
-// Eight codes of one word -> eight bf16 weights RN(fl(s q + b)) packed in a uint4:
-// (128 + q) - 128 is exact, s q is exact, so each weight takes one fp32 rounding,
-// then one to bf16. Columns 2j and 2j+1 share a packed pair.
+// Eight codes of one word -> eight 16-bit weights RN(fl(s q + b)) packed in a uint4,
+// fp16 (F16) or bf16: (128 + q) - 128 is exact, s q is exact, so each weight takes
+// one fp32 rounding, then one to 16 bits. Columns 2j and 2j+1 share a packed pair.
+template <bool F16>
 __device__ __forceinline__ uint4 dequant8(uint32_t q, float s, float b) {
     const uint32_t lo = q & 0x0f0f0f0fu, hi = (q >> 4) & 0x0f0f0f0fu;  // codes 0,2,4,6 / 1,3,5,7
     const unsigned long long S2 = pk2(s, s), B2 = pk2(b, b), M2 = pk2(-128.0f, -128.0f);
@@ -284,8 +322,13 @@ __device__ __forceinline__ uint4 dequant8(uint32_t q, float s, float b) {
     for (int j = 0; j < 4; ++j) {
         float a, c;
         unpk2(w[j], a, c);
-        const __nv_bfloat162 v = __floats2bfloat162_rn(a, c);
-        o[j] = *reinterpret_cast<const uint32_t*>(&v);
+        if constexpr (F16) {
+            const __half2 v = __floats2half2_rn(a, c);
+            o[j] = *reinterpret_cast<const uint32_t*>(&v);
+        } else {
+            const __nv_bfloat162 v = __floats2bfloat162_rn(a, c);
+            o[j] = *reinterpret_cast<const uint32_t*>(&v);
+        }
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
@@ -338,13 +381,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (warp == 0) {
         // ================================================ TMA producer
         if (lane == 0) {
-            int ci = 0, bi = 0, ai = 0, it_local = 0;
+            int ci = 0, bi = 0, ai = 0, it_local = 0, si = 0;
             bool ok = true;
             for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
                 const Item it = decode_item(p, w);
                 const int sbi = it_local & 1;
                 if (!p.a_bf16) {
-                    if (!(ok = wait_bar(bar(BAR_SE + sbi), ((it_local >> 1) & 1) ^ 1, abort_flag, p.err))) break;
+                    if (!(ok = wait_bar(bar(BAR_SE + sbi), ((it_local >> 1) & 1) ^ 1, abort_flag, p.err,
+                                        p.dep_limit_ns)))
+                        break;
+                    ++si;
                     const uint32_t sb_bytes = (uint32_t)(BM * gpr * 4);
                     mbar_expect_tx(bar(BAR_SF + sbi), sb_bytes);
                     bulk_g2s(smem_u32(smem + OFF_SB + sbi * SB_MAX),
@@ -356,7 +402,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 for (int ks = 0; ks < KS; ++ks) {
                     if (p.a_bf16) {
                         const int as = ai % NA;
-                        if (!(ok = wait_bar(bar(BAR_AE + as), ((ai / NA) & 1) ^ 1, abort_flag, p.err))) break;
+                        if (!(ok = wait_bar(bar(BAR_AE + as), ((ai / NA) & 1) ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
                         mbar_expect_tx(bar(BAR_AF + as), A_BYTES);
                         const uint32_t dst = smem_u32(smem + OFF_A + as * A_BYTES);
                         if (p.mode == 0) {
@@ -373,14 +419,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         ++ai;
                     } else {
                         const int cs = ci % NCS;
-                        if (!(ok = wait_bar(bar(BAR_CE + cs), ((ci / NCS) & 1) ^ 1, abort_flag, p.err))) break;
+                        if (!(ok = wait_bar(bar(BAR_CE + cs), ((ci / NCS) & 1) ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
                         mbar_expect_tx(bar(BAR_CF + cs), C_BYTES);
                         tma_load_3d(smem_u32(smem + OFF_C + cs * C_BYTES), &tmA, (ks0 + ks) * (BK / 2), it.mt * BM, it.e,
                                     bar(BAR_CF + cs));
                         ++ci;
                     }
                     const int bs = bi % NBST;
-                    if (!(ok = wait_bar(bar(BAR_BE + bs), ((bi / NBST) & 1) ^ 1, abort_flag, p.err))) break;
+                    if (!(ok = wait_bar(bar(BAR_BE + bs), ((bi / NBST) & 1) ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
                     mbar_expect_tx(bar(BAR_BF + bs), (uint32_t)(nbox * BOX_ROWS * BK * 2));
                     for (int r = 0; r < nbox; ++r)
                         tma_load_2d(smem_u32(smem + OFF_B + bs * B_BYTES + r * BOX_ROWS * BK * 2), &tmB, (ks0 + ks) * BK,
@@ -388,13 +434,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     ++bi;
                 }
             }
-            // let every copy this thread issued land before the CTA can exit
+            // let every copy this thread issued land before the CTA can exit (also after an abort)
             for (int j = ci - NCS; j < ci; ++j)
-                if (j >= 0) wait_bar(bar(BAR_CF + j % NCS), (j / NCS) & 1, abort_flag, p.err);
+                if (j >= 0) wait_own(bar(BAR_CF + j % NCS), (j / NCS) & 1, p.err);
             for (int j = bi - NBST; j < bi; ++j)
-                if (j >= 0) wait_bar(bar(BAR_BF + j % NBST), (j / NBST) & 1, abort_flag, p.err);
+                if (j >= 0) wait_own(bar(BAR_BF + j % NBST), (j / NBST) & 1, p.err);
             for (int j = ai - NA; j < ai; ++j)
-                if (j >= 0) wait_bar(bar(BAR_AF + j % NA), (j / NA) & 1, abort_flag, p.err);
+                if (j >= 0) wait_own(bar(BAR_AF + j % NA), (j / NA) & 1, p.err);
+            for (int j = si - 2; j < si; ++j)   // the {s,b} copies of the last two items
+                if (j >= 0) wait_own(bar(BAR_SF + (j & 1)), (j >> 1) & 1, p.err);
         }
     } else if (warp == 1) {
         // ================================================ MMA issuer
@@ -404,15 +452,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
                 const Item it = decode_item(p, w);
                 const int ab = it_local & 1;
-                if (!(ok = wait_bar(bar(BAR_DE + ab), ((it_local >> 1) & 1) ^ 1, abort_flag, p.err))) break;
+                if (!(ok = wait_bar(bar(BAR_DE + ab), ((it_local >> 1) & 1) ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
                 tc_fence_after();
                 const int n_mma = ((it.nrows + 15) / 16) * 16;
-                const uint32_t idesc = idesc_bf16(n_mma);
+                const uint32_t idesc = idesc_f16(n_mma, !p.f16);
                 const uint32_t d_tmem = tmem + (uint32_t)(ab * NB);
                 for (int ks = 0; ks < KS; ++ks) {
                     const int as = ai % NA, bs = bi % NBST;
-                    if (!(ok = wait_bar(bar(BAR_AF + as), (ai / NA) & 1, abort_flag, p.err))) break;
-                    if (!(ok = wait_bar(bar(BAR_BF + bs), (bi / NBST) & 1, abort_flag, p.err))) break;
+                    if (!(ok = wait_bar(bar(BAR_AF + as), (ai / NA) & 1, abort_flag, p.err, p.dep_limit_ns))) break;
+                    if (!(ok = wait_bar(bar(BAR_BF + bs), (bi / NBST) & 1, abort_flag, p.err, p.dep_limit_ns))) break;
                     tc_fence_after();
                     const uint64_t ad = sw128_desc(smem_u32(smem + OFF_A + as * A_BYTES));
                     const uint64_t bd = sw128_desc(smem_u32(smem + OFF_B + bs * B_BYTES));
@@ -427,8 +475,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 if (!ok) break;
                 tc_commit(bar(BAR_DF + ab));
             }
-            // the MMAs issued so far complete before TMEM is released
-            if (ai > 0) wait_bar(bar(BAR_AE + (ai - 1) % NA), ((ai - 1) / NA) & 1, abort_flag, p.err);
+            // the MMAs issued so far complete before TMEM is released (also after an abort)
+            if (ai > 0) wait_own(bar(BAR_AE + (ai - 1) % NA), ((ai - 1) / NA) & 1, p.err);
         }
     } else if (warp >= 4 && warp < 8) {
         // ================================================ epilogue
@@ -439,7 +487,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const Item it = decode_item(p, w);
             const int ab = it_local & 1;
             int okw = 1;
-            if (lane == 0) okw = wait_bar(bar(BAR_DF + ab), (it_local >> 1) & 1, abort_flag, p.err);
+            if (lane == 0) okw = wait_bar(bar(BAR_DF + ab), (it_local >> 1) & 1, abort_flag, p.err, p.dep_limit_ns);
             if (!__shfl_sync(FULL, okw, 0)) break;
             tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * NB);
@@ -470,7 +518,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         const float g = up ? other : v[i], u = up ? v[i] : other;
                         const int n = c * 8 + i;
                         if ((i & 1) == (int)up && n < it.nrows) {
-                            const float hv = gelu_tanh(g) * u;
+                            const float sc = __ldg(p.col_scale + it.row0 + n);
+                            const float hv = gelu_tanh(__fmul_rn(sc, g)) * __fmul_rn(sc, u);
                             p.hout[(size_t)(it.row0 + n) * p.ldo + j] = f2bf(hv);
                         }
                     }
@@ -500,15 +549,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
             const int sbi = it_local & 1;
             int okw = 1;
-            if (lane == 0) okw = wait_bar(bar(BAR_SF + sbi), (it_local >> 1) & 1, abort_flag, p.err);
+            if (lane == 0) okw = wait_bar(bar(BAR_SF + sbi), (it_local >> 1) & 1, abort_flag, p.err, p.dep_limit_ns);
             if (!(ok = __shfl_sync(FULL, okw, 0))) break;
             const uint32_t* sbrow = reinterpret_cast<const uint32_t*>(smem + OFF_SB + sbi * SB_MAX) + r * gpr;
             for (int ks = 0; ks < KS; ++ks) {
                 const int cs = ci % NCS, as = ai % NA;
                 okw = 1;
                 if (lane == 0) {
-                    okw = wait_bar(bar(BAR_CF + cs), (ci / NCS) & 1, abort_flag, p.err);
-                    if (okw) okw = wait_bar(bar(BAR_AE + as), ((ai / NA) & 1) ^ 1, abort_flag, p.err);
+                    okw = wait_bar(bar(BAR_CF + cs), (ci / NCS) & 1, abort_flag, p.err, p.dep_limit_ns);
+                    if (okw) okw = wait_bar(bar(BAR_AE + as), ((ai / NA) & 1) ^ 1, abort_flag, p.err, p.dep_limit_ns);
                 }
                 if (!(ok = __shfl_sync(FULL, okw, 0))) break;
                 const uint4 qv = *reinterpret_cast<const uint4*>(smem + OFF_C + cs * C_BYTES + r * 32 + hf * 16);
@@ -519,7 +568,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int chunk = hf * 4 + c;  // 16-byte chunk of the 128-byte row
-                    *reinterpret_cast<uint4*>(arow + ((chunk ^ (r & 7)) << 4)) = dequant8(qw[c], s, b);
+                    *reinterpret_cast<uint4*>(arow + ((chunk ^ (r & 7)) << 4)) =
+                        p.f16 ? dequant8<true>(qw[c], s, b) : dequant8<false>(qw[c], s, b);
                 }
                 fence_proxy_async();  // generic-proxy writes, read next by the tensor core
                 __syncwarp();
@@ -548,9 +598,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 // One CTA: tokens per expert, exclusive scan, GEMM tile prefixes.
 __global__ void __launch_bounds__(1024) k_group_hist(const int32_t* __restrict__ idx, int P, int E, int mt_gu,
                                                       int mt_d, int32_t* counts, int32_t* offsets, int32_t* tiles_gu,
-                                                      int32_t* tiles_d) {
+                                                      int32_t* tiles_d, uint32_t* err) {
     __shared__ int32_t cnt[TF_MAX_E];
     __shared__ int32_t wsum[32];
+    if (threadIdx.x == 0) *err = 0u;   // a new call: no GEMM wait has given up yet
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
     for (int p = threadIdx.x; p < P; p += blockDim.x) {
@@ -657,10 +708,11 @@ __global__ void k_shared_plan(int T, int mt_gu, int mt_d, int ks_gu, int ks_d, i
     }
 }
 
-// Split-K shared gate/up: h[t][j] = bf16(gelu(g) u), g and u summed over the K
-// chunks in order (gate row of column j and its up row 8 rows further, per the
-// 8-row interleave of the tiles).
-__global__ void k_shared_gu_combine(const float* __restrict__ part, int ks, int T, int S, uint16_t* hs) {
+// Split-K shared gate/up: h[t][j] = bf16(gelu(r_t g) r_t u), g and u summed over
+// the K chunks in order (gate row of column j and its up row 8 rows further, per
+// the 8-row interleave of the tiles), r_t the token's RMS scale.
+__global__ void k_shared_gu_combine(const float* __restrict__ part, const float* __restrict__ rms, int ks, int T,
+                                    int S, uint16_t* hs) {
     const int t = blockIdx.y;
     const int j = blockIdx.x * blockDim.x + threadIdx.x;
     if (j >= S) return;
@@ -672,7 +724,8 @@ __global__ void k_shared_gu_combine(const float* __restrict__ part, int ks, int 
         g += pr[rg];
         u += pr[rg + 8];
     }
-    hs[(size_t)t * S + j] = f2bf(gelu_tanh(g) * u);
+    const float r = rms[t];
+    hs[(size_t)t * S + j] = f2bf(gelu_tanh(__fmul_rn(r, g)) * __fmul_rn(r, u));
 }
 
 // Split-K shared down: ys[t][i] = sum of the K chunks in order.
@@ -694,25 +747,31 @@ __global__ void k_group_rms(const uint16_t* __restrict__ x, int T, int H, float 
     if (lane == 0) rms[t] = r;
 }
 
-// Row pos of the permuted activations: bf16(r_t * x_t), t = perm[pos] / k
-// (perm NULL: t = pos, the rows in token order).
+// bf16 pair times a power of two p -> fp16 pair (the product is exact; the
+// conversion rounds only values in the fp16 subnormal range).
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w, float p) {
+    const __half2 h = __floats2half2_rn(bf_lo(w) * p, bf_hi(w) * p);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Row pos of the permuted activations: x_t p_t as fp16 (t = perm[pos] / k, p_t the
+// power of two of the RMS scale r_t = m_t p_t, m_t in [1, 2)), and m_t, the scale
+// of the row's gate and up sums.
 __global__ void k_group_gather(const uint16_t* __restrict__ x, const float* __restrict__ rms,
-                               const int32_t* __restrict__ perm, int P, int k, int H, uint16_t* xp) {
+                               const int32_t* __restrict__ perm, int P, int k, int H, uint16_t* xp,
+                               float* __restrict__ rp) {
     const int pos = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (pos >= P) return;
-    const int t = perm ? __ldg(perm + pos) / k : pos;
-    const float r = __ldg(rms + t);
+    const int t = __ldg(perm + pos) / k;
+    const uint32_t rb = __float_as_uint(__ldg(rms + t));
+    const float p = __uint_as_float(rb & 0x7f800000u);                 // 2^e (r > 0 is a normal fp32 value)
+    if (lane == 0) rp[pos] = __uint_as_float((rb & 0x007fffffu) | 0x3f800000u);   // m = r / p, exact
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
     uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)pos * H);
     for (int v = lane; v < H / 8; v += 32) {
         const uint4 a = __ldg(src + v);
-        uint4 o;
-        o.x = (uint32_t)f2bf(__fmul_rn(r, bf_lo(a.x))) | ((uint32_t)f2bf(__fmul_rn(r, bf_hi(a.x))) << 16);
-        o.y = (uint32_t)f2bf(__fmul_rn(r, bf_lo(a.y))) | ((uint32_t)f2bf(__fmul_rn(r, bf_hi(a.y))) << 16);
-        o.z = (uint32_t)f2bf(__fmul_rn(r, bf_lo(a.z))) | ((uint32_t)f2bf(__fmul_rn(r, bf_hi(a.z))) << 16);
-        o.w = (uint32_t)f2bf(__fmul_rn(r, bf_lo(a.w))) | ((uint32_t)f2bf(__fmul_rn(r, bf_hi(a.w))) << 16);
-        dst[v] = o;
+        dst[v] = make_uint4(bf2_to_h2(a.x, p), bf2_to_h2(a.y, p), bf2_to_h2(a.z, p), bf2_to_h2(a.w, p));
     }
 }
 
@@ -759,8 +818,8 @@ __global__ void k_group_combine(const uint16_t* __restrict__ x, const float* __r
 // ------------------------------------------------------------------ host
 
 struct Carve {
-    size_t err, counts, offsets, tiles_gu, tiles_d, perm, inv, rms, xp, hb, y;
-    size_t s_plan, xn, hs, ys, spart;  // shared expert (S > 0): plan arrays, n in token order, h, y, split-K sums
+    size_t err, counts, offsets, tiles_gu, tiles_d, perm, inv, rms, rp, xp, hb, y;
+    size_t s_plan, hs, ys, spart;  // shared expert (S > 0): plan arrays, h, y, split-K sums
     size_t total;
 };
 
@@ -776,13 +835,13 @@ Carve carve(int T, int H, int I, int E, int k, int S) {
     c.perm = o; o += align_up(P * 4, 256);
     c.inv = o; o += align_up(P * 4, 256);
     c.rms = o; o += align_up((size_t)T * 4, 256);
+    c.rp = o; o += align_up(P * 4, 256);
     c.xp = o; o += align_up(P * H * 2, 256);
     c.hb = o; o += align_up(P * I * 2, 256);
     c.y = o; o += align_up(P * H * 4, 256);
-    c.s_plan = c.xn = c.hs = c.ys = c.spart = 0;
+    c.s_plan = c.hs = c.ys = c.spart = 0;
     if (S > 0) {
         c.s_plan = o; o += 256;  // counts[1], offsets[2], tiles_gu[2], tiles_d[2]
-        c.xn = o; o += align_up((size_t)T * H * 2, 256);
         c.hs = o; o += align_up((size_t)T * S * 2, 256);
         c.ys = o; o += align_up((size_t)T * H * 4, 256);
         // split-K partial sums, used while the tokens fit one 256-row tile (at most 4 chunks)
@@ -820,12 +879,14 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, 
     return r == CUDA_SUCCESS;
 }
 
-// Row-major bf16 [rows, cols] as a 2-D SW128 map with boxes of 64 columns (128 bytes) x box_rows rows.
-bool encode_rows(CUtensorMap* m, const void* base, int cols, int rows, int box_rows) {
+// Row-major 16-bit [rows, cols] (bf16, or fp16 with f16 = true) as a 2-D SW128 map with boxes of 64 columns
+// (128 bytes) x box_rows rows.
+bool encode_rows(CUtensorMap* m, const void* base, int cols, int rows, int box_rows, bool f16 = false) {
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t str[1] = {(cuuint64_t)cols * 2};
     cuuint32_t box[2] = {BK, (cuuint32_t)box_rows};
-    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    return encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, str, box,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace grouped
@@ -878,11 +939,11 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     int32_t* perm = reinterpret_cast<int32_t*>(ws + c.perm);
     int32_t* inv = reinterpret_cast<int32_t*>(ws + c.inv);
     float* rms = reinterpret_cast<float*>(ws + c.rms);
+    float* rp = reinterpret_cast<float*>(ws + c.rp);
     uint16_t* xp = reinterpret_cast<uint16_t*>(ws + c.xp);
     uint16_t* hb = reinterpret_cast<uint16_t*>(ws + c.hb);
     float* y = reinterpret_cast<float*>(ws + c.y);
     int32_t* s_plan = S > 0 ? reinterpret_cast<int32_t*>(ws + c.s_plan) : nullptr;
-    uint16_t* xn = S > 0 ? reinterpret_cast<uint16_t*>(ws + c.xn) : nullptr;
     uint16_t* hs = S > 0 ? reinterpret_cast<uint16_t*>(ws + c.hs) : nullptr;
     float* ys = S > 0 ? reinterpret_cast<float*>(ws + c.ys) : nullptr;
     const int P = T * k;
@@ -906,14 +967,14 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
                     CU_TENSOR_MAP_SWIZZLE_NONE))
             return fail(TF_ERR_CUDA, "%s: tensor map of the down codes", fn);
     }
-    if (!encode_rows(&tmB_gu, xp, H, P, BOX_ROWS))
+    if (!encode_rows(&tmB_gu, xp, H, P, BOX_ROWS, true))
         return fail(TF_ERR_CUDA, "%s: tensor map of the permuted activations", fn);
     if (!encode_rows(&tmB_d, hb, I, P, BOX_ROWS)) return fail(TF_ERR_CUDA, "%s: tensor map of h", fn);
     // shared expert: bf16 weights as SW128 row boxes (8 rows for the interleaved gate/up tile, 128 for down)
     CUtensorMap tmS_g, tmS_u, tmS_d, tmS_xn, tmS_h;
     if (S > 0) {
         if (!encode_rows(&tmS_g, a.Wsg, H, S, 8) || !encode_rows(&tmS_u, a.Wsu, H, S, 8) ||
-            !encode_rows(&tmS_d, a.Wsd, S, H, BM) || !encode_rows(&tmS_xn, xn, H, T, BOX_ROWS) ||
+            !encode_rows(&tmS_d, a.Wsd, S, H, BM) || !encode_rows(&tmS_xn, a.x, H, T, BOX_ROWS) ||
             !encode_rows(&tmS_h, hs, S, T, BOX_ROWS))
             return fail(TF_ERR_CUDA, "%s: tensor maps of the shared expert", fn);
     }
@@ -928,10 +989,10 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     const uint16_t* x16 = static_cast<const uint16_t*>(a.x);
     prof_before(TF_KERNEL_PERMUTE, stream);
     k_group_rms<<<(T + 7) / 8, 256, 0, st>>>(x16, T, H, a.eps, rms);
-    k_group_hist<<<1, 1024, 0, st>>>(a.idx, P, E, mt_gu, mt_d, counts, offsets, tiles_gu, tiles_d);
+    k_group_hist<<<1, 1024, 0, st>>>(a.idx, P, E, mt_gu, mt_d, counts, offsets, tiles_gu, tiles_d, err);
     k_group_pos<<<E, 1024, 0, st>>>(a.idx, P, offsets, perm, inv);
     k_group_inv_init<<<(P + 255) / 256, 256, 0, st>>>(a.idx, P, E, inv);
-    k_group_gather<<<(P + 7) / 8, 256, 0, st>>>(x16, rms, perm, P, k, H, xp);
+    k_group_gather<<<(P + 7) / 8, 256, 0, st>>>(x16, rms, perm, P, k, H, xp, rp);
     // the shared expert has few weight tiles (2S/128 and H/128); while the tokens fit one tile row, split K
     // so that more SMs stream its weights (chunks of at least 4 stages)
     auto split_of = [](int kstages) {
@@ -944,7 +1005,6 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     const int ks_d = (S > 0 && one_block) ? split_of(S / BK) : 1;
     float* spart = S > 0 ? reinterpret_cast<float*>(ws + c.spart) : nullptr;
     if (S > 0) {
-        k_group_gather<<<(T + 7) / 8, 256, 0, st>>>(x16, rms, nullptr, T, 1, H, xn);
         k_shared_plan<<<1, 32, 0, st>>>(T, 2 * S / BM, H / BM, ks_gu, ks_d, s_plan, s_plan + 1, s_plan + 3,
                                         s_plan + 5);
     }
@@ -960,6 +1020,7 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     gp.offsets = offsets;
     gp.err = err;
     gp.ksplit = 1;
+    gp.dep_limit_ns = test_wait_limit_ns();
 
     prof_before(TF_KERNEL_GEMM, stream);
     gp.off_sb = lay.gu_sb;
@@ -969,6 +1030,8 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     gp.mode = 0;
     gp.hout = hb;
     gp.ldo = I;
+    gp.col_scale = rp;
+    gp.f16 = 1;
     k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmA_gu, tmB_gu, tmA_gu, gp);
     gp.off_sb = lay.d_sb;
     gp.K = I;
@@ -978,6 +1041,7 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     gp.hout = nullptr;
     gp.yout = y;
     gp.ldo = H;
+    gp.f16 = 0;
     k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmA_d, tmB_d, tmA_d, gp);
     if (S > 0) {
         GemmParams sp;
@@ -986,6 +1050,7 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
         sp.counts = s_plan;
         sp.offsets = s_plan + 1;
         sp.err = err;
+        sp.dep_limit_ns = gp.dep_limit_ns;
         sp.a_bf16 = 1;
         sp.pair_log2 = 3;
         sp.ntok = T;
@@ -996,10 +1061,11 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
         sp.mode = 0;
         sp.hout = hs;
         sp.ldo = S;
+        sp.col_scale = rms;          // the shared expert's token rows are the tokens in order
         sp.ksplit = ks_gu;
         sp.mrows = 2 * S;
         k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmS_g, tmS_xn, tmS_u, sp);
-        if (ks_gu > 1) k_shared_gu_combine<<<dim3((S + 255) / 256, T), 256, 0, st>>>(spart, ks_gu, T, S, hs);
+        if (ks_gu > 1) k_shared_gu_combine<<<dim3((S + 255) / 256, T), 256, 0, st>>>(spart, rms, ks_gu, T, S, hs);
         sp.K = S;
         sp.MT = H / BM;
         sp.tiles = s_plan + 5;

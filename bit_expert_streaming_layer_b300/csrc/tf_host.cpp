@@ -273,6 +273,8 @@ tf_status tf_expert_cache_state(tf_expert_cache* c, int layer, int32_t* expert, 
 }
 
 tf_status tf_expert_cache_destroy(tf_expert_cache* c) {
+    if (c)
+        for (cudaEvent_t ev : c->copy_events) cudaEventDestroy(ev);
     delete c;
     return TF_OK;
 }

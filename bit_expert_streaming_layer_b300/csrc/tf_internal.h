@@ -2,6 +2,8 @@
 // of libtf.so. Not part of the ABI (see include/tf.h).
 #pragma once
 
+#include <cuda_runtime.h>
+
 #include <cstddef>
 #include <cstdint>
 #include <string>
@@ -61,11 +63,20 @@ struct DecodeParams {
     const uint16_t* Wsd;         // bf16 [H,S]
     float* h_routed;             // fp32 [k, I]
     float* h_shared;             // fp32 [S]
+    float* ys;                   // nullable fp32 [H]: the shared down projection, written by a shared-only down
+                                 // launch and added by a routed-only one (so the two can run apart)
     size_t off_gu_sb, off_d_codes, off_d_sb;
 };
 
 // Descriptor a layer handle was created with (tf_api.cu).
 void layer_desc_of(const tf_layer* l, tf_layer_desc* out);
+// Decode-kernel parameters of a layer handle for input x and output out (tf_api.cu).
+DecodeParams decode_params(const tf_layer* l, const void* x, void* out, float* delta, const ExpertRef& ex,
+                           const float* w, const float* rms_in);
+
+// Limit (ns) of a device-side wait on another warp, role or CTA in the persistent
+// kernels: 2 s, unless tf_test_set_wait_limit_ns shortened it (tf_api.cu).
+unsigned long long test_wait_limit_ns();
 
 // Raises a kernel's dynamic shared-memory limit to `bytes` on the current
 // device, once per (kernel, device); thread-safe. Returns a cudaError_t.
@@ -81,9 +92,11 @@ int launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* Wr, int 
                        uint32_t* counters, float eps, void* stream);
 // Row-pair units [u0, u1): routed units are [0, k*I), shared units [k*I, k*I + S).
 int launch_gateup(const DecodeParams& p, int u0, int u1, void* stream);
-// Down projection + combine: with_routed / with_shared select the terms.
+// Down projection + combine: with_routed / with_shared select the terms. Without p.ys:
+// out = x + the selected terms. With p.ys: a shared-only launch writes ys = the shared
+// term (and no output); a routed-only launch writes out = x + (ys + the routed terms).
 int launch_down(const DecodeParams& p, int with_routed, int with_shared, void* stream);
-int launch_dequant(const char* blob, int H, int I, int matrix, int as_bf16, void* out,
+int launch_dequant(const char* blob, int H, int I, int matrix, int format, void* out,
                    size_t off_sb, size_t off_codes, void* stream);
 
 // The grouped (batched / prefill) layer of tf_grouped.cu: routed experts by
@@ -123,4 +136,27 @@ struct tf_expert_cache {
     std::vector<int64_t> count;      // uses since admission
     std::vector<int64_t> last_use;   // step of the last use
     std::vector<tf_cache_event> trace;
+    std::vector<cudaStream_t> copy_streams;   // set by tf_expert_cache_set_copy_streams (empty: the call's)
+    std::vector<cudaEvent_t> copy_events;     // one per copy stream, owned
+};
+
+// A layer handle: its descriptor and the buffers carved from its workspace (tf_api.cu).
+struct tf_layer {
+    tf_layer_desc d;
+    int T_max = 0;
+    tf::ExpertLayout lay;
+    char* ws = nullptr;
+    size_t ws_bytes = 0;
+    char* grouped_ws = nullptr;      // T_max > 1 only
+    size_t grouped_bytes = 0;
+    uint32_t* counters = nullptr;
+    float* logits = nullptr;
+    int32_t* idx = nullptr;
+    float* w = nullptr;
+    float* rms = nullptr;
+    float* h_routed = nullptr;
+    float* h_shared = nullptr;
+    float* ys = nullptr;             // fp32 [H]: the shared down projection of the cached steps
+    int32_t* h_idx = nullptr;        // pinned staging for the cached step
+    cudaEvent_t ev_idx = nullptr, ev_copies = nullptr, ev_t0 = nullptr, ev_shared = nullptr, ev_c0 = nullptr;
 };

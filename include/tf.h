@@ -168,9 +168,10 @@ typedef struct {
 } tf_expert_table;
 
 /* Dequantise one matrix (0 gate, 1 up, 2 down) of a packed device expert to a
- * dense row-major device array: fp32 (as_bf16 = 0) or bf16 (as_bf16 = 1).
- * Parity export. */
-tf_status tf_dequant_expert(const void* blob, int H, int I, int matrix, int as_bf16, void* out,
+ * dense row-major device array: fp32 (format = 0), bf16 (format = 1) or fp16
+ * (format = 2), each the round-to-nearest-even of the fp32 weight s q + b (the
+ * grouped GEMMs take fp16 gate/up and bf16 down weights). Parity export. */
+tf_status tf_dequant_expert(const void* blob, int H, int I, int matrix, int format, void* out,
                             void* stream);
 
 /* ------------------------------------------------------------- MoE FFN */
@@ -223,10 +224,19 @@ tf_status tf_moe_ffn_decode_noalloc(const void* x, void* out, const tf_expert_ta
 /*
  * Grouped (batched / prefill) routed-expert FFN for T tokens: tokens are
  * grouped by expert (histogram, exclusive scan, stable permutation by
- * (expert, token, rank)), each expert's rows run as one dequant-to-bf16
+ * (expert, token, rank)), each expert's rows run as one dequant-to-16-bit
  * tensor-core GEMM with fp32 accumulation (gate/up with the GELU gate fused,
  * then down), and each token sums its k results in top-k order:
  *   out[t] = x[t] + sum_i w[t,i] * E_idx[t,i](RMSNorm(x[t]))
+ * Numerics (tcgen05 kind::f16, fp32 accumulation): the gate/up GEMM takes fp16
+ * operands, the weights dequantised to fp16 (RN of the fp32 s q + b) and x p,
+ * p = 2^e the power of two of the token's RMS scale r = m 2^e (m in [1, 2)), an
+ * exact scaling that keeps the operand near unit size; m multiplies the gate
+ * and up sums in fp32 (g = m (Wg (x p))), equal in real arithmetic to Wg (r x).
+ * The down GEMM takes bf16 operands: the weights dequantised to bf16 and h
+ * rounded to bf16. In tf_layer_step with T > 1 the shared expert's GEMMs take
+ * its bf16 weights with x itself and h in bf16, r applied after the gate and up
+ * sums.
  * Devtrends page, section "Desempenho no mundo real": during prefill one
  * loaded expert is applied to a whole group of rows at once.
  *   x, out     device bf16 [T, H] (out must not alias x)
@@ -283,6 +293,58 @@ tf_status tf_expert_cache_state(tf_expert_cache* c, int layer, int32_t* expert, 
                                 int64_t* last_use);
 tf_status tf_expert_cache_destroy(tf_expert_cache* c);
 
+/*
+ * Copy streams for the miss fills of tf_layer_step (the pages' parallel reads
+ * of several experts, HN page, section "Abordagem tecnica (MoE + streaming por
+ * SSD)": parallel pread instead of mmap). With n >= 1 streams set, the k-th
+ * miss of a step is copied on streams[k mod n] (instead of the call's
+ * copy_stream) and the compute stream waits for all of them. n = 0 goes back
+ * to the call's copy_stream. The streams must outlive their use.
+ */
+tf_status tf_expert_cache_set_copy_streams(tf_expert_cache* c, void* const* streams, int n);
+
+/* ------------------------------------------------- device-side cache metadata */
+
+/*
+ * The same per-layer LFU expert cache, with its metadata in device memory, so
+ * that a cached step never waits on the host. Per layer and token:
+ *  - a one-warp kernel applies the policy of tf_expert_cache (lookup, then the
+ *    misses in top-k order: lowest empty slot, else the smallest count among
+ *    the slots not holding one of the step's ids, then the oldest last use,
+ *    then the lowest slot) to the k ids the router wrote, updates the slot map
+ *    (expert -> slot) and writes the layer's miss list;
+ *  - a copy kernel moves every missing expert from the pinned host store into
+ *    its slot, its CTAs reading host memory directly over the bus;
+ *  - the routed experts then read their weights through the slot map.
+ * The step number of each layer is counted on the device (0 for the layer's
+ * first lookup, then 1, 2, ...), as last_use and in the trace.
+ * The caller owns d_state (tf_device_cache_state_bytes, 256-byte aligned), the
+ * slot pool (n_layers * n_slots slots of slot_bytes; slot s of layer l at
+ * d_slot_pool + (l * n_slots + s) * slot_bytes) and the host store (pinned and
+ * mapped for device access, which cudaHostAlloc and cudaHostRegister memory is
+ * on 64-bit systems with unified addressing; expert (l, e) at
+ * h_expert_store + (l * n_experts + e) * slot_bytes). tf_device_cache_create
+ * initialises d_state synchronously (every slot empty). Up to trace_capacity
+ * events (step, layer, expert, hit, slot, evicted) are recorded on the device.
+ * 1 <= n_slots <= 1024, n_experts <= TF_MAX_E.
+ */
+typedef struct tf_device_cache tf_device_cache;
+size_t tf_device_cache_state_bytes(int n_layers, int n_slots, int n_experts, size_t trace_capacity);
+tf_status tf_device_cache_create(int n_layers, int n_slots, int n_experts, size_t slot_bytes, void* d_slot_pool,
+                                 const void* h_expert_store, void* d_state, size_t state_bytes,
+                                 size_t trace_capacity, tf_device_cache** out);
+/* CTAs of the copy kernel (default 32). */
+tf_status tf_device_cache_set_fetch_ctas(tf_device_cache* c, int ctas);
+/* Totals since creation: lookups that hit, misses (= experts copied) and events recorded. Synchronises stream. */
+tf_status tf_device_cache_counters(tf_device_cache* c, int64_t* hits, int64_t* misses, int64_t* events,
+                                   void* stream);
+/* Up to cap recorded events, oldest first; *n = events recorded in total. Synchronises stream. */
+tf_status tf_device_cache_trace(tf_device_cache* c, tf_cache_event* buf, size_t cap, size_t* n, void* stream);
+/* Slot contents of one layer (expert or -1, count, last_use). Synchronises stream. */
+tf_status tf_device_cache_state(tf_device_cache* c, int layer, int32_t* expert, int64_t* count, int64_t* last_use,
+                                void* stream);
+tf_status tf_device_cache_destroy(tf_device_cache* c);
+
 /* ------------------------------------------------------------ layer step */
 
 /*
@@ -338,8 +400,8 @@ size_t tf_struct_bytes(int which);
  * all T tokens, then the grouped path of tf_moe_ffn_grouped (same requirements:
  * H a multiple of 128 up to 2816, I a multiple of 64) with the shared expert
  * (S a multiple of 64) run by the same tcgen05 GEMM kernel on its bf16
- * weights; out = bf16(x + shared + sum_i w_i y_i), each operand of the GEMMs
- * rounded to bf16 as in tf_moe_ffn_grouped. stats stay zero for T > 1.
+ * weights; out = bf16(x + shared + sum_i w_i y_i), with the numerics of
+ * tf_moe_ffn_grouped. stats stay zero for T > 1.
  * With a cache (T = 1), the call enqueues the router and the shared branch,
  * waits on the host for the k selected ids (one small device->host copy: the
  * CPU decides the I/O), updates the LFU metadata for layer `layer` at `step`,
@@ -354,6 +416,22 @@ tf_status tf_layer_step(tf_layer* l, tf_expert_cache* cache, int layer, int64_t 
                         const void* h_expert_store, const void* x, void* out, int T,
                         const float* logit_bias, int bias_stride, void* compute_stream,
                         void* copy_stream, int measure, tf_step_stats* stats);
+
+/*
+ * One token through layer `layer` with a device-metadata cache: on
+ * compute_stream the router and the shared-expert branch (gate/up and down,
+ * the latter into an fp32 buffer); on fetch_stream, after the router, the LFU
+ * kernel and the copy kernel; then compute_stream waits for fetch_stream and
+ * runs the routed experts and the combine, out = bf16(x + shared + sum w_i y_i),
+ * the same arithmetic as tf_layer_step. Nothing waits on the host: the call
+ * only enqueues (its `step` is counted on the device), unless measure = 1,
+ * which synchronises to fill stats (hits, misses, bytes of this call; the
+ * shared-branch and copy times, and the stall of the routed experts beyond the
+ * shared branch). stats may be NULL.
+ */
+tf_status tf_layer_step_device_cache(tf_layer* l, tf_device_cache* c, int layer, const void* x, void* out,
+                                     const float* logit_bias, int bias_stride, void* compute_stream,
+                                     void* fetch_stream, int measure, tf_step_stats* stats);
 
 /*
  * A decode step through L resident layers for one token: x_{l+1} = layer_l(x_l),
@@ -438,7 +516,7 @@ enum {
     TF_KERNEL_DOWN = 2,        /* down GEMV + weighted combine */
     TF_KERNEL_LAYER = 3,       /* fused persistent decode-layer kernel */
     TF_KERNEL_PERMUTE = 4,     /* token x expert histogram / scan / permute */
-    TF_KERNEL_GEMM = 5,        /* grouped dequant-to-bf16 tensor-core GEMM */
+    TF_KERNEL_GEMM = 5,        /* grouped dequant-to-16-bit tensor-core GEMM */
     TF_KERNEL_COMBINE = 6,     /* unpermute-combine */
     TF_KERNEL_OTHER = 7,
     TF_KERNEL_COUNT = 8
@@ -455,6 +533,19 @@ tf_status tf_profile_end(double* ms, int64_t* launches);
  * n = 0 disarms. Used to test the roll-back of admitted cache slots.
  */
 tf_status tf_test_fail_nth_copy(int n);
+
+/*
+ * Limit of the device-side waits on other warps, roles or CTAs in the fused
+ * decode kernel (tf_stack_step) and the grouped GEMMs (tf_moe_ffn_grouped, the
+ * batched tf_layer_step), for launches enqueued from now on; 0 restores the
+ * default of 2 s. A test shortens it to a few ns so that those waits run out
+ * without any fault: the kernels record TF_ERR_TIMEOUT (tf_stack_check reports
+ * it and resets the stack; the grouped outputs become NaN) and return. Waits of
+ * a warp for its own copies and MMAs keep their fixed 2 s bound and ignore the
+ * failure, so that no kernel leaves while data is still landing in its shared
+ * memory or TMEM.
+ */
+tf_status tf_test_set_wait_limit_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

@@ -3,9 +3,10 @@ CPU oracle, through the C ABI.
 
 T tokens go through the router, the grouped routed experts and the bf16 shared
 expert, both on the tcgen05 GEMM kernel. The oracle is the per-token decode
-layer with the shared expert, in its bf16-operand reading (n, every weight and
-h rounded to bf16, fp32 accumulation) and in its plain fp32 reading (the
-contract). Checked per token: the RMS scale, the router logits and top-k ids
+layer with the shared expert, in its tensor-core reading (x fed as it is with
+the RMS scale applied after the gate/up sums; fp16 weights and h for the routed
+experts, bf16 h for the shared expert; fp32 accumulation) and in its plain fp32
+reading (the contract). Checked per token: the RMS scale, the router logits and top-k ids
 bit for bit, the weights to a few ulp, and the output and its update within
 the contract tolerance against both readings. The layer step exposes no fp32
 update, so the update is out - x, allowed the bf16 output's own rounding
@@ -61,7 +62,7 @@ def _check(seed, cfg, st, x_bits, out_bits, route, tokens):
             if int(e) not in cache:
                 cache[int(e)] = W.expert(seed, 0, int(e), H, I)
         ex = [cache[int(e)] for e in idx]
-        out_o, delta_o = O.layer_combine(x_bits[t], r, ex, w, shared, bf16_ops=True)
+        out_o, delta_o = O.layer_combine(x_bits[t], r, ex, w, shared, tc=True)
         got = bf16_to_f64(out_bits[t])
         assert not np.isnan(got).any(), t
         assert max_rel_err(got, bf16_to_f64(out_o)) <= CONTRACT_TOL, t
@@ -70,7 +71,7 @@ def _check(seed, cfg, st, x_bits, out_bits, route, tokens):
         worst = max(worst, err)
         # the contract as written: the bf16 tensor-core path against the plain fp32 oracle (the bf16 output
         # against the oracle's exact x + delta, allowing the output's own rounding to bf16)
-        _, delta_f = O.layer_combine(x_bits[t], r, ex, w, shared, bf16_ops=False)
+        _, delta_f = O.layer_combine(x_bits[t], r, ex, w, shared, tc=False)
         err_fo = out_rel_err(out_bits[t], x_bits[t], delta_f)
         assert err_fo <= CONTRACT_TOL, (t, err_fo)
         err_f = delta_rel_err(out_bits[t], x_bits[t], delta_f)

@@ -98,7 +98,7 @@ def test_dequant_expert_bitexact(H, I):
     for m, name in enumerate(("gate", "up", "down")):
         R, K = ex[name][0].shape
         want = O.dequant_matrix(*ex[name])
-        want_bf = O.dequant_matrix(*ex[name], bf16_ops=True)
+        want_bf = O.dequant_matrix(*ex[name], fmt="bf16")
         out = nan_f32(R, K)
         B.tf_dequant_expert(d_blob, H, I, m, 0, out)
         out_bf = nan_bf16(R, K)
@@ -107,6 +107,13 @@ def test_dequant_expert_bitexact(H, I):
         assert np.array_equal(f32_bits(out), want.view(np.uint32)), name
         got_bf = bf16_to_f64(bf16_bits(out_bf)).astype(np.float32)
         assert np.array_equal(got_bf.view(np.uint32), want_bf.astype(np.float32).view(np.uint32)), name
+        # fp16: the operand of the grouped tensor-core GEMMs
+        want_h = O.dequant_matrix(*ex[name], fmt="fp16")
+        out_h = torch.full((R, K), float("nan"), dtype=torch.float16, device=DEV)
+        B.tf_dequant_expert(d_blob, H, I, m, 2, out_h)
+        torch.cuda.synchronize()
+        got_h = out_h.cpu().numpy().astype(np.float32)
+        assert np.array_equal(got_h.view(np.uint32), want_h.astype(np.float32).view(np.uint32)), name
 
 
 # --------------------------------------------------------------- decode FFN

@@ -2,10 +2,10 @@
 tf_moe_ffn_grouped, against the CPU oracle, through the C ABI.
 
 The oracle is the per-token decode layer, looped over tokens, in two readings:
-its dequant-to-bf16 reading (n, every dequantised weight and h rounded to
-bf16, fp32 accumulation; the kernel's own roundings) and its plain fp32
-reading (the contract: the bf16 tensor-core path within 1e-2 of the fp32
-oracle). Checked:
+its tensor-core reading (x fed as it is, the RMS scale applied after the
+gate/up sums, every dequantised weight and h rounded to fp16, fp32
+accumulation; the kernel's own roundings) and its plain fp32 reading (the
+contract: the tensor-core path within 1e-2 of the fp32 oracle). Checked:
   - the permutation and the per-expert counts exactly (a stable sort by expert
     of the (token, rank) pairs, and the histogram of the ids);
   - every token's output and update within the contract tolerance, on all
@@ -70,7 +70,7 @@ def _check_permutation(idx, perm, counts, E):
 
 
 def _check_tokens(seed, x_bits, idx, w, out_bits, delta, tokens, H, I, worst_fp32=None):
-    """Per token: output and update within the contract against the oracle's bf16-operand reading and
+    """Per token: output and update within the contract against the oracle's tensor-core reading and
     against its plain fp32 reading; returns the worst update error of the former (worst_fp32[0] gets the
     worst of the latter)."""
     worst_fp32 = worst_fp32 if worst_fp32 is not None else [0.0]
@@ -84,8 +84,8 @@ def _check_tokens(seed, x_bits, idx, w, out_bits, delta, tokens, H, I, worst_fp3
         ex = [cache[int(e)] for e in idx[t]]
         got_o = bf16_to_f64(out_bits[t])
         assert not np.isnan(got_o).any() and not np.isnan(delta[t]).any(), t
-        # the bf16-operand reading (the kernel's own roundings): tight
-        out_o, delta_o = O.layer_combine(x_bits[t], r, ex, w[t], None, bf16_ops=True)
+        # the tensor-core reading (the kernel's own roundings): tight
+        out_o, delta_o = O.layer_combine(x_bits[t], r, ex, w[t], None, tc=True)
         e_out = max_rel_err(got_o, bf16_to_f64(out_o))
         e_delta = max_rel_err(delta[t], delta_o)
         assert e_out <= CONTRACT_TOL, (t, e_out)
@@ -93,7 +93,7 @@ def _check_tokens(seed, x_bits, idx, w, out_bits, delta, tokens, H, I, worst_fp3
         worst = max(worst, e_delta)
         # the contract as written: the bf16 tensor-core path against the plain fp32 oracle (the bf16 output
         # against the oracle's exact x + delta, allowing the output's own rounding to bf16)
-        _, delta_f = O.layer_combine(x_bits[t], r, ex, w[t], None, bf16_ops=False)
+        _, delta_f = O.layer_combine(x_bits[t], r, ex, w[t], None, tc=False)
         e_f = max_rel_err(delta[t], delta_f)
         assert e_f <= CONTRACT_TOL, (t, e_f)
         e_fo = out_rel_err(out_bits[t], x_bits[t], delta_f)
@@ -163,3 +163,19 @@ def test_grouped_is_deterministic_and_token_order_equivariant():
     out3, d3, _, _ = _run(x[torch.from_numpy(order).to(DEV)].contiguous(), idx[order], w[order], d_exp, slot, E, k, H,
                           I)
     assert np.max(np.abs(bf16_to_f64(out3) - bf16_to_f64(out1[order]))) == 0.0
+
+
+def test_grouped_inputs_beyond_fp16_range():
+    """Hidden states far beyond the fp16 range (x scaled by 2^16, up to about 3e5): the fp16 operand is x times
+    the power of two of its RMS scale, so the outputs stay finite and within the contract of both readings."""
+    H, I, E, k, T, seed = 512, 256, 16, 4, 24, 37
+    d_exp, slot = _experts_device(seed, E, H, I)
+    x = hidden_tensor(seed, 0, T, H) * 65536.0
+    x_bits = bf16_bits(x)
+    assert np.max(np.abs(bf16_to_f64(x_bits))) > 65504.0
+    idx, w = _routing(seed, T, E, k, 0.0)
+    out, delta, perm, counts = _run(x, idx, w, d_exp, slot, E, k, H, I)
+    _check_permutation(idx, perm, counts, E)
+    worst_fp32 = [0.0]
+    worst = _check_tokens(seed, x_bits, idx, w, out, delta, range(T), H, I, worst_fp32)
+    assert worst < 5e-3 and worst_fp32[0] < CONTRACT_TOL
