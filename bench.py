@@ -77,7 +77,10 @@ set_layers(L)
 # 4-layer stack of the same kernel, scaled by 30/4 to the 30-layer launch. Reported only while the kernel's code
 # (its source and the headers it includes, without // comments and blank lines, plus the nvcc flags) is the one
 # that was captured; null otherwise.
-FUSED_TRAFFIC = {"code_sha256": None, "bytes_per_layer": None, "capture": None}
+FUSED_TRAFFIC = {"code_sha256": "d385345b58fb32d6fc13e8f8b0534573cad532eb5a1926794d085266b289f6d4",
+                 "bytes_per_layer": (252827136 + 2995968) / 4,
+                 "capture": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch of a 4-layer stack "
+                            "(profiles/k_fused_stack_decode30.md)"}
 FUSED_SOURCES = ("tf_fused.cu", "tf_device.cuh", "tf_internal.h")
 
 
@@ -1026,7 +1029,10 @@ def main():
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind + " (hbm_gbs)",
                      "bytes_per_launch": BYTES[dom],
-                     "traffic": fused_traffic(L) if (dom == "layer" and args.path == "fused") else None},
+                     "traffic": fused_traffic(L) if (dom == "layer" and args.path == "fused") else None,
+                     "traffic_source": "not measured in this run: ncu DRAM read + write bytes of one launch of this "
+                                       "kernel's code on a 4-layer stack, scaled by L / 4 (null once the code "
+                                       "changes)"},
         "kernels": per_kernel,
         "step_time": spread(step_ms),
         "gpu_launches": int(launches),
