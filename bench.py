@@ -355,6 +355,7 @@ def run_ours(args, rank, world):
 # ------------------------------------------------------------------ streamed experts (LFU cache, host store)
 
 STREAM_SEED, STREAM_ZIPF, STREAM_SLOTS = 2, 1.1, 16
+PREFILL_CHUNK, PREFILL_PROMPT = 128, 512     # chunked prefill through the cache: tokens per chunk, per prompt
 STREAM_ALPHA = 0.1     # Zipf bias scale
 STREAM_NOISE = 1.5     # sigma of the per-(step, layer) router-logit noise (the token-dependent part of the logits)
 STREAM_METRIC = "MoE decode tok/s with experts streamed from pinned host memory through a 16-slot LFU cache (1 B300)"
@@ -402,7 +403,8 @@ def run_streaming(args):
     seed, alpha, sigma = STREAM_SEED, args.alpha, args.noise
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    stack = SyntheticStack(seed, L, H=H, I=I, E=E, k=K_ACT, S=S, resident=False, n_slots=STREAM_SLOTS, device=dev)
+    stack = SyntheticStack(seed, L, H=H, I=I, E=E, k=K_ACT, S=S, resident=False, n_slots=STREAM_SLOTS,
+                           T_max=PREFILL_CHUNK, device=dev)
     zipf_h = np.stack([W.zipf_bias(seed, l, E, STREAM_ZIPF, alpha)[0] for l in range(L)])
     bias_h = torch.empty(L, E, dtype=torch.float32, pin_memory=True)
     bias_hn = bias_h.numpy()
@@ -559,6 +561,48 @@ def run_streaming(args):
                           "bytes_fetched_per_token": int(ts["bytes"] / args.steps),
                           "slot_pool_gb": round(L * n_slots * stack.slot / 1e9, 2)})
         c.close()
+    # chunked prefill through the cache (host metadata, a fresh cache): a prompt of PREFILL_PROMPT fresh tokens in
+    # chunks of PREFILL_CHUNK, each chunk through the 30 layers, the chunk's experts in waves of the 16 slots;
+    # router bias: the layers' Zipf popularity term
+    chunked = None
+    if not args.no_chunked_prefill:
+        pc = B.ExpertCache(L, STREAM_SLOTS, E, stack.slot, stack.pool)
+        bias_d.copy_(torch.from_numpy(zipf_h.astype(np.float32)))
+        prompt = hidden_tensor(seed, 1 << 20, PREFILL_PROMPT + PREFILL_CHUNK, H, device=dev)
+        cb = [torch.empty(PREFILL_CHUNK, H, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        lstep = [0] * L
+        tot_c = {"waves": 0, "hits": 0, "misses": 0, "bytes": 0}
+
+        def chunk(xc):
+            cur = xc
+            for l in range(L):
+                dst = cb[l % 2]
+                stc = B.tf_layer_prefill_cached(stack.layers[l], pc, l, lstep[l], stack.store, cur, dst, PREFILL_CHUNK,
+                                                bias_d[l], 0, stream, copy_streams[0])
+                lstep[l] += stc.waves
+                for k_, f in (("waves", "waves"), ("hits", "hits"), ("misses", "misses"), ("bytes", "bytes_fetched")):
+                    tot_c[k_] += getattr(stc, f)
+                cur = dst
+        chunk(prompt[PREFILL_PROMPT:])          # warm-up chunk (also fills the cache from cold)
+        torch.cuda.synchronize()
+        for k_ in tot_c:
+            tot_c[k_] = 0
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for ci in range(PREFILL_PROMPT // PREFILL_CHUNK):
+            chunk(prompt[ci * PREFILL_CHUNK:(ci + 1) * PREFILL_CHUNK])
+        c1.record(stream)
+        torch.cuda.synchronize()
+        cms = c0.elapsed_time(c1)
+        lookups_c = tot_c["hits"] + tot_c["misses"]
+        chunked = {"tokens": PREFILL_PROMPT, "chunk": PREFILL_CHUNK, "tok_s": round(PREFILL_PROMPT / (cms / 1000.0), 1),
+                   "ms_per_chunk": round(cms / (PREFILL_PROMPT // PREFILL_CHUNK), 3),
+                   "hit_rate": round(tot_c["hits"] / max(1, lookups_c), 4),
+                   "bytes_fetched_per_token": int(tot_c["bytes"] / PREFILL_PROMPT),
+                   "waves_per_chunk_layer": round(tot_c["waves"] / (L * (PREFILL_PROMPT // PREFILL_CHUNK)), 2),
+                   "fill_gbs": round(tot_c["bytes"] / (cms / 1000.0) / 1e9, 2)}
+        pc.close()
+
     # fetch-kernel width (device-metadata mode, 16 slots)
     fetch_sweep = []
     for ctas in [int(v) for v in args.fetch_sweep.split(",") if v.strip()]:
@@ -603,6 +647,8 @@ def run_streaming(args):
         line["slot_sweep"] = sweep_out
     if fetch_sweep:
         line["fetch_sweep"] = fetch_sweep
+    if chunked:
+        line["chunked_prefill"] = chunked
     line["host"] = host_info()
     if not args.no_cpu_baseline:
         base = oracle_baseline(args.oracle_layers)
@@ -957,6 +1003,8 @@ def main():
                     help="streaming: also measure these slot counts per layer, e.g. 8,32,64")
     ap.add_argument("--fetch-ctas", type=int, default=32,
                     help="streaming: CTAs of the kernel that copies missing experts from the host store")
+    ap.add_argument("--no-chunked-prefill", action="store_true",
+                    help="streaming: skip the chunked prefill through the cache")
     ap.add_argument("--fetch-sweep", default="",
                     help="streaming: also measure these fetch-kernel widths, e.g. 8,16,64")
     ap.add_argument("--noise", type=float, default=STREAM_NOISE,

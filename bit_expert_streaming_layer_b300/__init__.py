@@ -52,6 +52,11 @@ class StepStats(ctypes.Structure):
                 ("ids", ctypes.c_int32 * TF_MAX_K)]
 
 
+class PrefillStats(ctypes.Structure):
+    _fields_ = [("waves", ctypes.c_int32), ("hits", ctypes.c_int32), ("misses", ctypes.c_int32),
+                ("bytes_fetched", ctypes.c_uint64)]
+
+
 # exported symbols and their C signatures (restype, argtypes)
 _vp, _i32, _i64, _sz, _f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
 _S = ctypes.c_int32
@@ -98,6 +103,8 @@ SIGNATURES = {
                               ctypes.POINTER(_vp)]),
     "tf_layer_step": (_S, [_vp, _vp, _i32, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _vp, _i32,
                            ctypes.POINTER(StepStats)]),
+    "tf_layer_prefill_cached": (_S, [_vp, _vp, _i32, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _vp,
+                                     ctypes.POINTER(PrefillStats)]),
     "tf_stack_decode": (_S, [ctypes.POINTER(_vp), _i32, _vp, _vp, _vp, ctypes.POINTER(_vp), _vp]),
     "tf_stack_workspace_bytes": (_sz, [_i32, _i32]),
     "tf_stack_create": (_S, [ctypes.POINTER(_vp), _i32, ctypes.POINTER(_vp), _vp, _sz, ctypes.POINTER(_vp)]),
@@ -451,6 +458,17 @@ def tf_layer_step_device_cache(layer: Layer, cache: DeviceCache, layer_index: in
                                             _ptr(logit_bias), bias_stride, _stream(compute_stream),
                                             _stream(fetch_stream), measure, ctypes.byref(stats)),
            "tf_layer_step_device_cache")
+    return stats
+
+
+def tf_layer_prefill_cached(layer: Layer, cache: ExpertCache, layer_index: int, step0: int, h_expert_store, x, out,
+                            T: int, logit_bias=None, bias_stride: int = 0, compute_stream=None, copy_stream=None):
+    """A chunk of T tokens through one layer with its experts streamed through the LFU cache, in waves of the
+    cache's slot count; returns PrefillStats (waves, hits, misses, bytes_fetched)."""
+    stats = PrefillStats()
+    _check(lib().tf_layer_prefill_cached(layer.handle, cache.handle, layer_index, step0, _ptr(h_expert_store), _ptr(x),
+                                         _ptr(out), T, _ptr(logit_bias), bias_stride, _stream(compute_stream),
+                                         _stream(copy_stream), ctypes.byref(stats)), "tf_layer_prefill_cached")
     return stats
 
 

@@ -2,6 +2,7 @@
 // dequant export, layer handles, the (cached) layer step and the decode stack.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <cstring>
@@ -118,8 +119,10 @@ using namespace tf;
 namespace {
 
 struct LayerCarve {
-    size_t counters, logits, idx, w, rms, h_routed, h_shared, ys, grouped, grouped_bytes, total;
+    size_t counters, logits, idx, w, rms, h_routed, h_shared, ys, grouped, grouped_bytes, wave_maps, total;
 };
+
+int max_waves_of(const tf_layer_desc* d) { return (d->E + d->k - 1) / d->k; }
 
 LayerCarve layer_carve(const tf_layer_desc* d, int T_max) {
     LayerCarve c;
@@ -136,6 +139,8 @@ LayerCarve layer_carve(const tf_layer_desc* d, int T_max) {
     c.grouped = o;
     c.grouped_bytes = T_max > 1 ? grouped_workspace_bytes(T_max, d->H, d->I, d->E, d->k, d->S) : 0;
     o += align_up(c.grouped_bytes, 256);
+    c.wave_maps = o;   // chunked prefill through a cache: per wave the experts' mask and slot map
+    o += T_max > 1 ? align_up((size_t)max_waves_of(d) * 2 * d->E * 4, 256) : 0;
     c.total = o;
     return c;
 }
@@ -384,11 +389,20 @@ tf_status tf_layer_create(const tf_layer_desc* d, int T_max, void* workspace, si
     l->grouped_ws = c.grouped_bytes ? l->ws + c.grouped : nullptr;
     l->grouped_bytes = c.grouped_bytes;
     cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&l->h_idx), TF_MAX_K * sizeof(int32_t), cudaHostAllocDefault);
+    if (e == cudaSuccess && T_max > 1) {
+        l->max_waves = max_waves_of(d);
+        l->d_wave_maps = reinterpret_cast<int32_t*>(l->ws + c.wave_maps);
+        e = cudaHostAlloc(reinterpret_cast<void**>(&l->h_chunk_ids), (size_t)T_max * d->k * sizeof(int32_t),
+                          cudaHostAllocDefault);
+        if (e == cudaSuccess)
+            e = cudaHostAlloc(reinterpret_cast<void**>(&l->h_wave_maps),
+                              (size_t)l->max_waves * 2 * d->E * sizeof(int32_t), cudaHostAllocDefault);
+    }
     if (e != cudaSuccess) {
-        delete l;
+        tf_layer_destroy(l);
         return fail(TF_ERR_OOM, "%s: pinned staging: %s", fn, cudaGetErrorString(e));
     }
-    cudaEvent_t* evs[] = {&l->ev_idx, &l->ev_copies, &l->ev_t0, &l->ev_shared, &l->ev_c0};
+    cudaEvent_t* evs[] = {&l->ev_idx, &l->ev_copies, &l->ev_t0, &l->ev_shared, &l->ev_c0, &l->ev_wave};
     for (cudaEvent_t* ev : evs) {
         e = cudaEventCreate(ev);
         if (e != cudaSuccess) {
@@ -402,10 +416,12 @@ tf_status tf_layer_create(const tf_layer_desc* d, int T_max, void* workspace, si
 
 tf_status tf_layer_destroy(tf_layer* l) {
     if (!l) return TF_OK;
-    cudaEvent_t evs[] = {l->ev_idx, l->ev_copies, l->ev_t0, l->ev_shared, l->ev_c0};
+    cudaEvent_t evs[] = {l->ev_idx, l->ev_copies, l->ev_t0, l->ev_shared, l->ev_c0, l->ev_wave};
     for (cudaEvent_t ev : evs)
         if (ev) cudaEventDestroy(ev);
     if (l->h_idx) cudaFreeHost(l->h_idx);
+    if (l->h_chunk_ids) cudaFreeHost(l->h_chunk_ids);
+    if (l->h_wave_maps) cudaFreeHost(l->h_wave_maps);
     delete l;
     return TF_OK;
 }
@@ -648,6 +664,169 @@ tf_status tf_expert_cache_set_copy_streams(tf_expert_cache* c, void* const* stre
     c->copy_streams.clear();
     for (int j = 0; j < n; ++j) c->copy_streams.push_back(static_cast<cudaStream_t>(streams[j]));
     return TF_OK;
+}
+
+namespace {
+
+// One chunk's waves through the host-metadata cache (tf_layer_prefill_cached).
+struct PrefillWaves {
+    tf_layer* l;
+    tf_expert_cache* c;
+    int layer;
+    int64_t step0;
+    const char* store;
+    cudaStream_t cs, ps;
+    std::vector<std::vector<int32_t>> waves;
+    int hits = 0, misses = 0;
+    uint64_t bytes = 0;
+};
+
+// Before wave w: the copy stream waits until the earlier waves' GEMMs are done with the slots, the wave's
+// lookups and admissions (one LFU step, the wave's experts pinned), one copy per miss, the compute stream
+// waits for the copies; the wave's mask and slot map go to the pinned staging row w.
+int prefill_before_wave(void* ctx, int w, void* stream) {
+    PrefillWaves& P = *static_cast<PrefillWaves*>(ctx);
+    const char* fn = "tf_layer_prefill_cached";
+    tf_layer* l = P.l;
+    tf_expert_cache* c = P.c;
+    const int E = l->d.E;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (cudaError_t e = cudaEventRecord(l->ev_wave, cs)) return cuda_status(e, fn);
+    if (cudaError_t e = cudaStreamWaitEvent(P.ps, l->ev_wave, 0)) return cuda_status(e, fn);
+    const std::vector<int32_t>& ids = P.waves[w];
+    const int n = (int)ids.size();
+    const int64_t step = P.step0 + w;
+    std::vector<int32_t> slot((size_t)n);
+    std::vector<uint8_t> hit((size_t)n);
+    if (tf_status s = tf_expert_cache_lookup(c, P.layer, step, ids.data(), n, slot.data(), hit.data())) return s;
+    std::vector<int32_t> admitted;
+    char* pool = static_cast<char*>(c->d_slot_pool);
+    for (int i = 0; i < n; ++i) {
+        if (hit[i]) continue;
+        int32_t s = -1, evicted = -1;
+        tf_status st = tf_expert_cache_admit(c, P.layer, step, ids[i], ids.data(), n, &s, &evicted);
+        int e = 0;
+        if (st == TF_OK) {
+            slot[i] = s;
+            admitted.push_back(s);
+            char* dst = pool + ((size_t)P.layer * c->n_slots + s) * c->slot_bytes;
+            const char* src = P.store + ((size_t)P.layer * E + ids[i]) * c->slot_bytes;
+            if (g_copy_countdown > 0 && --g_copy_countdown == 0)
+                e = (int)cudaErrorInvalidValue;  // injected failure: the copy is not enqueued
+            else
+                e = (int)cudaMemcpyAsync(dst, src, l->lay.payload, cudaMemcpyHostToDevice, P.ps);
+            if (e) st = cuda_status(e, "tf_layer_prefill_cached: expert copy");
+            P.bytes += l->lay.payload;
+            ++P.misses;
+        }
+        if (st != TF_OK) {
+            for (int32_t a : admitted) tf_expert_cache_invalidate(c, P.layer, a);
+            std::string msg = tf_last_error();
+            return fail(st, "%s: miss fill failed, %zu admitted slot(s) of wave %d rolled back: %s", fn,
+                        admitted.size(), w, msg.c_str());
+        }
+    }
+    P.hits += n - (int)admitted.size();
+    int32_t* mask = l->h_wave_maps + (size_t)w * 2 * E;
+    int32_t* smap = mask + E;
+    for (int e2 = 0; e2 < E; ++e2) {
+        mask[e2] = 0;
+        smap[e2] = -1;
+    }
+    for (int i = 0; i < n; ++i) {
+        mask[ids[i]] = 1;
+        smap[ids[i]] = slot[i];
+    }
+    if (cudaError_t e = cudaEventRecord(l->ev_copies, P.ps)) return cuda_status(e, fn);
+    if (cudaError_t e = cudaStreamWaitEvent(cs, l->ev_copies, 0)) return cuda_status(e, fn);
+    return TF_OK;
+}
+
+}  // namespace
+
+tf_status tf_layer_prefill_cached(tf_layer* l, tf_expert_cache* c, int layer, int64_t step0, const void* h_expert_store,
+                                  const void* x, void* out, int T, const float* logit_bias, int bias_stride,
+                                  void* compute_stream, void* copy_stream, tf_prefill_stats* stats) {
+    const char* fn = "tf_layer_prefill_cached";
+    if (!l || !c || !h_expert_store || !x || !out || !copy_stream) return fail(TF_ERR_INVALID_ARG, "%s: null argument", fn);
+    const tf_layer_desc& d = l->d;
+    if (l->T_max < 2 || !l->h_chunk_ids) return fail(TF_ERR_INVALID_ARG, "%s: the layer handle needs T_max > 1", fn);
+    if (T < 1 || T > l->T_max) return fail(TF_ERR_INVALID_ARG, "%s: T=%d outside [1, %d]", fn, T, l->T_max);
+    if (layer < 0 || layer >= c->n_layers) return fail(TF_ERR_INVALID_ARG, "%s: bad layer %d", fn, layer);
+    if (!c->d_slot_pool || c->n_experts != d.E || c->slot_bytes < l->lay.payload || c->n_slots < d.k ||
+        c->slot_bytes % 16)
+        return fail(TF_ERR_INVALID_ARG, "%s: cache does not match the layer (pool, E, slot size or slot count)", fn);
+    if (logit_bias && bias_stride != 0 && bias_stride != d.E)
+        return fail(TF_ERR_INVALID_ARG, "%s: bias_stride must be 0 or E", fn);
+    if (stats) std::memset(stats, 0, sizeof(*stats));
+    clear_error();
+    cudaStream_t cs = static_cast<cudaStream_t>(compute_stream), ps = static_cast<cudaStream_t>(copy_stream);
+    const int k = d.k;
+    int e = launch_router_topk(static_cast<const uint16_t*>(x), T, d.H, static_cast<const uint16_t*>(d.W_r), d.E,
+                               logit_bias, bias_stride, k, l->idx, l->w, l->logits, l->rms, l->counters, d.eps, cs);
+    if (!e) e = cudaMemcpyAsync(l->h_chunk_ids, l->idx, (size_t)T * k * 4, cudaMemcpyDeviceToHost, cs);
+    if (!e) e = cudaEventRecord(l->ev_idx, cs);
+    if (!e) e = cudaEventSynchronize(l->ev_idx);   // the one host wait: the CPU decides the waves and the copies
+    if (e) return cuda_status(e, fn);
+    // the chunk's distinct experts in order of first use, in waves of n_slots
+    PrefillWaves P;
+    P.l = l;
+    P.c = c;
+    P.layer = layer;
+    P.step0 = step0;
+    P.store = static_cast<const char*>(h_expert_store);
+    P.cs = cs;
+    P.ps = ps;
+    std::vector<char> seen((size_t)d.E, 0);
+    std::vector<int32_t> order;
+    for (int i = 0; i < T * k; ++i) {
+        const int32_t id = l->h_chunk_ids[i];
+        if ((unsigned)id >= (unsigned)d.E) return fail(TF_ERR_CUDA, "%s: router id %d out of range", fn, id);
+        if (!seen[id]) {
+            seen[id] = 1;
+            order.push_back(id);
+        }
+    }
+    for (size_t i = 0; i < order.size(); i += (size_t)c->n_slots)
+        P.waves.emplace_back(order.begin() + i, order.begin() + std::min(order.size(), i + (size_t)c->n_slots));
+    if ((int)P.waves.size() > l->max_waves) return fail(TF_ERR_INVALID_ARG, "%s: too many waves", fn);
+    GroupedWaves wv;
+    wv.n = (int)P.waves.size();
+    wv.pool = static_cast<const char*>(c->d_slot_pool) + (size_t)layer * c->n_slots * c->slot_bytes;
+    wv.slot_bytes = c->slot_bytes;
+    wv.n_slots = c->n_slots;
+    wv.d_maps = l->d_wave_maps;
+    wv.h_maps = l->h_wave_maps;
+    wv.before_wave = prefill_before_wave;
+    wv.ctx = &P;
+    GroupedArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.x = x;
+    a.out = out;
+    a.T = T;
+    a.table = nullptr;
+    a.E = d.E;
+    a.k = k;
+    a.H = d.H;
+    a.I = d.I;
+    a.idx = l->idx;
+    a.w = l->w;
+    a.Wsg = d.W_sg;
+    a.Wsu = d.W_su;
+    a.Wsd = d.W_sd;
+    a.S = d.S;
+    a.eps = d.eps;
+    a.ws = l->grouped_ws;
+    a.ws_bytes = l->grouped_bytes;
+    a.waves = &wv;
+    tf_status st = grouped_run(a, cs, fn);
+    if (stats) {
+        stats->waves = wv.n;
+        stats->hits = P.hits;
+        stats->misses = P.misses;
+        stats->bytes_fetched = P.bytes;
+    }
+    return st;
 }
 
 tf_status tf_stack_decode(tf_layer* const* layers, int L, const void* x, void* out, void* scratch,

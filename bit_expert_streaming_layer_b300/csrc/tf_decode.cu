@@ -120,6 +120,7 @@ k_router_topk(const uint16_t* __restrict__ x, int H, const uint16_t* __restrict_
 constexpr int RTT_THREADS = 256;
 constexpr int RTT_TOKENS = RTT_THREADS / 4;   // tokens in flight per CTA (one per quad)
 constexpr int RTT_SMEM_MAX = 227 * 1024;      // the expert block of W_r as fp32 (TE * H * 4 bytes) fits this
+constexpr int RTT_AHEAD = 8;                  // loads of x in flight per thread
 
 __device__ __forceinline__ unsigned long long rt_pk2(float lo, float hi) {
     unsigned long long r;
@@ -180,24 +181,38 @@ k_router_tiled(const uint16_t* __restrict__ x, int T, int H, const uint16_t* __r
 #pragma unroll
             for (int e = 0; e < TE; ++e) acc[e][p] = 0ull;
         }
-#pragma unroll 2
-        for (int j = 0; j < H / 32; ++j) {
-            const uint4 xv = __ldg(xr + 4 * j + m);   // k = 32 j + 8 m .. 32 j + 8 m + 7
-            const unsigned long long x01 = rt_pk2(bf_lo(xv.x), bf_hi(xv.x)), x23 = rt_pk2(bf_lo(xv.y), bf_hi(xv.y));
-            const unsigned long long x45 = rt_pk2(bf_lo(xv.z), bf_hi(xv.z)), x67 = rt_pk2(bf_lo(xv.w), bf_hi(xv.w));
-            rt_fma2(sq[0], x01, x01);
-            rt_fma2(sq[1], x23, x23);
-            rt_fma2(sq[2], x45, x45);
-            rt_fma2(sq[3], x67, x67);
-            const float* wk = wsm + 32 * j + 8 * m;
+        // eight loads of x in flight ahead of the products (a register ring with fixed indices), so that their
+        // latency overlaps the products of the previous steps
+        const int nj = H / 32;
+        uint4 ring[RTT_AHEAD];
 #pragma unroll
-            for (int e = 0; e < TE; ++e) {
-                const float4 wa = *reinterpret_cast<const float4*>(wk + (size_t)e * H);
-                const float4 wb = *reinterpret_cast<const float4*>(wk + (size_t)e * H + 4);
-                rt_fma2(acc[e][0], rt_pk2(wa.x, wa.y), x01);
-                rt_fma2(acc[e][1], rt_pk2(wa.z, wa.w), x23);
-                rt_fma2(acc[e][2], rt_pk2(wb.x, wb.y), x45);
-                rt_fma2(acc[e][3], rt_pk2(wb.z, wb.w), x67);
+        for (int a = 0; a < RTT_AHEAD; ++a) ring[a] = a < nj ? __ldg(xr + 4 * a + m) : make_uint4(0u, 0u, 0u, 0u);
+        for (int j0 = 0; j0 < nj; j0 += RTT_AHEAD) {
+#pragma unroll
+            for (int a = 0; a < RTT_AHEAD; ++a) {
+                const int j = j0 + a;
+                if (j < nj) {
+                    const uint4 xv = ring[a];   // k = 32 j + 8 m .. 32 j + 8 m + 7
+                    if (j + RTT_AHEAD < nj) ring[a] = __ldg(xr + 4 * (j + RTT_AHEAD) + m);
+                    const unsigned long long x01 = rt_pk2(bf_lo(xv.x), bf_hi(xv.x));
+                    const unsigned long long x23 = rt_pk2(bf_lo(xv.y), bf_hi(xv.y));
+                    const unsigned long long x45 = rt_pk2(bf_lo(xv.z), bf_hi(xv.z));
+                    const unsigned long long x67 = rt_pk2(bf_lo(xv.w), bf_hi(xv.w));
+                    rt_fma2(sq[0], x01, x01);
+                    rt_fma2(sq[1], x23, x23);
+                    rt_fma2(sq[2], x45, x45);
+                    rt_fma2(sq[3], x67, x67);
+                    const float* wk = wsm + 32 * j + 8 * m;
+#pragma unroll
+                    for (int e = 0; e < TE; ++e) {
+                        const float4 wa = *reinterpret_cast<const float4*>(wk + (size_t)e * H);
+                        const float4 wb = *reinterpret_cast<const float4*>(wk + (size_t)e * H + 4);
+                        rt_fma2(acc[e][0], rt_pk2(wa.x, wa.y), x01);
+                        rt_fma2(acc[e][1], rt_pk2(wa.z, wa.w), x23);
+                        rt_fma2(acc[e][2], rt_pk2(wb.x, wb.y), x45);
+                        rt_fma2(acc[e][3], rt_pk2(wb.z, wb.w), x67);
+                    }
+                }
             }
         }
         const float ss = quad_canonical(sq);

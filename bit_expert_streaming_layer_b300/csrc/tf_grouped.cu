@@ -14,12 +14,17 @@
 // dequantised from int4 to bf16 in shared memory), the tokens are the N side
 // (up to 256 per tile, loaded by TMA). D[m, n] = sum_k W[m, k] X[n, k] lives in
 // TMEM as 128 lanes x N fp32 columns; two accumulators let the epilogue of one
-// tile overlap the MMAs of the next. Warp roles in a 512-thread CTA:
-//   warp 0      TMA producer: int4 codes (3-D tensor map over all experts),
-//               scales/biases (bulk copy), token rows (2-D tensor map, SW128)
+// tile overlap the MMAs of the next. Warp roles in a 768-thread CTA:
+//   warp 0      TMA producer of the weights: int4 codes (3-D tensor map over all
+//               experts, 128 bytes of each of 128 rows per copy = 4 K stages,
+//               128-byte swizzled) and scales/biases (bulk copy per tile)
 //   warp 1      TMEM owner; lane 0 issues tcgen05.mma and tcgen05.commit
+//   warp 2      TMA producer of the token rows (2-D tensor map, SW128)
 //   warps 4..7  epilogue: tcgen05.ld, GELU-gate (gate/up) or plain (down), store
-//   warps 8..15 dequant: codes -> bf16 = RN(s q + b) into the SW128 A tile
+//   warps 8..23 dequant, two groups of eight warps on alternate K stages:
+//               codes -> 16-bit RN(s q + b) into the SW128 A tile
+// Every ring (codes, A, tokens) is sized by the launch's shared-memory plan;
+// the weight producer runs ahead of the MMAs by as many code stages as fit.
 // Numerics: 16-bit operands, fp32 accumulation in TMEM. The token operand is
 // the layer input x itself and the RMS scale r of each token multiplies its
 // gate and up sums in the epilogue, as the router applies it after its dot
@@ -50,6 +55,7 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <type_traits>
 
 #include "tf_device.cuh"
 #include "tf_internal.h"
@@ -61,38 +67,47 @@ using namespace dev;
 
 constexpr int NB = 256;                // tokens per GEMM tile (MMA N <= 256)
 constexpr int BM = 128;                // weight rows per GEMM tile (MMA M)
-constexpr int BK = 64;                 // K per pipeline stage (one quant group, 128 bytes of bf16)
-constexpr int BOX_ROWS = 16;           // token rows per TMA box
-constexpr int NA = 3, NBST = 3, NCS = 4;
+constexpr int BK = 64;                 // K per pipeline stage (one quant group, 128 bytes of 16-bit values)
+constexpr int BOX_SMALL = 16;          // token rows per TMA box for tiles of up to 64 rows
+constexpr int BOX_BIG = 128;           // ... and for larger tiles (two loads per 256-row stage)
+constexpr int NBST = 3;                // token (B) stages
+constexpr int NA_MAX = 12, NCS_MAX = 8;    // weight (A) and code stages: as many as shared memory holds
+constexpr int CW = 4;                  // K stages per code stage: 128 contiguous bytes of each weight row per load
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB
-constexpr int B_BYTES = NB * BK * 2;             // 32 KB
-constexpr int C_BYTES = BM * BK / 2;             // 4 KB of codes per stage
+constexpr int C_BYTES = BM * BK * CW / 2;        // 16 KB of codes per code stage
 constexpr int SB_MAX = BM * (2816 / 64) * 4;     // 22,528 B of {s,b} per tile (K up to 2816)
-constexpr int GEMM_THREADS = 512;
-constexpr int N_DQ_WARPS = 8;
+constexpr int N_DQ_WARPS = 8;                  // warps of one dequant group: one weight row pair per thread pair
+constexpr int N_DQ_GROUPS = 2;                 // dequant groups, taking alternate K stages
+constexpr int GEMM_THREADS = (8 + N_DQ_GROUPS * N_DQ_WARPS) * 32;
 constexpr unsigned long long OWN_LIMIT_NS = 2000000000ull;   // waits for this thread's own copies and MMAs
-
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + NA * A_BYTES;
-constexpr int OFF_C = OFF_B + NBST * B_BYTES;
-constexpr int OFF_SB = OFF_C + NCS * C_BYTES;
-constexpr int OFF_BAR = OFF_SB + 2 * SB_MAX;
 enum {
-    BAR_CF = 0,                  // codes full [NCS]
-    BAR_CE = BAR_CF + NCS,       // codes empty [NCS]
-    BAR_AF = BAR_CE + NCS,       // A full [NA]
-    BAR_AE = BAR_AF + NA,        // A empty [NA]
-    BAR_BF = BAR_AE + NA,        // B full [NBST]
-    BAR_BE = BAR_BF + NBST,      // B empty [NBST]
-    BAR_SF = BAR_BE + NBST,      // sb full [2]
-    BAR_SE = BAR_SF + 2,         // sb empty [2]
-    BAR_DF = BAR_SE + 2,         // accumulator full [2]
-    BAR_DE = BAR_DF + 2,         // accumulator empty [2]
+    BAR_CF = 0,                      // codes full [NCS_MAX]
+    BAR_CE = BAR_CF + NCS_MAX,       // codes empty [NCS_MAX]
+    BAR_AF = BAR_CE + NCS_MAX,       // A full [NA_MAX]
+    BAR_AE = BAR_AF + NA_MAX,        // A empty [NA_MAX]
+    BAR_BF = BAR_AE + NA_MAX,        // B full [NBST]
+    BAR_BE = BAR_BF + NBST,          // B empty [NBST]
+    BAR_SF = BAR_BE + NBST,          // sb full [2]
+    BAR_SE = BAR_SF + 2,             // sb empty [2]
+    BAR_DF = BAR_SE + 2,             // accumulator full [2]
+    BAR_DE = BAR_DF + 2,             // accumulator empty [2]
     N_BARS = BAR_DE + 2
 };
-constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;   // tmem base, abort flag
-constexpr size_t GEMM_SMEM = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KB
-static_assert(OFF_B % 1024 == 0 && OFF_C % 1024 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "SW128 tiles");
+constexpr size_t GEMM_SMEM = 227 * 1024;                       // every launch takes a whole SM's shared memory
+constexpr int SMEM_USABLE = (int)GEMM_SMEM - 1024 - N_BARS * 8 - 16;   // after aligning the base to 1 KB
+static_assert(A_BYTES % 1024 == 0, "SW128 tiles");
+
+// Shared-memory plan of one launch (offsets from the 1 KB-aligned base). The
+// token stages are sized to the largest token tile the launch can see, and the
+// rest goes to the streamed operand: code stages (int4 weights, dequantised by
+// the CUDA cores) or weight stages (bf16 weights by TMA), so that enough bytes
+// are in flight per SM for small tiles too.
+struct Layout {
+    int na, ncs;        // A stages (3 when dequantised), code stages (0 for bf16 weights)
+    int b_stage;        // bytes of one token stage
+    int box_big;        // 1: tiles over 64 rows load 128-row boxes
+    int off_b, off_c, off_sb, off_bar;
+};
 
 struct GemmParams {
     const char* ebase;          // resident experts: expert e at ebase + e * estride
@@ -116,6 +131,8 @@ struct GemmParams {
     int ntok, mrows;
     const float* col_scale;     // gate/up: the RMS scale of each token row of the B operand (g, u *= it)
     int f16;                    // 1: fp16 operands (dequantised A and B), 0: bf16
+    const int32_t* slot_of;     // nullable [E]: expert e's weights are slot slot_of[e] of ebase (the cache's slots)
+    Layout lay;
     unsigned long long dep_limit_ns;   // limit of a wait on another role (2 s unless a test shortens it)
 };
 
@@ -256,6 +273,17 @@ __device__ bool wait_own(uint32_t bar, uint32_t parity, uint32_t* err) {
     }
 }
 
+// Slot and phase of a ring of n stages, advanced one stage at a time.
+struct Ring {
+    int i = 0, ph = 0;
+    __device__ __forceinline__ void next(int n) {
+        if (++i == n) {
+            i = 0;
+            ph ^= 1;
+        }
+    }
+};
+
 // Work item w -> (expert, token block, weight tile), weight tiles fastest so that
 // consecutive items share their token rows in L2.
 struct Item {
@@ -335,11 +363,15 @@ __device__ __forceinline__ uint4 dequant8(uint32_t q, float s, float b) {
 
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     k_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const __grid_constant__ CUtensorMap tmA2, GemmParams p) {
+                 const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, GemmParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    const int NA = p.lay.na, NCS = p.lay.ncs;
+    const int OFF_A = 0, OFF_B = p.lay.off_b, OFF_C = p.lay.off_c, OFF_SB = p.lay.off_sb;
+    const int B_BYTES = p.lay.b_stage;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.lay.off_bar);
+    const int OFF_MISC = p.lay.off_bar + N_BARS * 8;
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC + 4);
@@ -350,7 +382,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < NCS; ++i) {
             mbar_init(bar(BAR_CF + i), 1);
-            mbar_init(bar(BAR_CE + i), N_DQ_WARPS);
+            mbar_init(bar(BAR_CE + i), N_DQ_GROUPS * N_DQ_WARPS);
         }
         for (int i = 0; i < NA; ++i) {
             mbar_init(bar(BAR_AF + i), p.a_bf16 ? 1 : N_DQ_WARPS);  // TMA bytes, or the dequant warps
@@ -362,7 +394,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(BAR_SF + i), 1);
-            mbar_init(bar(BAR_SE + i), N_DQ_WARPS);
+            mbar_init(bar(BAR_SE + i), N_DQ_GROUPS * N_DQ_WARPS);
             mbar_init(bar(BAR_DF + i), 1);
             mbar_init(bar(BAR_DE + i), 4);
         }
@@ -378,60 +410,77 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ================================================ TMA producer
+    if (warp == 0 || warp == 2) {
+        // ================================================ TMA producers: the weights (warp 0: {s,b} and codes, or
+        // bf16 weight tiles) and the token tiles (warp 2) are issued by two threads, so that the weight stream
+        // runs as far ahead as its own ring allows instead of in step with the three token stages
         if (lane == 0) {
-            int ci = 0, bi = 0, ai = 0, it_local = 0, si = 0;
+            const bool wprod = warp == 0;
+            int ci = 0, bi = 0, ai = 0, it_local = 0, si = 0;   // copies issued (for the drains below)
+            Ring cr, br, ar;
             bool ok = true;
             for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
                 const Item it = decode_item(p, w);
-                const int sbi = it_local & 1;
-                if (!p.a_bf16) {
-                    if (!(ok = wait_bar(bar(BAR_SE + sbi), ((it_local >> 1) & 1) ^ 1, abort_flag, p.err,
-                                        p.dep_limit_ns)))
-                        break;
-                    ++si;
-                    const uint32_t sb_bytes = (uint32_t)(BM * gpr * 4);
-                    mbar_expect_tx(bar(BAR_SF + sbi), sb_bytes);
-                    bulk_g2s(smem_u32(smem + OFF_SB + sbi * SB_MAX),
-                             p.ebase + (size_t)it.e * p.estride + p.off_sb + (size_t)it.mt * BM * gpr * 4, sb_bytes,
-                             bar(BAR_SF + sbi));
-                }
-                const int nbox = (it.nrows + BOX_ROWS - 1) / BOX_ROWS;
                 const int ks0 = it.kc * KS;
-                for (int ks = 0; ks < KS; ++ks) {
-                    if (p.a_bf16) {
-                        const int as = ai % NA;
-                        if (!(ok = wait_bar(bar(BAR_AE + as), ((ai / NA) & 1) ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
-                        mbar_expect_tx(bar(BAR_AF + as), A_BYTES);
-                        const uint32_t dst = smem_u32(smem + OFF_A + as * A_BYTES);
-                        if (p.mode == 0) {
-                            // 8 gate rows, then the same 8 up rows, per 16-row band (1 KB boxes keep the SW128 atoms)
-                            for (int g = 0; g < BM / 16; ++g) {
-                                tma_load_2d(dst + g * 2048, &tmA, (ks0 + ks) * BK, it.mt * (BM / 2) + g * 8,
-                                            bar(BAR_AF + as));
-                                tma_load_2d(dst + g * 2048 + 1024, &tmA2, (ks0 + ks) * BK, it.mt * (BM / 2) + g * 8,
-                                            bar(BAR_AF + as));
-                            }
-                        } else {
-                            tma_load_2d(dst, &tmA, (ks0 + ks) * BK, it.mt * BM, bar(BAR_AF + as));
-                        }
-                        ++ai;
-                    } else {
-                        const int cs = ci % NCS;
-                        if (!(ok = wait_bar(bar(BAR_CE + cs), ((ci / NCS) & 1) ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
-                        mbar_expect_tx(bar(BAR_CF + cs), C_BYTES);
-                        tma_load_3d(smem_u32(smem + OFF_C + cs * C_BYTES), &tmA, (ks0 + ks) * (BK / 2), it.mt * BM, it.e,
-                                    bar(BAR_CF + cs));
-                        ++ci;
+                if (wprod) {
+                    const int se = p.slot_of ? __ldg(p.slot_of + it.e) : it.e;   // where the expert's weights are
+                    if (!p.a_bf16) {
+                        const int sbi = it_local & 1;
+                        if (!(ok = wait_bar(bar(BAR_SE + sbi), ((it_local >> 1) & 1) ^ 1, abort_flag, p.err,
+                                            p.dep_limit_ns)))
+                            break;
+                        ++si;
+                        const uint32_t sb_bytes = (uint32_t)(BM * gpr * 4);
+                        mbar_expect_tx(bar(BAR_SF + sbi), sb_bytes);
+                        bulk_g2s(smem_u32(smem + OFF_SB + sbi * SB_MAX),
+                                 p.ebase + (size_t)se * p.estride + p.off_sb + (size_t)it.mt * BM * gpr * 4, sb_bytes,
+                                 bar(BAR_SF + sbi));
                     }
-                    const int bs = bi % NBST;
-                    if (!(ok = wait_bar(bar(BAR_BE + bs), ((bi / NBST) & 1) ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
-                    mbar_expect_tx(bar(BAR_BF + bs), (uint32_t)(nbox * BOX_ROWS * BK * 2));
-                    for (int r = 0; r < nbox; ++r)
-                        tma_load_2d(smem_u32(smem + OFF_B + bs * B_BYTES + r * BOX_ROWS * BK * 2), &tmB, (ks0 + ks) * BK,
-                                    it.row0 + r * BOX_ROWS, bar(BAR_BF + bs));
-                    ++bi;
+                    for (int ks = 0; ks < KS; ++ks) {
+                        if (p.a_bf16) {
+                            const int as = ar.i;
+                            if (!(ok = wait_bar(bar(BAR_AE + as), ar.ph ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
+                            mbar_expect_tx(bar(BAR_AF + as), A_BYTES);
+                            const uint32_t dst = smem_u32(smem + OFF_A + as * A_BYTES);
+                            if (p.mode == 0) {
+                                // 8 gate rows, then the same 8 up rows, per 16-row band (1 KB boxes keep the SW128 atoms)
+                                for (int g = 0; g < BM / 16; ++g) {
+                                    tma_load_2d(dst + g * 2048, &tmA, (ks0 + ks) * BK, it.mt * (BM / 2) + g * 8,
+                                                bar(BAR_AF + as));
+                                    tma_load_2d(dst + g * 2048 + 1024, &tmA2, (ks0 + ks) * BK, it.mt * (BM / 2) + g * 8,
+                                                bar(BAR_AF + as));
+                                }
+                            } else {
+                                tma_load_2d(dst, &tmA, (ks0 + ks) * BK, it.mt * BM, bar(BAR_AF + as));
+                            }
+                            ++ai;
+                            ar.next(NA);
+                        } else if (ks % CW == 0) {
+                            // codes of the next CW stages: 128 contiguous bytes of each of the tile's 128 rows (past
+                            // the end of a row, as for the last stages of the down matrix, the box reads zeros)
+                            const int cs = cr.i;
+                            if (!(ok = wait_bar(bar(BAR_CE + cs), cr.ph ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
+                            mbar_expect_tx(bar(BAR_CF + cs), C_BYTES);
+                            tma_load_3d(smem_u32(smem + OFF_C + cs * C_BYTES), &tmA, (ks0 + ks) * (BK / 2), it.mt * BM,
+                                        se, bar(BAR_CF + cs));
+                            ++ci;
+                            cr.next(NCS);
+                        }
+                    }
+                } else {
+                    const bool big = p.lay.box_big && it.nrows > 64;
+                    const int box = big ? BOX_BIG : BOX_SMALL;
+                    const int nbox = (it.nrows + box - 1) / box;
+                    for (int ks = 0; ks < KS; ++ks) {
+                        const int bs = br.i;
+                        if (!(ok = wait_bar(bar(BAR_BE + bs), br.ph ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
+                        mbar_expect_tx(bar(BAR_BF + bs), (uint32_t)(nbox * box * BK * 2));
+                        for (int r = 0; r < nbox; ++r)
+                            tma_load_2d(smem_u32(smem + OFF_B + bs * B_BYTES + r * box * BK * 2), big ? &tmB2 : &tmB,
+                                        (ks0 + ks) * BK, it.row0 + r * box, bar(BAR_BF + bs));
+                        ++bi;
+                        br.next(NBST);
+                    }
                 }
             }
             // let every copy this thread issued land before the CTA can exit (also after an abort)
@@ -447,7 +496,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     } else if (warp == 1) {
         // ================================================ MMA issuer
         if (lane == 0) {
-            int ai = 0, bi = 0, it_local = 0;
+            int ai = 0, it_local = 0;
+            Ring ar, br;
             bool ok = true;
             for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
                 const Item it = decode_item(p, w);
@@ -458,9 +508,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const uint32_t idesc = idesc_f16(n_mma, !p.f16);
                 const uint32_t d_tmem = tmem + (uint32_t)(ab * NB);
                 for (int ks = 0; ks < KS; ++ks) {
-                    const int as = ai % NA, bs = bi % NBST;
-                    if (!(ok = wait_bar(bar(BAR_AF + as), (ai / NA) & 1, abort_flag, p.err, p.dep_limit_ns))) break;
-                    if (!(ok = wait_bar(bar(BAR_BF + bs), (bi / NBST) & 1, abort_flag, p.err, p.dep_limit_ns))) break;
+                    const int as = ar.i, bs = br.i;
+                    if (!(ok = wait_bar(bar(BAR_AF + as), ar.ph, abort_flag, p.err, p.dep_limit_ns))) break;
+                    if (!(ok = wait_bar(bar(BAR_BF + bs), br.ph, abort_flag, p.err, p.dep_limit_ns))) break;
                     tc_fence_after();
                     const uint64_t ad = sw128_desc(smem_u32(smem + OFF_A + as * A_BYTES));
                     const uint64_t bd = sw128_desc(smem_u32(smem + OFF_B + bs * B_BYTES));
@@ -470,7 +520,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     tc_commit(bar(BAR_AE + as));
                     tc_commit(bar(BAR_BE + bs));
                     ++ai;
-                    ++bi;
+                    ar.next(NA);
+                    br.next(NBST);
                 }
                 if (!ok) break;
                 tc_commit(bar(BAR_DF + ab));
@@ -541,49 +592,67 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (lane == 0) mbar_arrive(bar(BAR_DE + ab));
         }
     } else if (warp >= 8 && !p.a_bf16) {
-        // ================================================ dequant
-        const int t = threadIdx.x - 8 * 32;  // 0..255
-        const int r = t >> 1, hf = t & 1;    // weight row in the tile, half of the 64-code group
-        int ci = 0, ai = 0, it_local = 0;
-        bool ok = true;
-        for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
-            const int sbi = it_local & 1;
-            int okw = 1;
-            if (lane == 0) okw = wait_bar(bar(BAR_SF + sbi), (it_local >> 1) & 1, abort_flag, p.err, p.dep_limit_ns);
-            if (!(ok = __shfl_sync(FULL, okw, 0))) break;
-            const uint32_t* sbrow = reinterpret_cast<const uint32_t*>(smem + OFF_SB + sbi * SB_MAX) + r * gpr;
-            for (int ks = 0; ks < KS; ++ks) {
-                const int cs = ci % NCS, as = ai % NA;
-                okw = 1;
-                if (lane == 0) {
-                    okw = wait_bar(bar(BAR_CF + cs), (ci / NCS) & 1, abort_flag, p.err, p.dep_limit_ns);
-                    if (okw) okw = wait_bar(bar(BAR_AE + as), ((ai / NA) & 1) ^ 1, abort_flag, p.err, p.dep_limit_ns);
-                }
+        // ================================================ dequant: N_DQ_GROUPS groups of N_DQ_WARPS warps; group g
+        // takes the K stages whose running index is g modulo N_DQ_GROUPS, so that stages are dequantised side by
+        // side, and every warp walks every stage to keep the code and A rings in step
+        const int t = threadIdx.x - 8 * 32;
+        const int grp = t / (N_DQ_WARPS * 32);
+        const int r = (t >> 1) & (BM - 1), hf = t & 1;   // weight row in the tile, half of the 64-code group
+        auto run = [&](auto f16_tag) {
+            constexpr bool F16 = decltype(f16_tag)::value;
+            Ring cr, ar;
+            int g = 0, it_local = 0;   // g: the group whose stage is next
+            bool ok = true;
+            for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
+                const int sbi = it_local & 1;
+                int okw = 1;
+                if (lane == 0) okw = wait_bar(bar(BAR_SF + sbi), (it_local >> 1) & 1, abort_flag, p.err, p.dep_limit_ns);
                 if (!(ok = __shfl_sync(FULL, okw, 0))) break;
-                const uint4 qv = *reinterpret_cast<const uint4*>(smem + OFF_C + cs * C_BYTES + r * 32 + hf * 16);
-                const uint32_t sbw = sbrow[ks];
-                const float s = h2f(sbw & 0xffffu), b = h2f(sbw >> 16);
-                unsigned char* arow = smem + OFF_A + as * A_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
-                const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+                const uint32_t* sbrow = reinterpret_cast<const uint32_t*>(smem + OFF_SB + sbi * SB_MAX) + r * gpr;
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int sub = ks % CW;
+                    const bool mine = g == grp;
+                    okw = 1;
+                    if (lane == 0) {
+                        if (sub == 0) okw = wait_bar(bar(BAR_CF + cr.i), cr.ph, abort_flag, p.err, p.dep_limit_ns);
+                        if (okw && mine) okw = wait_bar(bar(BAR_AE + ar.i), ar.ph ^ 1, abort_flag, p.err, p.dep_limit_ns);
+                    }
+                    if (!(ok = __shfl_sync(FULL, okw, 0))) break;
+                    if (mine) {
+                        // the code box lands 128-byte swizzled: 16-byte chunk j of row r sits at chunk j ^ (r & 7),
+                        // so the 16 rows a warp reads spread over all banks
+                        const uint4 qv = *reinterpret_cast<const uint4*>(smem + OFF_C + cr.i * C_BYTES +
+                                                                         r * (CW * BK / 2) + (((sub * 2 + hf) ^ (r & 7)) << 4));
+                        const uint32_t sbw = sbrow[ks];
+                        const float s = h2f(sbw & 0xffffu), b = h2f(sbw >> 16);
+                        unsigned char* arow = smem + OFF_A + ar.i * A_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+                        const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int chunk = hf * 4 + c;  // 16-byte chunk of the 128-byte row
-                    *reinterpret_cast<uint4*>(arow + ((chunk ^ (r & 7)) << 4)) =
-                        p.f16 ? dequant8<true>(qw[c], s, b) : dequant8<false>(qw[c], s, b);
+                        for (int c = 0; c < 4; ++c) {
+                            const int chunk = hf * 4 + c;  // 16-byte chunk of the 128-byte row
+                            *reinterpret_cast<uint4*>(arow + ((chunk ^ (r & 7)) << 4)) = dequant8<F16>(qw[c], s, b);
+                        }
+                        fence_proxy_async();  // generic-proxy writes, read next by the tensor core
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(BAR_AF + ar.i));
+                    }
+                    if (sub == CW - 1 || ks == KS - 1) {   // the code stage is used up
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(BAR_CE + cr.i));
+                        cr.next(NCS);
+                    }
+                    ar.next(NA);
+                    if (++g == N_DQ_GROUPS) g = 0;
                 }
-                fence_proxy_async();  // generic-proxy writes, read next by the tensor core
+                if (!ok) break;
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bar(BAR_AF + as));
-                    mbar_arrive(bar(BAR_CE + cs));
-                }
-                ++ci;
-                ++ai;
+                if (lane == 0) mbar_arrive(bar(BAR_SE + sbi));
             }
-            if (!ok) break;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(BAR_SE + sbi));
-        }
+        };
+        if (p.f16)
+            run(std::true_type{});
+        else
+            run(std::false_type{});
     }
     tc_fence_before();
     __syncthreads();
@@ -594,6 +663,52 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 }
 
 // ------------------------------------------------------------------ routing -> permutation
+
+// Exclusive prefix sum of v over the threads of a 1024-thread CTA (thread order);
+// wsum is shared scratch of 32 ints.
+__device__ __forceinline__ int block_exclusive_scan(int v, int32_t* wsum) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULL, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int z = wsum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(FULL, z, o);
+            if (lane >= o) z += y;
+        }
+        wsum[lane] = z;
+    }
+    __syncthreads();
+    const int r = x - v + (warp > 0 ? wsum[warp - 1] : 0);
+    __syncthreads();
+    return r;
+}
+
+// One CTA: the GEMM tile prefixes of one wave of experts (experts outside the
+// wave get no tile; their rows keep their places in the permutation).
+__global__ void __launch_bounds__(1024) k_wave_plan(const int32_t* __restrict__ counts, const int32_t* __restrict__ mask,
+                                                     int E, int mt_gu, int mt_d, int32_t* tiles_gu, int32_t* tiles_d) {
+    __shared__ int32_t wsum[32];
+    const int e = threadIdx.x;
+    const int c = e < E && __ldg(mask + e) ? __ldg(counts + e) : 0;
+    const int nb = (c + NB - 1) / NB;
+    const int excl = block_exclusive_scan(nb, wsum);
+    if (e < E) {
+        tiles_gu[e] = excl * mt_gu;
+        tiles_d[e] = excl * mt_d;
+    }
+    if (e == E - 1) {
+        tiles_gu[E] = (excl + nb) * mt_gu;
+        tiles_d[E] = (excl + nb) * mt_d;
+    }
+}
 
 // One CTA: tokens per expert, exclusive scan, GEMM tile prefixes.
 __global__ void __launch_bounds__(1024) k_group_hist(const int32_t* __restrict__ idx, int P, int E, int mt_gu,
@@ -613,32 +728,7 @@ __global__ void __launch_bounds__(1024) k_group_hist(const int32_t* __restrict__
     const int e = threadIdx.x;
     const int c = e < E ? cnt[e] : 0;
     const int nb = (c + NB - 1) / NB;
-    int vals[2] = {c, nb};
-    int excl[2];
-    for (int s = 0; s < 2; ++s) {
-        int v = vals[s];
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        int x = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(FULL, x, o);
-            if (lane >= o) x += y;
-        }
-        if (lane == 31) wsum[warp] = x;
-        __syncthreads();
-        if (warp == 0) {
-            int z = wsum[lane];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(FULL, z, o);
-                if (lane >= o) z += y;
-            }
-            wsum[lane] = z;
-        }
-        __syncthreads();
-        excl[s] = x - v + (warp > 0 ? wsum[warp - 1] : 0);
-        __syncthreads();
-    }
+    const int excl[2] = {block_exclusive_scan(c, wsum), block_exclusive_scan(nb, wsum)};
     if (e < E) {
         counts[e] = c;
         offsets[e] = excl[0];
@@ -889,6 +979,36 @@ bool encode_rows(CUtensorMap* m, const void* base, int cols, int rows, int box_r
                   CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// Shared-memory plan for token tiles of up to max_rows rows: bf16 weights by TMA
+// (a_bf16) or int4 codes dequantised into three A stages.
+Layout plan_layout(int max_rows, bool a_bf16) {
+    Layout l;
+    std::memset(&l, 0, sizeof(l));
+    int rows = max_rows > 64 ? (max_rows + BOX_BIG - 1) / BOX_BIG * BOX_BIG : (max_rows + 15) / 16 * 16;
+    if (rows > NB) rows = NB;
+    l.box_big = max_rows > 64;
+    l.b_stage = rows * BK * 2;
+    const int b_region = NBST * l.b_stage;
+    if (a_bf16) {
+        l.ncs = 0;
+        l.na = (SMEM_USABLE - b_region) / A_BYTES;
+        if (l.na > NA_MAX) l.na = NA_MAX;
+        l.off_b = l.na * A_BYTES;
+        l.off_c = l.off_b + b_region;
+        l.off_sb = l.off_c;
+        l.off_bar = l.off_sb;
+    } else {
+        l.na = 3;
+        l.off_b = l.na * A_BYTES;
+        l.off_c = l.off_b + b_region;
+        l.ncs = (SMEM_USABLE - l.off_c - 2 * SB_MAX) / C_BYTES;
+        if (l.ncs > NCS_MAX) l.ncs = NCS_MAX;
+        l.off_sb = l.off_c + l.ncs * C_BYTES;
+        l.off_bar = l.off_sb + 2 * SB_MAX;
+    }
+    return l;
+}
+
 }  // namespace grouped
 
 size_t grouped_workspace_bytes(int T, int H, int I, int E, int k, int S) {
@@ -900,7 +1020,8 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     using namespace grouped;
     const int T = a.T, H = a.H, I = a.I, E = a.E, k = a.k, S = a.S;
     const tf_expert_table* table = a.table;
-    if (!a.x || !a.out || !table || !a.idx || !a.w || !a.ws) return fail(TF_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!a.x || !a.out || (!table && !a.waves) || !a.idx || !a.w || !a.ws)
+        return fail(TF_ERR_INVALID_ARG, "%s: null pointer", fn);
     if (a.x == a.out) return fail(TF_ERR_INVALID_ARG, "%s: out must not alias x", fn);
     if (T < 1) return fail(TF_ERR_INVALID_ARG, "%s: T=%d", fn, T);
     if (H % 128 || I % 64 || H > 2816 || H < 128 || I < 64)
@@ -913,13 +1034,19 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
                     S);
     if (S > 0 && (!aligned16(a.Wsg) || !aligned16(a.Wsu) || !aligned16(a.Wsd)))
         return fail(TF_ERR_INVALID_ARG, "%s: shared weights must be 16-byte aligned", fn);
-    if (!table->base || !aligned16(table->base) || table->stride % 16)
-        return fail(TF_ERR_INVALID_ARG, "%s: expert table base and stride must be 16-byte aligned", fn);
-    if (table->slot_of_expert)
-        return fail(TF_ERR_NOT_SUPPORTED, "%s: the grouped path takes a resident expert table (no slot map)", fn);
-    if (table->n_experts != 0 && table->n_experts != E)
-        return fail(TF_ERR_INVALID_ARG, "%s: the expert table's n_experts (%d) is not E (%d)", fn, table->n_experts,
-                    E);
+    if (a.waves) {
+        if (!a.waves->pool || !aligned16(a.waves->pool) || a.waves->slot_bytes % 16 || a.waves->n_slots < 1 ||
+            !a.waves->d_maps || !a.waves->h_maps || !a.waves->before_wave || a.waves->n < 0)
+            return fail(TF_ERR_INVALID_ARG, "%s: bad cache waves", fn);
+    } else {
+        if (!table->base || !aligned16(table->base) || table->stride % 16)
+            return fail(TF_ERR_INVALID_ARG, "%s: expert table base and stride must be 16-byte aligned", fn);
+        if (table->slot_of_expert)
+            return fail(TF_ERR_NOT_SUPPORTED, "%s: the grouped path takes a resident expert table (no slot map)", fn);
+        if (table->n_experts != 0 && table->n_experts != E)
+            return fail(TF_ERR_INVALID_ARG, "%s: the expert table's n_experts (%d) is not E (%d)", fn,
+                        table->n_experts, E);
+    }
     if (!aligned16(a.x) || !aligned16(a.out) || (a.delta && !aligned16(a.delta)))
         return fail(TF_ERR_INVALID_ARG, "%s: x, out and delta must be 16-byte aligned", fn);
     if ((size_t)T * k > (size_t)INT32_MAX / 4) return fail(TF_ERR_INVALID_ARG, "%s: T*k too large", fn);
@@ -928,7 +1055,8 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
         return fail(TF_ERR_INVALID_ARG, "%s: workspace misaligned or smaller than %zu bytes", fn, c.total);
     ExpertLayout lay;
     expert_layout(H, I, &lay);
-    if (table->stride < lay.payload) return fail(TF_ERR_INVALID_ARG, "%s: expert stride below the payload size", fn);
+    if ((a.waves ? a.waves->slot_bytes : table->stride) < lay.payload)
+        return fail(TF_ERR_INVALID_ARG, "%s: expert stride below the payload size", fn);
 
     char* ws = static_cast<char*>(a.ws);
     uint32_t* err = reinterpret_cast<uint32_t*>(ws + c.err);
@@ -948,34 +1076,40 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     float* ys = S > 0 ? reinterpret_cast<float*>(ws + c.ys) : nullptr;
     const int P = T * k;
 
-    // tensor maps: codes of every expert (3-D), permuted activations and h (2-D, SW128)
+    // tensor maps: codes of every expert (3-D; with waves, of every slot of the layer's cache), permuted
+    // activations and h (2-D, SW128)
     CUtensorMap tmA_gu, tmA_d, tmB_gu, tmB_d;
-    const char* base = static_cast<const char*>(table->base);
+    const char* base = a.waves ? a.waves->pool : static_cast<const char*>(table->base);
+    const size_t estride = a.waves ? a.waves->slot_bytes : table->stride;
+    const int n_units = a.waves ? a.waves->n_slots : E;    // the 3rd dimension of the code maps
     {
-        cuuint64_t dims[3] = {(cuuint64_t)H / 2, (cuuint64_t)2 * I, (cuuint64_t)E};
-        cuuint64_t str[2] = {(cuuint64_t)H / 2, (cuuint64_t)table->stride};
-        cuuint32_t box[3] = {BK / 2, BM, 1};
+        cuuint64_t dims[3] = {(cuuint64_t)H / 2, (cuuint64_t)2 * I, (cuuint64_t)n_units};
+        cuuint64_t str[2] = {(cuuint64_t)H / 2, (cuuint64_t)estride};
+        cuuint32_t box[3] = {CW * BK / 2, BM, 1};
         if (!encode(&tmA_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base + lay.gu_codes, dims, str, box,
-                    CU_TENSOR_MAP_SWIZZLE_NONE))
+                    CU_TENSOR_MAP_SWIZZLE_128B))
             return fail(TF_ERR_CUDA, "%s: tensor map of the gate/up codes", fn);
     }
     {
-        cuuint64_t dims[3] = {(cuuint64_t)I / 2, (cuuint64_t)H, (cuuint64_t)E};
-        cuuint64_t str[2] = {(cuuint64_t)I / 2, (cuuint64_t)table->stride};
-        cuuint32_t box[3] = {BK / 2, BM, 1};
+        cuuint64_t dims[3] = {(cuuint64_t)I / 2, (cuuint64_t)H, (cuuint64_t)n_units};
+        cuuint64_t str[2] = {(cuuint64_t)I / 2, (cuuint64_t)estride};
+        cuuint32_t box[3] = {CW * BK / 2, BM, 1};
         if (!encode(&tmA_d, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base + lay.d_codes, dims, str, box,
-                    CU_TENSOR_MAP_SWIZZLE_NONE))
+                    CU_TENSOR_MAP_SWIZZLE_128B))
             return fail(TF_ERR_CUDA, "%s: tensor map of the down codes", fn);
     }
-    if (!encode_rows(&tmB_gu, xp, H, P, BOX_ROWS, true))
+    CUtensorMap tmB_gu2, tmB_d2;
+    if (!encode_rows(&tmB_gu, xp, H, P, BOX_SMALL, true) || !encode_rows(&tmB_gu2, xp, H, P, BOX_BIG, true))
         return fail(TF_ERR_CUDA, "%s: tensor map of the permuted activations", fn);
-    if (!encode_rows(&tmB_d, hb, I, P, BOX_ROWS)) return fail(TF_ERR_CUDA, "%s: tensor map of h", fn);
+    if (!encode_rows(&tmB_d, hb, I, P, BOX_SMALL) || !encode_rows(&tmB_d2, hb, I, P, BOX_BIG))
+        return fail(TF_ERR_CUDA, "%s: tensor map of h", fn);
     // shared expert: bf16 weights as SW128 row boxes (8 rows for the interleaved gate/up tile, 128 for down)
-    CUtensorMap tmS_g, tmS_u, tmS_d, tmS_xn, tmS_h;
+    CUtensorMap tmS_g, tmS_u, tmS_d, tmS_xn, tmS_h, tmS_xn2, tmS_h2;
     if (S > 0) {
         if (!encode_rows(&tmS_g, a.Wsg, H, S, 8) || !encode_rows(&tmS_u, a.Wsu, H, S, 8) ||
-            !encode_rows(&tmS_d, a.Wsd, S, H, BM) || !encode_rows(&tmS_xn, a.x, H, T, BOX_ROWS) ||
-            !encode_rows(&tmS_h, hs, S, T, BOX_ROWS))
+            !encode_rows(&tmS_d, a.Wsd, S, H, BM) || !encode_rows(&tmS_xn, a.x, H, T, BOX_SMALL) ||
+            !encode_rows(&tmS_h, hs, S, T, BOX_SMALL) || !encode_rows(&tmS_xn2, a.x, H, T, BOX_BIG) ||
+            !encode_rows(&tmS_h2, hs, S, T, BOX_BIG))
             return fail(TF_ERR_CUDA, "%s: tensor maps of the shared expert", fn);
     }
     if (int e = smem_limit_once((const void*)k_group_gemm, (int)GEMM_SMEM)) return cuda_status(e, fn);
@@ -1014,7 +1148,7 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     GemmParams gp;
     std::memset(&gp, 0, sizeof(gp));
     gp.ebase = base;
-    gp.estride = table->stride;
+    gp.estride = estride;
     gp.E = E;
     gp.counts = counts;
     gp.offsets = offsets;
@@ -1022,27 +1156,49 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     gp.ksplit = 1;
     gp.dep_limit_ns = test_wait_limit_ns();
 
+    // the largest token tile of this call: an expert gets each token at most once
+    const int max_rows = T < NB ? T : NB;
+    auto routed_gemms = [&](const int32_t* slot_of) {
+        gp.slot_of = slot_of;
+        gp.off_sb = lay.gu_sb;
+        gp.K = H;
+        gp.MT = mt_gu;
+        gp.tiles = tiles_gu;
+        gp.mode = 0;
+        gp.hout = hb;
+        gp.yout = nullptr;
+        gp.ldo = I;
+        gp.col_scale = rp;
+        gp.f16 = 1;
+        gp.lay = plan_layout(max_rows, false);
+        k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmA_gu, tmB_gu, tmA_gu, tmB_gu2, gp);
+        gp.off_sb = lay.d_sb;
+        gp.K = I;
+        gp.MT = mt_d;
+        gp.tiles = tiles_d;
+        gp.mode = 1;
+        gp.hout = nullptr;
+        gp.yout = y;
+        gp.ldo = H;
+        gp.f16 = 0;
+        k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmA_d, tmB_d, tmA_d, tmB_d2, gp);
+    };
     prof_before(TF_KERNEL_GEMM, stream);
-    gp.off_sb = lay.gu_sb;
-    gp.K = H;
-    gp.MT = mt_gu;
-    gp.tiles = tiles_gu;
-    gp.mode = 0;
-    gp.hout = hb;
-    gp.ldo = I;
-    gp.col_scale = rp;
-    gp.f16 = 1;
-    k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmA_gu, tmB_gu, tmA_gu, gp);
-    gp.off_sb = lay.d_sb;
-    gp.K = I;
-    gp.MT = mt_d;
-    gp.tiles = tiles_d;
-    gp.mode = 1;
-    gp.hout = nullptr;
-    gp.yout = y;
-    gp.ldo = H;
-    gp.f16 = 0;
-    k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmA_d, tmB_d, tmA_d, gp);
+    if (!a.waves) {
+        routed_gemms(nullptr);
+    } else {
+        // the chunk's experts in waves: each wave's fills, its slot map, its tile plan, then its GEMMs
+        const GroupedWaves& wv = *a.waves;
+        for (int w = 0; w < wv.n; ++w) {
+            if (int s = wv.before_wave(wv.ctx, w, stream)) return s;
+            int32_t* dmap = wv.d_maps + (size_t)w * 2 * E;
+            if (cudaError_t e = cudaMemcpyAsync(dmap, wv.h_maps + (size_t)w * 2 * E, (size_t)2 * E * 4,
+                                                cudaMemcpyHostToDevice, st))
+                return cuda_status(e, fn);
+            k_wave_plan<<<1, 1024, 0, st>>>(counts, dmap, E, mt_gu, mt_d, tiles_gu, tiles_d);
+            routed_gemms(dmap + E);
+        }
+    }
     if (S > 0) {
         GemmParams sp;
         std::memset(&sp, 0, sizeof(sp));
@@ -1064,7 +1220,8 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
         sp.col_scale = rms;          // the shared expert's token rows are the tokens in order
         sp.ksplit = ks_gu;
         sp.mrows = 2 * S;
-        k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmS_g, tmS_xn, tmS_u, sp);
+        sp.lay = plan_layout(max_rows, true);
+        k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmS_g, tmS_xn, tmS_u, tmS_xn2, sp);
         if (ks_gu > 1) k_shared_gu_combine<<<dim3((S + 255) / 256, T), 256, 0, st>>>(spart, rms, ks_gu, T, S, hs);
         sp.K = S;
         sp.MT = H / BM;
@@ -1075,7 +1232,7 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
         sp.ldo = H;
         sp.ksplit = ks_d;
         sp.mrows = H;
-        k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmS_d, tmS_h, tmS_d, sp);
+        k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmS_d, tmS_h, tmS_d, tmS_h2, sp);
         if (ks_d > 1) k_shared_down_combine<<<dim3((H + 255) / 256, T), 256, 0, st>>>(spart, ks_d, T, H, ys);
     }
     prof_after(TF_KERNEL_GEMM, stream);

@@ -75,6 +75,7 @@ size_t tf_struct_bytes(int which) {
         case 1: return sizeof(tf_layer_desc);
         case 2: return sizeof(tf_step_stats);
         case 3: return sizeof(tf_cache_event);
+        case 4: return sizeof(tf_prefill_stats);
         default: return 0;
     }
 }

@@ -99,6 +99,22 @@ int launch_down(const DecodeParams& p, int with_routed, int with_shared, void* s
 int launch_dequant(const char* blob, int H, int I, int matrix, int format, void* out,
                    size_t off_sb, size_t off_codes, void* stream);
 
+// Experts that stream through a cache while a chunk of tokens runs the grouped
+// path (tf_layer_prefill_cached): the chunk's experts are taken in waves; before
+// wave w the callback enqueues its fills and makes the compute stream wait for
+// them, and fills the wave's row of h_maps: [E] 1 for the wave's experts, then
+// [E] the slot of each of them in `pool`.
+struct GroupedWaves {
+    int n;                                 // waves
+    const char* pool;                      // this layer's slots: slot s at pool + s * slot_bytes
+    size_t slot_bytes;
+    int n_slots;
+    int32_t* d_maps;                       // device [n][2][E]
+    const int32_t* h_maps;                 // pinned host [n][2][E], filled by before_wave
+    int (*before_wave)(void* ctx, int w, void* compute_stream);   // a tf_status
+    void* ctx;
+};
+
 // The grouped (batched / prefill) layer of tf_grouped.cu: routed experts by
 // tcgen05 GEMMs over the token x expert permutation and, when S > 0, the bf16
 // shared expert by the same GEMM kernel with TMA-loaded weights.
@@ -120,6 +136,7 @@ struct GroupedArgs {
     float eps;
     void* ws;
     size_t ws_bytes;
+    const GroupedWaves* waves;     // nullable: the experts stream through a cache (else the table holds them all)
 };
 size_t grouped_workspace_bytes(int T, int H, int I, int E, int k, int S);
 tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn);
@@ -159,4 +176,10 @@ struct tf_layer {
     float* ys = nullptr;             // fp32 [H]: the shared down projection of the cached steps
     int32_t* h_idx = nullptr;        // pinned staging for the cached step
     cudaEvent_t ev_idx = nullptr, ev_copies = nullptr, ev_t0 = nullptr, ev_shared = nullptr, ev_c0 = nullptr;
+    // chunked prefill through a cache (T_max > 1): the chunk's ids and the waves' expert masks and slot maps
+    int max_waves = 0;               // ceil(E / k): a wave holds at least k experts (n_slots >= k)
+    int32_t* h_chunk_ids = nullptr;  // pinned [T_max * k]
+    int32_t* h_wave_maps = nullptr;  // pinned [max_waves][2][E]
+    int32_t* d_wave_maps = nullptr;  // workspace [max_waves][2][E]
+    cudaEvent_t ev_wave = nullptr;
 };

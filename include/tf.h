@@ -389,7 +389,7 @@ typedef struct {
 /*
  * Size in bytes of a structure of this ABI, for bindings to check their own
  * layout against the library's: which = 0 tf_expert_table, 1 tf_layer_desc,
- * 2 tf_step_stats, 3 tf_cache_event; 0 for any other value.
+ * 2 tf_step_stats, 3 tf_cache_event, 4 tf_prefill_stats; 0 for any other value.
  */
 size_t tf_struct_bytes(int which);
 
@@ -432,6 +432,37 @@ tf_status tf_layer_step(tf_layer* l, tf_expert_cache* cache, int layer, int64_t 
 tf_status tf_layer_step_device_cache(tf_layer* l, tf_device_cache* c, int layer, const void* x, void* out,
                                      const float* logit_bias, int bias_stride, void* compute_stream,
                                      void* fetch_stream, int measure, tf_step_stats* stats);
+
+/*
+ * Chunked prefill through the streamed-expert cache: T tokens (a chunk, at most
+ * the handle's T_max) through layer `layer` whose experts live in the pinned
+ * host store behind the LFU cache `c`. Devtrends page, section "Desempenho no
+ * mundo real": prefill runs in chunks and one loaded expert serves all of the
+ * chunk's rows that need it. Steps:
+ *  1. the router for the T tokens on compute_stream; the T x k ids to the host
+ *     (the call's one host wait);
+ *  2. the chunk's distinct experts in order of first use (token order, then
+ *     rank) are cut into waves of n_slots experts; wave w is one LFU step
+ *     (step0 + w) of layer `layer`: a lookup of its experts, then an admit of
+ *     each miss with the wave's experts pinned, and one cudaMemcpyAsync per
+ *     miss on copy_stream (after the previous wave's GEMMs are done with the
+ *     slots);
+ *  3. per wave, the grouped GEMMs of tf_moe_ffn_grouped on the wave's experts
+ *     and their rows, reading the weights from the slots;
+ *  4. the shared expert for the T tokens and the combine, as tf_layer_step with
+ *     T > 1: out = bf16(x + shared + sum_i w_i y_i), the same values.
+ * stats (nullable): waves, hits, misses and bytes copied; the next call on this
+ * layer uses step0 + stats->waves. A copy that cannot be enqueued rolls back
+ * the slots its wave admitted and returns TF_ERR_CUDA.
+ */
+typedef struct {
+    int32_t waves, hits, misses;
+    uint64_t bytes_fetched;
+} tf_prefill_stats;
+tf_status tf_layer_prefill_cached(tf_layer* l, tf_expert_cache* c, int layer, int64_t step0,
+                                  const void* h_expert_store, const void* x, void* out, int T,
+                                  const float* logit_bias, int bias_stride, void* compute_stream,
+                                  void* copy_stream, tf_prefill_stats* stats);
 
 /*
  * A decode step through L resident layers for one token: x_{l+1} = layer_l(x_l),

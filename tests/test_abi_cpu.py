@@ -35,9 +35,9 @@ def test_library_loads_and_exports_every_declared_symbol():
 
 def test_binding_structures_match_the_library_layout():
     L = B.lib()
-    for which, cls in enumerate([B.ExpertTable, B.LayerDesc, B.StepStats, B.CacheEvent]):
+    for which, cls in enumerate([B.ExpertTable, B.LayerDesc, B.StepStats, B.CacheEvent, B.PrefillStats]):
         assert L.tf_struct_bytes(which) == ctypes.sizeof(cls), cls.__name__
-    assert L.tf_struct_bytes(4) == 0
+    assert L.tf_struct_bytes(5) == 0
 
 
 def test_version_and_status_strings():

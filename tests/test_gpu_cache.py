@@ -13,7 +13,10 @@ CPU oracle's LFU simulator (oracle.LFU) and against the resident path:
     event for event, and every layer output must equal the resident path's bit
     for bit;
   - the host metadata with the miss fills striped over several copy streams
-    (tf_expert_cache_set_copy_streams), at 8 and 32 slots per layer.
+    (tf_expert_cache_set_copy_streams), at 8 and 32 slots per layer;
+  - chunked prefill through the cache (tf_layer_prefill_cached): a chunk's
+    experts stream through the slots in waves, each loaded expert serving all
+    of the chunk's rows that need it.
 
 The router logits carry the streaming workload's bias (Zipf popularity,
 per-step noise, a repeat of the previous step's experts), so that steps mix
@@ -150,3 +153,81 @@ def test_device_cache_rejects_bad_arguments():
     assert e.value.status == B.TF_ERR_INVALID_ARG
     c.close()
     st.close()
+
+
+# ------------------------------------------------------------- chunked prefill through the cache
+
+def _waves(ids, n_slots):
+    """The chunk's distinct experts in order of first use (token order, then rank), cut into waves of n_slots."""
+    order = []
+    for e in ids.reshape(-1).tolist():
+        if e not in order:
+            order.append(e)
+    return [np.array(order[i:i + n_slots], np.int32) for i in range(0, len(order), n_slots)]
+
+
+@pytest.mark.parametrize("cfg,L,slots,T,chunks", [
+    (dict(H=512, I=256, E=24, k=4, S=128), 2, 6, 40, 3),
+    (FULL, 1, 16, 128, 2)], ids=["small", "full"])
+def test_chunked_prefill_through_the_cache(cfg, L, slots, T, chunks):
+    """Devtrends page, section "Desempenho no mundo real": prefill in chunks, one loaded expert serving all of the
+    chunk's rows. Every layer output equals the resident batched step's bit for bit; the LFU trace and the slots
+    equal the oracle's fed the same waves (each wave one step, its experts in order)."""
+    H, E, k = cfg["H"], cfg["E"], cfg["k"]
+    seed = 57
+    cached = SyntheticStack(seed, L, resident=False, n_slots=slots, T_max=T, **cfg)
+    resident = SyntheticStack(seed, L, resident=True, T_max=T, **cfg)
+    cs = torch.cuda.Stream()
+    lfu = O.LFU(L, slots)
+    want = []
+    step = [0] * L
+    for c in range(chunks):
+        x = hidden_tensor(seed, c, T, H)
+        cur_c, cur_r = x, x.clone()
+        for l in range(L):
+            out_c = torch.full_like(x, float("nan"))
+            out_r = torch.full_like(x, float("nan"))
+            st = B.tf_layer_prefill_cached(cached.layers[l], cached.cache, l, step[l], cached.store, cur_c, out_c, T,
+                                           None, 0, None, cs)
+            B.tf_layer_step(resident.layers[l], None, l, 0, None, cur_r, out_r, T)
+            torch.cuda.synchronize()
+            ids = cached.layers[l].routing_tensors(T)[0].cpu().numpy()
+            waves = _waves(ids, slots)
+            assert st.waves == len(waves)
+            ev = []
+            for w, wave in enumerate(waves):
+                ev += lfu.step(step[l] + w, l, wave)
+            want += ev
+            assert st.misses == sum(1 for e in ev if not e[3]) and st.hits + st.misses == len(ev)
+            assert st.bytes_fetched == st.misses * cached.payload
+            step[l] += st.waves
+            assert torch.equal(out_c.view(torch.int16), out_r.view(torch.int16)), (c, l)
+            cur_c, cur_r = out_c, out_r
+    assert cached.cache.trace() == want
+    for l in range(L):
+        got, exp = cached.cache.state(l), lfu.state(l)
+        assert all(np.array_equal(a, b) for a, b in zip(got, exp)), l
+    assert any(not e[3] and e[5] >= 0 for e in want)       # evictions inside chunks
+    cached.close()
+    resident.close()
+
+
+def test_chunked_prefill_copy_failure_rolls_back():
+    cfg = dict(H=512, I=256, E=24, k=4, S=128)
+    st = SyntheticStack(58, 1, resident=False, n_slots=6, T_max=16, **cfg)
+    cs = torch.cuda.Stream()
+    x = hidden_tensor(58, 0, 16, cfg["H"])
+    out = torch.empty_like(x)
+    B.tf_test_fail_nth_copy(2)            # the first wave's second copy fails
+    with pytest.raises(B.TFError) as e:
+        B.tf_layer_prefill_cached(st.layers[0], st.cache, 0, 0, st.store, x, out, 16, None, 0, None, cs)
+    B.tf_test_fail_nth_copy(0)
+    assert e.value.status == B.TF_ERR_CUDA and "rolled back" in str(e.value)
+    torch.cuda.synchronize()
+    ex, cnt, lu = st.cache.state(0)
+    assert (ex >= 0).sum() == 0
+    s2 = B.tf_layer_prefill_cached(st.layers[0], st.cache, 0, 1, st.store, x, out, 16, None, 0, None, cs)
+    torch.cuda.synchronize()
+    assert s2.waves >= 1 and not torch.isnan(out.float()).any()
+    st.close()
+
