@@ -531,6 +531,7 @@ tf_status tf_layer_step(tf_layer* l, tf_expert_cache* cache, int layer, int64_t 
         a.Wsd = d.W_sd;
         a.S = d.S;
         a.eps = d.eps;
+        a.rms_in = l->rms;   // written by the router above for every token
         a.ws = l->grouped_ws;
         a.ws_bytes = l->grouped_bytes;
         return grouped_run(a, cs, fn);
@@ -816,6 +817,7 @@ tf_status tf_layer_prefill_cached(tf_layer* l, tf_expert_cache* c, int layer, in
     a.Wsd = d.W_sd;
     a.S = d.S;
     a.eps = d.eps;
+    a.rms_in = l->rms;   // written by this chunk's router for every token
     a.ws = l->grouped_ws;
     a.ws_bytes = l->grouped_bytes;
     a.waves = &wv;

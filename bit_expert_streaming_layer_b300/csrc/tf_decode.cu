@@ -104,130 +104,115 @@ k_router_topk(const uint16_t* __restrict__ x, int H, const uint16_t* __restrict_
 
 // ----------------------------------------------------- router for many tokens
 //
-// The same logits as k_router_topk, computed for a tile of tokens against a
-// block of TE experts whose rows are held in shared memory as fp32 (converted
+// The same logits as k_router_topk, computed for a run of tokens against a
+// block of EW experts whose rows are held in shared memory as fp32 (converted
 // once per CTA, reused by every token of the CTA). The fixed summation order is
-// kept exactly: the canonical sum has 32 partials, partial r summing the terms
-// k = r, r + 32, r + 64, ... in increasing k, then a xor butterfly 16, 8, 4, 2,
-// 1. Here a quad of four threads owns one token; thread m of the quad keeps the
-// eight partials r = 8m .. 8m + 7 (one 16-byte load of x covers its eight k of
-// a 32-wide step, in increasing k for every partial). The butterfly steps 16
-// and 8 pair partials of threads m ^ 2 and m ^ 1 (shuffles inside the quad), the
-// steps 4, 2 and 1 pair partials inside a thread. Products of two bf16 values
-// are exact in fp32, so each fused multiply-add rounds once, as in the
-// canonical sum.
+// kept exactly: the canonical sum has 32 partials, partial p summing the terms
+// k = p, p + 32, p + 64, ... in increasing k, then a xor butterfly 16, 8, 4, 2,
+// 1. Here lane p of a warp owns partial p (so a warp reads 32 consecutive
+// values of x and of each W_r row per step: coalesced, no bank conflicts) of
+// TT tokens x EW experts at a time (each W_r value read from shared memory
+// serves TT tokens), and the butterfly runs across the lanes.
+// Products of two bf16 values are exact in fp32, so each fused multiply-add
+// rounds once, as in the canonical sum; fp32 addition is commutative, so every
+// lane ends with the canonical value.
 
-constexpr int RTT_THREADS = 256;
-constexpr int RTT_TOKENS = RTT_THREADS / 4;   // tokens in flight per CTA (one per quad)
-constexpr int RTT_SMEM_MAX = 227 * 1024;      // the expert block of W_r as fp32 (TE * H * 4 bytes) fits this
-constexpr int RTT_AHEAD = 8;                  // loads of x in flight per thread
+constexpr int RL_THREADS = 256;
+constexpr int RL_WARPS = RL_THREADS / 32;
+constexpr int RL_SMEM_MAX = 227 * 1024;   // the expert block of W_r as fp32 (EW * H * 4 bytes) fits this
+constexpr int RL_WLOADS = 6;              // loads of W_r in flight per thread while the block is filled
 
-__device__ __forceinline__ unsigned long long rt_pk2(float lo, float hi) {
-    unsigned long long r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void rt_unpk2(unsigned long long v, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ void rt_fma2(unsigned long long& acc, unsigned long long a, unsigned long long b) {
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
-}
-// The quad's butterfly of the 32 partials held as four packed pairs per thread
-// (pair p = partials 8m + 2p, 8m + 2p + 1): the canonical sum, equal in all four threads.
-__device__ __forceinline__ float quad_canonical(const unsigned long long (&a)[4]) {
-    float v[8];
+__device__ __forceinline__ float lane_butterfly(float v) {
 #pragma unroll
-    for (int p = 0; p < 4; ++p) rt_unpk2(a[p], v[2 * p], v[2 * p + 1]);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = __fadd_rn(v[i], __shfl_xor_sync(FULL, v[i], 2));   // step 16
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = __fadd_rn(v[i], __shfl_xor_sync(FULL, v[i], 1));   // step 8
-    const float u0 = __fadd_rn(v[0], v[4]), u1 = __fadd_rn(v[1], v[5]);                   // step 4
-    const float u2 = __fadd_rn(v[2], v[6]), u3 = __fadd_rn(v[3], v[7]);
-    const float w0 = __fadd_rn(u0, u2), w1 = __fadd_rn(u1, u3);                           // step 2
-    return __fadd_rn(w0, w1);                                                               // step 1
+    for (int d = 16; d; d >>= 1) v = __fadd_rn(v, __shfl_xor_sync(FULL, v, d));
+    return v;
 }
 
-template <int TE>
-__global__ void __launch_bounds__(RTT_THREADS)
-k_router_tiled(const uint16_t* __restrict__ x, int T, int H, const uint16_t* __restrict__ Wr, int E,
+template <int EW, int TT, int AHEAD = 8>   // AHEAD: steps of x loaded ahead of their products
+__global__ void __launch_bounds__(RL_THREADS)
+k_router_lanes(const uint16_t* __restrict__ x, int T, int H, const uint16_t* __restrict__ Wr, int E,
                const float* __restrict__ bias, int bias_stride, float* __restrict__ logits,
                float* __restrict__ rms, float eps, int tokens_per_cta) {
-    extern __shared__ float4 rts4[];
-    float* wsm = reinterpret_cast<float*>(rts4);   // [TE][H] fp32
-    const int e0 = blockIdx.x * TE;
+    extern __shared__ float4 rl4[];
+    float* wsm = reinterpret_cast<float*>(rl4);   // [EW][H] fp32
+    const int e0 = blockIdx.x * EW;
     const int nv = H / 8;
-    for (int v = threadIdx.x; v < TE * nv; v += blockDim.x) {
-        const int e = v / nv, c = v - e * nv;
-        uint4 wv = make_uint4(0u, 0u, 0u, 0u);
-        if (e0 + e < E) wv = __ldg(reinterpret_cast<const uint4*>(Wr + (size_t)(e0 + e) * H) + c);
-        float4* d = reinterpret_cast<float4*>(wsm + (size_t)e * H + 8 * c);
-        d[0] = make_float4(bf_lo(wv.x), bf_hi(wv.x), bf_lo(wv.y), bf_hi(wv.y));
-        d[1] = make_float4(bf_lo(wv.z), bf_hi(wv.z), bf_lo(wv.w), bf_hi(wv.w));
+    // the block's rows, RL_WLOADS 16-byte loads in flight per thread before their conversions
+    for (int v0 = threadIdx.x; v0 < EW * nv; v0 += RL_WLOADS * RL_THREADS) {
+        uint4 wv[RL_WLOADS];
+#pragma unroll
+        for (int u = 0; u < RL_WLOADS; ++u) {
+            const int v = v0 + u * RL_THREADS, e = v / nv, c = v - e * nv;
+            wv[u] = v < EW * nv && e0 + e < E ? __ldg(reinterpret_cast<const uint4*>(Wr + (size_t)(e0 + e) * H) + c)
+                                              : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < RL_WLOADS; ++u) {
+            const int v = v0 + u * RL_THREADS, e = v / nv, c = v - e * nv;
+            if (v < EW * nv) {
+                float4* d = reinterpret_cast<float4*>(wsm + (size_t)e * H + 8 * c);
+                d[0] = make_float4(bf_lo(wv[u].x), bf_hi(wv[u].x), bf_lo(wv[u].y), bf_hi(wv[u].y));
+                d[1] = make_float4(bf_lo(wv[u].z), bf_hi(wv[u].z), bf_lo(wv[u].w), bf_hi(wv[u].w));
+            }
+        }
     }
     __syncthreads();
-    const int quad = threadIdx.x >> 2, m = threadIdx.x & 3;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.y * tokens_per_cta;
     const int t1 = min(T, t0 + tokens_per_cta);
-    for (int base = t0; base < t1; base += RTT_TOKENS) {   // uniform trip count: every quad takes part
-        const int t = base + quad;
-        const bool valid = t < t1;
-        const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)(valid ? t : t0) * H);
-        unsigned long long acc[TE][4], sq[4];
+    const int nj = H / 32;
+    for (int tb = t0 + warp * TT; tb < t1; tb += RL_WARPS * TT) {
+        const uint16_t* xr[TT];
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            sq[p] = 0ull;
+        for (int i = 0; i < TT; ++i) xr[i] = x + (size_t)(tb + i < t1 ? tb + i : tb) * H + lane;
+        float acc[TT][EW], sq[TT];
 #pragma unroll
-            for (int e = 0; e < TE; ++e) acc[e][p] = 0ull;
+        for (int i = 0; i < TT; ++i) {
+            sq[i] = 0.0f;
+#pragma unroll
+            for (int e = 0; e < EW; ++e) acc[i][e] = 0.0f;
         }
-        // eight loads of x in flight ahead of the products (a register ring with fixed indices), so that their
-        // latency overlaps the products of the previous steps
-        const int nj = H / 32;
-        uint4 ring[RTT_AHEAD];
+        for (int j0 = 0; j0 < nj; j0 += AHEAD) {
+            float xv[AHEAD][TT];
 #pragma unroll
-        for (int a = 0; a < RTT_AHEAD; ++a) ring[a] = a < nj ? __ldg(xr + 4 * a + m) : make_uint4(0u, 0u, 0u, 0u);
-        for (int j0 = 0; j0 < nj; j0 += RTT_AHEAD) {
+            for (int a = 0; a < AHEAD; ++a)
 #pragma unroll
-            for (int a = 0; a < RTT_AHEAD; ++a) {
-                const int j = j0 + a;
-                if (j < nj) {
-                    const uint4 xv = ring[a];   // k = 32 j + 8 m .. 32 j + 8 m + 7
-                    if (j + RTT_AHEAD < nj) ring[a] = __ldg(xr + 4 * (j + RTT_AHEAD) + m);
-                    const unsigned long long x01 = rt_pk2(bf_lo(xv.x), bf_hi(xv.x));
-                    const unsigned long long x23 = rt_pk2(bf_lo(xv.y), bf_hi(xv.y));
-                    const unsigned long long x45 = rt_pk2(bf_lo(xv.z), bf_hi(xv.z));
-                    const unsigned long long x67 = rt_pk2(bf_lo(xv.w), bf_hi(xv.w));
-                    rt_fma2(sq[0], x01, x01);
-                    rt_fma2(sq[1], x23, x23);
-                    rt_fma2(sq[2], x45, x45);
-                    rt_fma2(sq[3], x67, x67);
-                    const float* wk = wsm + 32 * j + 8 * m;
+                for (int i = 0; i < TT; ++i)
+                    xv[a][i] = j0 + a < nj ? __uint_as_float((uint32_t)__ldg(xr[i] + 32 * (j0 + a)) << 16) : 0.0f;
 #pragma unroll
-                    for (int e = 0; e < TE; ++e) {
-                        const float4 wa = *reinterpret_cast<const float4*>(wk + (size_t)e * H);
-                        const float4 wb = *reinterpret_cast<const float4*>(wk + (size_t)e * H + 4);
-                        rt_fma2(acc[e][0], rt_pk2(wa.x, wa.y), x01);
-                        rt_fma2(acc[e][1], rt_pk2(wa.z, wa.w), x23);
-                        rt_fma2(acc[e][2], rt_pk2(wb.x, wb.y), x45);
-                        rt_fma2(acc[e][3], rt_pk2(wb.z, wb.w), x67);
+            for (int a = 0; a < AHEAD; ++a) {
+                if (j0 + a < nj) {   // partial `lane`, term k = 32 (j0 + a) + lane: increasing k
+                    const float* wk = wsm + 32 * (j0 + a) + lane;
+#pragma unroll
+                    for (int i = 0; i < TT; ++i) sq[i] = __fmaf_rn(xv[a][i], xv[a][i], sq[i]);
+#pragma unroll
+                    for (int e = 0; e < EW; ++e) {
+                        const float w = wk[(size_t)e * H];
+#pragma unroll
+                        for (int i = 0; i < TT; ++i) acc[i][e] = __fmaf_rn(w, xv[a][i], acc[i][e]);
                     }
                 }
             }
         }
-        const float ss = quad_canonical(sq);
-        const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)H), eps)));
 #pragma unroll
-        for (int e = 0; e < TE; ++e) {
-            const float d = quad_canonical(acc[e]);
-            const int ge = e0 + e;
-            if (valid && (e & 3) == m && ge < E) {
-                float z = __fmul_rn(r, d);
+        for (int i = 0; i < TT; ++i) {
+            const int t = tb + i;
+            const float ss = lane_butterfly(sq[i]);
+            const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)H), eps)));
+            float mine = 0.0f;
+#pragma unroll
+            for (int e = 0; e < EW; ++e) {
+                const float d = lane_butterfly(acc[i][e]);
+                if (lane == e) mine = d;
+            }
+            const int ge = e0 + lane;
+            if (t < t1 && lane < EW && ge < E) {
+                float z = __fmul_rn(r, mine);
                 if (bias) z = __fadd_rn(z, bias[(size_t)t * bias_stride + ge]);
                 logits[(size_t)t * E + ge] = z;
             }
+            if (t < t1 && lane == 0 && blockIdx.x == 0 && rms) rms[t] = r;
         }
-        if (valid && m == 0 && blockIdx.x == 0 && rms) rms[t] = r;
     }
 }
 
@@ -520,25 +505,34 @@ static int sm_count();
 static int launch_router_many(const uint16_t* x, int T, int H, const uint16_t* Wr, int E, const float* bias,
                               int bias_stride, int k, int32_t* idx, float* w, float* logits, float* rms, float eps,
                               cudaStream_t st) {
-    const bool wide = T >= 512;
-    const int TE = wide ? 8 : 2;
-    const int gx = (E + TE - 1) / TE;
+    // eight experts per CTA where their rows fit shared memory, else two; a warp takes one token at a time
+    // for small batches (more CTAs) and four for large ones (four tokens per load of W_r; eight measured slower)
+    const bool ew8 = (size_t)8 * H * 4 <= (size_t)RL_SMEM_MAX;
+    const int EW = ew8 ? 8 : 2;
+    if ((size_t)EW * H * 4 > (size_t)RL_SMEM_MAX) return (int)cudaErrorInvalidValue;   // H beyond one CTA
+    const bool wide = T > 256;
+    const int TT = wide ? 4 : 1;
+    const int gx = (E + EW - 1) / EW;
+    const int step = RL_WARPS * TT;                 // tokens of one pass of the CTA's warps
     const int target = 2 * sm_count();
     int gy = (target + gx - 1) / gx;
     int per = (T + gy - 1) / gy;
-    per = (per + RTT_TOKENS - 1) / RTT_TOKENS * RTT_TOKENS;   // whole passes of one token per quad
+    per = (per + step - 1) / step * step;
     gy = (T + per - 1) / per;
-    const size_t smem = (size_t)TE * H * 4;
-    if (smem > (size_t)RTT_SMEM_MAX) return (int)cudaErrorInvalidValue;   // H beyond what one CTA can hold
+    const size_t smem = (size_t)EW * H * 4;
+    const void* kern = ew8 ? (wide ? (const void*)k_router_lanes<8, 4> : (const void*)k_router_lanes<8, 1>)
+                           : (wide ? (const void*)k_router_lanes<2, 4> : (const void*)k_router_lanes<2, 1>);
     // the limit is raised once to the largest size any call may ask for (a smaller one would refuse later calls)
-    const void* kern = wide ? (const void*)k_router_tiled<8> : (const void*)k_router_tiled<2>;
-    if (int e = smem_limit_once(kern, RTT_SMEM_MAX)) return e;
-    if (wide)
-        k_router_tiled<8><<<dim3(gx, gy), RTT_THREADS, smem, st>>>(x, T, H, Wr, E, bias, bias_stride, logits, rms,
-                                                                   eps, per);
+    if (int e = smem_limit_once(kern, RL_SMEM_MAX)) return e;
+    const dim3 grid(gx, gy);
+    if (ew8 && wide)
+        k_router_lanes<8, 4><<<grid, RL_THREADS, smem, st>>>(x, T, H, Wr, E, bias, bias_stride, logits, rms, eps, per);
+    else if (ew8)
+        k_router_lanes<8, 1><<<grid, RL_THREADS, smem, st>>>(x, T, H, Wr, E, bias, bias_stride, logits, rms, eps, per);
+    else if (wide)
+        k_router_lanes<2, 4><<<grid, RL_THREADS, smem, st>>>(x, T, H, Wr, E, bias, bias_stride, logits, rms, eps, per);
     else
-        k_router_tiled<2><<<dim3(gx, gy), RTT_THREADS, smem, st>>>(x, T, H, Wr, E, bias, bias_stride, logits, rms,
-                                                                   eps, per);
+        k_router_lanes<2, 1><<<grid, RL_THREADS, smem, st>>>(x, T, H, Wr, E, bias, bias_stride, logits, rms, eps, per);
     const size_t tk_smem = (size_t)8 * E * 5;   // <= 40 KB for E <= 1024: within the default limit
     k_topk_rows<<<(T + 7) / 8, 256, tk_smem, st>>>(logits, T, E, k, idx, w);
     return (int)cudaGetLastError();
@@ -547,7 +541,7 @@ static int launch_router_many(const uint16_t* x, int T, int H, const uint16_t* W
 int launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* Wr, int E, const float* bias,
                        int bias_stride, int k, int32_t* idx, float* w, float* logits, float* rms,
                        uint32_t* counters, float eps, void* stream) {
-    if (T > 1 && (size_t)(T >= 512 ? 8 : 2) * H * 4 <= (size_t)RTT_SMEM_MAX) {
+    if (T > 1 && (size_t)2 * H * 4 <= (size_t)RL_SMEM_MAX) {
         prof_before(TF_KERNEL_ROUTER, stream);
         const int e = launch_router_many(x, T, H, Wr, E, bias, bias_stride, k, idx, w, logits, rms, eps,
                                          (cudaStream_t)stream);

@@ -22,7 +22,10 @@
 //   warp 2      TMA producer of the token rows (2-D tensor map, SW128)
 //   warps 4..7  epilogue: tcgen05.ld, GELU-gate (gate/up) or plain (down), store
 //   warps 8..23 dequant, two groups of eight warps on alternate K stages:
-//               codes -> 16-bit RN(s q + b) into the SW128 A tile
+//               codes -> 16-bit RN(s q + b) into the SW128 A tile; the first
+//               warp of a group also waits for the stage's token tile, so that
+//               "A full" stands for both operands and the MMA warp, the serial
+//               part of the pipeline, waits once per stage.
 // Every ring (codes, A, tokens) is sized by the launch's shared-memory plan;
 // the weight producer runs ahead of the MMAs by as many code stages as fit.
 // Numerics: 16-bit operands, fp32 accumulation in TMEM. The token operand is
@@ -70,12 +73,12 @@ constexpr int BM = 128;                // weight rows per GEMM tile (MMA M)
 constexpr int BK = 64;                 // K per pipeline stage (one quant group, 128 bytes of 16-bit values)
 constexpr int BOX_SMALL = 16;          // token rows per TMA box for tiles of up to 64 rows
 constexpr int BOX_BIG = 128;           // ... and for larger tiles (two loads per 256-row stage)
-constexpr int NBST = 3;                // token (B) stages
+constexpr int NBST_MAX = 8;            // token (B) stages: as many as the plan gives
 constexpr int NA_MAX = 12, NCS_MAX = 8;    // weight (A) and code stages: as many as shared memory holds
 constexpr int CW = 4;                  // K stages per code stage: 128 contiguous bytes of each weight row per load
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB
 constexpr int C_BYTES = BM * BK * CW / 2;        // 16 KB of codes per code stage
-constexpr int SB_MAX = BM * (2816 / 64) * 4;     // 22,528 B of {s,b} per tile (K up to 2816)
+constexpr int SMALL_DEPTH = 5;         // A and token stages for tiles of up to 64 token rows
 constexpr int N_DQ_WARPS = 8;                  // warps of one dequant group: one weight row pair per thread pair
 constexpr int N_DQ_GROUPS = 2;                 // dequant groups, taking alternate K stages
 constexpr int GEMM_THREADS = (8 + N_DQ_GROUPS * N_DQ_WARPS) * 32;
@@ -85,9 +88,9 @@ enum {
     BAR_CE = BAR_CF + NCS_MAX,       // codes empty [NCS_MAX]
     BAR_AF = BAR_CE + NCS_MAX,       // A full [NA_MAX]
     BAR_AE = BAR_AF + NA_MAX,        // A empty [NA_MAX]
-    BAR_BF = BAR_AE + NA_MAX,        // B full [NBST]
-    BAR_BE = BAR_BF + NBST,          // B empty [NBST]
-    BAR_SF = BAR_BE + NBST,          // sb full [2]
+    BAR_BF = BAR_AE + NA_MAX,        // B full [NBST_MAX]
+    BAR_BE = BAR_BF + NBST_MAX,      // B empty [NBST_MAX]
+    BAR_SF = BAR_BE + NBST_MAX,      // sb full [2]
     BAR_SE = BAR_SF + 2,             // sb empty [2]
     BAR_DF = BAR_SE + 2,             // accumulator full [2]
     BAR_DE = BAR_DF + 2,             // accumulator empty [2]
@@ -103,7 +106,8 @@ static_assert(A_BYTES % 1024 == 0, "SW128 tiles");
 // the CUDA cores) or weight stages (bf16 weights by TMA), so that enough bytes
 // are in flight per SM for small tiles too.
 struct Layout {
-    int na, ncs;        // A stages (3 when dequantised), code stages (0 for bf16 weights)
+    int na, ncs, nb;    // A stages, code stages (0 for bf16 weights), token (B) stages
+    int sb_stage;       // bytes of one tile's {s,b} words (two buffers; 0 for bf16 weights)
     int b_stage;        // bytes of one token stage
     int box_big;        // 1: tiles over 64 rows load 128-row boxes
     int off_b, off_c, off_sb, off_bar;
@@ -273,6 +277,20 @@ __device__ bool wait_own(uint32_t bar, uint32_t parity, uint32_t* err) {
     }
 }
 
+// The same wait by every lane of a warp (they read the same barrier state);
+// lane 0's verdict is the warp's.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, uint32_t* err,
+                                          unsigned long long limit) {
+    const int ok = wait_bar(bar, parity, abort_flag, err, limit) ? 1 : 0;
+    return __shfl_sync(FULL, ok, 0) != 0;
+}
+// One lane of a converged warp, chosen by the hardware.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t e;
+    asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n" : "=r"(e));
+    return e != 0;
+}
+
 // Slot and phase of a ring of n stages, advanced one stage at a time.
 struct Ring {
     int i = 0, ph = 0;
@@ -333,11 +351,10 @@ __device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigne
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
 }
-// Eight codes of one word -> eight 16-bit weights RN(fl(s q + b)) packed in a uint4,
-// fp16 (F16) or bf16: (128 + q) - 128 is exact, s q is exact, so each weight takes
-// one fp32 rounding, then one to 16 bits. Columns 2j and 2j+1 share a packed pair.
-template <bool F16>
-__device__ __forceinline__ uint4 dequant8(uint32_t q, float s, float b) {
+// Eight codes of one word -> eight bf16 weights RN(fl(s q + b)) packed in a uint4, in
+// the natural K order: (128 + q) - 128 is exact, s q is exact, so each weight takes
+// one fp32 rounding, then one to bf16. Columns 2j and 2j+1 share a packed pair.
+__device__ __forceinline__ uint4 dequant8_bf16(uint32_t q, float s, float b) {
     const uint32_t lo = q & 0x0f0f0f0fu, hi = (q >> 4) & 0x0f0f0f0fu;  // codes 0,2,4,6 / 1,3,5,7
     const unsigned long long S2 = pk2(s, s), B2 = pk2(b, b), M2 = pk2(-128.0f, -128.0f);
     const unsigned long long q0 = add2(pk2(byte128<0>(lo), byte128<0>(hi)), M2);
@@ -350,13 +367,38 @@ __device__ __forceinline__ uint4 dequant8(uint32_t q, float s, float b) {
     for (int j = 0; j < 4; ++j) {
         float a, c;
         unpk2(w[j], a, c);
-        if constexpr (F16) {
-            const __half2 v = __floats2half2_rn(a, c);
-            o[j] = *reinterpret_cast<const uint32_t*>(&v);
-        } else {
-            const __nv_bfloat162 v = __floats2bfloat162_rn(a, c);
-            o[j] = *reinterpret_cast<const uint32_t*>(&v);
-        }
+        const __nv_bfloat162 v = __floats2bfloat162_rn(a, c);
+        o[j] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Order of the K columns inside every block of 8 in the fp16 operands of the routed gate/up GEMM:
+// position p of a block holds column KPERM[p] = (0, 4, 1, 5, 2, 6, 3, 7)[p] (column c sits at
+// position 2 (c & 3) + (c >> 2)). Both operands take the same order, so the products and their
+// sum over K are those of the natural order; the order lets one mask pick two codes of a word.
+constexpr int kperm_pos(int c) { return ((c & 3) << 1) | (c >> 2); }
+static_assert(kperm_pos(0) == 0 && kperm_pos(4) == 1 && kperm_pos(1) == 2 && kperm_pos(5) == 3 && kperm_pos(2) == 4 &&
+                  kperm_pos(6) == 5 && kperm_pos(3) == 6 && kperm_pos(7) == 7,
+              "K order of the fp16 gate/up operands");
+
+// Eight codes of one word (code 2j in the low nibble of byte j, 2j+1 in the high one) -> eight
+// fp16 weights RN(s q + b), one rounding of the exact value (fma.rn.f16x2; s, b and the integer q
+// are exact fp16 operands), in the K order above. A nibble at bits 0-3 of a half under the
+// exponent of 1024 (0x6400) reads 1024 + q, one at bits 4-7 under that of 64 (0x5400) reads
+// 64 + q; the subtraction of 1024 or 64 is exact. s2, b2: (s, s) and (b, b).
+__device__ __forceinline__ uint4 dequant8_f16(uint32_t q, uint32_t s2, uint32_t b2) {
+    const uint32_t q8 = q >> 8;
+    const uint32_t t[4] = {(q & 0x000f000fu) | 0x64006400u,    // codes 0, 4
+                           (q & 0x00f000f0u) | 0x54005400u,    // codes 1, 5
+                           (q8 & 0x000f000fu) | 0x64006400u,   // codes 2, 6
+                           (q8 & 0x00f000f0u) | 0x54005400u};  // codes 3, 7
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t v;
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(v) : "r"(t[j]), "r"((j & 1) ? 0x54005400u : 0x64006400u));
+        asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(o[j]) : "r"(s2), "r"(v), "r"(b2));
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
@@ -367,7 +409,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int NA = p.lay.na, NCS = p.lay.ncs;
+    const int NA = p.lay.na, NCS = p.lay.ncs, NBST = p.lay.nb;
     const int OFF_A = 0, OFF_B = p.lay.off_b, OFF_C = p.lay.off_c, OFF_SB = p.lay.off_sb;
     const int B_BYTES = p.lay.b_stage;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.lay.off_bar);
@@ -412,34 +454,37 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
     if (warp == 0 || warp == 2) {
         // ================================================ TMA producers: the weights (warp 0: {s,b} and codes, or
-        // bf16 weight tiles) and the token tiles (warp 2) are issued by two threads, so that the weight stream
-        // runs as far ahead as its own ring allows instead of in step with the three token stages
-        if (lane == 0) {
-            const bool wprod = warp == 0;
-            int ci = 0, bi = 0, ai = 0, it_local = 0, si = 0;   // copies issued (for the drains below)
-            Ring cr, br, ar;
-            bool ok = true;
-            for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
-                const Item it = decode_item(p, w);
-                const int ks0 = it.kc * KS;
-                if (wprod) {
-                    const int se = p.slot_of ? __ldg(p.slot_of + it.e) : it.e;   // where the expert's weights are
-                    if (!p.a_bf16) {
-                        const int sbi = it_local & 1;
-                        if (!(ok = wait_bar(bar(BAR_SE + sbi), ((it_local >> 1) & 1) ^ 1, abort_flag, p.err,
-                                            p.dep_limit_ns)))
-                            break;
-                        ++si;
+        // bf16 weight tiles) and the token tiles (warp 2) have a warp each, so that the weight stream runs as far
+        // ahead as its own ring allows instead of in step with the three token stages. The whole warp walks the
+        // loop and waits; one elected lane issues.
+        const bool wprod = warp == 0;
+        int ci = 0, bi = 0, ai = 0, it_local = 0, si = 0;   // copies issued (for the drains below)
+        Ring cr, br, ar;
+        bool ok = true;
+        for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
+            const Item it = decode_item(p, w);
+            const int ks0 = it.kc * KS;
+            if (wprod) {
+                const int se = p.slot_of ? __ldg(p.slot_of + it.e) : it.e;   // where the expert's weights are
+                if (!p.a_bf16) {
+                    const int sbi = it_local & 1;
+                    if (!(ok = warp_wait(bar(BAR_SE + sbi), ((it_local >> 1) & 1) ^ 1, abort_flag, p.err, p.dep_limit_ns)))
+                        break;
+                    ++si;
+                    if (elect_one()) {
                         const uint32_t sb_bytes = (uint32_t)(BM * gpr * 4);
                         mbar_expect_tx(bar(BAR_SF + sbi), sb_bytes);
-                        bulk_g2s(smem_u32(smem + OFF_SB + sbi * SB_MAX),
+                        bulk_g2s(smem_u32(smem + OFF_SB + sbi * p.lay.sb_stage),
                                  p.ebase + (size_t)se * p.estride + p.off_sb + (size_t)it.mt * BM * gpr * 4, sb_bytes,
                                  bar(BAR_SF + sbi));
                     }
-                    for (int ks = 0; ks < KS; ++ks) {
-                        if (p.a_bf16) {
-                            const int as = ar.i;
-                            if (!(ok = wait_bar(bar(BAR_AE + as), ar.ph ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
+                    __syncwarp();
+                }
+                for (int ks = 0; ks < KS; ++ks) {
+                    if (p.a_bf16) {
+                        const int as = ar.i;
+                        if (!(ok = warp_wait(bar(BAR_AE + as), ar.ph ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
+                        if (elect_one()) {
                             mbar_expect_tx(bar(BAR_AF + as), A_BYTES);
                             const uint32_t dst = smem_u32(smem + OFF_A + as * A_BYTES);
                             if (p.mode == 0) {
@@ -453,82 +498,95 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             } else {
                                 tma_load_2d(dst, &tmA, (ks0 + ks) * BK, it.mt * BM, bar(BAR_AF + as));
                             }
-                            ++ai;
-                            ar.next(NA);
-                        } else if (ks % CW == 0) {
-                            // codes of the next CW stages: 128 contiguous bytes of each of the tile's 128 rows (past
-                            // the end of a row, as for the last stages of the down matrix, the box reads zeros)
-                            const int cs = cr.i;
-                            if (!(ok = wait_bar(bar(BAR_CE + cs), cr.ph ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
+                        }
+                        __syncwarp();
+                        ++ai;
+                        ar.next(NA);
+                    } else if (ks % CW == 0) {
+                        // codes of the next CW stages: 128 contiguous bytes of each of the tile's 128 rows (past
+                        // the end of a row, as for the last stages of the down matrix, the box reads zeros)
+                        const int cs = cr.i;
+                        if (!(ok = warp_wait(bar(BAR_CE + cs), cr.ph ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
+                        if (elect_one()) {
                             mbar_expect_tx(bar(BAR_CF + cs), C_BYTES);
                             tma_load_3d(smem_u32(smem + OFF_C + cs * C_BYTES), &tmA, (ks0 + ks) * (BK / 2), it.mt * BM,
                                         se, bar(BAR_CF + cs));
-                            ++ci;
-                            cr.next(NCS);
                         }
+                        __syncwarp();
+                        ++ci;
+                        cr.next(NCS);
                     }
-                } else {
-                    const bool big = p.lay.box_big && it.nrows > 64;
-                    const int box = big ? BOX_BIG : BOX_SMALL;
-                    const int nbox = (it.nrows + box - 1) / box;
-                    for (int ks = 0; ks < KS; ++ks) {
-                        const int bs = br.i;
-                        if (!(ok = wait_bar(bar(BAR_BE + bs), br.ph ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
+                }
+            } else {
+                const bool big = p.lay.box_big && it.nrows > 64;
+                const int box = big ? BOX_BIG : BOX_SMALL;
+                const int nbox = (it.nrows + box - 1) / box;
+                for (int ks = 0; ks < KS; ++ks) {
+                    // with dequantised weights the token ring is the A ring (same depth): a token slot is free
+                    // when the MMAs of its stage have completed, as the A slot
+                    const int bs = br.i;
+                    if (!(ok = warp_wait(bar((p.a_bf16 ? BAR_BE : BAR_AE) + bs), br.ph ^ 1, abort_flag, p.err,
+                                         p.dep_limit_ns)))
+                        break;
+                    if (elect_one()) {
                         mbar_expect_tx(bar(BAR_BF + bs), (uint32_t)(nbox * box * BK * 2));
                         for (int r = 0; r < nbox; ++r)
                             tma_load_2d(smem_u32(smem + OFF_B + bs * B_BYTES + r * box * BK * 2), big ? &tmB2 : &tmB,
                                         (ks0 + ks) * BK, it.row0 + r * box, bar(BAR_BF + bs));
-                        ++bi;
-                        br.next(NBST);
                     }
+                    __syncwarp();
+                    ++bi;
+                    br.next(NBST);
                 }
             }
-            // let every copy this thread issued land before the CTA can exit (also after an abort)
-            for (int j = ci - NCS; j < ci; ++j)
-                if (j >= 0) wait_own(bar(BAR_CF + j % NCS), (j / NCS) & 1, p.err);
-            for (int j = bi - NBST; j < bi; ++j)
-                if (j >= 0) wait_own(bar(BAR_BF + j % NBST), (j / NBST) & 1, p.err);
-            for (int j = ai - NA; j < ai; ++j)
-                if (j >= 0) wait_own(bar(BAR_AF + j % NA), (j / NA) & 1, p.err);
-            for (int j = si - 2; j < si; ++j)   // the {s,b} copies of the last two items
-                if (j >= 0) wait_own(bar(BAR_SF + (j & 1)), (j >> 1) & 1, p.err);
         }
+        // let every copy this warp issued land before the CTA can exit (also after an abort)
+        for (int j = ci - NCS; j < ci; ++j)
+            if (j >= 0) wait_own(bar(BAR_CF + j % NCS), (j / NCS) & 1, p.err);
+        for (int j = bi - NBST; j < bi; ++j)
+            if (j >= 0) wait_own(bar(BAR_BF + j % NBST), (j / NBST) & 1, p.err);
+        for (int j = ai - NA; j < ai; ++j)
+            if (j >= 0) wait_own(bar(BAR_AF + j % NA), (j / NA) & 1, p.err);
+        for (int j = si - 2; j < si; ++j)   // the {s,b} copies of the last two items
+            if (j >= 0) wait_own(bar(BAR_SF + (j & 1)), (j >> 1) & 1, p.err);
     } else if (warp == 1) {
-        // ================================================ MMA issuer
-        if (lane == 0) {
-            int ai = 0, it_local = 0;
-            Ring ar, br;
-            bool ok = true;
-            for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
-                const Item it = decode_item(p, w);
-                const int ab = it_local & 1;
-                if (!(ok = wait_bar(bar(BAR_DE + ab), ((it_local >> 1) & 1) ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
+        // ================================================ MMA issuer: the whole warp waits, one elected lane issues
+        int ai = 0, it_local = 0;
+        Ring ar, br;
+        bool ok = true;
+        for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
+            const Item it = decode_item(p, w);
+            const int ab = it_local & 1;
+            if (!(ok = warp_wait(bar(BAR_DE + ab), ((it_local >> 1) & 1) ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
+            tc_fence_after();
+            const int n_mma = ((it.nrows + 15) / 16) * 16;
+            const uint32_t idesc = idesc_f16(n_mma, !p.f16);
+            const uint32_t d_tmem = tmem + (uint32_t)(ab * NB);
+            for (int ks = 0; ks < KS; ++ks) {
+                const int as = ar.i, bs = br.i;
+                if (!(ok = warp_wait(bar(BAR_AF + as), ar.ph, abort_flag, p.err, p.dep_limit_ns))) break;
+                if (p.a_bf16 && !(ok = warp_wait(bar(BAR_BF + bs), br.ph, abort_flag, p.err, p.dep_limit_ns))) break;
                 tc_fence_after();
-                const int n_mma = ((it.nrows + 15) / 16) * 16;
-                const uint32_t idesc = idesc_f16(n_mma, !p.f16);
-                const uint32_t d_tmem = tmem + (uint32_t)(ab * NB);
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int as = ar.i, bs = br.i;
-                    if (!(ok = wait_bar(bar(BAR_AF + as), ar.ph, abort_flag, p.err, p.dep_limit_ns))) break;
-                    if (!(ok = wait_bar(bar(BAR_BF + bs), br.ph, abort_flag, p.err, p.dep_limit_ns))) break;
-                    tc_fence_after();
+                if (elect_one()) {
                     const uint64_t ad = sw128_desc(smem_u32(smem + OFF_A + as * A_BYTES));
                     const uint64_t bd = sw128_desc(smem_u32(smem + OFF_B + bs * B_BYTES));
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)  // 32 bytes of K per MMA: +2 in the start-address field
                         tc_mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (ks | k) != 0);
                     tc_commit(bar(BAR_AE + as));
-                    tc_commit(bar(BAR_BE + bs));
-                    ++ai;
-                    ar.next(NA);
-                    br.next(NBST);
+                    if (p.a_bf16) tc_commit(bar(BAR_BE + bs));
                 }
-                if (!ok) break;
-                tc_commit(bar(BAR_DF + ab));
+                __syncwarp();
+                ++ai;
+                ar.next(NA);
+                br.next(NBST);
             }
-            // the MMAs issued so far complete before TMEM is released (also after an abort)
-            if (ai > 0) wait_own(bar(BAR_AE + (ai - 1) % NA), ((ai - 1) / NA) & 1, p.err);
+            if (!ok) break;
+            if (elect_one()) tc_commit(bar(BAR_DF + ab));
+            __syncwarp();
         }
+        // the MMAs issued so far complete before TMEM is released (also after an abort)
+        if (ai > 0) wait_own(bar(BAR_AE + (ai - 1) % NA), ((ai - 1) / NA) & 1, p.err);
     } else if (warp >= 4 && warp < 8) {
         // ================================================ epilogue
         const int q = warp & 3;
@@ -608,32 +666,41 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 int okw = 1;
                 if (lane == 0) okw = wait_bar(bar(BAR_SF + sbi), (it_local >> 1) & 1, abort_flag, p.err, p.dep_limit_ns);
                 if (!(ok = __shfl_sync(FULL, okw, 0))) break;
-                const uint32_t* sbrow = reinterpret_cast<const uint32_t*>(smem + OFF_SB + sbi * SB_MAX) + r * gpr;
+                const uint32_t* sbrow = reinterpret_cast<const uint32_t*>(smem + OFF_SB + sbi * p.lay.sb_stage) + r * gpr;
                 for (int ks = 0; ks < KS; ++ks) {
                     const int sub = ks % CW;
                     const bool mine = g == grp;
-                    okw = 1;
-                    if (lane == 0) {
-                        if (sub == 0) okw = wait_bar(bar(BAR_CF + cr.i), cr.ph, abort_flag, p.err, p.dep_limit_ns);
-                        if (okw && mine) okw = wait_bar(bar(BAR_AE + ar.i), ar.ph ^ 1, abort_flag, p.err, p.dep_limit_ns);
-                    }
-                    if (!(ok = __shfl_sync(FULL, okw, 0))) break;
+                    if (sub == 0 && !(ok = warp_wait(bar(BAR_CF + cr.i), cr.ph, abort_flag, p.err, p.dep_limit_ns))) break;
+                    if (mine && !(ok = warp_wait(bar(BAR_AE + ar.i), ar.ph ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
                     if (mine) {
                         // the code box lands 128-byte swizzled: 16-byte chunk j of row r sits at chunk j ^ (r & 7),
                         // so the 16 rows a warp reads spread over all banks
                         const uint4 qv = *reinterpret_cast<const uint4*>(smem + OFF_C + cr.i * C_BYTES +
                                                                          r * (CW * BK / 2) + (((sub * 2 + hf) ^ (r & 7)) << 4));
                         const uint32_t sbw = sbrow[ks];
-                        const float s = h2f(sbw & 0xffffu), b = h2f(sbw >> 16);
                         unsigned char* arow = smem + OFF_A + ar.i * A_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
                         const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+                        if constexpr (F16) {
+                            const uint32_t s2 = __byte_perm(sbw, 0, 0x1010), b2 = __byte_perm(sbw, 0, 0x3232);
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const int chunk = hf * 4 + c;  // 16-byte chunk of the 128-byte row
-                            *reinterpret_cast<uint4*>(arow + ((chunk ^ (r & 7)) << 4)) = dequant8<F16>(qw[c], s, b);
+                            for (int c = 0; c < 4; ++c) {
+                                const int chunk = hf * 4 + c;  // 16-byte chunk (8 columns) of the 128-byte row
+                                *reinterpret_cast<uint4*>(arow + ((chunk ^ (r & 7)) << 4)) = dequant8_f16(qw[c], s2, b2);
+                            }
+                        } else {
+                            const float s = h2f(sbw & 0xffffu), b = h2f(sbw >> 16);
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                const int chunk = hf * 4 + c;
+                                *reinterpret_cast<uint4*>(arow + ((chunk ^ (r & 7)) << 4)) = dequant8_bf16(qw[c], s, b);
+                            }
                         }
                         fence_proxy_async();  // generic-proxy writes, read next by the tensor core
                         __syncwarp();
+                        // the stage's token tile has landed before its A stage is reported full
+                        if ((warp & (N_DQ_WARPS - 1)) == 0 &&
+                            !(ok = warp_wait(bar(BAR_BF + ar.i), ar.ph, abort_flag, p.err, p.dep_limit_ns)))
+                            break;
                         if (lane == 0) mbar_arrive(bar(BAR_AF + ar.i));
                     }
                     if (sub == CW - 1 || ks == KS - 1) {   // the code stage is used up
@@ -845,8 +912,9 @@ __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w, float p) {
 }
 
 // Row pos of the permuted activations: x_t p_t as fp16 (t = perm[pos] / k, p_t the
-// power of two of the RMS scale r_t = m_t p_t, m_t in [1, 2)), and m_t, the scale
-// of the row's gate and up sums.
+// power of two of the RMS scale r_t = m_t p_t, m_t in [1, 2)), its columns in the
+// order kperm_pos gives within each block of 8, and m_t, the scale of the row's
+// gate and up sums.
 __global__ void k_group_gather(const uint16_t* __restrict__ x, const float* __restrict__ rms,
                                const int32_t* __restrict__ perm, int P, int k, int H, uint16_t* xp,
                                float* __restrict__ rp) {
@@ -861,7 +929,10 @@ __global__ void k_group_gather(const uint16_t* __restrict__ x, const float* __re
     uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)pos * H);
     for (int v = lane; v < H / 8; v += 32) {
         const uint4 a = __ldg(src + v);
-        dst[v] = make_uint4(bf2_to_h2(a.x, p), bf2_to_h2(a.y, p), bf2_to_h2(a.z, p), bf2_to_h2(a.w, p));
+        const uint32_t h01 = bf2_to_h2(a.x, p), h23 = bf2_to_h2(a.y, p), h45 = bf2_to_h2(a.z, p), h67 = bf2_to_h2(a.w, p);
+        // columns (0, 4, 1, 5, 2, 6, 3, 7) of the block, the order of the dequantised gate/up weights
+        dst[v] = make_uint4(__byte_perm(h01, h45, 0x5410), __byte_perm(h01, h45, 0x7632), __byte_perm(h23, h67, 0x5410),
+                            __byte_perm(h23, h67, 0x7632));
     }
 }
 
@@ -871,11 +942,12 @@ __global__ void k_group_combine(const uint16_t* __restrict__ x, const float* __r
                                 const float* __restrict__ ys,
                                 const int32_t* __restrict__ inv, const float* __restrict__ w, int k, int H,
                                 const uint32_t* err, uint16_t* out, float* delta) {
-    const int t = blockIdx.x;
+    const int t = blockIdx.y;
+    const int j = (blockIdx.x * blockDim.x + threadIdx.x) * 4;   // four columns per thread
     if (*err) {  // a GEMM wait timed out: the outputs are NaN, never stale or partial values
-        for (int j = threadIdx.x; j < H; j += blockDim.x) {
-            out[(size_t)t * H + j] = 0x7fc0u;
-            if (delta) delta[(size_t)t * H + j] = __int_as_float(0x7fc00000);
+        for (int c = j; c < j + 4 && c < H; ++c) {
+            out[(size_t)t * H + c] = 0x7fc0u;
+            if (delta) delta[(size_t)t * H + c] = __int_as_float(0x7fc00000);
         }
         return;
     }
@@ -886,8 +958,9 @@ __global__ void k_group_combine(const uint16_t* __restrict__ x, const float* __r
         ws[threadIdx.x] = __ldg(w + (size_t)t * k + threadIdx.x);
     }
     __syncthreads();
-    for (int j = threadIdx.x * 4; j < H; j += blockDim.x * 4) {
+    if (j < H) {
         float4 acc = ys ? __ldg(reinterpret_cast<const float4*>(ys + (size_t)t * H + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
         for (int i = 0; i < k; ++i) {
             if (rows[i] < 0) continue;
             const float4 v = __ldg(reinterpret_cast<const float4*>(y + (size_t)rows[i] * H + j));
@@ -979,32 +1052,47 @@ bool encode_rows(CUtensorMap* m, const void* base, int cols, int rows, int box_r
                   CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// Shared-memory plan for token tiles of up to max_rows rows: bf16 weights by TMA
-// (a_bf16) or int4 codes dequantised into three A stages.
-Layout plan_layout(int max_rows, bool a_bf16) {
+// Shared-memory plan of one launch for token tiles of up to max_rows rows and a
+// reduction of K: bf16 weights by TMA (a_bf16) or int4 codes dequantised into A
+// stages. Tiles of up to 64 token rows stream weights: a stage's MMAs complete
+// about a microsecond after they are issued, so the A and token rings take
+// SMALL_DEPTH stages each (bf16 weights: as many as fit) and the rest goes to
+// code stages. Larger tiles are bound by the tensor core: three A and three
+// token stages, the rest to code stages (bf16 weights: to weight stages). na = 0
+// when nothing fits.
+Layout plan_layout(int max_rows, bool a_bf16, int K) {
     Layout l;
     std::memset(&l, 0, sizeof(l));
     int rows = max_rows > 64 ? (max_rows + BOX_BIG - 1) / BOX_BIG * BOX_BIG : (max_rows + 15) / 16 * 16;
     if (rows > NB) rows = NB;
-    l.box_big = max_rows > 64;
+    const bool small = max_rows <= 64;
+    l.box_big = !small;
     l.b_stage = rows * BK * 2;
-    const int b_region = NBST * l.b_stage;
     if (a_bf16) {
-        l.ncs = 0;
-        l.na = (SMEM_USABLE - b_region) / A_BYTES;
-        if (l.na > NA_MAX) l.na = NA_MAX;
+        if (small) {
+            l.na = SMEM_USABLE / (A_BYTES + l.b_stage);
+            if (l.na > NBST_MAX) l.na = NBST_MAX;
+            l.nb = l.na;
+        } else {
+            l.nb = 3;
+            l.na = (SMEM_USABLE - l.nb * l.b_stage) / A_BYTES;
+            if (l.na > NA_MAX) l.na = NA_MAX;
+        }
         l.off_b = l.na * A_BYTES;
-        l.off_c = l.off_b + b_region;
+        l.off_c = l.off_b + l.nb * l.b_stage;
         l.off_sb = l.off_c;
         l.off_bar = l.off_sb;
+        if (l.na < 2) l.na = 0;
     } else {
-        l.na = 3;
+        l.na = l.nb = small ? SMALL_DEPTH : 3;
+        l.sb_stage = BM * (K / 64) * 4;
         l.off_b = l.na * A_BYTES;
-        l.off_c = l.off_b + b_region;
-        l.ncs = (SMEM_USABLE - l.off_c - 2 * SB_MAX) / C_BYTES;
+        l.off_c = l.off_b + l.nb * l.b_stage;
+        l.ncs = (SMEM_USABLE - l.off_c - 2 * l.sb_stage) / C_BYTES;
         if (l.ncs > NCS_MAX) l.ncs = NCS_MAX;
         l.off_sb = l.off_c + l.ncs * C_BYTES;
-        l.off_bar = l.off_sb + 2 * SB_MAX;
+        l.off_bar = l.off_sb + 2 * l.sb_stage;
+        if (l.ncs < 1) l.na = 0;
     }
     return l;
 }
@@ -1057,6 +1145,12 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     expert_layout(H, I, &lay);
     if ((a.waves ? a.waves->slot_bytes : table->stride) < lay.payload)
         return fail(TF_ERR_INVALID_ARG, "%s: expert stride below the payload size", fn);
+    // the largest token tile of this call (an expert gets each token at most once) and the GEMMs' plans
+    const int max_rows = T < NB ? T : NB;
+    const Layout lay_gu = plan_layout(max_rows, false, H), lay_d = plan_layout(max_rows, false, I);
+    const Layout lay_sgu = plan_layout(max_rows, true, H), lay_sd = plan_layout(max_rows, true, S > 0 ? S : 64);
+    if (!lay_gu.na || !lay_d.na || !lay_sgu.na || !lay_sd.na)
+        return fail(TF_ERR_INVALID_ARG, "%s: H=%d I=%d do not fit the GEMM's shared memory", fn, H, I);
 
     char* ws = static_cast<char*>(a.ws);
     uint32_t* err = reinterpret_cast<uint32_t*>(ws + c.err);
@@ -1122,7 +1216,10 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     const int mt_gu = 2 * I / BM, mt_d = H / BM;
     const uint16_t* x16 = static_cast<const uint16_t*>(a.x);
     prof_before(TF_KERNEL_PERMUTE, stream);
-    k_group_rms<<<(T + 7) / 8, 256, 0, st>>>(x16, T, H, a.eps, rms);
+    if (a.rms_in)
+        rms = const_cast<float*>(a.rms_in);   // the router's scale of every token (the same canonical sum)
+    else
+        k_group_rms<<<(T + 7) / 8, 256, 0, st>>>(x16, T, H, a.eps, rms);
     k_group_hist<<<1, 1024, 0, st>>>(a.idx, P, E, mt_gu, mt_d, counts, offsets, tiles_gu, tiles_d, err);
     k_group_pos<<<E, 1024, 0, st>>>(a.idx, P, offsets, perm, inv);
     k_group_inv_init<<<(P + 255) / 256, 256, 0, st>>>(a.idx, P, E, inv);
@@ -1156,8 +1253,6 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     gp.ksplit = 1;
     gp.dep_limit_ns = test_wait_limit_ns();
 
-    // the largest token tile of this call: an expert gets each token at most once
-    const int max_rows = T < NB ? T : NB;
     auto routed_gemms = [&](const int32_t* slot_of) {
         gp.slot_of = slot_of;
         gp.off_sb = lay.gu_sb;
@@ -1170,7 +1265,7 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
         gp.ldo = I;
         gp.col_scale = rp;
         gp.f16 = 1;
-        gp.lay = plan_layout(max_rows, false);
+        gp.lay = lay_gu;
         k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmA_gu, tmB_gu, tmA_gu, tmB_gu2, gp);
         gp.off_sb = lay.d_sb;
         gp.K = I;
@@ -1181,6 +1276,7 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
         gp.yout = y;
         gp.ldo = H;
         gp.f16 = 0;
+        gp.lay = lay_d;
         k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmA_d, tmB_d, tmA_d, tmB_d2, gp);
     };
     prof_before(TF_KERNEL_GEMM, stream);
@@ -1220,7 +1316,7 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
         sp.col_scale = rms;          // the shared expert's token rows are the tokens in order
         sp.ksplit = ks_gu;
         sp.mrows = 2 * S;
-        sp.lay = plan_layout(max_rows, true);
+        sp.lay = lay_sgu;
         k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmS_g, tmS_xn, tmS_u, tmS_xn2, sp);
         if (ks_gu > 1) k_shared_gu_combine<<<dim3((S + 255) / 256, T), 256, 0, st>>>(spart, rms, ks_gu, T, S, hs);
         sp.K = S;
@@ -1232,6 +1328,7 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
         sp.ldo = H;
         sp.ksplit = ks_d;
         sp.mrows = H;
+        sp.lay = lay_sd;
         k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmS_d, tmS_h, tmS_d, tmS_h2, sp);
         if (ks_d > 1) k_shared_down_combine<<<dim3((H + 255) / 256, T), 256, 0, st>>>(spart, ks_d, T, H, ys);
     }
@@ -1239,7 +1336,8 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     if (cudaError_t e = cudaGetLastError()) return cuda_status(e, fn);
 
     prof_before(TF_KERNEL_COMBINE, stream);
-    k_group_combine<<<T, 256, 0, st>>>(x16, y, ys, inv, a.w, k, H, err, static_cast<uint16_t*>(a.out), a.delta);
+    k_group_combine<<<dim3((H / 4 + 127) / 128, T), 128, 0, st>>>(x16, y, ys, inv, a.w, k, H, err,
+                                                                  static_cast<uint16_t*>(a.out), a.delta);
     prof_after(TF_KERNEL_COMBINE, stream);
     if (a.perm_out) cudaMemcpyAsync(a.perm_out, perm, (size_t)P * 4, cudaMemcpyDeviceToDevice, st);
     if (a.counts_out) cudaMemcpyAsync(a.counts_out, counts, (size_t)E * 4, cudaMemcpyDeviceToDevice, st);

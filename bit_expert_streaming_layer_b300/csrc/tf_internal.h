@@ -134,6 +134,7 @@ struct GroupedArgs {
     const void* Wsd;               // bf16 [H, S]
     int S;
     float eps;
+    const float* rms_in;           // nullable device [T]: each token's RMS scale as the router computed it
     void* ws;
     size_t ws_bytes;
     const GroupedWaves* waves;     // nullable: the experts stream through a cache (else the table holds them all)
