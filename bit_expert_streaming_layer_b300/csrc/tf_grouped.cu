@@ -18,23 +18,31 @@
 //   warp 0      TMA producer of the weights: int4 codes (3-D tensor map over all
 //               experts, 128 bytes of each of 128 rows per copy = 4 K stages,
 //               128-byte swizzled) and scales/biases (bulk copy per tile)
-//   warp 1      TMEM owner; lane 0 issues tcgen05.mma and tcgen05.commit
+//   warp 1      TMEM owner and MMA issuer (one elected lane issues tcgen05.mma
+//               and tcgen05.commit; the warp waits as a whole)
 //   warp 2      TMA producer of the token rows (2-D tensor map, SW128)
+//   warp 3      second MMA issuer for tiles of up to 128 token rows: warps 1
+//               and 3 take the stages of even and odd running index into two
+//               accumulators, which the epilogue adds
 //   warps 4..7  epilogue: tcgen05.ld, GELU-gate (gate/up) or plain (down), store
 //   warps 8..23 dequant, two groups of eight warps on alternate K stages:
 //               codes -> 16-bit RN(s q + b) into the SW128 A tile; the first
 //               warp of a group also waits for the stage's token tile, so that
-//               "A full" stands for both operands and the MMA warp, the serial
-//               part of the pipeline, waits once per stage.
+//               "A full" stands for both operands and an MMA warp waits once
+//               per stage.
 // Every ring (codes, A, tokens) is sized by the launch's shared-memory plan;
-// the weight producer runs ahead of the MMAs by as many code stages as fit.
+// the weight producer runs ahead of the MMAs by as many code stages as fit. A
+// ring that two warps or groups read in turn has an even depth, so that a
+// waiter never skips a phase of a barrier it tests by parity.
 // Numerics: 16-bit operands, fp32 accumulation in TMEM. The token operand is
 // the layer input x itself and the RMS scale r of each token multiplies its
 // gate and up sums in the epilogue, as the router applies it after its dot
 // products: equal in real arithmetic to feeding r x, without rounding r x to
 // 16 bits (which alone cost up to 2.6 % against the fp32 layer in bf16). The
 // routed gate/up GEMM runs on fp16 operands: weights dequantised to fp16 (RN of
-// the fp32 s q + b) and x p, where p = 2^e is the power of two of the token's
+// the exact s q + b, one fma.rn.f16x2; the same as RN of the fp32 weight
+// whenever that is exact, as for every weight whose terms stay below 1 in
+// magnitude) and x p, where p = 2^e is the power of two of the token's
 // RMS scale r = m 2^e (m in [1, 2)): the scaling is exact and keeps the operand
 // near unit size (|x p| < 2 sqrt(H)) however large x grows, and m then
 // multiplies the gate and up sums. With the expert weights of the model
@@ -78,10 +86,9 @@ constexpr int NA_MAX = 12, NCS_MAX = 8;    // weight (A) and code stages: as man
 constexpr int CW = 4;                  // K stages per code stage: 128 contiguous bytes of each weight row per load
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB
 constexpr int C_BYTES = BM * BK * CW / 2;        // 16 KB of codes per code stage
-constexpr int SMALL_DEPTH = 5;         // A and token stages for tiles of up to 64 token rows
-constexpr int N_DQ_WARPS = 8;                  // warps of one dequant group: one weight row pair per thread pair
-constexpr int N_DQ_GROUPS = 2;                 // dequant groups, taking alternate K stages
-constexpr int GEMM_THREADS = (8 + N_DQ_GROUPS * N_DQ_WARPS) * 32;
+constexpr int N_DQ_WARPS = 8;          // warps of one dequant group: a weight row per pair of threads
+constexpr int N_DQ = 2 * N_DQ_WARPS;   // dequant warps (8 .. 23): two groups, taking alternate K stages
+constexpr int GEMM_THREADS = (8 + N_DQ) * 32;
 constexpr unsigned long long OWN_LIMIT_NS = 2000000000ull;   // waits for this thread's own copies and MMAs
 enum {
     BAR_CF = 0,                      // codes full [NCS_MAX]
@@ -108,6 +115,10 @@ static_assert(A_BYTES % 1024 == 0, "SW128 tiles");
 struct Layout {
     int na, ncs, nb;    // A stages, code stages (0 for bf16 weights), token (B) stages
     int sb_stage;       // bytes of one tile's {s,b} words (two buffers; 0 for bf16 weights)
+    int n_mma;          // MMA warps: 2 (tiles of up to 128 token rows: the stages of even / odd running index into
+                        // two accumulators, added by the epilogue) or 1
+    int acc_cols;       // TMEM columns of one accumulator (accumulator (item parity, MMA warp) at
+                        // column (parity * n_mma + warp) * acc_cols)
     int b_stage;        // bytes of one token stage
     int box_big;        // 1: tiles over 64 rows load 128-row boxes
     int off_b, off_c, off_sb, off_bar;
@@ -424,10 +435,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < NCS; ++i) {
             mbar_init(bar(BAR_CF + i), 1);
-            mbar_init(bar(BAR_CE + i), N_DQ_GROUPS * N_DQ_WARPS);
+            mbar_init(bar(BAR_CE + i), N_DQ);
         }
         for (int i = 0; i < NA; ++i) {
-            mbar_init(bar(BAR_AF + i), p.a_bf16 ? 1 : N_DQ_WARPS);  // TMA bytes, or the dequant warps
+            mbar_init(bar(BAR_AF + i), p.a_bf16 ? 1 : N_DQ_WARPS);  // TMA bytes, or a dequant group
             mbar_init(bar(BAR_AE + i), 1);
         }
         for (int i = 0; i < NBST; ++i) {
@@ -436,8 +447,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(BAR_SF + i), 1);
-            mbar_init(bar(BAR_SE + i), N_DQ_GROUPS * N_DQ_WARPS);
-            mbar_init(bar(BAR_DF + i), 1);
+            mbar_init(bar(BAR_SE + i), N_DQ);
+            mbar_init(bar(BAR_DF + i), p.lay.n_mma);
             mbar_init(bar(BAR_DE + i), 4);
         }
         *abort_flag = 0u;
@@ -549,10 +560,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (j >= 0) wait_own(bar(BAR_AF + j % NA), (j / NA) & 1, p.err);
         for (int j = si - 2; j < si; ++j)   // the {s,b} copies of the last two items
             if (j >= 0) wait_own(bar(BAR_SF + (j & 1)), (j >> 1) & 1, p.err);
-    } else if (warp == 1) {
-        // ================================================ MMA issuer: the whole warp waits, one elected lane issues
-        int ai = 0, it_local = 0;
-        Ring ar, br;
+    } else if (warp == 1 || (warp == 3 && p.lay.n_mma == 2)) {
+        // ================================================ MMA issuers: the whole warp waits, one elected lane issues.
+        // With two MMA warps, warp 1 takes the stages of even running index and warp 3 those of odd index, each
+        // into its own accumulator (their wait -> issue chains, the pipeline's serial part, then overlap); both walk
+        // every stage to keep the rings in step. The A ring's depth is a multiple of the MMA warps, so that an A
+        // slot is always read by the same warp and its barriers complete in that warp's order.
+        const int NMW = p.lay.n_mma, mw = warp == 1 ? 0 : 1;
+        int it_local = 0, issued = 0, j = 0;   // j: running index of the stage
+        Ring ar, br, last;   // last: ring position of this warp's latest stage (its MMAs complete before TMEM is freed)
         bool ok = true;
         for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
             const Item it = decode_item(p, w);
@@ -561,32 +577,39 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             tc_fence_after();
             const int n_mma = ((it.nrows + 15) / 16) * 16;
             const uint32_t idesc = idesc_f16(n_mma, !p.f16);
-            const uint32_t d_tmem = tmem + (uint32_t)(ab * NB);
-            for (int ks = 0; ks < KS; ++ks) {
-                const int as = ar.i, bs = br.i;
-                if (!(ok = warp_wait(bar(BAR_AF + as), ar.ph, abort_flag, p.err, p.dep_limit_ns))) break;
-                if (p.a_bf16 && !(ok = warp_wait(bar(BAR_BF + bs), br.ph, abort_flag, p.err, p.dep_limit_ns))) break;
-                tc_fence_after();
-                if (elect_one()) {
-                    const uint64_t ad = sw128_desc(smem_u32(smem + OFF_A + as * A_BYTES));
-                    const uint64_t bd = sw128_desc(smem_u32(smem + OFF_B + bs * B_BYTES));
+            const uint32_t d_tmem = tmem + (uint32_t)((ab * NMW + mw) * p.lay.acc_cols);
+            bool started = false;   // this warp's accumulator holds a sum of the item
+            for (int ks = 0; ks < KS; ++ks, ++j) {
+                if ((j & (NMW - 1)) == mw) {   // NMW is 1 or 2
+                    const int as = ar.i, bs = br.i;
+                    if (!(ok = warp_wait(bar(BAR_AF + as), ar.ph, abort_flag, p.err, p.dep_limit_ns))) break;
+                    if (p.a_bf16 && !(ok = warp_wait(bar(BAR_BF + bs), br.ph, abort_flag, p.err, p.dep_limit_ns)))
+                        break;
+                    tc_fence_after();
+                    if (elect_one()) {   // the same lane each time: the warp is converged and elect.sync picks its first
+                        const uint64_t ad = sw128_desc(smem_u32(smem + OFF_A + as * A_BYTES));
+                        const uint64_t bd = sw128_desc(smem_u32(smem + OFF_B + bs * B_BYTES));
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)  // 32 bytes of K per MMA: +2 in the start-address field
-                        tc_mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (ks | k) != 0);
-                    tc_commit(bar(BAR_AE + as));
-                    if (p.a_bf16) tc_commit(bar(BAR_BE + bs));
+                        for (int k = 0; k < BK / 16; ++k)  // 32 bytes of K per MMA: +2 in the start-address field
+                            tc_mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, started || k > 0);
+                        tc_commit(bar(BAR_AE + as));
+                        if (p.a_bf16) tc_commit(bar(BAR_BE + bs));
+                    }
+                    __syncwarp();
+                    started = true;
+                    last = ar;
+                    ++issued;
                 }
-                __syncwarp();
-                ++ai;
                 ar.next(NA);
                 br.next(NBST);
             }
             if (!ok) break;
-            if (elect_one()) tc_commit(bar(BAR_DF + ab));
+            // the accumulator is complete (a warp with no stage in this item arrives at once)
+            if (elect_one()) tc_commit(bar(BAR_DF + ab));   // the lane that issued the MMAs: a commit tracks its own
             __syncwarp();
         }
-        // the MMAs issued so far complete before TMEM is released (also after an abort)
-        if (ai > 0) wait_own(bar(BAR_AE + (ai - 1) % NA), ((ai - 1) / NA) & 1, p.err);
+        // the MMAs this warp issued complete before TMEM is released (also after an abort)
+        if (issued > 0) wait_own(bar(BAR_AE + last.i), last.ph, p.err);
     } else if (warp >= 4 && warp < 8) {
         // ================================================ epilogue
         const int q = warp & 3;
@@ -599,60 +622,93 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (lane == 0) okw = wait_bar(bar(BAR_DF + ab), (it_local >> 1) & 1, abort_flag, p.err, p.dep_limit_ns);
             if (!__shfl_sync(FULL, okw, 0)) break;
             tc_fence_after();
-            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * NB);
-            const int nchunks = (it.nrows + 7) / 8;
-            if (p.ksplit > 1) {
-                // raw partial sums of this K chunk, token-major so that the warp's rows are contiguous
-                const int row = it.mt * BM + m;
-                for (int c = 0; c < nchunks; ++c) {
-                    float v[8];
-                    tc_ld8(tbase + (uint32_t)(c * 8), v);
+            const int NMW = p.lay.n_mma;
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * NMW * p.lay.acc_cols);
+            // with two MMA warps the item's stages start at running index it_local * KS: a one-stage item has a
+            // sum in one accumulator only
+            const int j0 = it_local * KS;
+            const bool use0 = NMW == 1 || KS > 1 || (j0 & 1) == 0, use1 = NMW == 2 && (KS > 1 || (j0 & 1) == 1);
+            auto epi = [&](auto two_tag) {
+                constexpr bool TWO = decltype(two_tag)::value;   // two MMA warps: two accumulators
+                // columns c*8 .. c*8+7 of this row (with two accumulators: the even-stage one plus the odd-stage one)
+                auto ld_acc = [&](int c, float* v) {
+                    if constexpr (!TWO) {
+                        tc_ld8(tbase + (uint32_t)(c * 8), v);
+                    } else {
+                        if (use0) {
+                            tc_ld8(tbase + (uint32_t)(c * 8), v);
+                        } else {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int n = c * 8 + i;
-                        if (n < it.nrows) p.part[((size_t)it.kc * p.ntok + it.row0 + n) * p.mrows + row] = v[i];
+                            for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+                        }
+                        if (use1) {
+                            float v1[8];
+                            tc_ld8(tbase + (uint32_t)(p.lay.acc_cols + c * 8), v1);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) v[i] = use0 ? __fadd_rn(v[i], v1[i]) : v1[i];
+                        }
                     }
-                }
-            } else if (p.mode == 0) {
-                // h column of this row pair: 2^ps gate rows then their 2^ps up rows, repeated
-                const int ps = p.pair_log2;
-                const int j = it.mt * (BM / 2) + ((m >> (ps + 1)) << ps) + (m & ((1 << ps) - 1));
-                const bool up = (m >> ps) & 1;
-                for (int c = 0; c < nchunks; ++c) {
-                    float v[8];
-                    tc_ld8(tbase + (uint32_t)(c * 8), v);
+                };
+                const int nchunks = (it.nrows + 7) / 8;
+                if (p.ksplit > 1) {
+                    // raw partial sums of this K chunk, token-major so that the warp's rows are contiguous
+                    const int row = it.mt * BM + m;
+                    for (int c = 0; c < nchunks; ++c) {
+                        float v[8];
+                        ld_acc(c, v);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float other = __shfl_xor_sync(FULL, v[i], 1 << ps);
-                        const float g = up ? other : v[i], u = up ? v[i] : other;
-                        const int n = c * 8 + i;
-                        if ((i & 1) == (int)up && n < it.nrows) {
-                            const float sc = __ldg(p.col_scale + it.row0 + n);
-                            const float hv = gelu_tanh(__fmul_rn(sc, g)) * __fmul_rn(sc, u);
-                            p.hout[(size_t)(it.row0 + n) * p.ldo + j] = f2bf(hv);
+                        for (int i = 0; i < 8; ++i) {
+                            const int n = c * 8 + i;
+                            if (n < it.nrows) p.part[((size_t)it.kc * p.ntok + it.row0 + n) * p.mrows + row] = v[i];
+                        }
+                    }
+                } else if (p.mode == 0) {
+                    // h column of this row pair: 2^ps gate rows then their 2^ps up rows, repeated
+                    const int ps = p.pair_log2;
+                    const int j = it.mt * (BM / 2) + ((m >> (ps + 1)) << ps) + (m & ((1 << ps) - 1));
+                    const bool up = (m >> ps) & 1;
+                    for (int c = 0; c < nchunks; ++c) {
+                        float v[8];
+                        ld_acc(c, v);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float other = __shfl_xor_sync(FULL, v[i], 1 << ps);
+                            const float g = up ? other : v[i], u = up ? v[i] : other;
+                            const int n = c * 8 + i;
+                            if ((i & 1) == (int)up && n < it.nrows) {
+                                const float sc = __ldg(p.col_scale + it.row0 + n);
+                                const float hv = gelu_tanh(__fmul_rn(sc, g)) * __fmul_rn(sc, u);
+                                p.hout[(size_t)(it.row0 + n) * p.ldo + j] = f2bf(hv);
+                            }
+                        }
+                    }
+                } else {
+                    const int jg = it.mt * BM + m;
+                    for (int c = 0; c < nchunks; ++c) {
+                        float v[8];
+                        ld_acc(c, v);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int n = c * 8 + i;
+                            if (n < it.nrows) p.yout[(size_t)(it.row0 + n) * p.ldo + jg] = v[i];
                         }
                     }
                 }
-            } else {
-                const int jg = it.mt * BM + m;
-                for (int c = 0; c < nchunks; ++c) {
-                    float v[8];
-                    tc_ld8(tbase + (uint32_t)(c * 8), v);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int n = c * 8 + i;
-                        if (n < it.nrows) p.yout[(size_t)(it.row0 + n) * p.ldo + jg] = v[i];
-                    }
-                }
-            }
+            };
+            if (NMW == 2)
+                epi(std::true_type{});
+            else
+                epi(std::false_type{});
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(BAR_DE + ab));
         }
     } else if (warp >= 8 && !p.a_bf16) {
-        // ================================================ dequant: N_DQ_GROUPS groups of N_DQ_WARPS warps; group g
-        // takes the K stages whose running index is g modulo N_DQ_GROUPS, so that stages are dequantised side by
-        // side, and every warp walks every stage to keep the code and A rings in step
+        // ================================================ dequant: two groups of eight warps; group g takes the K
+        // stages whose running index is g modulo 2, so that stages are dequantised side by side, and every warp
+        // walks every stage to keep the code and A rings in step. A waiter never skips a phase of a barrier it
+        // tests by parity: the A ring's depth is even (tiles of up to 128 rows: each slot has one group and one
+        // MMA warp), or (three stages, one MMA warp) the in-order completion of the MMAs orders the phases.
         const int t = threadIdx.x - 8 * 32;
         const int grp = t / (N_DQ_WARPS * 32);
         const int r = (t >> 1) & (BM - 1), hf = t & 1;   // weight row in the tile, half of the 64-code group
@@ -663,9 +719,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             bool ok = true;
             for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
                 const int sbi = it_local & 1;
-                int okw = 1;
-                if (lane == 0) okw = wait_bar(bar(BAR_SF + sbi), (it_local >> 1) & 1, abort_flag, p.err, p.dep_limit_ns);
-                if (!(ok = __shfl_sync(FULL, okw, 0))) break;
+                if (!(ok = warp_wait(bar(BAR_SF + sbi), (it_local >> 1) & 1, abort_flag, p.err, p.dep_limit_ns))) break;
                 const uint32_t* sbrow = reinterpret_cast<const uint32_t*>(smem + OFF_SB + sbi * p.lay.sb_stage) + r * gpr;
                 for (int ks = 0; ks < KS; ++ks) {
                     const int sub = ks % CW;
@@ -709,7 +763,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         cr.next(NCS);
                     }
                     ar.next(NA);
-                    if (++g == N_DQ_GROUPS) g = 0;
+                    g ^= 1;
                 }
                 if (!ok) break;
                 __syncwarp();
@@ -1054,12 +1108,12 @@ bool encode_rows(CUtensorMap* m, const void* base, int cols, int rows, int box_r
 
 // Shared-memory plan of one launch for token tiles of up to max_rows rows and a
 // reduction of K: bf16 weights by TMA (a_bf16) or int4 codes dequantised into A
-// stages. Tiles of up to 64 token rows stream weights: a stage's MMAs complete
-// about a microsecond after they are issued, so the A and token rings take
-// SMALL_DEPTH stages each (bf16 weights: as many as fit) and the rest goes to
-// code stages. Larger tiles are bound by the tensor core: three A and three
-// token stages, the rest to code stages (bf16 weights: to weight stages). na = 0
-// when nothing fits.
+// stages. Tiles of up to 128 token rows stream weights: two MMA warps over four
+// A / token stages (bf16 weights: as many as fit, an even number); the rest goes
+// to code stages. Larger tiles are bound by the tensor core: one MMA warp, three
+// A and three token stages, the rest to code stages (bf16 weights: to weight
+// stages). A ring that two warps read in turn has an even depth, so that each
+// slot has one reader. na = 0 when nothing fits.
 Layout plan_layout(int max_rows, bool a_bf16, int K) {
     Layout l;
     std::memset(&l, 0, sizeof(l));
@@ -1068,15 +1122,22 @@ Layout plan_layout(int max_rows, bool a_bf16, int K) {
     const bool small = max_rows <= 64;
     l.box_big = !small;
     l.b_stage = rows * BK * 2;
+    l.n_mma = max_rows <= 128 ? 2 : 1;
+    l.acc_cols = l.n_mma == 2 ? 128 : NB;
     if (a_bf16) {
+        // with two MMA warps both rings have an even depth: a slot is read by one warp only
         if (small) {
             l.na = SMEM_USABLE / (A_BYTES + l.b_stage);
             if (l.na > NBST_MAX) l.na = NBST_MAX;
             l.nb = l.na;
         } else {
-            l.nb = 3;
+            l.nb = l.n_mma == 2 ? 4 : 3;
             l.na = (SMEM_USABLE - l.nb * l.b_stage) / A_BYTES;
             if (l.na > NA_MAX) l.na = NA_MAX;
+        }
+        if (l.n_mma == 2) {
+            l.na &= ~1;
+            l.nb &= ~1;
         }
         l.off_b = l.na * A_BYTES;
         l.off_c = l.off_b + l.nb * l.b_stage;
@@ -1084,7 +1145,9 @@ Layout plan_layout(int max_rows, bool a_bf16, int K) {
         l.off_bar = l.off_sb;
         if (l.na < 2) l.na = 0;
     } else {
-        l.na = l.nb = small ? SMALL_DEPTH : 3;
+        // up to 128 token rows: four A / token stages (an even depth: each slot has one dequant group and one of
+        // the two MMA warps); larger tiles: three stages, one MMA warp
+        l.na = l.nb = l.n_mma == 2 ? 4 : 3;
         l.sb_stage = BM * (K / 64) * 4;
         l.off_b = l.na * A_BYTES;
         l.off_c = l.off_b + l.nb * l.b_stage;
