@@ -106,6 +106,7 @@ enum {
 constexpr size_t GEMM_SMEM = 227 * 1024;                       // every launch takes a whole SM's shared memory
 constexpr int SMEM_USABLE = (int)GEMM_SMEM - 1024 - N_BARS * 8 - 16;   // after aligning the base to 1 KB
 static_assert(A_BYTES % 1024 == 0, "SW128 tiles");
+static_assert(CW % 2 == 0, "a pipeline stage of one or two K blocks never spans two code stages");
 
 // Shared-memory plan of one launch (offsets from the 1 KB-aligned base). The
 // token stages are sized to the largest token tile the launch can see, and the
@@ -119,7 +120,9 @@ struct Layout {
                         // two accumulators, added by the epilogue) or 1
     int acc_cols;       // TMEM columns of one accumulator (accumulator (item parity, MMA warp) at
                         // column (parity * n_mma + warp) * acc_cols)
-    int b_stage;        // bytes of one token stage
+    int sw;             // K blocks (of BK) per pipeline stage: 2 for int4 tiles of up to 128 tokens (one wait, one
+                        // fence and one arrival per 128 of K), else 1
+    int b_stage;        // bytes of one token stage (sw sub-tiles of b_stage / sw bytes, one per K block)
     int box_big;        // 1: tiles over 64 rows load 128-row boxes
     int off_b, off_c, off_sb, off_bar;
 };
@@ -420,15 +423,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int NA = p.lay.na, NCS = p.lay.ncs, NBST = p.lay.nb;
+    const int NA = p.lay.na, NCS = p.lay.ncs, NBST = p.lay.nb, SW = p.lay.sw;
     const int OFF_A = 0, OFF_B = p.lay.off_b, OFF_C = p.lay.off_c, OFF_SB = p.lay.off_sb;
-    const int B_BYTES = p.lay.b_stage;
+    const int B_BYTES = p.lay.b_stage, B_SUB = B_BYTES / SW, A_STAGE = SW * A_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.lay.off_bar);
     const int OFF_MISC = p.lay.off_bar + N_BARS * 8;
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC + 4);
-    const int KS = p.K / BK / p.ksplit;  // K stages per item
+    const int KS = p.K / BK / p.ksplit;  // K blocks (of BK) per item
+    const int NST = (KS + SW - 1) / SW;  // pipeline stages per item (the last may hold fewer than SW blocks)
     const int total = __ldg(p.tiles + p.E);
     const int gpr = p.K / 64;  // quant groups per weight row
 
@@ -532,18 +536,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const bool big = p.lay.box_big && it.nrows > 64;
                 const int box = big ? BOX_BIG : BOX_SMALL;
                 const int nbox = (it.nrows + box - 1) / box;
-                for (int ks = 0; ks < KS; ++ks) {
+                for (int st = 0; st < NST; ++st) {
                     // with dequantised weights the token ring is the A ring (same depth): a token slot is free
                     // when the MMAs of its stage have completed, as the A slot
-                    const int bs = br.i;
+                    const int bs = br.i, kb0 = st * SW, nk = KS - kb0 < SW ? KS - kb0 : SW;
                     if (!(ok = warp_wait(bar((p.a_bf16 ? BAR_BE : BAR_AE) + bs), br.ph ^ 1, abort_flag, p.err,
                                          p.dep_limit_ns)))
                         break;
                     if (elect_one()) {
-                        mbar_expect_tx(bar(BAR_BF + bs), (uint32_t)(nbox * box * BK * 2));
-                        for (int r = 0; r < nbox; ++r)
-                            tma_load_2d(smem_u32(smem + OFF_B + bs * B_BYTES + r * box * BK * 2), big ? &tmB2 : &tmB,
-                                        (ks0 + ks) * BK, it.row0 + r * box, bar(BAR_BF + bs));
+                        mbar_expect_tx(bar(BAR_BF + bs), (uint32_t)(nk * nbox * box * BK * 2));
+                        for (int t = 0; t < nk; ++t)
+                            for (int r = 0; r < nbox; ++r)
+                                tma_load_2d(smem_u32(smem + OFF_B + bs * B_BYTES + t * B_SUB + r * box * BK * 2),
+                                            big ? &tmB2 : &tmB, (ks0 + kb0 + t) * BK, it.row0 + r * box,
+                                            bar(BAR_BF + bs));
                     }
                     __syncwarp();
                     ++bi;
@@ -566,50 +572,63 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // into its own accumulator (their wait -> issue chains, the pipeline's serial part, then overlap); both walk
         // every stage to keep the rings in step. The A ring's depth is a multiple of the MMA warps, so that an A
         // slot is always read by the same warp and its barriers complete in that warp's order.
-        const int NMW = p.lay.n_mma, mw = warp == 1 ? 0 : 1;
-        int it_local = 0, issued = 0, j = 0;   // j: running index of the stage
-        Ring ar, br, last;   // last: ring position of this warp's latest stage (its MMAs complete before TMEM is freed)
-        bool ok = true;
-        for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
-            const Item it = decode_item(p, w);
-            const int ab = it_local & 1;
-            if (!(ok = warp_wait(bar(BAR_DE + ab), ((it_local >> 1) & 1) ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
-            tc_fence_after();
-            const int n_mma = ((it.nrows + 15) / 16) * 16;
-            const uint32_t idesc = idesc_f16(n_mma, !p.f16);
-            const uint32_t d_tmem = tmem + (uint32_t)((ab * NMW + mw) * p.lay.acc_cols);
-            bool started = false;   // this warp's accumulator holds a sum of the item
-            for (int ks = 0; ks < KS; ++ks, ++j) {
-                if ((j & (NMW - 1)) == mw) {   // NMW is 1 or 2
-                    const int as = ar.i, bs = br.i;
-                    if (!(ok = warp_wait(bar(BAR_AF + as), ar.ph, abort_flag, p.err, p.dep_limit_ns))) break;
-                    if (p.a_bf16 && !(ok = warp_wait(bar(BAR_BF + bs), br.ph, abort_flag, p.err, p.dep_limit_ns)))
-                        break;
-                    tc_fence_after();
-                    if (elect_one()) {   // the same lane each time: the warp is converged and elect.sync picks its first
-                        const uint64_t ad = sw128_desc(smem_u32(smem + OFF_A + as * A_BYTES));
-                        const uint64_t bd = sw128_desc(smem_u32(smem + OFF_B + bs * B_BYTES));
-#pragma unroll
-                        for (int k = 0; k < BK / 16; ++k)  // 32 bytes of K per MMA: +2 in the start-address field
-                            tc_mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, started || k > 0);
-                        tc_commit(bar(BAR_AE + as));
-                        if (p.a_bf16) tc_commit(bar(BAR_BE + bs));
+        // the stage width is a compile-time constant of each copy of the role (one or two K blocks)
+        auto mma_role = [&](auto sw_tag) {
+            constexpr int TSW = decltype(sw_tag)::value;
+            const int NMW = p.lay.n_mma, mw = warp == 1 ? 0 : 1;
+            int it_local = 0, issued = 0, j = 0;   // j: running index of the stage
+            Ring ar, br, last;   // last: ring position of this warp's latest stage (its MMAs complete before TMEM is freed)
+            bool ok = true;
+            for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it_local) {
+                const Item it = decode_item(p, w);
+                const int ab = it_local & 1;
+                if (!(ok = warp_wait(bar(BAR_DE + ab), ((it_local >> 1) & 1) ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
+                tc_fence_after();
+                const int n_mma = ((it.nrows + 15) / 16) * 16;
+                const uint32_t idesc = idesc_f16(n_mma, !p.f16);
+                const uint32_t d_tmem = tmem + (uint32_t)((ab * NMW + mw) * p.lay.acc_cols);
+                bool started = false;   // this warp's accumulator holds a sum of the item
+                for (int st = 0; st < NST; ++st, ++j) {
+                    if ((j & (NMW - 1)) == mw) {   // NMW is 1 or 2
+                        const int as = ar.i, bs = br.i, nk = KS - st * TSW < TSW ? KS - st * TSW : TSW;
+                        if (!(ok = warp_wait(bar(BAR_AF + as), ar.ph, abort_flag, p.err, p.dep_limit_ns))) break;
+                        if (p.a_bf16 && !(ok = warp_wait(bar(BAR_BF + bs), br.ph, abort_flag, p.err, p.dep_limit_ns)))
+                            break;
+                        tc_fence_after();
+                        if (elect_one()) {   // the same lane each time: the warp is converged and elect.sync picks its first
+    #pragma unroll
+                            for (int t = 0; t < TSW; ++t) {   // the stage's K blocks (nk of them)
+                                if (TSW == 1 || t < nk) {
+                                    const uint64_t ad = sw128_desc(smem_u32(smem + OFF_A + as * A_STAGE + t * A_BYTES));
+                                    const uint64_t bd = sw128_desc(smem_u32(smem + OFF_B + bs * B_BYTES + t * B_SUB));
+    #pragma unroll
+                                    for (int k = 0; k < BK / 16; ++k)  // 32 bytes of K per MMA: +2 in the start-address field
+                                        tc_mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, started || t > 0 || k > 0);
+                                }
+                            }
+                            tc_commit(bar(BAR_AE + as));
+                            if (p.a_bf16) tc_commit(bar(BAR_BE + bs));
+                        }
+                        __syncwarp();
+                        started = true;
+                        last = ar;
+                        ++issued;
                     }
-                    __syncwarp();
-                    started = true;
-                    last = ar;
-                    ++issued;
+                    ar.next(NA);
+                    br.next(NBST);
                 }
-                ar.next(NA);
-                br.next(NBST);
+                if (!ok) break;
+                // the accumulator is complete (a warp with no stage in this item arrives at once)
+                if (elect_one()) tc_commit(bar(BAR_DF + ab));   // the lane that issued the MMAs: a commit tracks its own
+                __syncwarp();
             }
-            if (!ok) break;
-            // the accumulator is complete (a warp with no stage in this item arrives at once)
-            if (elect_one()) tc_commit(bar(BAR_DF + ab));   // the lane that issued the MMAs: a commit tracks its own
-            __syncwarp();
-        }
-        // the MMAs this warp issued complete before TMEM is released (also after an abort)
-        if (issued > 0) wait_own(bar(BAR_AE + last.i), last.ph, p.err);
+            // the MMAs this warp issued complete before TMEM is released (also after an abort)
+            if (issued > 0) wait_own(bar(BAR_AE + last.i), last.ph, p.err);
+        };
+        if (SW == 2)
+            mma_role(std::integral_constant<int, 2>{});
+        else
+            mma_role(std::integral_constant<int, 1>{});
     } else if (warp >= 4 && warp < 8) {
         // ================================================ epilogue
         const int q = warp & 3;
@@ -624,10 +643,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             tc_fence_after();
             const int NMW = p.lay.n_mma;
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * NMW * p.lay.acc_cols);
-            // with two MMA warps the item's stages start at running index it_local * KS: a one-stage item has a
+            // with two MMA warps the item's stages start at running index it_local * NST: a one-stage item has a
             // sum in one accumulator only
-            const int j0 = it_local * KS;
-            const bool use0 = NMW == 1 || KS > 1 || (j0 & 1) == 0, use1 = NMW == 2 && (KS > 1 || (j0 & 1) == 1);
+            const int j0 = it_local * NST;
+            const bool use0 = NMW == 1 || NST > 1 || (j0 & 1) == 0, use1 = NMW == 2 && (NST > 1 || (j0 & 1) == 1);
             auto epi = [&](auto two_tag) {
                 constexpr bool TWO = decltype(two_tag)::value;   // two MMA warps: two accumulators
                 // columns c*8 .. c*8+7 of this row (with two accumulators: the even-stage one plus the odd-stage one)
@@ -712,8 +731,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int t = threadIdx.x - 8 * 32;
         const int grp = t / (N_DQ_WARPS * 32);
         const int r = (t >> 1) & (BM - 1), hf = t & 1;   // weight row in the tile, half of the 64-code group
-        auto run = [&](auto f16_tag) {
+        auto run = [&](auto f16_tag, auto sw_tag) {
             constexpr bool F16 = decltype(f16_tag)::value;
+            constexpr int TSW = decltype(sw_tag)::value;   // K blocks per stage, a compile-time constant
             Ring cr, ar;
             int g = 0, it_local = 0;   // g: the group whose stage is next
             bool ok = true;
@@ -721,32 +741,40 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const int sbi = it_local & 1;
                 if (!(ok = warp_wait(bar(BAR_SF + sbi), (it_local >> 1) & 1, abort_flag, p.err, p.dep_limit_ns))) break;
                 const uint32_t* sbrow = reinterpret_cast<const uint32_t*>(smem + OFF_SB + sbi * p.lay.sb_stage) + r * gpr;
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int sub = ks % CW;
+                for (int st = 0; st < NST; ++st) {
+                    const int kb0 = st * TSW, nk = KS - kb0 < TSW ? KS - kb0 : TSW;   // K blocks of this stage
                     const bool mine = g == grp;
-                    if (sub == 0 && !(ok = warp_wait(bar(BAR_CF + cr.i), cr.ph, abort_flag, p.err, p.dep_limit_ns))) break;
+                    // a stage never spans two code stages (SW divides CW)
+                    if (kb0 % CW == 0 && !(ok = warp_wait(bar(BAR_CF + cr.i), cr.ph, abort_flag, p.err, p.dep_limit_ns)))
+                        break;
                     if (mine && !(ok = warp_wait(bar(BAR_AE + ar.i), ar.ph ^ 1, abort_flag, p.err, p.dep_limit_ns))) break;
                     if (mine) {
-                        // the code box lands 128-byte swizzled: 16-byte chunk j of row r sits at chunk j ^ (r & 7),
-                        // so the 16 rows a warp reads spread over all banks
-                        const uint4 qv = *reinterpret_cast<const uint4*>(smem + OFF_C + cr.i * C_BYTES +
-                                                                         r * (CW * BK / 2) + (((sub * 2 + hf) ^ (r & 7)) << 4));
-                        const uint32_t sbw = sbrow[ks];
-                        unsigned char* arow = smem + OFF_A + ar.i * A_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
-                        const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-                        if constexpr (F16) {
-                            const uint32_t s2 = __byte_perm(sbw, 0, 0x1010), b2 = __byte_perm(sbw, 0, 0x3232);
 #pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                const int chunk = hf * 4 + c;  // 16-byte chunk (8 columns) of the 128-byte row
-                                *reinterpret_cast<uint4*>(arow + ((chunk ^ (r & 7)) << 4)) = dequant8_f16(qw[c], s2, b2);
-                            }
-                        } else {
-                            const float s = h2f(sbw & 0xffffu), b = h2f(sbw >> 16);
+                        for (int t = 0; t < TSW; ++t) {   // the stage's K blocks (nk of them)
+                            if (TSW > 1 && t >= nk) break;
+                            const int kb = kb0 + t, sub = kb % CW;
+                            // the code box lands 128-byte swizzled: 16-byte chunk j of row r sits at chunk
+                            // j ^ (r & 7), so the 16 rows a warp reads spread over all banks
+                            const uint4 qv = *reinterpret_cast<const uint4*>(smem + OFF_C + cr.i * C_BYTES +
+                                                                             r * (CW * BK / 2) + (((sub * 2 + hf) ^ (r & 7)) << 4));
+                            const uint32_t sbw = sbrow[kb];
+                            unsigned char* arow =
+                                smem + OFF_A + ar.i * A_STAGE + t * A_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+                            const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+                            if constexpr (F16) {
+                                const uint32_t s2 = __byte_perm(sbw, 0, 0x1010), b2 = __byte_perm(sbw, 0, 0x3232);
 #pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                const int chunk = hf * 4 + c;
-                                *reinterpret_cast<uint4*>(arow + ((chunk ^ (r & 7)) << 4)) = dequant8_bf16(qw[c], s, b);
+                                for (int c = 0; c < 4; ++c) {
+                                    const int chunk = hf * 4 + c;  // 16-byte chunk (8 columns) of the 128-byte row
+                                    *reinterpret_cast<uint4*>(arow + ((chunk ^ (r & 7)) << 4)) = dequant8_f16(qw[c], s2, b2);
+                                }
+                            } else {
+                                const float s = h2f(sbw & 0xffffu), b = h2f(sbw >> 16);
+#pragma unroll
+                                for (int c = 0; c < 4; ++c) {
+                                    const int chunk = hf * 4 + c;
+                                    *reinterpret_cast<uint4*>(arow + ((chunk ^ (r & 7)) << 4)) = dequant8_bf16(qw[c], s, b);
+                                }
                             }
                         }
                         fence_proxy_async();  // generic-proxy writes, read next by the tensor core
@@ -757,7 +785,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             break;
                         if (lane == 0) mbar_arrive(bar(BAR_AF + ar.i));
                     }
-                    if (sub == CW - 1 || ks == KS - 1) {   // the code stage is used up
+                    if ((kb0 + nk) % CW == 0 || kb0 + nk == KS) {   // the code stage is used up
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar(BAR_CE + cr.i));
                         cr.next(NCS);
@@ -770,10 +798,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 if (lane == 0) mbar_arrive(bar(BAR_SE + sbi));
             }
         };
-        if (p.f16)
-            run(std::true_type{});
-        else
-            run(std::false_type{});
+        using W1 = std::integral_constant<int, 1>;
+        using W2 = std::integral_constant<int, 2>;
+        if (p.f16) {
+            if (SW == 2) run(std::true_type{}, W2{}); else run(std::true_type{}, W1{});
+        } else {
+            if (SW == 2) run(std::false_type{}, W2{}); else run(std::false_type{}, W1{});
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -1108,12 +1139,13 @@ bool encode_rows(CUtensorMap* m, const void* base, int cols, int rows, int box_r
 
 // Shared-memory plan of one launch for token tiles of up to max_rows rows and a
 // reduction of K: bf16 weights by TMA (a_bf16) or int4 codes dequantised into A
-// stages. Tiles of up to 128 token rows stream weights: two MMA warps over four
-// A / token stages (bf16 weights: as many as fit, an even number); the rest goes
-// to code stages. Larger tiles are bound by the tensor core: one MMA warp, three
-// A and three token stages, the rest to code stages (bf16 weights: to weight
-// stages). A ring that two warps read in turn has an even depth, so that each
-// slot has one reader. na = 0 when nothing fits.
+// stages. Tiles of up to 128 token rows stream weights: two MMA warps over two
+// A / token stages of two K blocks each (bf16 weights: as many one-block stages
+// as fit, an even number); the rest goes to code stages. Larger tiles are bound
+// by the tensor core: one MMA warp, three A and three token stages of one K
+// block, the rest to code stages (bf16 weights: to weight stages). A ring that
+// two warps read in turn has an even depth, so that each slot has one reader.
+// na = 0 when nothing fits.
 Layout plan_layout(int max_rows, bool a_bf16, int K) {
     Layout l;
     std::memset(&l, 0, sizeof(l));
@@ -1121,7 +1153,8 @@ Layout plan_layout(int max_rows, bool a_bf16, int K) {
     if (rows > NB) rows = NB;
     const bool small = max_rows <= 64;
     l.box_big = !small;
-    l.b_stage = rows * BK * 2;
+    l.sw = !a_bf16 && max_rows <= 128 ? 2 : 1;
+    l.b_stage = l.sw * rows * BK * 2;
     l.n_mma = max_rows <= 128 ? 2 : 1;
     l.acc_cols = l.n_mma == 2 ? 128 : NB;
     if (a_bf16) {
@@ -1145,11 +1178,11 @@ Layout plan_layout(int max_rows, bool a_bf16, int K) {
         l.off_bar = l.off_sb;
         if (l.na < 2) l.na = 0;
     } else {
-        // up to 128 token rows: four A / token stages (an even depth: each slot has one dequant group and one of
-        // the two MMA warps); larger tiles: three stages, one MMA warp
-        l.na = l.nb = l.n_mma == 2 ? 4 : 3;
+        // up to 128 token rows: two stages of two K blocks (an even depth: each slot has one dequant group and
+        // one of the two MMA warps); larger tiles: three stages of one, one MMA warp
+        l.na = l.nb = l.sw == 2 ? 2 : 3;
         l.sb_stage = BM * (K / 64) * 4;
-        l.off_b = l.na * A_BYTES;
+        l.off_b = l.na * l.sw * A_BYTES;
         l.off_c = l.off_b + l.nb * l.b_stage;
         l.ncs = (SMEM_USABLE - l.off_c - 2 * l.sb_stage) / C_BYTES;
         if (l.ncs > NCS_MAX) l.ncs = NCS_MAX;
