@@ -133,6 +133,8 @@ __global__ void __launch_bounds__(RL_THREADS)
 k_router_lanes(const uint16_t* __restrict__ x, int T, int H, const uint16_t* __restrict__ Wr, int E,
                const float* __restrict__ bias, int bias_stride, float* __restrict__ logits,
                float* __restrict__ rms, float eps, int tokens_per_cta) {
+    dev::pdl_wait();
+    dev::pdl_trigger();
     extern __shared__ float4 rl4[];
     float* wsm = reinterpret_cast<float*>(rl4);   // [EW][H] fp32
     const int e0 = blockIdx.x * EW;
@@ -219,6 +221,8 @@ k_router_lanes(const uint16_t* __restrict__ x, int T, int H, const uint16_t* __r
 // One warp per token: top-k of its logits and the softmax over the selected ones.
 __global__ void __launch_bounds__(256) k_topk_rows(const float* __restrict__ logits, int T, int E, int k,
                                                    int32_t* __restrict__ idx, float* __restrict__ wout) {
+    dev::pdl_wait();
+    dev::pdl_trigger();
     extern __shared__ float tks[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float* z = tks + (size_t)warp * E;
@@ -526,15 +530,19 @@ static int launch_router_many(const uint16_t* x, int T, int H, const uint16_t* W
     if (int e = smem_limit_once(kern, RL_SMEM_MAX)) return e;
     const dim3 grid(gx, gy);
     if (ew8 && wide)
-        k_router_lanes<8, 4><<<grid, RL_THREADS, smem, st>>>(x, T, H, Wr, E, bias, bias_stride, logits, rms, eps, per);
+        launch_dependent(k_router_lanes<8, 4>, grid, dim3(RL_THREADS), smem, st, x, T, H, Wr, E, bias, bias_stride, logits, rms,
+                         eps, per);
     else if (ew8)
-        k_router_lanes<8, 1><<<grid, RL_THREADS, smem, st>>>(x, T, H, Wr, E, bias, bias_stride, logits, rms, eps, per);
+        launch_dependent(k_router_lanes<8, 1>, grid, dim3(RL_THREADS), smem, st, x, T, H, Wr, E, bias, bias_stride, logits, rms,
+                         eps, per);
     else if (wide)
-        k_router_lanes<2, 4><<<grid, RL_THREADS, smem, st>>>(x, T, H, Wr, E, bias, bias_stride, logits, rms, eps, per);
+        launch_dependent(k_router_lanes<2, 4>, grid, dim3(RL_THREADS), smem, st, x, T, H, Wr, E, bias, bias_stride, logits, rms,
+                         eps, per);
     else
-        k_router_lanes<2, 1><<<grid, RL_THREADS, smem, st>>>(x, T, H, Wr, E, bias, bias_stride, logits, rms, eps, per);
+        launch_dependent(k_router_lanes<2, 1>, grid, dim3(RL_THREADS), smem, st, x, T, H, Wr, E, bias, bias_stride, logits, rms,
+                         eps, per);
     const size_t tk_smem = (size_t)8 * E * 5;   // <= 40 KB for E <= 1024: within the default limit
-    k_topk_rows<<<(T + 7) / 8, 256, tk_smem, st>>>(logits, T, E, k, idx, w);
+    launch_dependent(k_topk_rows, dim3((T + 7) / 8), dim3(256), tk_smem, st, logits, T, E, k, idx, w);
     return (int)cudaGetLastError();
 }
 

@@ -19,6 +19,15 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 __device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
 __device__ __forceinline__ float h2f(uint32_t h16) { return __half2float(__ushort_as_half((unsigned short)h16)); }
 
+// Programmatic dependent launch (the kernels of the grouped path and the many-token
+// router): pdl_wait returns once the stream's preceding kernel has completed and its
+// writes are visible (at once when this kernel was not launched as a dependent);
+// pdl_trigger lets the next kernel of the stream start its CTAs, which then wait in
+// their own pdl_wait. A kernel calls pdl_wait before it reads anything an earlier
+// kernel wrote, so every earlier kernel has completed by then.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -174,4 +183,22 @@ __device__ __forceinline__ void warp_topk_softmax(float* z, unsigned char* taken
 }
 
 }  // namespace dev
+
+// Launch a kernel as a programmatic dependent of the stream's preceding kernel
+// (its CTAs may start while that kernel finishes; they wait in dev::pdl_wait).
+template <typename... K, typename... A>
+inline cudaError_t launch_dependent(void (*kern)(K...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                    A&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<A&&>(args)...);
+}
 }  // namespace tf

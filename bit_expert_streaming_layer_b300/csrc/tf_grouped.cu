@@ -420,6 +420,8 @@ __device__ __forceinline__ uint4 dequant8_f16(uint32_t q, uint32_t s2, uint32_t 
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     k_group_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, GemmParams p) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -847,6 +849,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int32_t* wsum) {
 // wave get no tile; their rows keep their places in the permutation).
 __global__ void __launch_bounds__(1024) k_wave_plan(const int32_t* __restrict__ counts, const int32_t* __restrict__ mask,
                                                      int E, int mt_gu, int mt_d, int32_t* tiles_gu, int32_t* tiles_d) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int32_t wsum[32];
     const int e = threadIdx.x;
     const int c = e < E && __ldg(mask + e) ? __ldg(counts + e) : 0;
@@ -866,6 +870,8 @@ __global__ void __launch_bounds__(1024) k_wave_plan(const int32_t* __restrict__ 
 __global__ void __launch_bounds__(1024) k_group_hist(const int32_t* __restrict__ idx, int P, int E, int mt_gu,
                                                       int mt_d, int32_t* counts, int32_t* offsets, int32_t* tiles_gu,
                                                       int32_t* tiles_d, uint32_t* err) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int32_t cnt[TF_MAX_E];
     __shared__ int32_t wsum[32];
     if (threadIdx.x == 0) *err = 0u;   // a new call: no GEMM wait has given up yet
@@ -899,6 +905,8 @@ __global__ void __launch_bounds__(1024) k_group_hist(const int32_t* __restrict__
 __global__ void __launch_bounds__(1024) k_group_pos(const int32_t* __restrict__ idx, int P,
                                                      const int32_t* __restrict__ offsets, int32_t* perm,
                                                      int32_t* inv) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int32_t wcnt[32];
     __shared__ int32_t base_s;
     const int e = blockIdx.x;
@@ -931,6 +939,8 @@ __global__ void __launch_bounds__(1024) k_group_pos(const int32_t* __restrict__ 
 
 // Pairs whose expert id is out of range get no row: their inverse is -1.
 __global__ void k_group_inv_init(const int32_t* __restrict__ idx, int P, int E, int32_t* inv) {
+    pdl_wait();
+    pdl_trigger();
     const int p = blockIdx.x * blockDim.x + threadIdx.x;
     if (p < P && (unsigned)__ldg(idx + p) >= (unsigned)E) inv[p] = -1;
 }
@@ -938,6 +948,8 @@ __global__ void k_group_inv_init(const int32_t* __restrict__ idx, int P, int E, 
 // Work plan of the shared expert: one "expert" holding all T tokens in order.
 __global__ void k_shared_plan(int T, int mt_gu, int mt_d, int ks_gu, int ks_d, int32_t* counts, int32_t* offsets,
                               int32_t* tiles_gu, int32_t* tiles_d) {
+    pdl_wait();
+    pdl_trigger();
     if (threadIdx.x == 0) {
         const int nb = (T + NB - 1) / NB;
         counts[0] = T;
@@ -955,6 +967,8 @@ __global__ void k_shared_plan(int T, int mt_gu, int mt_d, int ks_gu, int ks_d, i
 // the 8-row interleave of the tiles), r_t the token's RMS scale.
 __global__ void k_shared_gu_combine(const float* __restrict__ part, const float* __restrict__ rms, int ks, int T,
                                     int S, uint16_t* hs) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.y;
     const int j = blockIdx.x * blockDim.x + threadIdx.x;
     if (j >= S) return;
@@ -972,6 +986,8 @@ __global__ void k_shared_gu_combine(const float* __restrict__ part, const float*
 
 // Split-K shared down: ys[t][i] = sum of the K chunks in order.
 __global__ void k_shared_down_combine(const float* __restrict__ part, int ks, int T, int H, float* ys) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.y;
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= H) return;
@@ -982,6 +998,8 @@ __global__ void k_shared_down_combine(const float* __restrict__ part, int ks, in
 
 // r_t = 1/sqrt(mean(x_t^2) + eps) in the canonical order, one warp per token.
 __global__ void k_group_rms(const uint16_t* __restrict__ x, int T, int H, float eps, float* rms) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (t >= T) return;
@@ -1003,6 +1021,8 @@ __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w, float p) {
 __global__ void k_group_gather(const uint16_t* __restrict__ x, const float* __restrict__ rms,
                                const int32_t* __restrict__ perm, int P, int k, int H, uint16_t* xp,
                                float* __restrict__ rp) {
+    pdl_wait();
+    pdl_trigger();
     const int pos = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (pos >= P) return;
@@ -1027,6 +1047,8 @@ __global__ void k_group_combine(const uint16_t* __restrict__ x, const float* __r
                                 const float* __restrict__ ys,
                                 const int32_t* __restrict__ inv, const float* __restrict__ w, int k, int H,
                                 const uint32_t* err, uint16_t* out, float* delta) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.y;
     const int j = (blockIdx.x * blockDim.x + threadIdx.x) * 4;   // four columns per thread
     if (*err) {  // a GEMM wait timed out: the outputs are NaN, never stale or partial values
@@ -1315,11 +1337,11 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     if (a.rms_in)
         rms = const_cast<float*>(a.rms_in);   // the router's scale of every token (the same canonical sum)
     else
-        k_group_rms<<<(T + 7) / 8, 256, 0, st>>>(x16, T, H, a.eps, rms);
-    k_group_hist<<<1, 1024, 0, st>>>(a.idx, P, E, mt_gu, mt_d, counts, offsets, tiles_gu, tiles_d, err);
-    k_group_pos<<<E, 1024, 0, st>>>(a.idx, P, offsets, perm, inv);
-    k_group_inv_init<<<(P + 255) / 256, 256, 0, st>>>(a.idx, P, E, inv);
-    k_group_gather<<<(P + 7) / 8, 256, 0, st>>>(x16, rms, perm, P, k, H, xp, rp);
+        launch_dependent(k_group_rms, dim3((T + 7) / 8), dim3(256), 0, st, x16, T, H, a.eps, rms);
+    launch_dependent(k_group_hist, dim3(1), dim3(1024), 0, st, a.idx, P, E, mt_gu, mt_d, counts, offsets, tiles_gu, tiles_d, err);
+    launch_dependent(k_group_pos, dim3(E), dim3(1024), 0, st, a.idx, P, offsets, perm, inv);
+    launch_dependent(k_group_inv_init, dim3((P + 255) / 256), dim3(256), 0, st, a.idx, P, E, inv);
+    launch_dependent(k_group_gather, dim3((P + 7) / 8), dim3(256), 0, st, x16, rms, perm, P, k, H, xp, rp);
     // the shared expert has few weight tiles (2S/128 and H/128); while the tokens fit one tile row, split K
     // so that more SMs stream its weights (chunks of at least 4 stages)
     auto split_of = [](int kstages) {
@@ -1332,7 +1354,7 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
     const int ks_d = (S > 0 && one_block) ? split_of(S / BK) : 1;
     float* spart = S > 0 ? reinterpret_cast<float*>(ws + c.spart) : nullptr;
     if (S > 0) {
-        k_shared_plan<<<1, 32, 0, st>>>(T, 2 * S / BM, H / BM, ks_gu, ks_d, s_plan, s_plan + 1, s_plan + 3,
+        launch_dependent(k_shared_plan, dim3(1), dim3(32), 0, st, T, 2 * S / BM, H / BM, ks_gu, ks_d, s_plan, s_plan + 1, s_plan + 3,
                                         s_plan + 5);
     }
     prof_after(TF_KERNEL_PERMUTE, stream);
@@ -1362,7 +1384,7 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
         gp.col_scale = rp;
         gp.f16 = 1;
         gp.lay = lay_gu;
-        k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmA_gu, tmB_gu, tmA_gu, tmB_gu2, gp);
+        launch_dependent(k_group_gemm, dim3(sms), dim3(GEMM_THREADS), GEMM_SMEM, st, tmA_gu, tmB_gu, tmA_gu, tmB_gu2, gp);
         gp.off_sb = lay.d_sb;
         gp.K = I;
         gp.MT = mt_d;
@@ -1373,7 +1395,7 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
         gp.ldo = H;
         gp.f16 = 0;
         gp.lay = lay_d;
-        k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmA_d, tmB_d, tmA_d, tmB_d2, gp);
+        launch_dependent(k_group_gemm, dim3(sms), dim3(GEMM_THREADS), GEMM_SMEM, st, tmA_d, tmB_d, tmA_d, tmB_d2, gp);
     };
     prof_before(TF_KERNEL_GEMM, stream);
     if (!a.waves) {
@@ -1387,7 +1409,7 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
             if (cudaError_t e = cudaMemcpyAsync(dmap, wv.h_maps + (size_t)w * 2 * E, (size_t)2 * E * 4,
                                                 cudaMemcpyHostToDevice, st))
                 return cuda_status(e, fn);
-            k_wave_plan<<<1, 1024, 0, st>>>(counts, dmap, E, mt_gu, mt_d, tiles_gu, tiles_d);
+            launch_dependent(k_wave_plan, dim3(1), dim3(1024), 0, st, counts, dmap, E, mt_gu, mt_d, tiles_gu, tiles_d);
             routed_gemms(dmap + E);
         }
     }
@@ -1413,8 +1435,8 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
         sp.ksplit = ks_gu;
         sp.mrows = 2 * S;
         sp.lay = lay_sgu;
-        k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmS_g, tmS_xn, tmS_u, tmS_xn2, sp);
-        if (ks_gu > 1) k_shared_gu_combine<<<dim3((S + 255) / 256, T), 256, 0, st>>>(spart, rms, ks_gu, T, S, hs);
+        launch_dependent(k_group_gemm, dim3(sms), dim3(GEMM_THREADS), GEMM_SMEM, st, tmS_g, tmS_xn, tmS_u, tmS_xn2, sp);
+        if (ks_gu > 1) launch_dependent(k_shared_gu_combine, dim3(dim3((S + 255) / 256, T)), dim3(256), 0, st, spart, rms, ks_gu, T, S, hs);
         sp.K = S;
         sp.MT = H / BM;
         sp.tiles = s_plan + 5;
@@ -1425,14 +1447,14 @@ tf_status grouped_run(const GroupedArgs& a, void* stream, const char* fn) {
         sp.ksplit = ks_d;
         sp.mrows = H;
         sp.lay = lay_sd;
-        k_group_gemm<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(tmS_d, tmS_h, tmS_d, tmS_h2, sp);
-        if (ks_d > 1) k_shared_down_combine<<<dim3((H + 255) / 256, T), 256, 0, st>>>(spart, ks_d, T, H, ys);
+        launch_dependent(k_group_gemm, dim3(sms), dim3(GEMM_THREADS), GEMM_SMEM, st, tmS_d, tmS_h, tmS_d, tmS_h2, sp);
+        if (ks_d > 1) launch_dependent(k_shared_down_combine, dim3(dim3((H + 255) / 256, T)), dim3(256), 0, st, spart, ks_d, T, H, ys);
     }
     prof_after(TF_KERNEL_GEMM, stream);
     if (cudaError_t e = cudaGetLastError()) return cuda_status(e, fn);
 
     prof_before(TF_KERNEL_COMBINE, stream);
-    k_group_combine<<<dim3((H / 4 + 127) / 128, T), 128, 0, st>>>(x16, y, ys, inv, a.w, k, H, err,
+    launch_dependent(k_group_combine, dim3(dim3((H / 4 + 127) / 128, T)), dim3(128), 0, st, x16, y, ys, inv, a.w, k, H, err,
                                                                   static_cast<uint16_t*>(a.out), a.delta);
     prof_after(TF_KERNEL_COMBINE, stream);
     if (a.perm_out) cudaMemcpyAsync(a.perm_out, perm, (size_t)P * 4, cudaMemcpyDeviceToDevice, st);
