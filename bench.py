@@ -653,7 +653,7 @@ def run_streaming(args):
     if not args.no_cpu_baseline:
         base = oracle_baseline(args.oracle_layers)
         line["cpu_baseline"] = {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")}
-    print(json.dumps(line))
+    return line
 
 
 # ------------------------------------------------------------------ batched decode (64 tokens per step)
@@ -827,7 +827,7 @@ def run_batched(args):
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = batched_cpu_baseline(seed, x_bits)
-    print(json.dumps(line))
+    return line
 
 
 # ------------------------------------------------------------------ prefill-shaped layer (grouped path)
@@ -943,7 +943,7 @@ def run_prefill(args):
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = prefill_cpu_baseline(seed, bf16_bits(x), idx.cpu().numpy(), w.cpu().numpy())
-    print(json.dumps(line))
+    return line
 
 
 def run_reference(args):
@@ -1003,6 +1003,8 @@ def main():
                     help="streaming: also measure these slot counts per layer, e.g. 8,32,64")
     ap.add_argument("--fetch-ctas", type=int, default=32,
                     help="streaming: CTAs of the kernel that copies missing experts from the host store")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="default (decode) run: skip the short batched / prefill / streaming runs reported beside it")
     ap.add_argument("--no-chunked-prefill", action="store_true",
                     help="streaming: skip the chunked prefill through the cache")
     ap.add_argument("--fetch-sweep", default="",
@@ -1026,15 +1028,15 @@ def main():
 
     if args.workload == "prefill":
         if rank == 0:
-            run_prefill(args)
+            print(json.dumps(run_prefill(args)))
         return
     if args.workload == "streaming":
         if rank == 0:
-            run_streaming(args)
+            print(json.dumps(run_streaming(args)))
         return
     if args.workload == "batched":
         if rank == 0:
-            run_batched(args)
+            print(json.dumps(run_batched(args)))
         return
 
     if world > 1:
@@ -1091,7 +1093,36 @@ def main():
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"], line["cpu_baseline_all_cores"] = cpu_baselines(args.oracle_layers)
+    if world == 1 and not args.no_other_workloads:
+        line["other_workloads"] = other_workloads(args)
     print(json.dumps(line))
+
+
+def other_workloads(args):
+    """Short runs of the batched, prefill and streaming workloads in the same process (fewer steps than their own
+    --workload lines), summarised beside the decode line so that every workload has a number from this run."""
+    import copy
+    out = {}
+    plans = (("batched", run_batched, 16, 3), ("prefill", run_prefill, 5, 3), ("streaming", run_streaming, 6, 3))
+    for name, fn, steps, warmup in plans:
+        a = copy.copy(args)
+        a.steps, a.warmup, a.no_cpu_baseline, a.workload = steps, warmup, True, name
+        a.slot_sweep, a.fetch_sweep = "", ""
+        t0 = time.perf_counter()
+        try:
+            ln = fn(a)
+        except Exception as e:   # one workload failing must not hide the decode line
+            out[name] = {"error": "%s: %s" % (type(e).__name__, e)}
+            continue
+        keep = ("metric", "value", "unit", "steps", "warmup", "ms_per_step", "e2e", "hit_rate",
+                "bytes_fetched_per_token", "distinct_experts_per_layer", "chunked_prefill", "host_metadata")
+        summary = {k: ln[k] for k in keep if k in ln}
+        rf = ln.get("roofline", {})
+        summary["roofline"] = {k: rf[k] for k in ("bound", "kernel", "achieved", "peak", "unit", "frac") if k in rf}
+        summary["clocks"] = ln.get("clocks")
+        summary["wall_s"] = round(time.perf_counter() - t0, 1)
+        out[name] = summary
+    return out
 
 
 if __name__ == "__main__":
