@@ -42,9 +42,11 @@
 // GPU-scope fences cost microseconds while the SM's memory pipeline is full of
 // weight copies. Relaxed counters (bumped once per CTA per phase, unordered)
 // only tell the readers when to look. Four control warps per CTA do the
-// looking: they bring the whole tagged block (x, logits, h_shared, h_routed)
-// into shared memory with one bulk copy, check the tags in place (copying
-// again while any is stale), and publish to the workers with an mbarrier.
+// looking: they read the whole tagged block (x, logits, h_shared, h_routed)
+// with relaxed vector loads, one round trip for the 128 threads (a bulk copy
+// would queue behind the weight copies on the SM's copy engine), check the
+// tags, write the values to shared memory (reading again while any is stale),
+// and publish to the workers with an mbarrier.
 // Control warp 0 also computes the CTA's own copy of the top-8. The epoch
 // lives in the workspace; CTA 0 advances it once the last layer's output is
 // complete, so a launch needs nothing from the host but its pointers.
@@ -103,8 +105,7 @@ constexpr int OFF_XS = OFF_RING + NWORK * NS * STAGE;   // bf16 x [H]
 constexpr int OFF_N = OFF_XS + H * 2;                    // fp32 n in two halves per word: n[8w..8w+3] at
                                                          // float4 w, n[8w+4..8w+7] at float4 HW + w
 constexpr int OFF_SN = OFF_N + H * 4;                    // fp32 word sums of n [HW] (written, no longer read)
-constexpr int OFF_H = OFF_SN + HW * 4;                   // tagged fp32 h_routed [K*I], h_shared [S]; also the
-                                                         // landing zone of the tagged layer input
+constexpr int OFF_H = OFF_SN + HW * 4;                   // tagged fp32 h_routed [K*I], h_shared [S]
 constexpr int OFF_Z = OFF_H + H_FLOATS * 4;              // tagged logits [MAX_E] (64-bit words)
 constexpr int HG = H / 32;                               // 32-value blocks of n
 constexpr int DIG_WORDS = 28;                            // per block: 4 words x 6 digit words, scale, sum, pad
@@ -112,11 +113,10 @@ constexpr int OFF_DIG = OFF_Z + MAX_E * 8;               // n as byte digits for
 constexpr int OFF_RT = OFF_DIG + HG * DIG_WORDS * 4;     // routing cache [2 layers]: expert ptrs, weights, ids
 constexpr int RT_BYTES = 2 * (K * 8 + K * 4 + K * 4);
 constexpr int OFF_BAR = OFF_RT + RT_BYTES;               // mbarriers
-enum { B_X = NWORK * NS, B_XS, B_K, B_HS, B_HR, B_LOAD, N_BAR };  // B_XS: raw x staged; B_X: r and n too
+enum { B_X = NWORK * NS, B_XS, B_K, B_HS, B_HR, N_BAR };  // B_XS: raw x staged; B_X: r and n too
 constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;            // r, epoch, CTA phase counters, stale count
 constexpr int MAX_L = 64;                                // layers (tags are epoch * 64 + layer)
 constexpr int OFF_DESC = OFF_MISC + 32;                  // copies of the layer descriptors [MAX_L]
-static_assert(H * 4 <= H_FLOATS * 4, "the tagged layer input fits the h area");
 constexpr int HB = K * I / 32;                           // 32-value blocks of h_routed (22 per expert)
 static_assert(OFF_DIG % 16 == 0 && HG % 8 == 0 && I % 32 == 0, "digit blocks");
 static_assert(DIG_WORDS <= 32, "a digit block is no larger than the 32 fp32 values it replaces (in-place staging)");
@@ -270,6 +270,11 @@ __device__ __forceinline__ uint4 ld_relaxed_v4(const void* p) {
 }
 __device__ __forceinline__ void ld_relaxed_v2u64(const void* p, unsigned long long& a, unsigned long long& b) {
     asm volatile("ld.relaxed.gpu.global.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const void* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
 }
 __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
     uint32_t v;
@@ -600,27 +605,34 @@ __device__ __forceinline__ uint32_t tag4_of(uint32_t epoch, int l) { return 1u +
 __device__ __forceinline__ uint32_t tagged_f(float v, uint32_t tag4) { return (__float_as_uint(v) & ~15u) | tag4; }
 __device__ __forceinline__ void ctrl_sync() { asm volatile("bar.sync %0, %1;" ::"n"(CTRL_BAR), "n"(NCTRL * 32) : "memory"); }
 
-// ---- control warps: bulk-copy a tagged block into shared memory and check it.
-// All four control warps call this with the same arguments; warp 0 issues the
-// copy, each warp checks its quarter with `check` (which returns the number of
-// stale words it saw and may unpack them), and the copy is repeated while any
-// word is stale. `loads` counts the uses of the load mbarrier.
+// ---- control warps: read a tagged block into shared memory and check it.
+// 16-byte chunks c = cw * 32 + lane + 128 i (c < n16) of the block, read with
+// relaxed loads issued back to back (at most NMAX per thread), then handed to f(c, v).
+template <int NMAX, typename F>
+__device__ __forceinline__ void ctrl_read(const uint32_t* src, int n16, int cw, int lane, F f) {
+    uint4 v[NMAX];
+#pragma unroll
+    for (int i = 0; i < NMAX; ++i) {
+        const int c = cw * 32 + lane + i * NCTRL * 32;
+        if (c < n16) v[i] = ld_relaxed_v4(src + 4 * c);
+    }
+#pragma unroll
+    for (int i = 0; i < NMAX; ++i) {
+        const int c = cw * 32 + lane + i * NCTRL * 32;
+        if (c < n16) f(c, v[i]);
+    }
+}
+// All four control warps call this with the same arguments: each reads its
+// share of the block in `check` (which writes the values to shared memory and
+// returns the number of stale words it saw), and the block is read again while
+// any word is stale.
 template <typename Check>
-__device__ bool ctrl_load(const Params& P, const void* src, uint32_t bytes, unsigned char* dst, uint32_t bar_load,
-                          int& loads, uint32_t* stale, int cw, int lane, Check check) {
+__device__ bool ctrl_poll(const Params& P, uint32_t* stale, int cw, int lane, Check check) {
     const uint64_t t0 = gtimer();
     for (int round = 0;; ++round) {
-        if (cw == 0 && lane == 0) {
-            stale[0] = 0u;
-            fence_proxy_async();  // the area was last read through the generic proxy
-            mbar_expect_tx(bar_load, bytes);
-            bulk_g2s(smem_u32(dst), src, bytes, bar_load);
-        }
-        const bool got = warp_wait_own(bar_load, loads & 1, P.err, lane);
-        ++loads;
-        if (!got) {
-            if (lane == 0) atomicOr(&stale[1], 1u);
-        } else {
+        if (cw == 0 && lane == 0) stale[0] = 0u;
+        ctrl_sync();  // the count is reset before any warp adds to it
+        {
             const uint32_t bad = check();
             const uint32_t wbad = __reduce_add_sync(FULL, bad);
             if (wbad && lane == 0) atomicAdd(&stale[0], wbad);
@@ -643,7 +655,7 @@ __device__ bool ctrl_load(const Params& P, const void* src, uint32_t bytes, unsi
 // -> x (bf16; released to the router rows), then r, n = r x and the word sums
 // of n; all four control warps.
 __device__ bool stage_x(const Params& P, int l, uint32_t epoch, uint32_t hint_target, unsigned char* smem,
-                        uint32_t bar_load, uint32_t bar_xs, int& loads, uint32_t* stale, int cw, int lane) {
+                        uint32_t bar_xs, uint32_t* stale, int cw, int lane) {
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem + OFF_XS);
     if (l == 0) {
         const uint4* s4 = reinterpret_cast<const uint4*>(P.x);
@@ -654,18 +666,16 @@ __device__ bool stage_x(const Params& P, int l, uint32_t epoch, uint32_t hint_ta
         ctrl_sync();
         if (stale[1]) return false;
         const uint32_t tag16 = (epoch * 64u + (uint32_t)(l - 1)) & 0xffffu;
-        unsigned char* land = smem + OFF_H;
         auto check = [&]() -> uint32_t {
             uint32_t bad = 0;
-            for (int c = cw * 32 + lane; c < H / 4; c += NCTRL * 32) {  // 4 tagged words per chunk
-                const uint4 v = reinterpret_cast<const uint4*>(land)[c];
+            ctrl_read<(H / 4 + NCTRL * 32 - 1) / (NCTRL * 32)>(LD(l - 1).xt, H / 4, cw, lane, [&](int c, uint4 v) {
                 bad += ((v.x >> 16) != tag16) + ((v.y >> 16) != tag16) + ((v.z >> 16) != tag16) +
-                       ((v.w >> 16) != tag16);
+                       ((v.w >> 16) != tag16);  // 4 tagged words per chunk
                 reinterpret_cast<uint2*>(xs)[c] = make_uint2((v.x & 0xffffu) | (v.y << 16), (v.z & 0xffffu) | (v.w << 16));
-            }
+            });
             return bad;
         };
-        if (!ctrl_load(P, LD(l - 1).xt, H * 4, land, bar_load, loads, stale, cw, lane, check)) return false;
+        if (!ctrl_poll(P, stale, cw, lane, check)) return false;
         if (cw == 0 && lane == 0) trace_at(P, l, TR_X_READY);
     }
     ctrl_sync();
@@ -776,47 +786,88 @@ __device__ void stage_digits(unsigned char* smem, int t, int nt) {
 }
 
 // h_routed (fp32, in the h area) -> digit blocks in place, all four control
-// warps: block b's digits (112 bytes at 112 b) only cover fp32 blocks <= b, and
-// each round reads all its blocks before any of its digits are written.
-__device__ void digits_in_place(unsigned char* smem, int t) {
+// warps. The digits are those of block_digits; only the work is spread
+// differently: eight consecutive lanes hold one block (a float4 each, read
+// contiguously, so without bank conflicts), find its largest |v| and its sum
+// with three butterfly steps, convert their four values, and swap two with the
+// neighbouring lane, so that the even lane holds columns 0,2,4,6 and the odd
+// lane columns 1,3,5,7 of their 8-value word. Every thread holds all its values
+// in registers before any digit is written (the digits overwrite the fp32 area).
+__device__ void digits_in_place(unsigned char* smem, int cw, int lane) {
     const float4* h4 = reinterpret_cast<const float4*>(smem + OFF_H);
     uint32_t* dig = reinterpret_cast<uint32_t*>(smem + OFF_H);
-    for (int b0 = 0; b0 < HB; b0 += NCTRL * 32) {
-        const int b = b0 + t;
-        float v[32];
-        if (b < HB) {
+    constexpr int NQ = HB * 8, PER = NQ / (NCTRL * 32);  // float4s of h_routed, per thread
+    static_assert(NQ % (NCTRL * 32) == 0, "whole rounds of the control threads");
+    const int t = cw * 32 + lane;
+    float4 v[PER];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float4 a = h4[8 * b + c];
-                v[4 * c + 0] = a.x;
-                v[4 * c + 1] = a.y;
-                v[4 * c + 2] = a.z;
-                v[4 * c + 3] = a.w;
-            }
+    for (int k = 0; k < PER; ++k) v[k] = h4[t + NCTRL * 32 * k];
+    ctrl_sync();
+    const int c = lane & 7;  // float4 of the block: word c >> 1, columns 0-3 (even c) or 4-7 (odd c)
+    const bool odd = c & 1;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int b = (t + NCTRL * 32 * k) >> 3;
+        const float4 a = v[k];
+        float m = fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w)));
+        float sum = (a.x + a.y) + (a.z + a.w);
+        m = fmaxf(m, __shfl_xor_sync(FULL, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(FULL, m, 2));
+        m = fmaxf(m, __shfl_xor_sync(FULL, m, 4));
+        sum += __shfl_xor_sync(FULL, sum, 1);
+        sum += __shfl_xor_sync(FULL, sum, 2);
+        sum += __shfl_xor_sync(FULL, sum, 4);
+        float up = 0.0f, down = 0.0f;  // a block below 2^-100 counts as zero
+        if (m >= 7.8886e-31f) {
+            const int e = (int)((__float_as_uint(m) >> 23) & 0xffu) - 127;
+            up = __uint_as_float((uint32_t)(127 + 22 - e) << 23);
+            down = __uint_as_float((uint32_t)(127 + e - 22) << 23);
         }
-        ctrl_sync();
-        if (b < HB) block_digits(v, dig + b * DIG_WORDS);
-        ctrl_sync();
+        const int q0 = __float2int_rn(a.x * up), q1 = __float2int_rn(a.y * up), q2 = __float2int_rn(a.z * up),
+                  q3 = __float2int_rn(a.w * up);
+        // even lane: columns 0, 2 (own), 4, 6 (neighbour's q0, q2); odd: 1, 3 (neighbour's q1, q3), 5, 7 (own)
+        const int ra = __shfl_xor_sync(FULL, odd ? q0 : q1, 1), rb = __shfl_xor_sync(FULL, odd ? q2 : q3, 1);
+        uint32_t w0, w1, w2;
+        digit_words(odd ? ra : q0, odd ? rb : q2, odd ? q1 : ra, odd ? q3 : rb, w0, w1, w2);
+        uint32_t* d = dig + b * DIG_WORDS + 6 * (c >> 1) + (odd ? 1 : 0);
+        d[0] = w0;
+        d[2] = w1;
+        d[4] = w2;
+        if (c == 0) *reinterpret_cast<float2*>(dig + b * DIG_WORDS + 24) = make_float2(down, sum);
     }
 }
 
 // Control warp 0: the CTA's copy of the layer's top-k from the tagged logits.
 __device__ bool route_layer(const Params& P, int l, uint32_t tag, uint32_t epoch_x_e, unsigned char* smem, Route* rt,
-                            uint32_t bar_load, int& loads, int lane, int& sel, float& selz) {
+                            int lane, int& sel, float& selz) {
     const LayerDesc& D = LD(l);
     if (!wait_hint(D.cnt_z, epoch_x_e, P, lane)) return false;
-    const unsigned long long* zt = reinterpret_cast<const unsigned long long*>(smem + OFF_Z);
+    unsigned long long* zt = reinterpret_cast<unsigned long long*>(smem + OFF_Z);
     const uint64_t t0 = gtimer();
     for (;;) {
-        if (lane == 0) {
-            fence_proxy_async();
-            mbar_expect_tx(bar_load, (uint32_t)D.E * 8);
-            bulk_g2s(smem_u32(smem + OFF_Z), D.zt, (uint32_t)D.E * 8, bar_load);
+        // the tagged logits, two per lane and load (relaxed, issued back to back)
+        constexpr int NZ = MAX_E / 64;
+        unsigned long long za[NZ], zb[NZ];
+#pragma unroll
+        for (int i = 0; i < NZ; ++i) {
+            const int j = 2 * (lane + 32 * i);
+            if (j + 1 < D.E) ld_relaxed_v2u64(D.zt + j, za[i], zb[i]);
+            else if (j < D.E) za[i] = ld_relaxed_u64(D.zt + j);
         }
-        if (!warp_wait_own(bar_load, loads & 1, P.err, lane)) return false;
-        ++loads;
         int bad = 0;
-        for (int j = lane; j < D.E; j += 32) bad |= (uint32_t)(zt[j] >> 32) != tag;
+#pragma unroll
+        for (int i = 0; i < NZ; ++i) {
+            const int j = 2 * (lane + 32 * i);
+            if (j < D.E) {
+                zt[j] = za[i];
+                bad |= (uint32_t)(za[i] >> 32) != tag;
+            }
+            if (j + 1 < D.E) {
+                zt[j + 1] = zb[i];
+                bad |= (uint32_t)(zb[i] >> 32) != tag;
+            }
+        }
+        __syncwarp();
         if (!__any_sync(FULL, bad)) break;
         __nanosleep(128);
         if (err_set(P.err)) return false;
@@ -844,6 +895,44 @@ __device__ bool route_layer(const Params& P, int l, uint32_t tag, uint32_t epoch
     }
     selz = 0.0f;
     sel = -1;
+    if (D.E <= 128) {
+        // Four keys per lane, sorted (larger key first, then the lower expert);
+        // every round the best head over the warp is taken and its lane pops it.
+        uint32_t k0 = key[0], k1 = key[1], k2 = key[2], k3 = key[3];
+        uint32_t i0 = lane, i1 = lane + 32, i2 = lane + 64, i3 = lane + 96;
+        auto order = [](uint32_t& ka, uint32_t& ia, uint32_t& kb, uint32_t& ib) {
+            const bool sw = kb > ka || (kb == ka && ib < ia);
+            const uint32_t tk = sw ? kb : ka, ti = sw ? ib : ia;
+            kb = sw ? ka : kb;
+            ib = sw ? ia : ib;
+            ka = tk;
+            ia = ti;
+        };
+        order(k0, i0, k1, i1);
+        order(k2, i2, k3, i3);
+        order(k0, i0, k2, i2);
+        order(k1, i1, k3, i3);
+        order(k1, i1, k2, i2);
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            const uint32_t kmax = __reduce_max_sync(FULL, k0);
+            const uint32_t imin = __reduce_min_sync(FULL, k0 == kmax ? i0 : 0x7fffffffu);
+            if (lane == (int)(imin & 31u)) {
+                k0 = k1;
+                i0 = i1;
+                k1 = k2;
+                i1 = i2;
+                k2 = k3;
+                i2 = i3;
+                k3 = 0u;
+                i3 = 0x7fffffffu;
+            }
+            if (lane == i) {
+                sel = (int)imin;
+                selz = __uint_as_float((uint32_t)zt[imin]);
+            }
+        }
+    } else
 #pragma unroll 1
     for (int i = 0; i < K; ++i) {
         uint32_t bk = key[0];
@@ -920,8 +1009,7 @@ __device__ void route_weights(const Params& P, int l, unsigned char* smem, Route
 // h_shared or h_routed (tagged fp32 words) -> shared memory, in place, checked by
 // the four control warps; h_routed is then turned into digit blocks in place.
 __device__ bool stage_h(const Params& P, int l, uint32_t tag4, const uint32_t* hint, uint32_t hint_target,
-                        bool routed, unsigned char* smem, uint32_t bar_load, int& loads, uint32_t* stale, int cw,
-                        int lane) {
+                        bool routed, unsigned char* smem, uint32_t* stale, int cw, int lane) {
     const LayerDesc& D = LD(l);
     if (cw == 0 && !wait_hint(hint, hint_target, P, lane) && lane == 0) atomicOr(&stale[1], 1u);
     ctrl_sync();
@@ -930,16 +1018,14 @@ __device__ bool stage_h(const Params& P, int l, uint32_t tag4, const uint32_t* h
     uint32_t* h = reinterpret_cast<uint32_t*>(smem + OFF_H) + w0;
     auto check = [&]() -> uint32_t {
         uint32_t bad = 0;
-        for (int c = cw * 32 + lane; c < nw / 4; c += NCTRL * 32) {
-            const uint4 v = reinterpret_cast<const uint4*>(h)[c];
+        ctrl_read<(K * I / 4 + NCTRL * 32 - 1) / (NCTRL * 32)>(D.ht + w0, nw / 4, cw, lane, [&](int c, uint4 v) {
+            reinterpret_cast<uint4*>(h)[c] = v;
             bad += ((v.x & 15u) != tag4) + ((v.y & 15u) != tag4) + ((v.z & 15u) != tag4) + ((v.w & 15u) != tag4);
-        }
+        });
         return bad;
     };
-    if (!ctrl_load(P, D.ht + w0, (uint32_t)nw * 4, reinterpret_cast<unsigned char*>(h), bar_load, loads, stale, cw,
-                   lane, check))
-        return false;
-    if (routed) digits_in_place(smem, cw * 32 + lane);
+    if (!ctrl_poll(P, stale, cw, lane, check)) return false;
+    if (routed) digits_in_place(smem, cw, lane);
     ctrl_sync();
     return true;
 }
@@ -957,11 +1043,10 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
     const uint32_t bar_k = smem_u32(&bars[B_K]);
     const uint32_t bar_hs = smem_u32(&bars[B_HS]);
     const uint32_t bar_hr = smem_u32(&bars[B_HR]);
-    const uint32_t bar_load = smem_u32(&bars[B_LOAD]);
     Route* rt = reinterpret_cast<Route*>(smem + OFF_RT);
     uint32_t* s_epoch = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 4);
     uint32_t* cta_cnt = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 8);  // [0] hs, [1] hr, [2] out
-    uint32_t* stale = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 20);   // [0] stale words, [1] abort, [2] loads
+    uint32_t* stale = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 20);   // [0] stale words, [1] abort
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NWORK * NS; ++s) mbar_init(smem_u32(&bars[s]), 1);
@@ -970,10 +1055,9 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
         mbar_init(bar_k, 1);
         mbar_init(bar_hs, 1);
         mbar_init(bar_hr, 1);
-        mbar_init(bar_load, 1);
         *s_epoch = ld_relaxed_u32(P.epoch);
         cta_cnt[0] = cta_cnt[1] = cta_cnt[2] = 0;
-        stale[0] = stale[1] = stale[2] = 0;
+        stale[0] = stale[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     {  // the layer descriptors, copied once
@@ -989,20 +1073,19 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
     if (warp < NCTRL) {
         // ================================================= control warps
         const int cw = warp;
-        int loads = 0;
         bool ok = true;
         for (int l = 0; l < P.L && ok; ++l) {
             const LayerDesc& D = LD(l);
             const uint32_t tag = epoch * 64u + (uint32_t)l;
             const uint32_t tag4 = tag4_of(epoch, l);
-            if (!(ok = stage_x(P, l, epoch, hint_target, smem, bar_load, bar_xs, loads, stale, cw, lane))) break;
+            if (!(ok = stage_x(P, l, epoch, hint_target, smem, bar_xs, stale, cw, lane))) break;
             if (cw == 0 && lane == 0) {
                 mbar_arrive(bar_x);
                 trace_at(P, l, TR_X_STAGED);
             }
             int rok = 1, sel = -1;
             float selz = 0.0f;
-            if (cw == 0) rok = route_layer(P, l, tag, epoch * (uint32_t)E, smem, rt, bar_load, loads, lane, sel, selz);
+            if (cw == 0) rok = route_layer(P, l, tag, epoch * (uint32_t)E, smem, rt, lane, sel, selz);
             else
                 stage_digits(smem, (cw - 1) * 32 + lane, (NCTRL - 1) * 32);
             ctrl_sync();  // the digits are complete before the top-k (which the routed gate/up items wait for)
@@ -1012,7 +1095,6 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
                     trace_at(P, l, TR_TOPK);
                 }
                 if (!rok && lane == 0) atomicOr(&stale[1], 1u);
-                if (lane == 0) stale[2] = (uint32_t)loads;  // route_layer's copies: warp 0 tells the others
                 if (rok) route_weights(P, l, smem, rt, blockIdx.x == 0, lane, sel, selz);
             }
             ctrl_sync();
@@ -1020,13 +1102,12 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
                 ok = false;
                 break;
             }
-            loads = (int)stale[2];
-            if (!(ok = stage_h(P, l, tag4, D.cnt_hs, hint_target, false, smem, bar_load, loads, stale, cw, lane))) break;
+            if (!(ok = stage_h(P, l, tag4, D.cnt_hs, hint_target, false, smem, stale, cw, lane))) break;
             if (cw == 0 && lane == 0) {
                 mbar_arrive(bar_hs);
                 trace_at(P, l, TR_HS_STAGED);
             }
-            if (!(ok = stage_h(P, l, tag4, D.cnt_hr, hint_target, true, smem, bar_load, loads, stale, cw, lane))) break;
+            if (!(ok = stage_h(P, l, tag4, D.cnt_hr, hint_target, true, smem, stale, cw, lane))) break;
             if (cw == 0 && lane == 0) {
                 mbar_arrive(bar_hr);
                 trace_at(P, l, TR_HR_STAGED);
@@ -1236,35 +1317,37 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
                     else carry1 = acc;
                 } else {
                     // the 8 experts' down rows j0, j0 + 1 (int4, K = I) against the digit blocks of
-                    // h_routed: lane = (row lane & 1, expert (lane >> 1) & 7, block (lane >> 4) + 2 m)
+                    // h_routed: lane = (expert, 32-value block) pair, both rows per pair, so that each
+                    // block's digits are read once; the pairs' routing-weighted terms are summed over the warp
                     const uint32_t* dh = reinterpret_cast<const uint32_t*>(smem + OFF_H);
-                    const int jr = lane & 1, i = (lane >> 1) & (K - 1);
-                    const unsigned char* crow = st + i * 2 * D_ROW + jr * D_ROW;
-                    const uint32_t* sbrow = reinterpret_cast<const uint32_t*>(st + DN_SB_OFF + i * 4 * D_SB) +
-                                            ((j0 & 3) + jr) * (D_SB / 4);
-                    float acc = 0.0f;
-#pragma unroll 1
-                    for (int b = lane >> 4; b < I / 32; b += 2) {
-                        const uint4 q = *reinterpret_cast<const uint4*>(crow + 16 * b);
-                        const uint32_t* db = dh + (i * (I / 32) + b) * DIG_WORDS;
+                    constexpr int NB_E = I / 32, NPAIR = K * NB_E;
+                    float acc0 = 0.0f, acc1 = 0.0f;
+#pragma unroll 2
+                    for (int pr = lane; pr < NPAIR; pr += 32) {
+                        const int i = pr / NB_E, b = pr - i * NB_E;
+                        const uint32_t* db = dh + pr * DIG_WORDS;
                         const uint4* dp = reinterpret_cast<const uint4*>(db);
                         const uint4 d0 = dp[0], d1 = dp[1], d2 = dp[2], d3 = dp[3], d4 = dp[4], d5 = dp[5];
                         const float2 meta = *reinterpret_cast<const float2*>(db + 24);
-                        int s0 = 0, s1 = 0, s2 = 0;
-                        word_digits(q.x, d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, s0, s1, s2);
-                        word_digits(q.y, d1.z, d1.w, d2.x, d2.y, d2.z, d2.w, s0, s1, s2);
-                        word_digits(q.z, d3.x, d3.y, d3.z, d3.w, d4.x, d4.y, s0, s1, s2);
-                        word_digits(q.w, d4.z, d4.w, d5.x, d5.y, d5.z, d5.w, s0, s1, s2);
-                        const float pq = fmaf((float)s2, 65536.0f, fmaf((float)s1, 256.0f, (float)s0)) * meta.x;
-                        const uint32_t sbw = sbrow[b >> 1];
-                        acc = fmaf(h2f(sbw & 0xffffu), pq, fmaf(h2f(sbw >> 16), meta.y, acc));
+                        const float wi = rt->w[l & 1][i];
+                        const uint32_t* sbb = reinterpret_cast<const uint32_t*>(st + DN_SB_OFF + i * 4 * D_SB) +
+                                              (j0 & 3) * (D_SB / 4) + (b >> 1);
+#pragma unroll
+                        for (int jr = 0; jr < 2; ++jr) {
+                            const uint4 q = *reinterpret_cast<const uint4*>(st + i * 2 * D_ROW + jr * D_ROW + 16 * b);
+                            int s0 = 0, s1 = 0, s2 = 0;
+                            word_digits(q.x, d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, s0, s1, s2);
+                            word_digits(q.y, d1.z, d1.w, d2.x, d2.y, d2.z, d2.w, s0, s1, s2);
+                            word_digits(q.z, d3.x, d3.y, d3.z, d3.w, d4.x, d4.y, s0, s1, s2);
+                            word_digits(q.w, d4.z, d4.w, d5.x, d5.y, d5.z, d5.w, s0, s1, s2);
+                            const float pq = fmaf((float)s2, 65536.0f, fmaf((float)s1, 256.0f, (float)s0)) * meta.x;
+                            const uint32_t sbw = sbb[jr * (D_SB / 4)];
+                            const float yb = fmaf(h2f(sbw & 0xffffu), pq, h2f(sbw >> 16) * meta.y);
+                            if (jr == 0) acc0 = fmaf(wi, yb, acc0);
+                            else acc1 = fmaf(wi, yb, acc1);
+                        }
                     }
-                    acc += __shfl_xor_sync(FULL, acc, 16);     // both halves of the blocks: y of (row, expert)
-                    acc *= rt->w[l & 1][i];                    // routing weight
-                    acc += __shfl_xor_sync(FULL, acc, 2);      // sum over the experts
-                    acc += __shfl_xor_sync(FULL, acc, 4);
-                    acc += __shfl_xor_sync(FULL, acc, 8);
-                    const float y0 = __shfl_sync(FULL, acc, 0), y1 = __shfl_sync(FULL, acc, 1);
+                    const float y0 = warp_sum(acc0), y1 = warp_sum(acc1);
                     if (lane == 0) {
                         const uint32_t o0 = f2bf(bf2f(xs[j0]) + (carry0 + y0));
                         const uint32_t o1 = f2bf(bf2f(xs[j0 + 1]) + (carry1 + y1));
@@ -1284,8 +1367,11 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
         if (!hs_sig) signal_phase(P, l, -1, &cta_cnt[0], D.cnt_hs, lane);
         if (!hr_sig) signal_phase(P, l, TR_CTA_HR_DONE, &cta_cnt[1], D.cnt_hr, lane);
         // observe this layer's routing and h phases even without items that needed
-        // them, so that later parity tests never run two phases behind
-        try_issue();
+        // them, so that later parity tests never run two phases behind (the next
+        // copies go out first only when a phase is still pending: otherwise the
+        // layer's output is counted first)
+        const bool all_seen = n_ready && hs_ready && hr_ready && k_seen > l;
+        if (!all_seen) try_issue();
         if (!n_ready && !(ok = warp_wait_mbar(bar_x, l & 1, P, lane))) break;
         if (!topk_known(l)) {
             if (!(ok = warp_wait_mbar(bar_k, l & 1, P, lane))) break;
@@ -1295,6 +1381,7 @@ __global__ void __launch_bounds__(NT, 1) k_fused_stack(Params P) {
         if (!hr_ready && !(ok = warp_wait_mbar(bar_hr, l & 1, P, lane))) break;
         signal_phase(P, l, TR_CTA_OUT, &cta_cnt[2], D.cnt_out, lane);
         if (w0t) trace_at(P, l, TR_W_DONE);
+        if (all_seen) try_issue();
     }
 
     if (!ok && lane == 0) {
