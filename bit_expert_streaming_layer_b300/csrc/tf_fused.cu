@@ -92,7 +92,6 @@ constexpr int DN_SB_OFF = K * 2 * D_ROW;            // 5632
 constexpr int DN_BYTES = DN_SB_OFF + K * 4 * D_SB;  // 7040
 constexpr int H_FLOATS = K * I + S;                 // h_routed then h_shared
 constexpr unsigned long long OWN_LIMIT_NS = 2000000000ull;  // 2 s: waits for this warp's own copies
-constexpr uint32_t SUSPEND_NS = 1000;      // suspend hint of a blocking mbarrier test
 constexpr uint32_t HINT_SLEEP_NS = 64;     // pause between two reads of a hint counter
 constexpr int CTRL_BAR = 1;                // named barrier of the control warps
 static_assert(HW == 32 * WPL, "lane ownership of the K = H words");
@@ -220,7 +219,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Blocking test: the thread sleeps until the phase completes or about ns elapse.
 // Non-blocking test of a phase (try_wait may suspend the thread for a while).
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -228,15 +226,6 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
         "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(ns)
         : "memory");
     return ok != 0;
 }
@@ -303,12 +292,14 @@ __device__ __forceinline__ unsigned long long tag64(uint32_t tag, float v) {
 __device__ __forceinline__ bool err_set(const uint32_t* err) { return *(volatile const uint32_t*)err != 0; }
 
 // Bounded wait (one lane) on an mbarrier phase that other warps complete: false
-// (error recorded) after `limit` ns, or as soon as another CTA has failed.
+// (error recorded) after `limit` ns, or as soon as another CTA has failed. The
+// waits use try_wait with the hardware's own suspend time: a suspend-time hint
+// (1 us or 100 ns) measured about 1.3 % slower per decode step.
 __device__ bool wait_mbar(uint32_t bar, uint32_t parity, uint32_t* err, unsigned long long limit) {
     if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = gtimer();
     for (uint32_t n = 1;; ++n) {
-        if (mbar_wait_hint(bar, parity, SUSPEND_NS)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if ((n & 7u) == 0) {
             if (err_set(err)) return false;
             if (gtimer() - t0 > limit) {
@@ -330,7 +321,7 @@ __device__ bool wait_own(uint32_t bar, uint32_t parity, uint32_t* err) {
     if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = gtimer();
     for (uint32_t n = 1;; ++n) {
-        if (mbar_wait_hint(bar, parity, SUSPEND_NS)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if ((n & 7u) == 0 && gtimer() - t0 > OWN_LIMIT_NS) {
             atomicOr(err, ERR_TIMEOUT);
             return false;

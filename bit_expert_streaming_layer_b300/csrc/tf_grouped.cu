@@ -166,12 +166,13 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ bool mbar_wait_hint(uint32_t bar, uint32_t parity) {
+// try_wait with the hardware's own suspend time (no suspend-time hint).
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(1000u)
+        : "r"(bar), "r"(parity)
         : "memory");
     return ok != 0;
 }
@@ -262,10 +263,10 @@ __device__ __forceinline__ uint32_t idesc_f16(int n, int bf16) {
 // it returns false as soon as the flag is up.
 __device__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, uint32_t* err,
                          unsigned long long limit) {
-    if (mbar_wait_hint(bar, parity)) return true;
+    if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = gtimer();
     for (uint32_t n = 1;; ++n) {
-        if (mbar_wait_hint(bar, parity)) return true;
+        if (mbar_try(bar, parity)) return true;
         if ((n & 7u) == 0) {
             if (*abort_flag) return false;
             if (gtimer() - t0 > limit) {
@@ -280,10 +281,10 @@ __device__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort
 // (nothing may still write to shared memory or TMEM when the CTA releases them) and
 // is bounded by a fixed 2 s.
 __device__ bool wait_own(uint32_t bar, uint32_t parity, uint32_t* err) {
-    if (mbar_wait_hint(bar, parity)) return true;
+    if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = gtimer();
     for (uint32_t n = 1;; ++n) {
-        if (mbar_wait_hint(bar, parity)) return true;
+        if (mbar_try(bar, parity)) return true;
         if ((n & 7u) == 0 && gtimer() - t0 > OWN_LIMIT_NS) {
             atomicOr(err, 1u);
             return false;
