@@ -95,6 +95,8 @@ def lib(bits: int = 32, mt: bool = False):
         L.or_lfu_step.restype = i32
         L.or_lfu_step.argtypes = [vp, i32, i32, vp, i32, ctypes.POINTER(CacheEvent)]
         L.or_lfu_state.argtypes = [vp, i32, vp, vp, vp]
+        L.or_attn_decode.argtypes = [vp, i32, i32, i32, i32, ctypes.c_double, ctypes.c_double, i32, vp, vp, vp, vp,
+                                     vp, vp, vp, vp, vp]
         L.or_real_bytes.restype = i32
         L.or_threads.restype = i32
         _libs[key] = L
@@ -309,3 +311,30 @@ class LFU:
             self._L.or_lfu_free(self._h)
         except Exception:
             pass
+
+
+# ------------------------------------------------------------------------ attention
+
+def attn_decode(x, pos: int, Wq, Wk, Wv, Wo, k_cache, v_cache, nq: int, nkv: int, d: int,
+                theta: float = 10000.0, eps: float = EPS, bits: int = 64):
+    """Attention half of a decoder layer for one token at position pos (see or_attn_decode).
+
+    x: bf16 bits [H]; W*: bf16 bits, Wq [nq*d, H], Wk/Wv [nkv*d, H], Wo [H, nq*d]; k_cache, v_cache: fp16
+    bits [max_seq, nkv, d] (uint16 arrays, updated in place at row pos). Returns (out bf16 bits [H],
+    scores of q head 0 [pos + 1], attention output a [nq*d])."""
+    H = int(np.asarray(x).size)
+    assert k_cache.dtype == np.uint16 and v_cache.dtype == np.uint16
+    assert k_cache.flags["C_CONTIGUOUS"] and v_cache.flags["C_CONTIGUOUS"]
+    assert k_cache.size >= (pos + 1) * nkv * d and v_cache.size >= (pos + 1) * nkv * d
+    xa, xp = _c(x, np.uint16)
+    ws = [_c(w, np.uint16) for w in (Wq, Wk, Wv, Wo)]
+    assert ws[0][0].size == nq * d * H and ws[1][0].size == nkv * d * H and ws[2][0].size == nkv * d * H
+    assert ws[3][0].size == H * nq * d
+    dt = _dt(bits)
+    out = np.zeros(H, dtype=np.uint16)
+    sc = np.zeros(pos + 1, dtype=dt)
+    a = np.zeros(nq * d, dtype=dt)
+    lib(bits).or_attn_decode(xp, H, nq, nkv, d, float(eps), float(theta), int(pos), ws[0][1], ws[1][1], ws[2][1],
+                             ws[3][1], k_cache.ctypes.data, v_cache.ctypes.data, out.ctypes.data, sc.ctypes.data,
+                             a.ctypes.data)
+    return out, sc, a

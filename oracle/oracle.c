@@ -33,6 +33,12 @@
  *  - Combine: delta = shared + sum_i w_i * y_i in top-k order; out = bf16(x + delta).
  *  - 16-slot LFU expert cache per layer (devtrends page, "Qual e o principal
  *    truque da arquitetura": 16 slots, LFU). Reading: textbook LFU, see or_lfu_step.
+ *  - The attention half of a decoder layer for one token with RoPE and an FP16
+ *    KV cache (devtrends page, "Qual e o principal truque da arquitetura": the
+ *    shared core and the FP16 KV cache stay resident; "Sem dependencias do
+ *    llama.cpp e MLX": hand-written attention and RoPE kernels). The pages give
+ *    no attention shapes or conventions; the reading is a plain pre-norm
+ *    grouped-query attention, see or_attn_decode.
  *
  * Threads. The plain build is single-threaded. The same file is also built with
  * -fopenmp (liboracle32mt.so), which only spreads the independent output rows
@@ -506,6 +512,104 @@ void or_lfu_state(const or_lfu* c, int layer, int32_t* expert, int64_t* count, i
     memcpy(expert, c->expert + o, sizeof(int32_t) * (size_t)c->n_slots);
     memcpy(count, c->count + o, sizeof(int64_t) * (size_t)c->n_slots);
     memcpy(last_use, c->last_use + o, sizeof(int64_t) * (size_t)c->n_slots);
+}
+
+/* --------------------------------------------------------------- attention */
+
+/*
+ * Attention half of a decoder layer for one token at position pos (0-based),
+ * grouped-query, with RoPE and an FP16 KV cache (reading of the pages, which
+ * name the kernels and the FP16 cache but give no shapes):
+ *   r = 1/sqrt(sum x^2 / H + eps) (as or_rms_scale), n = r x;
+ *   q = Wq n [nq*d], k = Wk n [nkv*d], v = Wv n [nkv*d]  (bf16 weights, row-major [out][H]);
+ *   RoPE on every head of q and k: for j < d/2 the pair (j, j + d/2) turns by
+ *     the angle pos * theta^(-2j/d):  a' = a cos - b sin,  b' = b cos + a sin
+ *     (the angle, its cosine and sine in double precision);
+ *   K[pos] = fp16(k'), V[pos] = fp16(v)   (caches fp16 [max_seq][nkv][d]);
+ *   for each q head h, with kv head g = h / (nq / nkv):
+ *     s_t = (q'_h . K[t]_g) / sqrt(d), t = 0..pos;  p = softmax(s);
+ *     a_h = sum_t p_t V[t]_g;
+ *   out = bf16(x + Wo a)   (Wo bf16 [H][nq*d]).
+ * Sums run sequentially in increasing index. scores (nullable) receives s for
+ * q head 0 (pos + 1 values); attn (nullable) receives a [nq*d].
+ */
+void or_attn_decode(const uint16_t* x, int H, int nq, int nkv, int d, double eps, double theta, int pos,
+                    const uint16_t* Wq, const uint16_t* Wk, const uint16_t* Wv, const uint16_t* Wo,
+                    uint16_t* Kc, uint16_t* Vc, uint16_t* out, REAL* scores, REAL* attn) {
+    const int QD = nq * d, KD = nkv * d, half = d / 2;
+    REAL r = or_rms_scale(x, H, eps);
+    REAL* n = (REAL*)malloc(sizeof(REAL) * (size_t)H);
+    or_normalise(x, H, r, n);
+    REAL* q = (REAL*)malloc(sizeof(REAL) * (size_t)QD);
+    REAL* k = (REAL*)malloc(sizeof(REAL) * (size_t)KD);
+    REAL* v = (REAL*)malloc(sizeof(REAL) * (size_t)KD);
+    const uint16_t* Ws[3] = {Wq, Wk, Wv};
+    REAL* ys[3] = {q, k, v};
+    const int rows[3] = {QD, KD, KD};
+    for (int m = 0; m < 3; ++m)
+        for (int j = 0; j < rows[m]; ++j) {
+            REAL acc = (REAL)0;
+            for (int c = 0; c < H; ++c) acc = acc + (REAL)or_bf16_to_float(Ws[m][(size_t)j * H + c]) * n[c];
+            ys[m][j] = acc;
+        }
+    /* RoPE */
+    for (int m = 0; m < 2; ++m) {
+        REAL* y = ys[m];
+        const int heads = m == 0 ? nq : nkv;
+        for (int h = 0; h < heads; ++h)
+            for (int j = 0; j < half; ++j) {
+                double ang = (double)pos * pow(theta, -2.0 * (double)j / (double)d);
+                REAL cs = (REAL)cos(ang), sn = (REAL)sin(ang);
+                REAL a = y[h * d + j], b = y[h * d + j + half];
+                y[h * d + j] = a * cs - b * sn;
+                y[h * d + j + half] = b * cs + a * sn;
+            }
+    }
+    /* the cache rows of this position */
+    for (int i = 0; i < KD; ++i) {
+        Kc[(size_t)pos * KD + i] = or_float_to_half((float)k[i]);
+        Vc[(size_t)pos * KD + i] = or_float_to_half((float)v[i]);
+    }
+    /* attention over positions 0..pos */
+    REAL* a = (REAL*)calloc((size_t)QD, sizeof(REAL));
+    REAL* s = (REAL*)malloc(sizeof(REAL) * (size_t)(pos + 1));
+    const REAL inv_sqrt_d = (REAL)1 / R_SQRT((REAL)d);
+    for (int h = 0; h < nq; ++h) {
+        const int g = h / (nq / nkv);
+        REAL mx = -INFINITY;
+        for (int t = 0; t <= pos; ++t) {
+            REAL acc = (REAL)0;
+            for (int j = 0; j < d; ++j)
+                acc = acc + q[h * d + j] * (REAL)or_half_to_float(Kc[((size_t)t * nkv + g) * d + j]);
+            s[t] = acc * inv_sqrt_d;
+            if (s[t] > mx) mx = s[t];
+        }
+        if (h == 0 && scores)
+            for (int t = 0; t <= pos; ++t) scores[t] = s[t];
+        REAL l = (REAL)0;
+        for (int t = 0; t <= pos; ++t) {
+            s[t] = R_EXP(s[t] - mx);
+            l = l + s[t];
+        }
+        for (int j = 0; j < d; ++j) {
+            REAL acc = (REAL)0;
+            for (int t = 0; t <= pos; ++t) acc = acc + s[t] * (REAL)or_half_to_float(Vc[((size_t)t * nkv + g) * d + j]);
+            a[h * d + j] = acc / l;
+        }
+    }
+    if (attn) memcpy(attn, a, sizeof(REAL) * (size_t)QD);
+    /* output projection and residual */
+    for (int i = 0; i < H; ++i) {
+        REAL acc = (REAL)0;
+        for (int c = 0; c < QD; ++c) acc = acc + (REAL)or_bf16_to_float(Wo[(size_t)i * QD + c]) * a[c];
+        out[i] = or_float_to_bf16((float)((REAL)or_bf16_to_float(x[i]) + acc));
+    }
+    free(n);
+    free(q);
+    free(k);
+    free(v);
+    free(a);
+    free(s);
 }
 
 int or_real_bytes(void) { return (int)sizeof(REAL); }
