@@ -946,6 +946,97 @@ def run_prefill(args):
     return line
 
 
+ATTN_SHAPE = dict(H=2816, nq=16, nkv=8, d=128)
+ATTN_CTX = 4096          # cached positions before the decoded token
+ATTN_LAYERS = 4          # distinct layers cycled through, so that weights and caches exceed the L2
+
+
+def run_attention(args):
+    """The attention half of a decoder layer (tf_attn_decode): one decode token at position ATTN_CTX over a
+    filled FP16 KV cache, 16 q heads and 8 kv heads of 128 (synthetic Gemma-like shape; the pages give none).
+    Steps cycle through ATTN_LAYERS layers with their own weights and caches (about 270 MB in all). The
+    roofline counts the step's algorithmic bytes: the four weight matrices once (bf16) plus the K and V rows
+    0..pos of the layer's kv heads (fp16)."""
+    import torch
+    import bit_expert_streaming_layer_b300 as B
+    import workload as W
+
+    sh = ATTN_SHAPE
+    Hh, nq, nkv, d = sh["H"], sh["nq"], sh["nkv"], sh["d"]
+    pos, max_seq = ATTN_CTX, ATTN_CTX + 1
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+
+    def dev16(a):
+        return torch.from_numpy(a.reshape(-1).view("int16")).to(dev)
+
+    layers = []
+    for l in range(ATTN_LAYERS):
+        ws = [dev16(m) for m in W.attention_weights(7, l, Hh, nq, nkv, d)]
+        desc = B.attn_desc(Hh, nq, nkv, d, max_seq, *ws)
+        k, v = W.cache_rows(7, l, pos, nkv, d)
+        kc = torch.zeros(B.tf_attn_cache_bytes(desc) // 2, dtype=torch.int16, device=dev)
+        vc = torch.zeros_like(kc)
+        kc[:k.size] = dev16(k)
+        vc[:v.size] = dev16(v)
+        layers.append((desc, ws, kc, vc))
+    wsb = B.tf_attn_workspace_bytes(layers[0][0])
+    wsp = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+    x = dev16(W.hidden(7, 0, 1, Hh)[0])
+    out = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        desc, _, kc, vc = layers[i % ATTN_LAYERS]
+        B.tf_attn_decode(desc, x, out, pos, kc, vc, wsp, wsb, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(0)
+    sampler.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    weight_bytes = (nq * d * Hh + 2 * nkv * d * Hh + Hh * nq * d) * 2
+    cache_bytes = 2 * (pos + 1) * nkv * d * 2
+    step_bytes = weight_bytes + cache_bytes
+    peak, peak_kind = peaks()
+    achieved = step_bytes / (ms / 1e3) / 1e9
+    # end to end: the token's x in from pinned host memory and out back, every step
+    hx = torch.empty(Hh, dtype=torch.int16, pin_memory=True)
+    hy = torch.empty(Hh, dtype=torch.int16, pin_memory=True)
+    hx.copy_(x.cpu())
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        x.copy_(hx, non_blocking=True)
+        step(i)
+        hy.copy_(out, non_blocking=True)
+        stream.synchronize()
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    return {
+        "metric": "attention half of a decoder layer, decode tok/s (1 B300)", "value": round(1e3 / ms, 1),
+        "unit": "tok/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "attention decode, H=2816, 16 q / 8 kv heads of 128, position 4096 over a filled "
+                   "FP16 KV cache", "l2": "4 layers cycled, %.0f MB of weights and caches" %
+                   (ATTN_LAYERS * (weight_bytes + 2 * max_seq * nkv * d * 2) / 1e6)},
+        "roofline": {"bound": "hbm", "kernel": "attention step (4 launches)", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": peak_kind + " (hbm_gbs)", "bytes_per_step": step_bytes, "traffic": None},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "e2e": {"value": round(1.0 / e2e_s, 1), "unit": "tok/s", "h2d_bytes_per_step": Hh * 2,
+                "d2h_bytes_per_step": Hh * 2},
+    }
+
+
 def run_reference(args):
     """The CPU oracle, as it stands (single-threaded fp32 C), on the decode workload. One step of this arm is one
     layer of the stack: step s runs layer s mod 30 on the previous step's output (the token's layers in order, the
@@ -991,10 +1082,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefetch", action="store_true",
                     help="fused path: prefetch the next layer's shared weights into L2 (measured slower)")
-    ap.add_argument("--workload", choices=["decode", "prefill", "streaming", "batched"], default="decode",
+    ap.add_argument("--workload", choices=["decode", "prefill", "streaming", "batched", "attention"], default="decode",
                     help="decode: the 30-layer decode stack (the headline line); prefill: the 4096-token grouped "
                          "layer; streaming: the decode stack through the 16-slot LFU cache with a host store; "
-                         "batched: the stack with 64 tokens per step")
+                         "batched: the stack with 64 tokens per step; attention: the attention half of a "
+                         "decoder layer (RoPE, FP16 KV cache) at position 4096")
     ap.add_argument("--alpha", type=float, default=STREAM_ALPHA,
                     help="streaming: scale of the Zipf(1.1) router bias")
     ap.add_argument("--no-graph", action="store_true",
@@ -1037,6 +1129,10 @@ def main():
     if args.workload == "batched":
         if rank == 0:
             print(json.dumps(run_batched(args)))
+        return
+    if args.workload == "attention":
+        if rank == 0:
+            print(json.dumps(run_attention(args)))
         return
 
     if world > 1:
@@ -1103,7 +1199,8 @@ def other_workloads(args):
     --workload lines), summarised beside the decode line so that every workload has a number from this run."""
     import copy
     out = {}
-    plans = (("batched", run_batched, 16, 3), ("prefill", run_prefill, 5, 3), ("streaming", run_streaming, 6, 3))
+    plans = (("batched", run_batched, 16, 3), ("prefill", run_prefill, 5, 3), ("streaming", run_streaming, 6, 3),
+             ("attention", run_attention, 64, 8))
     for name, fn, steps, warmup in plans:
         a = copy.copy(args)
         a.steps, a.warmup, a.no_cpu_baseline, a.workload = steps, warmup, True, name

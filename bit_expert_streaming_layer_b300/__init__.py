@@ -57,6 +57,13 @@ class PrefillStats(ctypes.Structure):
                 ("bytes_fetched", ctypes.c_uint64)]
 
 
+class AttnDesc(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("max_seq", ctypes.c_int), ("eps", ctypes.c_float),
+                ("rope_theta", ctypes.c_float), ("W_q", ctypes.c_void_p), ("W_k", ctypes.c_void_p),
+                ("W_v", ctypes.c_void_p), ("W_o", ctypes.c_void_p)]
+
+
 # exported symbols and their C signatures (restype, argtypes)
 _vp, _i32, _i64, _sz, _f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
 _S = ctypes.c_int32
@@ -107,6 +114,9 @@ SIGNATURES = {
                                      ctypes.POINTER(PrefillStats)]),
     "tf_stack_decode": (_S, [ctypes.POINTER(_vp), _i32, _vp, _vp, _vp, ctypes.POINTER(_vp), _vp]),
     "tf_stack_workspace_bytes": (_sz, [_i32, _i32]),
+    "tf_attn_workspace_bytes": (_sz, [ctypes.POINTER(AttnDesc)]),
+    "tf_attn_cache_bytes": (_sz, [ctypes.POINTER(AttnDesc)]),
+    "tf_attn_decode": (_S, [ctypes.POINTER(AttnDesc), _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
     "tf_stack_create": (_S, [ctypes.POINTER(_vp), _i32, ctypes.POINTER(_vp), _vp, _sz, ctypes.POINTER(_vp)]),
     "tf_stack_set_prefetch": (_S, [_vp, _i32]),
     "tf_stack_set_trace": (_S, [_vp, _vp, _sz]),
@@ -555,3 +565,25 @@ def tf_test_fail_nth_copy(n: int) -> None:
 def tf_test_set_wait_limit_ns(ns: int) -> None:
     """Limit of the kernels' waits on other warps / CTAs for later launches (0: the default 2 s)."""
     _check(lib().tf_test_set_wait_limit_ns(ns), "tf_test_set_wait_limit_ns")
+
+
+# ----------------------------------------------------------------- attention
+
+def attn_desc(H: int, n_q_heads: int, n_kv_heads: int, head_dim: int, max_seq: int, W_q, W_k, W_v, W_o,
+              eps: float = 1e-6, rope_theta: float = 10000.0) -> AttnDesc:
+    """Descriptor of the attention half of a decoder layer (W_*: device bf16 tensors or pointers)."""
+    return AttnDesc(H, n_q_heads, n_kv_heads, head_dim, max_seq, eps, rope_theta, _ptr(W_q), _ptr(W_k), _ptr(W_v),
+                    _ptr(W_o))
+
+
+def tf_attn_workspace_bytes(d: AttnDesc) -> int:
+    return lib().tf_attn_workspace_bytes(ctypes.byref(d))
+
+
+def tf_attn_cache_bytes(d: AttnDesc) -> int:
+    return lib().tf_attn_cache_bytes(ctypes.byref(d))
+
+
+def tf_attn_decode(d: AttnDesc, x, out, pos: int, k_cache, v_cache, workspace, ws_bytes: int, stream=None) -> None:
+    _check(lib().tf_attn_decode(ctypes.byref(d), _ptr(x), _ptr(out), pos, _ptr(k_cache), _ptr(v_cache),
+                                _ptr(workspace), ws_bytes, _stream(stream)), "tf_attn_decode")

@@ -76,6 +76,7 @@ size_t tf_struct_bytes(int which) {
         case 2: return sizeof(tf_step_stats);
         case 3: return sizeof(tf_cache_event);
         case 4: return sizeof(tf_prefill_stats);
+        case 5: return sizeof(tf_attn_desc);
         default: return 0;
     }
 }

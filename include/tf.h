@@ -389,7 +389,8 @@ typedef struct {
 /*
  * Size in bytes of a structure of this ABI, for bindings to check their own
  * layout against the library's: which = 0 tf_expert_table, 1 tf_layer_desc,
- * 2 tf_step_stats, 3 tf_cache_event, 4 tf_prefill_stats; 0 for any other value.
+ * 2 tf_step_stats, 3 tf_cache_event, 4 tf_prefill_stats, 5 tf_attn_desc; 0 for
+ * any other value.
  */
 size_t tf_struct_bytes(int which);
 
@@ -502,6 +503,53 @@ tf_status tf_stack_decode(tf_layer* const* layers, int L, const void* x, void* o
  * with one power-of-two scale per 32 values (integer sums, exact per block),
  * so the outputs differ from tf_stack_decode only by rounding.
  */
+/*
+ * Attention half of a decoder layer for one decode token: grouped-query
+ * self-attention with RoPE and an FP16 KV cache kept in device memory. The
+ * devtrends page names hand-written attention and RoPE kernels (section "Sem
+ * dependencias do llama.cpp e MLX") and keeps the FP16 KV cache resident
+ * (section "Qual e o principal truque da arquitetura"); it gives no shapes or
+ * conventions. The operation (the reading this library takes):
+ *   r = 1/sqrt(sum(x^2)/H + eps), n = r x            (unit gain, as the MoE layer)
+ *   q = Wq n [nq*d], k = Wk n [nkv*d], v = Wv n [nkv*d] (fp32 sums of bf16 products)
+ *   RoPE on every head of q and k: for j < d/2 the pair (j, j + d/2) turns by
+ *     the angle pos * rope_theta^(-2j/d):  a' = a cos - b sin, b' = b cos + a sin
+ *   k_cache[pos] = fp16(k'), v_cache[pos] = fp16(v)   (round to nearest even)
+ *   for each q head h, kv head g = h / (nq / nkv):
+ *     s_t = (q'_h . k_cache[t]_g) / sqrt(d), t = 0..pos;  a_h = sum_t softmax(s)_t v_cache[t]_g
+ *   out = bf16(x + Wo a)
+ * A decoder layer is this call followed by the MoE layer (tf_layer_step) on its
+ * output. pos is the 0-based position of the token: the call writes the cache
+ * rows of pos and reads rows 0..pos, so rows 0..pos-1 must hold the earlier
+ * tokens' keys and values (written by earlier calls, or by the caller).
+ */
+typedef struct {
+    int H;                      /* hidden size: a multiple of 8, at most 12000 */
+    int n_q_heads, n_kv_heads;  /* n_q_heads a multiple of n_kv_heads */
+    int head_dim;               /* 64, 128 or 256; n_q_heads * head_dim at most 12288 */
+    int max_seq;                /* rows of each cache */
+    float eps;                  /* RMS epsilon, > 0 */
+    float rope_theta;           /* RoPE base, > 0 */
+    const void* W_q;            /* device bf16 [n_q_heads*head_dim, H], row-major, 16-byte aligned */
+    const void* W_k;            /* device bf16 [n_kv_heads*head_dim, H] */
+    const void* W_v;            /* device bf16 [n_kv_heads*head_dim, H] */
+    const void* W_o;            /* device bf16 [H, n_q_heads*head_dim] */
+} tf_attn_desc;
+
+/* Workspace bytes of tf_attn_decode (0 for an invalid descriptor). */
+size_t tf_attn_workspace_bytes(const tf_attn_desc* d);
+/* Bytes of one cache (K or V): fp16 [max_seq, n_kv_heads, head_dim] (0 for an invalid descriptor). */
+size_t tf_attn_cache_bytes(const tf_attn_desc* d);
+/*
+ * out = attention half of the layer on x (device bf16 [H]; out may not alias x)
+ * for the token at position pos, 0 <= pos < max_seq. k_cache, v_cache: device
+ * fp16 caches of tf_attn_cache_bytes each, 16-byte aligned, owned by the
+ * caller. Four kernels on `stream`, each a programmatic dependent launch of
+ * the previous one; the workspace needs no zero-fill.
+ */
+tf_status tf_attn_decode(const tf_attn_desc* d, const void* x, void* out, int pos, void* k_cache, void* v_cache,
+                         void* workspace, size_t ws_bytes, void* stream);
+
 typedef struct tf_stack tf_stack;
 size_t tf_stack_workspace_bytes(int L, int E);
 tf_status tf_stack_create(tf_layer* const* layers, int L, const float* const* logit_bias, void* workspace,

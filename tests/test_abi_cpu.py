@@ -35,9 +35,10 @@ def test_library_loads_and_exports_every_declared_symbol():
 
 def test_binding_structures_match_the_library_layout():
     L = B.lib()
-    for which, cls in enumerate([B.ExpertTable, B.LayerDesc, B.StepStats, B.CacheEvent, B.PrefillStats]):
+    for which, cls in enumerate([B.ExpertTable, B.LayerDesc, B.StepStats, B.CacheEvent, B.PrefillStats,
+                                 B.AttnDesc]):
         assert L.tf_struct_bytes(which) == ctypes.sizeof(cls), cls.__name__
-    assert L.tf_struct_bytes(5) == 0
+    assert L.tf_struct_bytes(6) == 0
 
 
 def test_version_and_status_strings():
@@ -231,3 +232,28 @@ def test_product_lfu_rejects_misuse_and_rolls_back():
     c.invalidate(0, 1)
     ex, cnt, lu = c.state(0)
     assert ex.tolist() == [1, -1] and cnt.tolist() == [1, 0]
+
+
+def test_attention_descriptor_checks_and_sizes():
+    """The attention entry points check their descriptor on the host (no launch, no device needed)."""
+    good = B.attn_desc(2816, 16, 8, 128, 4096, 16, 16, 16, 16)
+    assert B.tf_attn_cache_bytes(good) == 4096 * 8 * 128 * 2
+    assert B.tf_attn_workspace_bytes(good) >= (2 * 2048 + 16 * 16 * (128 + 2)) * 4
+    for bad in (B.attn_desc(2816, 16, 8, 96, 4096, 16, 16, 16, 16),       # head_dim not 64/128/256
+                B.attn_desc(2816, 12, 8, 128, 4096, 16, 16, 16, 16),      # n_q_heads not a multiple of n_kv_heads
+                B.attn_desc(2820, 16, 8, 128, 4096, 16, 16, 16, 16),      # H not a multiple of 8
+                B.attn_desc(2816, 16, 8, 128, 0, 16, 16, 16, 16),         # no cache rows
+                B.attn_desc(2816, 16, 8, 128, 4096, 16, 16, 16, 8),       # unaligned W_o
+                B.attn_desc(2816, 16, 8, 128, 4096, 16, 16, 16, 0)):      # NULL W_o
+        assert B.tf_attn_workspace_bytes(bad) == 0
+        assert B.tf_attn_cache_bytes(bad) == 0
+        with pytest.raises(B.TFError) as e:
+            B.tf_attn_decode(bad, 16, 32, 0, 64, 64, 128, 1 << 20, stream=0)
+        assert e.value.status == B.TF_ERR_INVALID_ARG
+    for pos in (-1, 4096):
+        with pytest.raises(B.TFError) as e:
+            B.tf_attn_decode(good, 16, 32, pos, 64, 64, 128, 1 << 20, stream=0)
+        assert e.value.status == B.TF_ERR_INVALID_ARG
+    with pytest.raises(B.TFError) as e:   # workspace too small
+        B.tf_attn_decode(good, 16, 32, 0, 64, 64, 128, 64, stream=0)
+    assert e.value.status == B.TF_ERR_INVALID_ARG

@@ -33,6 +33,7 @@ T_SH = 6         # shared-expert bf16 weights (matrix 0 gate, 1 up, 2 down)
 T_ZIPF = 7       # Zipf rank -> expert permutation
 T_COIN = 8       # per-(step, layer) coin of the repeat-previous-top-k workload
 T_NOISE = 9      # per-(step, layer) router-logit noise of the streaming workload
+T_ATTN = 10      # attention weights (matrix 0 q, 1 k, 2 v, 3 o) and synthetic cache contents (matrix 4 k, 5 v)
 
 GATE, UP, DOWN = 0, 1, 2
 GROUP = 64
@@ -152,6 +153,28 @@ def shared_weights(seed: int, layer: int, H: int, S: int):
     u = normal_bf16(key(seed, T_SH, layer, 0, UP), S * H, SHARED_SIGMA).reshape(S, H)
     d = normal_bf16(key(seed, T_SH, layer, 0, DOWN), H * S, SHARED_SIGMA).reshape(H, S)
     return g, u, d
+
+
+def attention_weights(seed: int, layer: int, H: int, nq: int, nkv: int, d: int):
+    """Attention projections as bf16 bits: Wq [nq*d, H], Wk, Wv [nkv*d, H] ~ N(0, 1/sqrt(H)),
+    Wo [H, nq*d] ~ N(0, 0.5/sqrt(nq*d))."""
+    sq, so = float(H) ** -0.5, 0.5 * float(nq * d) ** -0.5
+    q = normal_bf16(key(seed, T_ATTN, layer, 0, 0), nq * d * H, sq).reshape(nq * d, H)
+    k = normal_bf16(key(seed, T_ATTN, layer, 0, 1), nkv * d * H, sq).reshape(nkv * d, H)
+    v = normal_bf16(key(seed, T_ATTN, layer, 0, 2), nkv * d * H, sq).reshape(nkv * d, H)
+    o = normal_bf16(key(seed, T_ATTN, layer, 0, 3), H * nq * d, so).reshape(H, nq * d)
+    return q, k, v, o
+
+
+def cache_rows(seed: int, layer: int, rows: int, nkv: int, d: int):
+    """Synthetic contents of the first `rows` rows of an fp16 K and V cache, ~ N(0, 1) (k) and N(0, 0.5) (v),
+    as fp16 bits [rows, nkv, d] (drawn as bf16 values, which fp16 holds exactly in this range)."""
+    out = []
+    for m, sigma in ((4, 1.0), (5, 0.5)):
+        b = normal_bf16(key(seed, T_ATTN, layer, 0, m), rows * nkv * d, sigma)
+        f = np.clip((b.astype(np.uint32) << 16).view(np.float32), -60000.0, 60000.0)
+        out.append(f.astype(np.float16).view(np.uint16).reshape(rows, nkv, d))
+    return out[0], out[1]
 
 
 def expert_matrix(seed: int, layer: int, expert: int, matrix: int, R: int, K: int):
